@@ -1,0 +1,409 @@
+"""Benchmark: biased-attention fwd+bwd TFLOP/s and fraction of roofline on one GB300.
+
+One step = one pass of the whole hot path on one synthetic graph:
+SPD build (gt_spd_build) + forward (gt_bias_attn_fwd) + backward
+(gt_bias_attn_bwd) for every layer, inputs resident in HBM.  Default workload
+(--config 4): N = 16384 nodes, a disjoint union of 64 Barabasi-Albert graphs
+(m = 3, 256 nodes each), H = 8 heads, head dim 16, bf16, clip D = 24.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gt|reference]
+                    [--config 1..5]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (the path needs no exchange between GPUs); value = work of all
+ranks / max time over ranks.  `--impl reference` times the fp64 CPU oracle on
+a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gt_inputs as gi  # noqa: E402
+
+METRIC = "biased-attention fwd+bwd TFLOP/s and % of roofline on 1 GB300"
+
+# Exp throughput of one GB300 SM: 32 ex2.approx.f32 results per clock, measured
+# with a dependent-chain-free ex2 loop on 152 SMs (packed f16x2/bf16x2 ex2 gives
+# the same 32 results per clock).  152 SMs at the 2070 MHz maximum clock.
+EX2_PER_CLK_SM = 32.0
+SMS = 152
+
+
+def attn_flops(w: gi.Workload) -> float:
+    """Algorithmic flops of one fwd+bwd over all layers: 14 N^2 H d per layer
+    (4 N^2 H d forward: QK^T and PV; 10 N^2 H d backward: QK^T again, dO V^T,
+    P^T dO, dS^T Q, dS K)."""
+    return 14.0 * w.n * w.n * w.heads * w.head_dim * w.layers
+
+
+def exps(w: gi.Workload) -> float:
+    """exp evaluations of one fwd+bwd: N^2 H forward plus N^2 H to recompute P."""
+    return 2.0 * w.n * w.n * w.heads * w.layers
+
+
+def algo_bytes(w: gi.Workload) -> float:
+    """HBM bytes of one fwd+bwd per the path's algorithm: the N^2 SPD bytes read
+    twice per layer plus the [N][H][d] tensors (fwd: q k v o; bwd: q k v o dO dq
+    dk dv) and the fp32 lse/D vectors."""
+    e = 4 if w.dtype == "f32" else 2
+    nhd = w.n * w.heads * w.head_dim * e
+    return w.layers * (2.0 * w.n * w.n + 12 * nhd + 4 * w.n * w.heads * 4)
+
+
+def workload_config(w: gi.Workload) -> dict:
+    return {"workload": f"{w.name}: N={w.n} {w.graph_kind} graph, H={w.heads}, d={w.head_dim}, "
+                        f"D={w.D}, layers={w.layers}, kv_block={w.kv_block}",
+            "n": w.n, "heads": w.heads, "head_dim": w.head_dim, "D": w.D, "layers": w.layers,
+            "kv_block": w.kv_block, "graph": w.graph_kind,
+            "l2": "inputs larger than L2: the int8 SPD matrix (N^2 bytes) is re-read every step"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            for ln in open(self.path):
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks not sampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        smax = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# -------------------------------------------------------------- GPU arm
+
+def measured_peaks() -> dict:
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_launches_per_step(w: gi.Workload, gt) -> int:
+    """Kernels of libgt launched by one step (memsets are not counted)."""
+    per = gt.launches_per_call(w.dtype, w.heads, w.head_dim, w.n, w.kv_block)
+    return per["spd"] + w.layers * (per["fwd"] + per["bwd"])
+
+
+def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
+    import torch
+    import graph_transformer_attention_gb300 as gt
+    from graph_transformer_attention_gb300 import build as gtb
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(gt.library_path()):
+        gtb.build()
+    if world > 1:
+        torch.distributed.barrier()
+    gt.load_library()
+    stream = torch.cuda.current_stream()
+
+    g = gi.config_graph(w)
+    layers = [gi.config_layer_tensors(w, li) for li in range(w.layers)]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dt_code = gt.GT_BF16 if w.dtype == "bf16" else gt.GT_F32
+
+    # pinned host copies for the end-to-end measurement
+    h_ip = torch.from_numpy(g.indptr).pin_memory()
+    h_ix = torch.from_numpy(g.indices).pin_memory()
+    h_layers = [{k: torch.from_numpy(x[k]).to(tdt if k != "T" else torch.float32).pin_memory()
+                 for k in ("q", "k", "v", "dO", "T")} for x in layers]
+    d_ip, d_ix = h_ip.to(dev), h_ix.to(dev)
+    d_layers = [{k: t.to(dev) for k, t in hl.items()} for hl in h_layers]
+    n, H, d = w.n, w.heads, w.head_dim
+    spd = torch.empty((n, gt.spd_ld(n)), dtype=torch.int8, device=dev)
+    ws_spd = torch.empty(gt.gt_spd_workspace_size(n, g.nnz, w.D), dtype=torch.uint8, device=dev)
+    ws_attn = torch.empty(max(256, gt.gt_bias_attn_workspace_size(dt_code, n, H, d, w.kv_block)),
+                          dtype=torch.uint8, device=dev)
+    outs = [dict(o=torch.empty((n, H, d), dtype=tdt, device=dev),
+                 lse=torch.empty((H, n), dtype=torch.float32, device=dev),
+                 dq=torch.empty((n, H, d), dtype=tdt, device=dev),
+                 dk=torch.empty((n, H, d), dtype=tdt, device=dev),
+                 dv=torch.empty((n, H, d), dtype=tdt, device=dev),
+                 dT=torch.empty((H, w.nb), dtype=torch.float32, device=dev))
+            for _ in range(w.layers)]
+    h_outs = [{k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in oo.items()
+               if k in ("o", "dq", "dk", "dv", "dT")} for oo in outs]
+
+    def step(ev=None):
+        # ev: [spd0, spd1, fwd0, fwd1, bwd0, bwd1] events around the parts of layer 0
+        if ev:
+            ev[0].record(stream)
+        gt.gt_spd_build(d_ip, d_ix, n, w.D, out=spd, workspace=ws_spd)
+        if ev:
+            ev[1].record(stream)
+        for li in range(w.layers):
+            x, oo = d_layers[li], outs[li]
+            if ev and li == 0:
+                ev[2].record(stream)
+            gt.gt_bias_attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], kv_block=w.kv_block,
+                                out=oo["o"], lse=oo["lse"], workspace=ws_attn)
+            if ev and li == 0:
+                ev[3].record(stream)
+                ev[4].record(stream)
+            gt.gt_bias_attn_bwd(x["q"], x["k"], x["v"], oo["o"], x["dO"], oo["lse"], spd, x["T"],
+                                dq=oo["dq"], dk=oo["dk"], dv=oo["dv"], dT=oo["dT"],
+                                workspace=ws_attn)
+            if ev and li == 0:
+                ev[5].record(stream)
+
+    def e2e_step():
+        d_ip.copy_(h_ip, non_blocking=True)
+        d_ix.copy_(h_ix, non_blocking=True)
+        for li in range(w.layers):
+            for k in d_layers[li]:
+                d_layers[li][k].copy_(h_layers[li][k], non_blocking=True)
+        step()
+        for li in range(w.layers):
+            for k, t in h_outs[li].items():
+                t.copy_(outs[li][k], non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    gt.gt_check_device_status()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # device-timed region: K steps, per-part events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t0.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t1.record(stream)
+        barrier()
+    ms_total = t0.elapsed_time(t1)
+    clocks = clk.summary()
+    gt.gt_check_device_status()
+    part_ms = {"spd": float(np.mean([e[0].elapsed_time(e[1]) for e in evs])),
+               "fwd": float(np.mean([e[2].elapsed_time(e[3]) for e in evs])),
+               "bwd": float(np.mean([e[4].elapsed_time(e[5]) for e in evs]))}
+
+    # end-to-end through the public API, host buffers in and out
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    e2e_ms = (time.perf_counter() - e0) * 1e3
+
+    h2d = h_ip.numel() * 8 + h_ix.numel() * 4 + sum(t.numel() * t.element_size()
+                                                    for hl in h_layers for t in hl.values())
+    d2h = sum(t.numel() * t.element_size() for ho in h_outs for t in ho.values())
+
+    ms = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
+    ms_total, e2e_ms = float(ms[0]), float(ms[1])
+    if rank != 0:
+        return None
+
+    ms_step = ms_total / args.steps
+    flops = attn_flops(w)
+    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    e2e_value = world * flops * args.steps / (e2e_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    clk_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    exp_peak = SMS * EX2_PER_CLK_SM * clk_mhz * 1e6           # exps / s
+    tensor_peak = float(peaks.get("bf16_tflops_sustained", 1700.0)) * 1e12
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0)) * 1e9
+    dom = "bwd" if part_ms["bwd"] >= part_ms["fwd"] else "fwd"
+    t_dom = part_ms[dom] * 1e-3
+    achieved = (n * n * H) / t_dom / 1e12 if t_dom > 0 else 0.0
+    # whole-path roofline: the slowest of tensor pipe, HBM and exp unit
+    t_attn = (part_ms["fwd"] + part_ms["bwd"]) * w.layers * 1e-3
+    t_roof = max(flops / tensor_peak, algo_bytes(w) / hbm_peak, exps(w) / exp_peak)
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded random graph and N(0,1) tensors)",
+        "config": workload_config(w),
+        "parts_ms": {k: round(v, 4) for k, v in part_ms.items()},
+        "node_pairs_per_s": {"spd": round(n * n / (part_ms["spd"] * 1e-3), 1),
+                             "attn_fwd_bwd": round(n * n * w.layers / t_attn, 1)},
+        "roofline": {"kernel": f"bias_attn_{dom}", "bound": "alu", "achieved": round(achieved, 4),
+                     "peak": round(exp_peak / 1e12, 3), "unit": "Texp/s",
+                     "frac": round(achieved * 1e12 / exp_peak, 4), "traffic": None,
+                     "peak_source": f"{SMS} SMs x {EX2_PER_CLK_SM:g} ex2/clk/SM (measured) x "
+                                    f"{clk_mhz:g} MHz"},
+        "path_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "t_attn_ms": round(t_attn * 1e3, 4),
+                          "frac": round(t_roof / t_attn, 4) if t_attn > 0 else None,
+                          "bound": "exp unit (MUFU)"},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(kernel_launches_per_step(w, gt) * args.steps),
+        "clocks": clocks,
+        "cpu_baseline": None,
+    }
+
+
+# --------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(w: gi.Workload, rows_per_step: int, seed: int = 0):
+    """Time the fp64 oracle on a bounded sample: forward, dq and dT over
+    `rows_per_step` rows plus dk, dv over as many columns, on the full graph
+    (the SPD matrix is built once, outside the timing).  Returns (seconds,
+    flops credited = 14 R N H d, threads)."""
+    from oracle import oracle as O
+    g = gi.config_graph(w)
+    spd = O.spd(g.n, g.indptr, g.indices, w.D)
+    x = gi.config_layer_tensors(w, 0)
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.n, rows_per_step, replace=False)).astype(np.int32)
+    nt = O.default_threads()
+    t0 = time.perf_counter()
+    o_r, lse_r = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], rows=rows, nthreads=nt)
+    Dv_rows = (o_r * x["dO"][rows].astype(np.float64)).sum(-1).T
+    lse_full = np.zeros((w.heads, w.n)); Dv_full = np.zeros((w.heads, w.n))
+    lse_full[:, rows] = lse_r; Dv_full[:, rows] = Dv_rows
+    O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_full, Dv_full, rows=rows,
+               want_dkdv=False, nthreads=nt)
+    # dk/dv for R columns: the oracle's cost does not depend on the values, so the
+    # lse/D of unsampled rows are left as placeholders and the results discarded
+    O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_full, Dv_full,
+               cols=rows, want_dq=False, want_dT=False, nthreads=nt)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * rows_per_step * w.n * w.heads * w.head_dim
+    return dt, flops, nt
+
+
+def run_reference(args, w: gi.Workload) -> dict:
+    rows = int(args.oracle_rows) or max(8, w.n // 8)
+    dts, fl, nt = [], 0.0, 1
+    for s in range(args.warmup + args.steps):
+        dt, fl, nt = oracle_sample(w, rows, seed=s)
+        if s >= args.warmup:
+            dts.append(dt)
+    tot = sum(dts)
+    value = fl * len(dts) / tot / 1e12
+    sample = (f"{rows} of {w.n} rows: forward, dq and dT over those rows plus dk, dv over {rows} "
+              f"columns, of layer 0 on the full graph; flops credited 14*R*N*H*d")
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / len(dts) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random graph and N(0,1) tensors)",
+        "config": workload_config(w), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gt", "reference"], default="gt")
+    ap.add_argument("--config", type=int, default=4, choices=sorted(gi.CONFIGS))
+    ap.add_argument("--oracle-rows", type=int, default=0,
+                    help="rows (and columns) the CPU oracle processes per sample "
+                         "(default: N/2 for the baseline line, N/8 per reference step)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = gi.CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_gpu(args, w, rank, world)
+    if rank == 0 and line is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            rows = args.oracle_rows or max(8, w.n // 2)
+            dt, fl, nt = oracle_sample(w, rows)
+            line["cpu_baseline"] = {
+                "value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                "sample": f"{rows} of {w.n} rows (fwd, dq, dT) and as many columns (dk, dv) of "
+                          f"layer 0; flops credited 14*R*N*H*d; {dt:.1f} s wall"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

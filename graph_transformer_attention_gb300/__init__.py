@@ -1,0 +1,213 @@
+"""Topology-biased graph attention on one GB300 (thin Python binding of libgt).
+
+Every step of the computation runs in the CUDA kernels of libgt.so; this module
+only marshals torch tensors into the C ABI declared in include/gt_attn.h (raw
+device pointers, sizes, the current CUDA stream) and allocates outputs and
+workspace with torch.  There is no CPU path: if libgt.so is missing or cannot
+be loaded the calls raise.
+
+Functions (same names as the C entry points):
+    gt_spd_build(indptr, indices, n, D)                       -> spd int8 [n][ld]
+    gt_bias_attn_fwd(q, k, v, spd, T, scale=None, kv_block=0) -> (o, lse)
+    gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T, scale=None) -> (dq, dk, dv, dT)
+The operation follows MegaGraph (abstract: attention scores plus a
+topology-aware bias matrix; Fig. 4: blockwise KV streaming with the bias column
+slice formed per block) with the Graphormer bias b[h][i][j] = T[h][spd[i][j]].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "GtError", "load_library", "library_path", "gt_spd_build", "gt_bias_attn_fwd",
+    "gt_bias_attn_bwd", "gt_spd_workspace_size", "gt_bias_attn_workspace_size",
+    "gt_check_device_status", "gt_status_string", "spd_ld", "GT_F32", "GT_BF16",
+]
+
+GT_F32 = 0
+GT_BF16 = 1
+GT_OK = 0
+_STATUS = {0: "GT_OK", -1: "GT_ERR_INVALID_ARG", -2: "GT_ERR_UNSUPPORTED", -3: "GT_ERR_CUDA",
+           -4: "GT_ERR_TIMEOUT", -5: "GT_ERR_WORKSPACE"}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgt.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GtError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        text = _lib.gt_status_string(status).decode() if _lib is not None else ""
+        super().__init__(f"{call} returned {_STATUS.get(status, status)}: {text}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libgt.so (build it with graph_transformer_attention_gb300.build first)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libgt.so not found at {_LIB_PATH}; run "
+                               "`python -m graph_transformer_attention_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64, sz, f32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
+                                ctypes.c_float)
+        lib.gt_status_string.argtypes = [ctypes.c_int]
+        lib.gt_status_string.restype = ctypes.c_char_p
+        lib.gt_spd_workspace_size.argtypes = [i32, i64, i32]
+        lib.gt_spd_workspace_size.restype = sz
+        lib.gt_spd_build.argtypes = [P, P, i32, i64, i32, P, i64, P, sz, P]
+        lib.gt_spd_build.restype = ctypes.c_int
+        lib.gt_bias_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.gt_bias_attn_workspace_size.restype = sz
+        lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
+                                         P, P, P, sz, P]
+        lib.gt_bias_attn_fwd.restype = ctypes.c_int
+        lib.gt_bias_attn_bwd.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, i32, f32,
+                                         P, P, P, P, P, sz, P]
+        lib.gt_bias_attn_bwd.restype = ctypes.c_int
+        lib.gt_check_device_status.argtypes = [P]
+        lib.gt_check_device_status.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(call: str, rc: int):
+    if rc != GT_OK:
+        raise GtError(call, rc)
+
+
+def _stream_handle(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GT_F32
+    if t.dtype == torch.bfloat16:
+        return GT_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("libgt works on CUDA tensors only")
+            if not t.is_contiguous():
+                raise ValueError("libgt needs contiguous tensors")
+
+
+def spd_ld(n: int) -> int:
+    """Row stride of the SPD matrix: n rounded up to a multiple of 16 bytes."""
+    return (n + 15) // 16 * 16
+
+
+def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0) -> dict:
+    """Number of libgt kernels each entry point launches for these sizes (memsets
+    not counted), mirroring the dispatch in gt_abi.cu."""
+    nsplit = -(-n // kv_block) if kv_block and kv_block < n else 1
+    fwd = 1 + (1 if nsplit > 1 else 0)
+    bwd = 4
+    return {"spd": 4, "fwd": fwd, "bwd": bwd}
+
+
+def gt_status_string(status: int) -> str:
+    return load_library().gt_status_string(status).decode()
+
+
+def gt_spd_workspace_size(n: int, nnz: int, D: int) -> int:
+    return int(load_library().gt_spd_workspace_size(n, nnz, D))
+
+
+def gt_bias_attn_workspace_size(dtype: int, n: int, h: int, d: int, kv_block: int = 0) -> int:
+    return int(load_library().gt_bias_attn_workspace_size(dtype, n, h, d, kv_block))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def gt_spd_build(indptr: torch.Tensor, indices: torch.Tensor, n: int, D: int,
+                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Clipped shortest-path bucket matrix, int8 [n][spd_ld(n)] (columns >= n unspecified)."""
+    lib = load_library()
+    _need_cuda(indptr, indices)
+    if indptr.dtype != torch.int64 or indices.dtype != torch.int32:
+        raise TypeError("indptr must be int64 and indices int32")
+    if out is None:
+        out = torch.empty((n, spd_ld(n)), dtype=torch.int8, device=indptr.device)
+    if workspace is None:
+        workspace = _workspace(lib.gt_spd_workspace_size(n, indices.numel(), D), indptr.device)
+    rc = lib.gt_spd_build(_ptr(indptr), _ptr(indices), n, indices.numel(), D, _ptr(out),
+                          out.stride(0), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check("gt_spd_build", rc)
+    return out
+
+
+def gt_bias_attn_fwd(q, k, v, spd, T, scale: float | None = None, kv_block: int = 0,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Biased attention forward; q, k, v [n][h][d] (fp32 or bf16), spd int8 [n][ld], T fp32 [h][nb]."""
+    lib = load_library()
+    _need_cuda(q, k, v, spd, T)
+    n, h, d = q.shape
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((h, n), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(lib.gt_bias_attn_workspace_size(dt, n, h, d, kv_block), q.device)
+    rc = lib.gt_bias_attn_fwd(dt, n, h, d, _ptr(q), _ptr(k), _ptr(v), _ptr(spd), spd.stride(0),
+                              _ptr(T), T.shape[1], float(scale), kv_block, _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check("gt_bias_attn_fwd", rc)
+    return out, lse
+
+
+def gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T, scale: float | None = None,
+                     dq=None, dk=None, dv=None, dT=None, workspace=None, stream=None):
+    """Gradients of sum(o * dO): returns (dq, dk, dv, dT)."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, dO, lse, spd, T)
+    n, h, d = q.shape
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dT = torch.empty_like(T) if dT is None else dT
+    if workspace is None:
+        workspace = _workspace(lib.gt_bias_attn_workspace_size(dt, n, h, d, 0), q.device)
+    rc = lib.gt_bias_attn_bwd(dt, n, h, d, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                              _ptr(spd), spd.stride(0), _ptr(T), T.shape[1], float(scale),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dT), _ptr(workspace),
+                              workspace.numel(), _stream_handle(stream))
+    _check("gt_bias_attn_bwd", rc)
+    return dq, dk, dv, dT
+
+
+def gt_check_device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel gave up a bounded wait."""
+    _check("gt_check_device_status", load_library().gt_check_device_status(_stream_handle(stream)))

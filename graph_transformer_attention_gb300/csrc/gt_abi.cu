@@ -1,0 +1,180 @@
+// gt_abi.cu -- the extern "C" entry points of libgt: argument checks,
+// workspace layout and kernel dispatch.  Declarations and the contract of every
+// call are in include/gt_attn.h.
+#include <cuda_runtime.h>
+#include <mutex>
+#include <stdint.h>
+
+#include "gt_attn.h"
+#include "gt_common.cuh"
+
+__device__ int g_gt_status = 0;
+
+namespace gt {
+
+// implemented in the kernel files
+size_t spd_workspace_bytes(int32_t n, int32_t D);
+int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t D, int8_t* spd,
+              int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
+int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                  const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
+                  void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s);
+int attn_bwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                  const void* o, const void* dO, const float* lse, const int8_t* spd, int64_t ld,
+                  const float* T, int nb, float scale, void* dq, void* dk, void* dv, float* dT,
+                  float* Dv, double* dT64, cudaStream_t s);
+
+int* device_status_ptr() {
+    static std::mutex mu;
+    static int* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gt_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+namespace {
+
+bool valid_dtype(int dtype) { return dtype == GT_F32 || dtype == GT_BF16; }
+
+int check_common(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                 const int8_t* spd, int64_t ld, const float* T, int nb) {
+    if (!valid_dtype(dtype)) return GT_ERR_INVALID_ARG;
+    if (n < 1 || h < 1 || d < 1 || nb < 1) return GT_ERR_INVALID_ARG;
+    if (!q || !k || !v || !spd || !T) return GT_ERR_INVALID_ARG;
+    if (ld < n || (ld % 16) != 0) return GT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(spd)) return GT_ERR_INVALID_ARG;
+    if (nb > 128) return GT_ERR_UNSUPPORTED;
+    if (h > 16 || d > 64) return GT_ERR_UNSUPPORTED;
+    return GT_OK;
+}
+
+struct FwdWs {
+    float* o_part;
+    float* lse_part;
+};
+
+struct BwdWs {
+    float* Dv;
+    double* dT64;
+};
+
+size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
+    Carve c(base, cap);
+    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    FwdWs w{nullptr, nullptr};
+    if (nsplit > 1) {
+        w.o_part = c.take<float>((size_t)nsplit * n * h * d);
+        w.lse_part = c.take<float>((size_t)nsplit * h * n);
+    }
+    if (out) *out = w;
+    return c.off;
+}
+
+size_t bwd_ws(int n, int h, int d, void* base, size_t cap, BwdWs* out) {
+    (void)d;
+    Carve c(base, cap);
+    BwdWs w;
+    w.Dv = c.take<float>((size_t)h * n);
+    w.dT64 = c.take<double>((size_t)h * 128);
+    if (out) *out = w;
+    return c.off;
+}
+
+}  // namespace
+}  // namespace gt
+
+extern "C" {
+
+const char* gt_status_string(int status) {
+    switch (status) {
+        case GT_OK: return "ok";
+        case GT_ERR_INVALID_ARG: return "invalid argument (NULL pointer, size, alignment or layout)";
+        case GT_ERR_UNSUPPORTED: return "shape not supported by this build";
+        case GT_ERR_CUDA: return "CUDA runtime error";
+        case GT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case GT_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+size_t gt_spd_workspace_size(int32_t n, int64_t nnz, int32_t D) {
+    (void)nnz;
+    if (n < 1 || D < 1 || D > GT_MAX_D) return 0;
+    return gt::spd_workspace_bytes(n, D);
+}
+
+int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t nnz, int32_t D,
+                 int8_t* spd, int64_t ld_spd, void* workspace, size_t ws_bytes, void* stream) {
+    if (!indptr || !spd || n < 1 || nnz < 0 || D < 1 || D > GT_MAX_D) return GT_ERR_INVALID_ARG;
+    if (nnz > 0 && !indices) return GT_ERR_INVALID_ARG;
+    if (ld_spd < n || (ld_spd % 16) != 0 || !gt::aligned16(spd)) return GT_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < gt::spd_workspace_bytes(n, D)) return GT_ERR_WORKSPACE;
+    return gt::spd_build(indptr, indices, n, D, spd, ld_spd, workspace, ws_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
+    if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
+    size_t a = gt::fwd_ws(n, h, d, kv_block, nullptr, 0, nullptr);
+    size_t b = gt::bwd_ws(n, h, d, nullptr, 0, nullptr);
+    return (a > b ? a : b) + 256;
+}
+
+int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,
+                     const void* v, const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                     float scale, int32_t kv_block, void* o, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream) {
+    int rc = gt::check_common(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb);
+    if (rc != GT_OK) return rc;
+    if (!o || !lse || !gt::aligned16(o)) return GT_ERR_INVALID_ARG;
+    if (kv_block < 0 || (kv_block > 0 && kv_block % 128 != 0)) return GT_ERR_INVALID_ARG;
+    if (kv_block >= n) kv_block = 0;
+    const size_t need = gt::fwd_ws(n, h, d, kv_block, nullptr, 0, nullptr);
+    if (need > 0 && (!workspace || ws_bytes < need)) return GT_ERR_WORKSPACE;
+    gt::FwdWs w;
+    gt::fwd_ws(n, h, d, kv_block, workspace, ws_bytes, &w);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return gt::attn_fwd_simt(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb, scale, kv_block, o, lse,
+                             w.o_part, w.lse_part, s);
+}
+
+int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,
+                     const void* v, const void* o, const void* dO, const float* lse,
+                     const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb, float scale,
+                     void* dq, void* dk, void* dv, float* dT, void* workspace, size_t ws_bytes,
+                     void* stream) {
+    int rc = gt::check_common(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb);
+    if (rc != GT_OK) return rc;
+    if (!o || !dO || !lse || !dq || !dk || !dv || !dT) return GT_ERR_INVALID_ARG;
+    if (!gt::aligned16(o) || !gt::aligned16(dO) || !gt::aligned16(dq) || !gt::aligned16(dk) ||
+        !gt::aligned16(dv))
+        return GT_ERR_INVALID_ARG;
+    const size_t need = gt::bwd_ws(n, h, d, nullptr, 0, nullptr);
+    if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
+    gt::BwdWs w;
+    gt::bwd_ws(n, h, d, workspace, ws_bytes, &w);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
+                             dv, dT, w.Dv, w.dT64, s);
+}
+
+int gt_check_device_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GT_ERR_CUDA;
+    int* p = gt::device_status_ptr();
+    if (!p) return GT_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyAsync(&word, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GT_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return GT_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GT_ERR_CUDA;
+    if (word & gt::kStatusTimeout) return GT_ERR_TIMEOUT;
+    return GT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,386 @@
+// gt_attn_simt.cu -- CUDA-core biased attention (exact fp32 arithmetic).
+//
+// This is the path for fp32 storage (fp32 products and softmax statistics;
+// tensor cores would round the products to tf32) and for shapes the
+// tensor-core kernels do not take.  It follows the blockwise form of the
+// MegaGraph paper's Fig. 4: each thread block streams KV tiles of 64 columns
+// past its rows, and the bias of the current tile is formed from the int8
+// bucket codes and a per-head table in shared memory.
+//
+// Forward: one thread per (row i, head h); online softmax in fp32 with expf.
+// Backward: D_i = <dO_i, o_i> first; then a row pass (dq and dT, dS summed per
+// bucket in shared memory, then added in fp64 to a global table) and a column
+// pass (dk, dv), each recomputing p from lse.  No atomics touch dq, dk or dv.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gt_common.cuh"
+
+namespace gt {
+namespace {
+
+constexpr int kRows = 128;   // rows (or columns) per thread block, one per thread
+constexpr int kTile = 64;    // streamed tile of the other dimension
+constexpr int kCodes = 256;  // every byte value has a table slot
+
+template <typename TE, int DP>
+__device__ __forceinline__ void load_vec(const TE* __restrict__ src, int d, float scale, float* dst) {
+#pragma unroll
+    for (int c = 0; c < DP; ++c) dst[c] = c < d ? scale * to_f32(src[c]) : 0.f;
+}
+
+// Stage a [kTile][DP] tile of x (rows r0..r0+kTile of head h) into shared fp32.
+template <typename TE, int DP>
+__device__ __forceinline__ void stage_tile(float (*dst)[DP], const TE* __restrict__ x, int n, int h,
+                                           int d, int head, int r0) {
+    for (int idx = threadIdx.x; idx < kTile * DP; idx += blockDim.x) {
+        int r = idx / DP, c = idx % DP;
+        int row = r0 + r;
+        dst[r][c] = (row < n && c < d) ? to_f32(x[((int64_t)row * h + head) * d + c]) : 0.f;
+    }
+}
+
+// Forward.  grid = (ceil(n/128), h, nsplit); block = 128.
+// nsplit == 1: writes o (TE) and lse.  Otherwise writes fp32 partials
+// o_part[z][n][h][d] and lse_part[z][h][n] for the KV columns of split z.
+template <typename TE, int DP>
+__global__ void __launch_bounds__(kRows)
+fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
+         const TE* __restrict__ v, const uint8_t* __restrict__ spd, int64_t ld,
+         const float* __restrict__ T, int nb, float scale, int kv_block,
+         TE* __restrict__ o, float* __restrict__ lse, float* __restrict__ o_part,
+         float* __restrict__ lse_part) {
+    __shared__ float sK[kTile][DP];
+    __shared__ float sV[kTile][DP];
+    __shared__ float sT[kCodes];
+    const int head = blockIdx.y;
+    const int i = blockIdx.x * kRows + threadIdx.x;
+    const int split = blockIdx.z;
+    const int j_begin = kv_block > 0 ? split * kv_block : 0;
+    const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
+
+    float qi[DP], acc[DP];
+    const bool live = i < n;
+    load_vec<TE, DP>(q + ((int64_t)(live ? i : 0) * h + head) * d, d, scale, qi);
+#pragma unroll
+    for (int c = 0; c < DP; ++c) acc[c] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    const uint8_t* row = spd + (int64_t)(live ? i : 0) * ld;
+
+    for (int j0 = j_begin; j0 < j_end; j0 += kTile) {
+        __syncthreads();
+        stage_tile<TE, DP>(sK, k, n, h, d, head, j0);
+        stage_tile<TE, DP>(sV, v, n, h, d, head, j0);
+        __syncthreads();
+        const int jn = min(kTile, j_end - j0);
+#pragma unroll 1
+        for (int jj = 0; jj < jn; ++jj) {
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < DP; ++c) dot = fmaf(qi[c], sK[jj][c], dot);
+            const float x = dot + sT[row[j0 + jj]];
+            if (x > m) {                          // new running max: rescale what we have
+                const float corr = expf(m - x);   // 0 for the first column (m = -inf)
+                l *= corr;
+#pragma unroll
+                for (int c = 0; c < DP; ++c) acc[c] *= corr;
+                m = x;
+            }
+            const float p = expf(x - m);
+            l += p;
+#pragma unroll
+            for (int c = 0; c < DP; ++c) acc[c] = fmaf(p, sV[jj][c], acc[c]);
+        }
+    }
+    if (!live) return;
+    const float inv = 1.f / l;
+    if (gridDim.z == 1) {
+        TE* oi = o + ((int64_t)i * h + head) * d;
+#pragma unroll
+        for (int c = 0; c < DP; ++c)
+            if (c < d) oi[c] = from_f32<TE>(acc[c] * inv);
+        lse[(int64_t)head * n + i] = m + logf(l);
+    } else {
+        float* oi = o_part + (((int64_t)split * n + i) * h + head) * d;
+#pragma unroll
+        for (int c = 0; c < DP; ++c)
+            if (c < d) oi[c] = acc[c] * inv;
+        lse_part[((int64_t)split * h + head) * n + i] = m + logf(l);
+    }
+}
+
+// D[h][n] = <dO_i, o_i> in fp32.
+template <typename TE>
+__global__ void bwd_delta(int n, int h, int d, const TE* __restrict__ o, const TE* __restrict__ dO,
+                          float* __restrict__ Dv) {
+    const int64_t total = (int64_t)n * h;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(x / h), head = (int)(x % h);
+        const TE* a = o + x * d;
+        const TE* b = dO + x * d;
+        float acc = 0.f;
+        for (int c = 0; c < d; ++c) acc = fmaf(to_f32(a[c]), to_f32(b[c]), acc);
+        Dv[(int64_t)head * n + i] = acc;
+    }
+}
+
+// Row pass: dq_i and dS summed per bucket.  grid = (ceil(n/128), h); block = 128.
+template <typename TE, int DP>
+__global__ void __launch_bounds__(kRows)
+bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
+              const TE* __restrict__ v, const TE* __restrict__ dO, const float* __restrict__ lse,
+              const float* __restrict__ Dv, const uint8_t* __restrict__ spd, int64_t ld,
+              const float* __restrict__ T, int nb, float scale, TE* __restrict__ dq,
+              double* __restrict__ dT64) {
+    __shared__ float sK[kTile][DP];
+    __shared__ float sV[kTile][DP];
+    __shared__ float sT[kCodes];
+    __shared__ float sH[kCodes];
+    const int head = blockIdx.y;
+    const int i = blockIdx.x * kRows + threadIdx.x;
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) {
+        sT[c] = c < nb ? T[head * nb + c] : 0.f;
+        sH[c] = 0.f;
+    }
+    const bool live = i < n;
+    const int ii = live ? i : 0;
+    float qi[DP], gi[DP], acc[DP];
+    load_vec<TE, DP>(q + ((int64_t)ii * h + head) * d, d, scale, qi);
+    load_vec<TE, DP>(dO + ((int64_t)ii * h + head) * d, d, 1.f, gi);
+#pragma unroll
+    for (int c = 0; c < DP; ++c) acc[c] = 0.f;
+    const float L = lse[(int64_t)head * n + ii];
+    const float Di = Dv[(int64_t)head * n + ii];
+    const uint8_t* row = spd + (int64_t)ii * ld;
+
+    for (int j0 = 0; j0 < n; j0 += kTile) {
+        __syncthreads();
+        stage_tile<TE, DP>(sK, k, n, h, d, head, j0);
+        stage_tile<TE, DP>(sV, v, n, h, d, head, j0);
+        __syncthreads();
+        if (!live) continue;
+        const int jn = min(kTile, n - j0);
+#pragma unroll 1
+        for (int jj = 0; jj < jn; ++jj) {
+            float dot = 0.f, dp = 0.f;
+#pragma unroll
+            for (int c = 0; c < DP; ++c) {
+                dot = fmaf(qi[c], sK[jj][c], dot);
+                dp = fmaf(gi[c], sV[jj][c], dp);
+            }
+            const int code = row[j0 + jj];
+            const float p = expf(dot + sT[code] - L);
+            const float ds = p * (dp - Di);
+#pragma unroll
+            for (int c = 0; c < DP; ++c) acc[c] = fmaf(ds, sK[jj][c], acc[c]);
+            atomicAdd(&sH[code], ds);
+        }
+    }
+    if (live) {
+        TE* out = dq + ((int64_t)i * h + head) * d;
+#pragma unroll
+        for (int c = 0; c < DP; ++c)
+            if (c < d) out[c] = from_f32<TE>(acc[c] * scale);
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < nb; c += blockDim.x)
+        if (sH[c] != 0.f) atomicAdd(&dT64[head * nb + c], (double)sH[c]);
+}
+
+// Column pass: dk_j, dv_j.  grid = (ceil(n/128), h); block = 128.
+template <typename TE, int DP>
+__global__ void __launch_bounds__(kRows)
+bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
+              const TE* __restrict__ v, const TE* __restrict__ dO, const float* __restrict__ lse,
+              const float* __restrict__ Dv, const uint8_t* __restrict__ spd, int64_t ld,
+              const float* __restrict__ T, int nb, float scale, TE* __restrict__ dk,
+              TE* __restrict__ dv) {
+    __shared__ float sQ[kTile][DP];
+    __shared__ float sG[kTile][DP];
+    __shared__ float sL[kTile], sD[kTile];
+    __shared__ uint8_t sS[kTile][kRows];
+    __shared__ float sT[kCodes];
+    const int head = blockIdx.y;
+    const int j = blockIdx.x * kRows + threadIdx.x;
+    const int jbase = blockIdx.x * kRows;
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
+    const bool live = j < n;
+    const int jj_ = live ? j : 0;
+    float kj[DP], vj[DP], ak[DP], av[DP];
+    load_vec<TE, DP>(k + ((int64_t)jj_ * h + head) * d, d, scale, kj);
+    load_vec<TE, DP>(v + ((int64_t)jj_ * h + head) * d, d, 1.f, vj);
+#pragma unroll
+    for (int c = 0; c < DP; ++c) ak[c] = av[c] = 0.f;
+
+    for (int i0 = 0; i0 < n; i0 += kTile) {
+        __syncthreads();
+        stage_tile<TE, DP>(sQ, q, n, h, d, head, i0);
+        stage_tile<TE, DP>(sG, dO, n, h, d, head, i0);
+        for (int x = threadIdx.x; x < kTile; x += blockDim.x) {
+            const int row = i0 + x;
+            sL[x] = row < n ? lse[(int64_t)head * n + row] : 0.f;
+            sD[x] = row < n ? Dv[(int64_t)head * n + row] : 0.f;
+        }
+        for (int x = threadIdx.x; x < kTile * kRows; x += blockDim.x) {
+            const int r = x / kRows, c = x % kRows;
+            const int row = i0 + r, col = jbase + c;
+            sS[r][c] = (row < n && col < n) ? spd[(int64_t)row * ld + col] : 0;
+        }
+        __syncthreads();
+        if (!live) continue;
+        const int in_ = min(kTile, n - i0);
+#pragma unroll 1
+        for (int r = 0; r < in_; ++r) {
+            float dot = 0.f, dp = 0.f;
+#pragma unroll
+            for (int c = 0; c < DP; ++c) {
+                dot = fmaf(sQ[r][c], kj[c], dot);
+                dp = fmaf(sG[r][c], vj[c], dp);
+            }
+            const float p = expf(dot + sT[sS[r][threadIdx.x]] - sL[r]);
+            const float ds = p * (dp - sD[r]);
+#pragma unroll
+            for (int c = 0; c < DP; ++c) {
+                ak[c] = fmaf(ds, sQ[r][c], ak[c]);
+                av[c] = fmaf(p, sG[r][c], av[c]);
+            }
+        }
+    }
+    if (!live) return;
+    TE* ok = dk + ((int64_t)j * h + head) * d;
+    TE* ov = dv + ((int64_t)j * h + head) * d;
+#pragma unroll
+    for (int c = 0; c < DP; ++c)
+        if (c < d) {
+            ok[c] = from_f32<TE>(ak[c] * scale);
+            ov[c] = from_f32<TE>(av[c]);
+        }
+}
+
+__global__ void dT_finalize(int count, const double* __restrict__ dT64, float* __restrict__ dT) {
+    for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < count; x += gridDim.x * blockDim.x)
+        dT[x] = (float)dT64[x];
+}
+
+// Exact merge of per-split partials: lse = log sum_z e^{lse_z};
+// o = sum_z e^{lse_z - lse} o_z.
+template <typename TE>
+__global__ void merge_splits(int n, int h, int d, int nsplit, const float* __restrict__ o_part,
+                             const float* __restrict__ lse_part, TE* __restrict__ o,
+                             float* __restrict__ lse) {
+    const int64_t total = (int64_t)n * h;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(x / h), head = (int)(x % h);
+        float mx = -INFINITY;
+        for (int z = 0; z < nsplit; ++z) mx = fmaxf(mx, lse_part[((int64_t)z * h + head) * n + i]);
+        float sum = 0.f;
+        for (int z = 0; z < nsplit; ++z) sum += expf(lse_part[((int64_t)z * h + head) * n + i] - mx);
+        const float L = mx + logf(sum);
+        for (int c = 0; c < d; ++c) {
+            float acc = 0.f;
+            for (int z = 0; z < nsplit; ++z) {
+                const float w = expf(lse_part[((int64_t)z * h + head) * n + i] - L);
+                acc = fmaf(w, o_part[(((int64_t)z * n + i) * h + head) * d + c], acc);
+            }
+            o[x * d + c] = from_f32<TE>(acc);
+        }
+        lse[(int64_t)head * n + i] = L;
+    }
+}
+
+int grid_for(int64_t total) {
+    const int64_t b = (total + 255) / 256;
+    return (int)(b < 4096 ? (b > 0 ? b : 1) : 4096);
+}
+
+template <typename TE, int DP>
+int fwd_simt_launch(int n, int h, int d, const void* q, const void* k, const void* v,
+                    const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                    int kv_block, void* o, float* lse, float* o_part, float* lse_part,
+                    cudaStream_t s) {
+    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    dim3 grid((n + kRows - 1) / kRows, h, nsplit);
+    fwd_simt<TE, DP><<<grid, kRows, 0, s>>>(
+        n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld, T, nb, scale,
+        nsplit > 1 ? kv_block : 0, (TE*)o, lse, o_part, lse_part);
+    if (nsplit > 1)
+        merge_splits<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
+                                                                  (TE*)o, lse);
+    return check_launch();
+}
+
+template <typename TE, int DP>
+int bwd_simt_launch(int n, int h, int d, const void* q, const void* k, const void* v,
+                    const void* o, const void* dO, const float* lse, const int8_t* spd,
+                    int64_t ld, const float* T, int nb, float scale, void* dq, void* dk, void* dv,
+                    float* dT, float* Dv, double* dT64, cudaStream_t s) {
+    if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)h * nb, s) != cudaSuccess) return GT_ERR_CUDA;
+    bwd_delta<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, (const TE*)o, (const TE*)dO, Dv);
+    dim3 grid((n + kRows - 1) / kRows, h);
+    bwd_rows_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
+                                                 (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
+                                                 nb, scale, (TE*)dq, dT64);
+    bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
+                                                 (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
+                                                 nb, scale, (TE*)dk, (TE*)dv);
+    dT_finalize<<<1, 256, 0, s>>>(h * nb, dT64, dT);
+    return check_launch();
+}
+
+template <typename TE>
+int fwd_simt_dispatch(int n, int h, int d, const void* q, const void* k, const void* v,
+                      const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                      int kv_block, void* o, float* lse, float* o_part, float* lse_part,
+                      cudaStream_t s) {
+    if (d <= 8) return fwd_simt_launch<TE, 8>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+    if (d <= 16) return fwd_simt_launch<TE, 16>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+    if (d <= 32) return fwd_simt_launch<TE, 32>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+    return fwd_simt_launch<TE, 64>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+}
+
+template <typename TE>
+int bwd_simt_dispatch(int n, int h, int d, const void* q, const void* k, const void* v,
+                      const void* o, const void* dO, const float* lse, const int8_t* spd,
+                      int64_t ld, const float* T, int nb, float scale, void* dq, void* dk,
+                      void* dv, float* dT, float* Dv, double* dT64, cudaStream_t s) {
+    if (d <= 8) return bwd_simt_launch<TE, 8>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+    if (d <= 16) return bwd_simt_launch<TE, 16>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+    if (d <= 32) return bwd_simt_launch<TE, 32>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+    return bwd_simt_launch<TE, 64>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+}
+
+}  // namespace
+
+int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                  const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
+                  void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s) {
+    if (dtype == GT_F32)
+        return fwd_simt_dispatch<float>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+    return fwd_simt_dispatch<__nv_bfloat16>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+}
+
+int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
+                   const float* lse_part, void* o, float* lse, cudaStream_t s) {
+    if (dtype == GT_F32)
+        merge_splits<float><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
+                                                                     (float*)o, lse);
+    else
+        merge_splits<__nv_bfloat16><<<grid_for((int64_t)n * h), 256, 0, s>>>(
+            n, h, d, nsplit, o_part, lse_part, (__nv_bfloat16*)o, lse);
+    return check_launch();
+}
+
+int attn_bwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                  const void* o, const void* dO, const float* lse, const int8_t* spd, int64_t ld,
+                  const float* T, int nb, float scale, void* dq, void* dk, void* dv, float* dT,
+                  float* Dv, double* dT64, cudaStream_t s) {
+    if (dtype == GT_F32)
+        return bwd_simt_dispatch<float>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+    return bwd_simt_dispatch<__nv_bfloat16>(n, h, d, q, k, v, o, dO, lse, spd, ld, T, nb, scale, dq, dk, dv, dT, Dv, dT64, s);
+}
+
+}  // namespace gt

@@ -1,0 +1,296 @@
+// gt_spd.cu -- clipped shortest-path buckets of an undirected graph.
+//
+// spd[i][j] = min(dist(i,j), D) for reachable pairs, D+1 otherwise (the
+// topology behind the bias matrix of the MegaGraph abstract; Graphormer's
+// spatial-encoding buckets).
+//
+// Design (one GPU, CSR in HBM):
+//  1. Connected components by lock-free union-find (hook the larger root under
+//     the smaller with atomicCAS, then compress).  Pairs that the breadth-first
+//     search below does not reach within D-1 levels get D when they share a
+//     component and D+1 when they do not.
+//  2. Bit-parallel multi-source BFS: each CTA owns a batch of 64 consecutive
+//     sources, one bit per source in a 64-bit word per vertex.  A level pushes
+//     the frontier word of every queued vertex to its neighbours with atomicOr
+//     (work is proportional to the edges of the active frontier, so a batch that
+//     lives in one small component touches only that component), then keeps the
+//     bits not seen before.  Distances are stored bit-sliced: slice k holds bit k
+//     of the level at which each source reached the vertex.
+//  3. The same CTA writes its 64 output rows, 4 bytes per store, coalesced along
+//     the row, then clears only the state it touched.
+// Every loop is bounded: union-find retries and the level loop have hard caps.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gt_common.cuh"
+
+namespace gt {
+namespace {
+
+constexpr int kSpdThreads = 1024;
+constexpr int kUfRetryCap = 1 << 22;
+
+__device__ __forceinline__ int uf_find(int* parent, int x) {
+    // Path halving; parents only ever move to smaller ids, so this terminates.
+    for (int it = 0; it < (1 << 30); ++it) {
+        int p = __ldcg(parent + x);
+        if (p == x) return x;
+        int gp = __ldcg(parent + p);
+        if (gp != p) atomicMin(parent + x, gp);
+        x = gp;
+    }
+    return x;
+}
+
+__global__ void uf_init(int* parent, int n) {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n; v += gridDim.x * blockDim.x)
+        parent[v] = v;
+}
+
+// One warp per vertex u, lanes over its neighbours; each edge (u, w) with w > u
+// unites the two trees.
+__global__ void uf_hook(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices,
+                        int* parent, int n, int* status) {
+    const int lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int u = warp; u < n; u += nwarps) {
+        const int64_t e0 = indptr[u], e1 = indptr[u + 1];
+        for (int64_t e = e0 + lane; e < e1; e += 32) {
+            int w = indices[e];
+            if (w <= u || w >= n) continue;
+            int a = u, b = w;
+            int tries = 0;
+            while (true) {
+                a = uf_find(parent, a);
+                b = uf_find(parent, b);
+                if (a == b) break;
+                if (a > b) { int t = a; a = b; b = t; }
+                // hook root b under the smaller root a
+                if (atomicCAS(parent + b, b, a) == b) break;
+                if (++tries > kUfRetryCap) { atomicOr(status, kStatusTimeout); break; }
+            }
+        }
+    }
+}
+
+__global__ void uf_compress(int* parent, int n) {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n; v += gridDim.x * blockDim.x)
+        parent[v] = uf_find(parent, v);
+}
+
+struct BfsState {
+    uint64_t* vis;     // [n] sources that reached v
+    uint64_t* fr;      // [n] bits new at v in the previous level
+    uint64_t* acc;     // [n] bits pushed to v in the current level
+    uint64_t* db;      // [nslices][n] bit-sliced distances
+    int32_t* qa;       // [n] frontier queue
+    int32_t* qb;       // [n] next frontier queue
+    int32_t* cand;     // [n] vertices that received a push this level
+    int32_t* touched;  // [n] vertices with vis != 0
+};
+
+__device__ __forceinline__ BfsState bfs_slice(char* base, size_t per_cta, int cta, int n, int nslices) {
+    char* p = base + per_cta * (size_t)cta;
+    BfsState s;
+    size_t w = (size_t)n * sizeof(uint64_t);
+    s.vis = reinterpret_cast<uint64_t*>(p); p += w;
+    s.fr = reinterpret_cast<uint64_t*>(p); p += w;
+    s.acc = reinterpret_cast<uint64_t*>(p); p += w;
+    s.db = reinterpret_cast<uint64_t*>(p); p += w * (size_t)nslices;
+    size_t q = (size_t)n * sizeof(int32_t);
+    s.qa = reinterpret_cast<int32_t*>(p); p += q;
+    s.qb = reinterpret_cast<int32_t*>(p); p += q;
+    s.cand = reinterpret_cast<int32_t*>(p); p += q;
+    s.touched = reinterpret_cast<int32_t*>(p);
+    return s;
+}
+
+// Four codes of columns 4c..4c+3 of one output row; the ragged end of the row
+// is written byte by byte so that columns >= n stay untouched.
+__device__ __forceinline__ void store_codes(int8_t* row, int c, int n, uint32_t word) {
+    if (4 * c + 4 <= n) {
+        *reinterpret_cast<uint32_t*>(row + 4 * c) = word;
+    } else {
+        for (int t = 0; 4 * c + t < n; ++t) row[4 * c + t] = (int8_t)(word >> (8 * t));
+    }
+}
+
+__global__ void __launch_bounds__(kSpdThreads)
+bfs_batches(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices,
+            const int* __restrict__ comp, int n, int D, int nslices,
+            int8_t* __restrict__ spd, int64_t ld, char* ws, size_t per_cta) {
+    __shared__ int s_qlen, s_nlen, s_clen, s_tlen;
+    __shared__ int s_comp[64];
+    BfsState st = bfs_slice(ws, per_cta, blockIdx.x, n, nslices);
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int nbatches = (n + 63) / 64;
+
+    for (int batch = blockIdx.x; batch < nbatches; batch += gridDim.x) {
+        const int s0 = batch * 64;
+        const int nsrc = min(64, n - s0);
+        // level 0: every source reaches itself
+        if (tid < nsrc) {
+            int s = s0 + tid;
+            st.vis[s] = 1ull << tid;
+            st.fr[s] = 1ull << tid;
+            st.qa[tid] = s;
+            st.touched[tid] = s;
+            s_comp[tid] = comp[s];
+        }
+        if (tid == 0) { s_qlen = nsrc; s_tlen = nsrc; }
+        __syncthreads();
+
+        int32_t* q = st.qa;
+        int32_t* qn = st.qb;
+        for (int level = 1; level < D; ++level) {
+            const int qlen = s_qlen;
+            if (qlen == 0) break;
+            if (tid == 0) { s_clen = 0; s_nlen = 0; }
+            __syncthreads();
+            // push: one warp per queued vertex, lanes over its neighbours
+            for (int qi = warp; qi < qlen; qi += nwarps) {
+                const int u = q[qi];
+                const uint64_t w = st.fr[u];
+                const int64_t e0 = indptr[u], e1 = indptr[u + 1];
+                for (int64_t e = e0 + lane; e < e1; e += 32) {
+                    const int v = indices[e];
+                    if ((unsigned)v >= (unsigned)n) continue;
+                    unsigned long long old = atomicOr(reinterpret_cast<unsigned long long*>(st.acc + v),
+                                                      (unsigned long long)w);
+                    if (old == 0ull) st.cand[atomicAdd(&s_clen, 1)] = v;
+                }
+            }
+            __syncthreads();
+            const int clen = s_clen;
+            // keep the bits not seen before (acc is only touched in L2)
+            for (int ci = tid; ci < clen; ci += blockDim.x) {
+                const int v = st.cand[ci];
+                const uint64_t a = __ldcg(reinterpret_cast<const unsigned long long*>(st.acc + v));
+                __stcg(reinterpret_cast<unsigned long long*>(st.acc + v), 0ull);
+                const uint64_t seen = st.vis[v];
+                const uint64_t nw = a & ~seen;
+                if (nw) {
+                    if (seen == 0) st.touched[atomicAdd(&s_tlen, 1)] = v;
+                    st.vis[v] = seen | nw;
+                    st.fr[v] = nw;
+                    for (int k = 0; k < nslices; ++k)
+                        if ((level >> k) & 1) st.db[(size_t)k * n + v] |= nw;
+                    qn[atomicAdd(&s_nlen, 1)] = v;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) s_qlen = s_nlen;
+            int32_t* t = q; q = qn; qn = t;
+            __syncthreads();
+        }
+
+        // write rows s0 .. s0+nsrc-1, four columns per store
+        const int nchunks = (n + 3) / 4;
+        const int8_t Dc = (int8_t)D, Dfar = (int8_t)(D + 1);
+        for (int c = tid; c < nchunks; c += blockDim.x) {
+            uint64_t vis4[4];
+            int comp4[4];
+            bool any = false;
+            for (int t = 0; t < 4; ++t) {
+                int v = 4 * c + t;
+                vis4[t] = v < n ? st.vis[v] : 0ull;
+                comp4[t] = v < n ? comp[v] : -1;
+                any |= vis4[t] != 0ull;
+            }
+            if (!any) {
+                for (int b = 0; b < nsrc; ++b) {
+                    const int cs = s_comp[b];
+                    uint32_t word = 0;
+                    for (int t = 0; t < 4; ++t)
+                        word |= (uint32_t)(uint8_t)(comp4[t] == cs ? Dc : Dfar) << (8 * t);
+                    store_codes(spd + (int64_t)(s0 + b) * ld, c, n, word);
+                }
+            } else {
+                uint64_t db4[4][7];
+                for (int t = 0; t < 4; ++t) {
+                    int v = 4 * c + t;
+                    for (int k = 0; k < 7; ++k)
+                        db4[t][k] = (v < n && k < nslices) ? st.db[(size_t)k * n + v] : 0ull;
+                }
+                for (int b = 0; b < nsrc; ++b) {
+                    const int cs = s_comp[b];
+                    uint32_t word = 0;
+                    for (int t = 0; t < 4; ++t) {
+                        int code;
+                        if ((vis4[t] >> b) & 1ull) {
+                            code = 0;
+                            for (int k = 0; k < 7; ++k) code |= (int)((db4[t][k] >> b) & 1ull) << k;
+                        } else {
+                            code = comp4[t] == cs ? D : D + 1;
+                        }
+                        word |= (uint32_t)(uint8_t)code << (8 * t);
+                    }
+                    store_codes(spd + (int64_t)(s0 + b) * ld, c, n, word);
+                }
+            }
+        }
+        __syncthreads();
+        // clear what this batch touched
+        const int tlen = s_tlen;
+        for (int ti = tid; ti < tlen; ti += blockDim.x) {
+            const int v = st.touched[ti];
+            st.vis[v] = 0;
+            for (int k = 0; k < nslices; ++k) st.db[(size_t)k * n + v] = 0;
+        }
+        __syncthreads();
+    }
+}
+
+int slices_for(int D) {
+    int s = 0;
+    while ((1 << s) <= D - 1) ++s;   // levels recorded are 1 .. D-1
+    return s;
+}
+
+size_t per_cta_bytes(int n, int nslices) {
+    size_t b = (size_t)n * sizeof(uint64_t) * (size_t)(3 + nslices) + (size_t)n * sizeof(int32_t) * 4;
+    return (b + 255) & ~size_t(255);
+}
+
+int spd_ctas(int n) {
+    int nb = (n + 63) / 64;
+    int sms = num_sms();
+    return nb < sms ? nb : sms;
+}
+
+}  // namespace
+
+size_t spd_workspace_bytes(int32_t n, int32_t D) {
+    Carve c(nullptr, 0);
+    c.take<int>((size_t)n);
+    c.take<char>(per_cta_bytes(n, slices_for(D)) * (size_t)spd_ctas(n));
+    return c.off + 256;
+}
+
+int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t D,
+              int8_t* spd, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    Carve c(ws, ws_bytes);
+    int* comp = c.take<int>((size_t)n);
+    const int nslices = slices_for(D);
+    const size_t per = per_cta_bytes(n, nslices);
+    const int nctas = spd_ctas(n);
+    char* bfs_ws = c.take<char>(per * (size_t)nctas);
+    if (!c.fits()) return GT_ERR_WORKSPACE;
+    int* status = device_status_ptr();
+    if (!status) return GT_ERR_CUDA;
+    const int sms = num_sms();
+    uf_init<<<sms * 4, 256, 0, stream>>>(comp, n);
+    uf_hook<<<sms * 8, 256, 0, stream>>>(indptr, indices, comp, n, status);
+    uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
+    // the BFS keeps vis / acc / db zero between batches; start from zero
+    if (cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess) return GT_ERR_CUDA;
+    bfs_batches<<<nctas, kSpdThreads, 0, stream>>>(indptr, indices, comp, n, D, nslices, spd, ld,
+                                                   bfs_ws, per);
+    return check_launch();
+}
+
+}  // namespace gt

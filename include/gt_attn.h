@@ -1,0 +1,146 @@
+/*
+ * gt_attn.h -- C ABI of libgt: topology-biased graph attention on one GB300.
+ *
+ * The operation (MegaGraph, "Towards Efficient Training of Large-Scale Graph
+ * Transformers with Automated Hybrid Parallelism"):
+ *   - abstract: a Graph Transformer layer carries, besides the attention score
+ *     matrix, a topology-aware bias matrix of the same N x N shape per head;
+ *   - Fig. 4: attention is computed KV block by KV block, and the bias columns
+ *     that go with each incoming KV block are sliced on the fly.
+ * The bias is the Graphormer spatial encoding over clipped shortest-path
+ * distances:  b[h][i][j] = T[h][ spd[i][j] ],  spd[i][j] = min(dist(i,j), D) for
+ * reachable pairs and D+1 otherwise, so T has nb = D+2 columns.  Per head h:
+ *   s_ij = scale * <q_i, k_j> + b[h][i][j],   o_i = sum_j softmax_j(s_i) v_j,
+ *   lse_i = log sum_j exp(s_ij)  (natural log),
+ * and the backward pass returns dq, dk, dv and dT[h][c] = sum over pairs with
+ * spd[i][j] = c of dS_ij, where dS_ij = p_ij (<dO_i, v_j> - <dO_i, o_i>).
+ * Neither the N x N scores nor the N x N x H bias is ever stored.
+ *
+ * Conventions for every call below
+ *   - Pointers named as device buffers must be device memory of the current
+ *     CUDA device.  The caller owns and allocates every buffer, including the
+ *     workspace; the library allocates nothing and keeps no state between
+ *     calls (apart from one device status word, see gt_check_device_status).
+ *   - Layouts are dense row-major: q, k, v, o, dO, dq, dk, dv are [n][h][d]
+ *     (node, head, channel); lse is [h][n] fp32; T and dT are [h][nb] fp32;
+ *     spd is int8 [n][ld_spd] (row i holds the bucket codes of pairs (i, *)).
+ *   - `dtype` selects the element type of q, k, v, o, dO, dq, dk, dv:
+ *     GT_F32 (exact fp32 arithmetic) or GT_BF16 (bf16 storage, tensor-core
+ *     products with fp32 accumulation, fp32 softmax statistics).
+ *   - All calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream).  They check their arguments on the host before any
+ *     launch and return a negative gt_status without launching if a check
+ *     fails.  GT_OK means the work was enqueued.
+ *   - Bucket codes are read as unsigned bytes; codes >= nb select a zero bias
+ *     in the forward and are dropped from dT (they never occur in the output of
+ *     gt_spd_build).
+ */
+#ifndef GT_ATTN_H
+#define GT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GT_OK = 0,
+    GT_ERR_INVALID_ARG = -1,  /* NULL, size, alignment or layout check failed */
+    GT_ERR_UNSUPPORTED = -2,  /* shape valid but not handled by this build */
+    GT_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+    GT_ERR_TIMEOUT = -4,      /* a kernel gave up a bounded wait (see below) */
+    GT_ERR_WORKSPACE = -5     /* workspace NULL or smaller than the size query */
+} gt_status;
+
+typedef enum { GT_F32 = 0, GT_BF16 = 1 } gt_dtype;
+
+/* Largest clip distance: codes 0..D+1 must fit a signed byte. */
+#define GT_MAX_D 126
+
+/*
+ * Bytes of device workspace gt_spd_build needs for this graph size on the
+ * current device.
+ */
+size_t gt_spd_workspace_size(int32_t n, int64_t nnz, int32_t D);
+
+/*
+ * gt_spd_build: clipped shortest-path bucket matrix of an undirected graph
+ * (the topology the bias of the MegaGraph abstract is built from).
+ *   indptr  device int64[n+1], indices device int32[nnz]: CSR adjacency with
+ *           both directions of every edge stored (self-loops and repeated
+ *           entries are harmless).
+ *   n >= 1, 1 <= D <= GT_MAX_D.
+ *   spd     device int8 [n][ld_spd], written for columns 0..n-1 of every row:
+ *           spd[i][j] = min(dist(i,j), D) if j is reachable from i, D+1 if not,
+ *           0 on the diagonal.  ld_spd >= n and ld_spd % 16 == 0; spd 16-byte
+ *           aligned.  Columns n..ld_spd-1 are not written.
+ *   workspace/ws_bytes: device scratch of at least gt_spd_workspace_size().
+ * Errors: GT_ERR_INVALID_ARG for NULL pointers, n < 1, nnz < 0, D out of range,
+ * bad ld_spd or alignment; GT_ERR_WORKSPACE for a short workspace.
+ */
+int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t nnz,
+                 int32_t D, int8_t* spd, int64_t ld_spd,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of device workspace needed by gt_bias_attn_fwd (with this kv_block)
+ * and by gt_bias_attn_bwd for these sizes; one buffer of this size serves both.
+ */
+size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d,
+                                   int32_t kv_block);
+
+/*
+ * gt_bias_attn_fwd: o = softmax(scale * q k^T + T[h][spd]) v per head, plus lse.
+ *   q, k, v  device [n][h][d] of `dtype`, 16-byte aligned.
+ *   spd      device int8 [n][ld_spd] bucket codes (ld_spd >= n, % 16 == 0,
+ *            16-byte aligned).
+ *   T        device fp32 [h][nb], nb <= 128.
+ *   scale    multiplies q.k before the bias is added (1/sqrt(d) is usual).
+ *   kv_block 0: every Q tile streams all n KV columns in one pass.
+ *            > 0 (a multiple of 128): the columns are cut into blocks of
+ *            kv_block (the KV blocks of Fig. 4); each block yields a partial
+ *            (o, lse) and the partials are merged exactly through their lse.
+ *   o        device [n][h][d] of `dtype` (output); lse device fp32 [h][n].
+ *   workspace/ws_bytes: at least gt_bias_attn_workspace_size(...).
+ * Supported: n >= 1, 1 <= h <= 16, 1 <= d <= 64.  GT_BF16 with h = 8 and
+ * d in {8, 16} runs on the tensor cores; other shapes run on a CUDA-core kernel.
+ */
+int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
+                     const void* q, const void* k, const void* v,
+                     const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                     float scale, int32_t kv_block,
+                     void* o, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gt_bias_attn_bwd: gradients of sum(o * dO) with respect to q, k, v and T.
+ *   o, lse   the forward's outputs for the same inputs.
+ *   dO       device [n][h][d] of `dtype`, the upstream gradient.
+ *   dq, dk, dv device [n][h][d] of `dtype` (outputs, overwritten).
+ *   dT       device fp32 [h][nb] (output, overwritten).
+ * Other arguments and the supported shapes are as for gt_bias_attn_fwd.
+ */
+int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
+                     const void* q, const void* k, const void* v, const void* o,
+                     const void* dO, const float* lse,
+                     const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                     float scale, void* dq, void* dk, void* dv, float* dT,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Static English text for a gt_status value. */
+const char* gt_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports GT_ERR_TIMEOUT if any kernel of this
+ * library gave up a bounded wait since the last check (kernels never spin
+ * without a limit; on giving up they record it in a device status word and
+ * return), GT_ERR_CUDA if the stream reports an error, else GT_OK.  The status
+ * word is cleared by the call.
+ */
+int gt_check_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GT_ATTN_H */

@@ -1,0 +1,98 @@
+"""The C ABI of libgt on the host (no GPU needed, no kernel launched).
+
+Checks that the library builds and loads, that it exports every function that
+include/gt_attn.h declares, and that argument checks reject bad calls with the
+documented status codes before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gt_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from graph_transformer_attention_gb300 import build
+    build.build()
+    import graph_transformer_attention_gb300 as gt
+    return gt.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gt_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("gt_spd_build", "gt_bias_attn_fwd", "gt_bias_attn_bwd"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libgt.so does not export {name}"
+
+
+def test_status_strings(lib):
+    import graph_transformer_attention_gb300 as gt
+    for code in (0, -1, -2, -3, -4, -5):
+        s = gt.gt_status_string(code)
+        assert s and s != "unknown status"
+    assert gt.gt_status_string(42) == "unknown status"
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)      # never dereferenced: every call below fails its host checks
+    # gt_spd_build: NULL indptr, bad n, bad D, bad ld, misaligned output
+    assert lib.gt_spd_build(None, fake, 4, 2, 2, fake, 16, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 0, 2, 2, fake, 16, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 4, 2, 0, fake, 16, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 4, 2, 127, fake, 16, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 4, 2, 3, fake, 8, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 20, 2, 3, fake, 24, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build(fake, fake, 4, 2, 3, P(0x1001), 16, fake, 1 << 20, None) == -1
+    # forward: bad dtype, NULL q, misaligned q, bad ld, nb too large, bad kv_block
+    args = lambda **kw: [kw.get("dt", 1), kw.get("n", 64), kw.get("h", 8), kw.get("d", 8),
+                         kw.get("q", fake), fake, fake, fake, kw.get("ld", 64), fake,
+                         kw.get("nb", 18), ctypes.c_float(0.35), kw.get("kvb", 0), fake, fake,
+                         fake, 1 << 30, None]
+    assert lib.gt_bias_attn_fwd(*args(dt=7)) == -1
+    assert lib.gt_bias_attn_fwd(*args(q=None)) == -1
+    assert lib.gt_bias_attn_fwd(*args(q=P(0x1008))) == -1
+    assert lib.gt_bias_attn_fwd(*args(ld=63)) == -1
+    assert lib.gt_bias_attn_fwd(*args(ld=48)) == -1
+    assert lib.gt_bias_attn_fwd(*args(n=0)) == -1
+    assert lib.gt_bias_attn_fwd(*args(nb=129)) == -2
+    assert lib.gt_bias_attn_fwd(*args(d=65)) == -2
+    assert lib.gt_bias_attn_fwd(*args(kvb=100)) == -1
+    assert lib.gt_bias_attn_fwd(*args(kvb=-128)) == -1
+    # backward: NULL dT
+    bargs = [1, 64, 8, 8, fake, fake, fake, fake, fake, fake, fake, 64, fake, 18,
+             ctypes.c_float(0.35), fake, fake, fake, None, fake, 1 << 30, None]
+    assert lib.gt_bias_attn_bwd(*bargs) == -1
+    # workspace too small
+    bargs[18] = fake
+    bargs[20] = 0
+    assert lib.gt_bias_attn_bwd(*bargs) == -5
+
+
+def test_workspace_sizes(lib):
+    import graph_transformer_attention_gb300 as gt
+    a = gt.gt_bias_attn_workspace_size(1, 4096, 8, 8, 0)
+    b = gt.gt_bias_attn_workspace_size(1, 32768, 8, 8, 4096)
+    assert a > 0 and b > a
+    assert gt.gt_bias_attn_workspace_size(9, 4096, 8, 8, 0) == 0
+    assert gt.gt_spd_workspace_size(0, 0, 16) == 0
+    assert gt.gt_spd_workspace_size(512, 4000, 16) > 0
+
+
+def test_spd_ld():
+    import graph_transformer_attention_gb300 as gt
+    assert [gt.spd_ld(n) for n in (1, 16, 17, 6800)] == [16, 16, 32, 6800]

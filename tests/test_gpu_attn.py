@@ -1,0 +1,204 @@
+"""GPU parity of gt_bias_attn_fwd / gt_bias_attn_bwd against the fp64 CPU oracle.
+
+Tolerances: fp32 storage max-abs <= 1e-4; bf16 storage relative L2 <= 2e-2 per
+output tensor (o, lse, dq, dk, dv, dT).  The oracle runs on exactly the values
+the GPU sees (bf16-rounded inputs upcast to fp64).  Bucket matrices come from
+the oracle's own BFS or are drawn at random (not symmetric), never from the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gt_inputs as gi
+from oracle import oracle as O
+from tests.helpers import assert_close, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gt():
+    import graph_transformer_attention_gb300 as m
+    from graph_transformer_attention_gb300 import build
+    build.build()
+    m.load_library()
+    return m
+
+
+def _spd_dev(spd: np.ndarray) -> torch.Tensor:
+    n = spd.shape[0]
+    ld = (n + 15) // 16 * 16
+    buf = np.zeros((n, ld), np.int8)
+    buf[:, :n] = spd
+    return torch.from_numpy(buf).cuda()
+
+
+def _run_gpu(gt, x, spd, dtype, kv_block=0, scale=None):
+    q, k, v, dO = (to_dev(x[a], dtype) for a in ("q", "k", "v", "dO"))
+    T = torch.from_numpy(x["T"]).cuda()
+    sp = _spd_dev(spd)
+    o, lse = gt.gt_bias_attn_fwd(q, k, v, sp, T, scale=scale, kv_block=kv_block)
+    dq, dk, dv, dT = gt.gt_bias_attn_bwd(q, k, v, o, dO, lse, sp, T, scale=scale)
+    gt.gt_check_device_status()
+    return dict(o=host(o), lse=host(lse), dq=host(dq), dk=host(dk), dv=host(dv), dT=host(dT))
+
+
+def _compare_full(got, ref, dtype, names=("o", "lse", "dq", "dk", "dv", "dT")):
+    return {nm: assert_close(nm, got[nm], ref[nm], dtype) for nm in names}
+
+
+SMALL = [
+    # n, h, d, dtype, nb, kv_block, graph-or-random
+    (1, 8, 8, "f32", 18, 0, "random"),
+    (2, 8, 8, "bf16", 18, 0, "random"),
+    (37, 8, 8, "f32", 18, 0, "graph"),
+    (130, 8, 8, "bf16", 18, 0, "random"),
+    (300, 8, 16, "bf16", 26, 0, "graph"),
+    (513, 8, 8, "bf16", 34, 128, "graph"),
+    (257, 4, 32, "f32", 7, 0, "random"),
+    (200, 2, 64, "f32", 5, 0, "random"),
+    (1000, 8, 8, "bf16", 22, 256, "random"),
+    (640, 8, 16, "bf16", 26, 0, "graph"),
+    (129, 4, 16, "bf16", 9, 0, "random"),
+]
+
+
+@pytest.mark.parametrize("n,h,d,dtype,nb,kv_block,kind", SMALL)
+def test_small_parity(gt, n, h, d, dtype, nb, kv_block, kind):
+    seed = 10 * n + d
+    x = gi.make_layer_tensors(n, h, d, nb, dtype, seed=seed)
+    if kind == "graph":
+        g = gi.barabasi_albert(n, 2, seed=seed) if n > 3 else gi.erdos_renyi(n, 0.5, seed)
+        spd = O.spd(n, g.indptr, g.indices, nb - 2)
+    else:
+        spd = np.random.default_rng(seed).integers(0, nb, size=(n, n)).astype(np.int8)
+    got = _run_gpu(gt, x, spd, dtype, kv_block=kv_block)
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, dtype)
+
+
+def test_large_bias_values(gt):
+    """Bias up to +-30 makes the running max jump between KV blocks."""
+    n, h, d, nb = 700, 8, 8, 18
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=3)
+    x["T"] = (np.random.default_rng(4).uniform(-30, 30, size=(h, nb))).astype(np.float32)
+    spd = np.random.default_rng(5).integers(0, nb, size=(n, n)).astype(np.int8)
+    got = _run_gpu(gt, x, spd, "bf16")
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, "bf16")
+
+
+def test_growing_scores(gt):
+    """Scores that keep growing along the row force repeated rescales of the output."""
+    n, h, d, nb = 600, 8, 16, 26
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=13)
+    # s_ij ~ (q_i + 1).(k_j + r_j) / 4 rises by about 4 r_j along every row
+    ramp = np.linspace(0.0, 6.0, n, dtype=np.float32)[:, None, None]
+    x["q"] = gi.round_to_bf16(x["q"] + 1.0)
+    x["k"] = gi.round_to_bf16(x["k"] + ramp)
+    spd = np.random.default_rng(14).integers(0, nb, size=(n, n)).astype(np.int8)
+    got = _run_gpu(gt, x, spd, "bf16")
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_unreachable_and_single_bucket(gt, dtype):
+    n, h, d, D = 300, 8, 8, 16
+    x = gi.make_layer_tensors(n, h, d, D + 2, dtype, seed=21)
+    empty = gi.csr_from_edges(n, np.zeros(0, np.int64), np.zeros(0, np.int64))
+    spd = O.spd(n, empty.indptr, empty.indices, D)   # 0 on the diagonal, D+1 elsewhere
+    got = _run_gpu(gt, x, spd, dtype)
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, dtype)
+    assert np.all(got["dT"][:, 1:D + 1] == 0.0)
+    spd1 = np.full((n, n), 3, np.int8)                  # one bucket everywhere
+    got = _run_gpu(gt, x, spd1, dtype)
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd1, x["T"])
+    _compare_full(got, ref, dtype, names=("o", "lse", "dq", "dk", "dv"))
+    # One bucket holds every pair, so dT[h][3] = sum_ij dS_ij.  Exactly that is
+    # sum_i <dO_i, o_i - o_i'> where o' is the output the backward was given: zero
+    # for exact o, and the bf16 rounding residual of o otherwise.
+    do64 = x["dO"].astype(np.float64)
+    predicted = ((ref["o"] - got["o"]) * do64).sum(axis=(0, 2))       # [h]
+    assert np.all(np.abs(got["dT"][:, 3] - predicted) <= 1e-3 + 2e-2 * np.abs(predicted))
+    assert np.all(got["dT"][:, np.arange(D + 2) != 3] == 0.0)
+
+
+def test_kv_block_matches_single_pass(gt):
+    n, h, d, nb = 1100, 8, 8, 34
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=8)
+    spd = np.random.default_rng(9).integers(0, nb, size=(n, n)).astype(np.int8)
+    a = _run_gpu(gt, x, spd, "bf16", kv_block=0)
+    b = _run_gpu(gt, x, spd, "bf16", kv_block=256)
+    for nm in ("o", "lse"):
+        assert np.linalg.norm(a[nm] - b[nm]) <= 1e-2 * np.linalg.norm(a[nm])
+
+
+def _config_spd(w):
+    g = gi.config_graph(w)
+    return O.spd(g.n, g.indptr, g.indices, w.D)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_config_full_parity(gt, cfg):
+    w = gi.CONFIGS[cfg]
+    spd = _config_spd(w)
+    x = gi.config_layer_tensors(w)
+    got = _run_gpu(gt, x, spd, w.dtype, kv_block=w.kv_block)
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, w.dtype)
+
+
+def _sampled_check(gt, w, spd, layer, rng, full_cols: bool):
+    x = gi.config_layer_tensors(w, layer)
+    got = _run_gpu(gt, x, spd, w.dtype, kv_block=w.kv_block)
+    n = w.n
+    rows = np.sort(np.concatenate([rng.choice(n, 96, replace=False), [0, n - 1]]))
+    o_r, lse_r = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], rows=rows)
+    assert_close("o[rows]", got["o"][rows], o_r, w.dtype)
+    assert_close("lse[rows]", got["lse"][:, rows], lse_r, w.dtype)
+    # row-local backward: D_i needs only o_i, so dq of sampled rows needs no full pass
+    Dv_rows = (o_r * x["dO"][rows].astype(np.float64)).sum(-1).T      # [h][rows]
+    lse_full = np.zeros((w.heads, n)); Dv_full = np.zeros((w.heads, n))
+    lse_full[:, rows] = lse_r; Dv_full[:, rows] = Dv_rows
+    g = O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_full, Dv_full,
+                   rows=rows, want_dT=False, want_dkdv=False)
+    assert_close("dq[rows]", got["dq"][rows], g["dq"], w.dtype)
+    # properties at any size: every row of dS sums to 0, so sum_c dT[h][c] = 0;
+    # rows of P sum to 1, so sum_j dv_j = sum_i dO_i
+    # (with o rounded to bf16, sum_c dT[h][c] = sum_i <dO_i, o_i - o_i'> exactly, which
+    # is bounded by half an ulp of o' per element)
+    dT = got["dT"]
+    ulp = 2.0 ** -8 if w.dtype == "bf16" else 2.0 ** -22
+    bound = ulp * np.abs(x["dO"].astype(np.float64) * got["o"]).sum(axis=(0, 2)) + 1e-4
+    assert np.all(np.abs(dT.sum(1)) <= bound), (dT.sum(1), bound)
+    dsum = got["dv"].sum(0)
+    assert np.linalg.norm(dsum - x["dO"].astype(np.float64).sum(0)) <= 2e-2 * np.linalg.norm(dsum) + 1e-3
+    if full_cols:
+        o_all, lse_all = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"])
+        Dv_all = O.bwd_delta(o_all, x["dO"])
+        cols = np.sort(np.concatenate([rng.choice(n, 96, replace=False), [0, n - 1]]))
+        g = O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_all, Dv_all,
+                       cols=cols, want_dq=False, want_dT=True)
+        assert_close("dk[cols]", got["dk"][cols], g["dk"], w.dtype)
+        assert_close("dv[cols]", got["dv"][cols], g["dv"], w.dtype)
+        assert_close("dT", got["dT"], g["dT"], w.dtype)
+        assert_close("o", got["o"], o_all, w.dtype)
+
+
+@pytest.mark.slow
+def test_config3_sixteen_layers(gt):
+    w = gi.CONFIGS[3]
+    spd = _config_spd(w)
+    rng = np.random.default_rng(33)
+    for layer in range(w.layers):
+        _sampled_check(gt, w, spd, layer, rng, full_cols=layer in (0, w.layers - 1))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [4, 5])
+def test_config_large_sampled_and_full_dT(gt, cfg):
+    w = gi.CONFIGS[cfg]
+    spd = _config_spd(w)
+    _sampled_check(gt, w, spd, 0, np.random.default_rng(40 + cfg), full_cols=True)
