@@ -128,6 +128,36 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
                      float scale, void* dq, void* dk, void* dv, float* dT,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * gt_bias_attn_bwd_noalloc: gt_bias_attn_bwd for callers that cannot allocate.
+ * The paper has no counterpart; this is a library convenience.
+ *
+ * Some callers cannot call cudaMalloc or any allocator (a host framework that
+ * owns all device memory, a real-time or embedded host that forbids allocation
+ * after start-up, a plain C host with no caching allocator).  This variant takes
+ * no workspace: it runs the same backward pass with its scratch in an array of
+ * GT_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that loads
+ * the library holds until the process exits.  Inputs and outputs are passed and
+ * owned by the caller exactly as for gt_bias_attn_bwd, and the results match it.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current); make
+ *     that first call before any stream capture.  No call allocates or frees
+ *     device memory.
+ *   - Every call shares the one array and leaves its contents behind (the pass
+ *     clears what must start at zero).  Calls whose GPU work overlaps, on
+ *     different streams or host threads of one device, race on the array and
+ *     corrupt each other's results: serialise them.
+ *   - Returns GT_ERR_WORKSPACE, with nothing launched, when the problem needs
+ *     more scratch than GT_NOALLOC_SCRATCH_BYTES, i.e. when
+ *     gt_bias_attn_workspace_size(dtype, n, h, d, 0) exceeds it (about n*h <= 1M).
+ */
+#define GT_NOALLOC_SCRATCH_BYTES (4u << 20)
+int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
+                             const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse,
+                             const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                             float scale, void* dq, void* dk, void* dv, float* dT, void* stream);
+
 /* Static English text for a gt_status value. */
 const char* gt_status_string(int status);
 
