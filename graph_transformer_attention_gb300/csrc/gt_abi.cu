@@ -19,10 +19,19 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t 
 int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
                   void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s);
+bool fwd_tc_supported(int h, int d);
+int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
+                int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
+                float* o_part, float* lse_part, cudaStream_t s);
 int attn_bwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                   const void* o, const void* dO, const float* lse, const int8_t* spd, int64_t ld,
                   const float* T, int nb, float scale, void* dq, void* dk, void* dv, float* dT,
                   float* Dv, double* dT64, cudaStream_t s);
+bool bwd_tc_supported(int h, int d, int nb);
+int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
+                const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
+                int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
+                double* dT64, cudaStream_t s);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -62,6 +71,7 @@ struct FwdWs {
 struct BwdWs {
     float* Dv;
     double* dT64;
+    float* LD;
 };
 
 size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
@@ -82,6 +92,7 @@ size_t bwd_ws(int n, int h, int d, void* base, size_t cap, BwdWs* out) {
     BwdWs w;
     w.Dv = c.take<float>((size_t)h * n);
     w.dT64 = c.take<double>((size_t)h * 128);
+    w.LD = c.take<float>((size_t)n * 16);      // per-node (lse log2 e, D) rows, 8 heads
     if (out) *out = w;
     return c.off;
 }
@@ -140,6 +151,9 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     gt::FwdWs w;
     gt::fwd_ws(n, h, d, kv_block, workspace, ws_bytes, &w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GT_BF16 && gt::fwd_tc_supported(h, d))
+        return gt::attn_fwd_tc(n, d, q, k, v, spd, ld_spd, T, nb, scale, kv_block, o, lse, w.o_part,
+                               w.lse_part, s);
     return gt::attn_fwd_simt(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb, scale, kv_block, o, lse,
                              w.o_part, w.lse_part, s);
 }
@@ -160,6 +174,9 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     gt::BwdWs w;
     gt::bwd_ws(n, h, d, workspace, ws_bytes, &w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
+        return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
+                               w.LD, w.Dv, w.dT64, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

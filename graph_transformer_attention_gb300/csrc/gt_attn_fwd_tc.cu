@@ -1,0 +1,447 @@
+// gt_attn_fwd_tc.cu -- tensor-core forward of topology-biased graph attention
+// (bf16 storage, H = 8 heads, head dim 8 or 16) for sm_103a.
+//
+// Blockwise form of the MegaGraph paper's Fig. 4: KV blocks of 128 nodes stream
+// past a tile of 128 query rows; with each KV block comes the matching
+// 128 x 128 slice of the int8 bucket matrix, and the bias b = T[h][code] is formed
+// in registers from it.  Neither the scores nor the bias are ever stored.
+//
+// One CTA = one tile of 128 query rows, all 8 heads, 192 threads:
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Per chunk of
+//              16 KV columns it reads S for all 8 heads from TMEM, gathers the
+//              8 head biases of each (i, j) with two 16-byte shared loads (one
+//              bucket byte serves all heads), exponentiates in base 2, writes P
+//              (bf16) back over S in TMEM and keeps the row sums.
+//   warp 4     MMA issuer: S_h = Q_h K_h^T (M=128, N=16, K=16) into TMEM, then
+//              O_h += P_h V_h (A = P from TMEM, M=128, N=16, K=16).
+//   warp 5     TMA producer: the bucket tile (128x128 int8, 128B swizzle) and the
+//              K and V column slots (128 x 16 bf16, 32B swizzle) of each KV block,
+//              double-buffered.
+// TMEM (512 columns): O_h at columns 16h; three S/P stages of 8 heads x 16
+// columns each from column 128.  Head dim 8 uses the 16-column MMAs with the
+// neighbouring head's channels riding along: Q is zero-padded per head so the
+// extra K products vanish, and the extra output columns of O are ignored.
+//
+// Softmax statistics: the running maximum m is raised lazily.  P = 2^(x - m)
+// is formed against the current m and a chunk is redone against a new maximum
+// only when its row sum exceeds 2^8 (or is not finite); O is then rescaled in
+// TMEM.  The first chunk sets m exactly.
+//
+// Every mbarrier wait is bounded; on timeout the CTA records GT_ERR_TIMEOUT in
+// the device status word, all roles leave their loops, wait (bounded) for their
+// own copies and MMAs in flight, free TMEM and return.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gt_common.cuh"
+#include "gt_sm100.cuh"
+#include "gt_tma.cuh"
+
+namespace gt {
+namespace {
+
+using namespace sm100;
+
+constexpr int kH = 8;
+constexpr int kBQ = 128;
+constexpr int kBKV = 128;
+constexpr int kCH = 16;
+constexpr int kNCH = kBKV / kCH;
+constexpr int kKVST = 2;
+constexpr int kSST = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRedoSum = 256.f;   // 2^8: redo a chunk whose row sum exceeds this
+
+template <int HD>
+struct Cfg {
+    static constexpr int NSLOT = kH * HD / 16;
+    static constexpr uint32_t Q_BYTES = kH * kBQ * 32;
+    static constexpr uint32_t SPD_BYTES = kBQ * kBKV;
+    static constexpr uint32_t SLOT_BYTES = kBKV * 32;
+    static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_STAGE = Q_BYTES;
+    static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
+    static constexpr uint32_t T_BYTES = 256 * kH * 4;
+    static constexpr uint32_t OFF_BAR = OFF_T + T_BYTES;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base
+};
+
+struct Bars {
+    uint64_t kv_full[kKVST];
+    uint64_t kv_empty[kKVST];
+    uint64_t s_full[kSST];
+    uint64_t p_ready[kSST];
+    uint64_t pv_done[kSST];
+    uint64_t fin;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ uint32_t s_col(int stage) { return 128u + 128u * stage; }
+
+__device__ __forceinline__ void fail(Bars* bars, int* status) {
+    *(volatile int*)&bars->abort = 1;
+    atomicOr(status, kStatusTimeout);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+              const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
+              const float* __restrict__ T, int nb, int n, float scale_log2, int kv_block,
+              __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float* __restrict__ o_part,
+              float* __restrict__ lse_part, int* status) {
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+    float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = blockIdx.x * kBQ;
+    const int split = blockIdx.y;
+    const int j_begin = kv_block > 0 ? split * kv_block : 0;
+    const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
+    const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
+    const int nchunks = nblocks * kNCH;
+
+    if (tid == kThreads - 32) {
+        for (int s = 0; s < kKVST; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], kBQ + 1);
+        }
+        for (int s = 0; s < kSST; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->p_ready[s], kBQ);
+            mbar_init(&bars->pv_done[s], 1);
+        }
+        mbar_init(&bars->fin, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&mapK);
+        tma_prefetch_desc(&mapV);
+        tma_prefetch_desc(&mapS);
+    }
+    if (warp == 4) tmem_alloc(&bars->tmem_base, kTmemCols);
+    // bias table in base-2 units, one 32-byte row of 8 heads per bucket code
+    for (int x = tid; x < 256 * kH; x += kThreads) {
+        const int code = x / kH, h = x % kH;
+        Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
+    }
+    // per-head Q operands: [128 rows][16] bf16, 32-byte swizzle, K-major
+    if (warp < 4) {
+        const int row = i0 + tid;
+        const uint4* src = reinterpret_cast<const uint4*>(q + (int64_t)(row < n ? row : 0) * kH * HD);
+        const uint32_t sw = (uint32_t)((tid >> 2) & 1);
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            uint4 lo, hi;
+            if (HD == 8) {
+                const uint4 v = row < n ? src[h] : zero;
+                lo = (h & 1) ? zero : v;
+                hi = (h & 1) ? v : zero;
+            } else {
+                lo = row < n ? src[2 * h] : zero;
+                hi = row < n ? src[2 * h + 1] : zero;
+            }
+            uint8_t* dst = smem + C::OFF_Q + h * 4096 + tid * 32;
+            *reinterpret_cast<uint4*>(dst + ((0u ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dst + ((1u ^ sw) << 4)) = hi;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort;
+
+    if (warp == 5) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int b = 0; b < nblocks; ++b) {
+                const int ks = b & 1;
+                if (b >= kKVST &&
+                    !mbar_wait(&bars->kv_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    fail(bars, status);
+                    break;
+                }
+                uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
+                const int j0 = j_begin + b * kBKV;
+                mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
+                tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
+#pragma unroll
+                for (int s = 0; s < C::NSLOT; ++s) {
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * s, j0,
+                                &bars->kv_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV, 16 * s,
+                                j0, &bars->kv_full[ks]);
+                }
+                issued = b + 1;
+            }
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA goes away
+                int never = 0;
+                for (int b = issued - kKVST; b < issued; ++b)
+                    if (b >= 0) mbar_wait(&bars->kv_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
+            }
+        }
+    } else if (warp == 4) {
+        // ----------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idQK = idesc_bf16(128, 16, false, false);
+            const uint32_t idPV = idesc_bf16(128, 16, false, true);
+            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+            const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
+            bool ok = true;
+            auto issue_qk = [&](int tt) -> bool {
+                const int b = tt / kNCH, c = tt % kNCH, ks = b & 1, ss = tt % kSST;
+                if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                if (tt >= kSST &&
+                    !mbar_wait(&bars->pv_done[ss], ((tt / kSST) - 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                tc_fence_after();
+                const uint32_t kbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + c * 512;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    const int slot = h * HD / 16;
+                    const uint64_t da = smem_desc(q_base + h * 4096, 16, 256, 6);
+                    const uint64_t db = smem_desc(kbase + slot * C::SLOT_BYTES, 16, 256, 6);
+                    mma_ss(tbase + s_col(ss) + 16 * h, da, db, idQK, 0);
+                }
+                mma_commit(&bars->s_full[ss]);
+                return true;
+            };
+            ok = issue_qk(0);
+            if (ok && nchunks > 1) ok = issue_qk(1);
+            for (int tt = 0; ok && tt < nchunks; ++tt) {
+                const int ss = tt % kSST, b = tt / kNCH, c = tt % kNCH, ks = b & 1;
+                if (!mbar_wait(&bars->p_ready[ss], (tt / kSST) & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES +
+                                       C::NSLOT * C::SLOT_BYTES + c * 512;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    const int slot = h * HD / 16;
+                    const uint64_t db = smem_desc(vbase + slot * C::SLOT_BYTES, 256, 256, 6);
+                    mma_ts(tbase + 16 * h, tbase + s_col(ss) + 16 * h, db, idPV, tt > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->pv_done[ss]);
+                if (c == kNCH - 1) mma_commit(&bars->kv_empty[ks]);
+                if (tt + 2 < nchunks && !issue_qk(tt + 2)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) {
+                fail(bars, status);
+                int never = 0;
+                mma_commit(&bars->fin);
+                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int r = tid;                       // row within the tile = TMEM lane
+        const uint32_t lrow = tbase + ((uint32_t)(warp * 32) << 16);
+        const float4* T4 = reinterpret_cast<const float4*>(Ts);
+        float m[kH], l[kH];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+        int t = 0;
+        bool ok = true;
+        for (int b = 0; ok && b < nblocks; ++b) {
+            const int ks = b & 1;
+            if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            const uint8_t* sp = smem + C::OFF_STAGE + ks * C::STAGE_BYTES + r * 128;
+            const int j0 = j_begin + b * kBKV;
+            for (int c = 0; c < kNCH; ++c, ++t) {
+                const int ss = t % kSST;
+                if (!mbar_wait(&bars->s_full[ss], (t / kSST) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint4 codes = *reinterpret_cast<const uint4*>(sp + ((c ^ (r & 7)) << 4));
+                const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+                uint32_t raw[kH][16];
+#pragma unroll
+                for (int h = 0; h < kH; ++h) tmem_ld_x16(lrow + s_col(ss) + 16 * h, raw[h]);
+                tmem_wait_ld();
+                float x[kH][16];
+                const int jc = j0 + c * kCH;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t code = (cw[k >> 2] >> (8 * (k & 3))) & 0xffu;
+                    const float4 b0 = T4[code * 2], b1 = T4[code * 2 + 1];
+                    const float bias[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    const bool valid = jc + k < j_end;
+#pragma unroll
+                    for (int h = 0; h < kH; ++h)
+                        x[h][k] = valid ? fmaf(__uint_as_float(raw[h][k]), scale_log2, bias[h]) : -INFINITY;
+                }
+                if (t == 0) {
+#pragma unroll
+                    for (int h = 0; h < kH; ++h) {
+                        float mx = x[h][0];
+#pragma unroll
+                        for (int k = 1; k < 16; ++k) mx = fmaxf(mx, x[h][k]);
+                        m[h] = mx;
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    float p[16], ls = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) { p[k] = ex2(x[h][k] - m[h]); ls += p[k]; }
+                    const bool redo = !(ls <= kRedoSum);
+                    if (__any_sync(0xffffffffu, redo)) {
+                        // new maximum for this head: redo the chunk, rescale l and O
+                        float mx = m[h];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[h][k]);
+                        const float alpha = ex2(m[h] - mx);
+                        m[h] = mx;
+                        l[h] *= alpha;
+                        ls = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) { p[k] = ex2(x[h][k] - mx); ls += p[k]; }
+                        if (t > 0) {
+                            const int tp = t - 1;
+                            if (!mbar_wait(&bars->pv_done[tp % kSST], (tp / kSST) & 1, abort_flag, kWaitNs))
+                                ok = false;
+                            tc_fence_after();
+                            uint32_t ov[16];
+                            tmem_ld_x16(lrow + 16 * h, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                            tmem_st_x16(lrow + 16 * h, ov);
+                            tmem_wait_st();
+                        }
+                    }
+                    l[h] += ls;
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(p[2 * k], p[2 * k + 1]);
+                    tmem_st_x8(lrow + s_col(ss) + 16 * h, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_ready[ss]);
+                if (!ok) break;
+            }
+            if (!ok) break;
+            mbar_arrive(&bars->kv_empty[ks]);
+        }
+        if (!ok) {
+            fail(bars, status);
+        } else {
+            // ---------------------------------------------------- epilogue
+            const int tp = nchunks - 1;
+            if (!mbar_wait(&bars->pv_done[tp % kSST], (tp / kSST) & 1, abort_flag, kWaitNs)) {
+                fail(bars, status);
+            } else {
+                tc_fence_after();
+                const int row = i0 + r;
+                const bool live = row < n;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    uint32_t ov[16];
+                    tmem_ld_x16(lrow + 16 * h, ov);
+                    tmem_wait_ld();
+                    const float inv = 1.f / l[h];
+                    const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
+                    if (live) {
+                        if (gridDim.y == 1) {
+                            uint32_t w[HD / 2];
+#pragma unroll
+                            for (int k = 0; k < HD / 2; ++k)
+                                w[k] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * k]) * inv,
+                                                   __uint_as_float(ov[c0 + 2 * k + 1]) * inv);
+                            uint4* dst = reinterpret_cast<uint4*>(o + ((int64_t)row * kH + h) * HD);
+#pragma unroll
+                            for (int k = 0; k < HD / 8; ++k)
+                                dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                            lse[(int64_t)h * n + row] = (m[h] + log2f(l[h])) * kLn2;
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(
+                                o_part + (((int64_t)split * n + row) * kH + h) * HD);
+#pragma unroll
+                            for (int k = 0; k < HD / 4; ++k)
+                                dst[k] = make_float4(__uint_as_float(ov[c0 + 4 * k]) * inv,
+                                                     __uint_as_float(ov[c0 + 4 * k + 1]) * inv,
+                                                     __uint_as_float(ov[c0 + 4 * k + 2]) * inv,
+                                                     __uint_as_float(ov[c0 + 4 * k + 3]) * inv);
+                            lse_part[((int64_t)split * kH + h) * n + row] = (m[h] + log2f(l[h])) * kLn2;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+template <int HD>
+int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8_t* spd, int64_t ld,
+                  const float* T, int nb, float scale, int kv_block, void* o, float* lse,
+                  float* o_part, float* lse_part, cudaStream_t s) {
+    using C = Cfg<HD>;
+    CUtensorMap mk, mv, ms;
+    const uint64_t cols = (uint64_t)kH * HD;
+    if (!make_map_2d(&mk, const_cast<void*>(k), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     kBKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&mv, const_cast<void*>(v), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     kBKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, kBQ,
+                     kBKV, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GT_ERR_CUDA;
+    if (cudaFuncSetAttribute(fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess)
+        return GT_ERR_CUDA;
+    int* status = device_status_ptr();
+    if (!status) return GT_ERR_CUDA;
+    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    dim3 grid((n + kBQ - 1) / kBQ, nsplit);
+    fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
+        mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e,
+        nsplit > 1 ? kv_block : 0, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, status);
+    return check_launch();
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int h, int d) { return h == kH && (d == 8 || d == 16); }
+
+int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
+                   const float* lse_part, void* o, float* lse, cudaStream_t s);
+
+int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
+                int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
+                float* o_part, float* lse_part, cudaStream_t s) {
+    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    int rc = d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part,
+                                       lse_part, s)
+                    : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part,
+                                        lse_part, s);
+    if (rc != GT_OK || nsplit == 1) return rc;
+    return merge_partials(GT_BF16, n, kH, d, nsplit, o_part, lse_part, o, lse, s);
+}
+
+}  // namespace gt

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <type_traits>
 
 #include "gt_common.cuh"
 
@@ -371,6 +372,35 @@ int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_pa
     else
         merge_splits<__nv_bfloat16><<<grid_for((int64_t)n * h), 256, 0, s>>>(
             n, h, d, nsplit, o_part, lse_part, (__nv_bfloat16*)o, lse);
+    return check_launch();
+}
+
+// The column pass alone (dk, dv), given D [h][n].
+int attn_bwd_cols_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                       const void* dO, const float* lse, const float* Dv, const int8_t* spd,
+                       int64_t ld, const float* T, int nb, float scale, void* dk, void* dv,
+                       cudaStream_t s) {
+    dim3 grid((n + kRows - 1) / kRows, h);
+    auto go = [&](auto tag, auto dp) {
+        using TE = decltype(tag);
+        constexpr int DP = decltype(dp)::value;
+        bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k,
+                                                     (const TE*)v, (const TE*)dO, lse, Dv,
+                                                     (const uint8_t*)spd, ld, T, nb, scale,
+                                                     (TE*)dk, (TE*)dv);
+    };
+    using I8 = std::integral_constant<int, 8>;
+    using I16 = std::integral_constant<int, 16>;
+    using I32 = std::integral_constant<int, 32>;
+    using I64 = std::integral_constant<int, 64>;
+    if (dtype == GT_F32) {
+        if (d <= 8) go(float(), I8()); else if (d <= 16) go(float(), I16());
+        else if (d <= 32) go(float(), I32()); else go(float(), I64());
+    } else {
+        const __nv_bfloat16 z{};
+        if (d <= 8) go(z, I8()); else if (d <= 16) go(z, I16());
+        else if (d <= 32) go(z, I32()); else go(z, I64());
+    }
     return check_launch();
 }
 

@@ -149,7 +149,8 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
  *     corrupt each other's results: serialise them.
  *   - Returns GT_ERR_WORKSPACE, with nothing launched, when the problem needs
  *     more scratch than GT_NOALLOC_SCRATCH_BYTES, i.e. when
- *     gt_bias_attn_workspace_size(dtype, n, h, d, 0) exceeds it (about n*h <= 1M).
+ *     gt_bias_attn_workspace_size(dtype, n, h, d, 0) exceeds it (with H = 8 the
+ *     limit is N of about 43,000 nodes).
  */
 #define GT_NOALLOC_SCRATCH_BYTES (4u << 20)
 int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
