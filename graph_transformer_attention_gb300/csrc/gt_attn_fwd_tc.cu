@@ -6,21 +6,25 @@
 // 128 x 128 slice of the int8 bucket matrix, and the bias b = T[h][code] is formed
 // in registers from it.  Neither the scores nor the bias are ever stored.
 //
-// One CTA = one tile of 128 query rows, all 8 heads, 192 threads:
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Per chunk of
-//              16 KV columns it reads S for all 8 heads from TMEM, gathers the
-//              8 head biases of each (i, j) with two 16-byte shared loads (one
-//              bucket byte serves all heads), exponentiates in base 2, writes P
-//              (bf16) back over S in TMEM and keeps the row sums.
-//   warp 4     MMA issuer: S_h = Q_h K_h^T (M=128, N=16, K=16) into TMEM, then
-//              O_h += P_h V_h (A = P from TMEM, M=128, N=16, K=16).
-//   warp 5     TMA producer: the bucket tile (128x128 int8, 128B swizzle) and the
+// One CTA = one tile of 128 query rows, all 8 heads, 320 threads:
+//   warps 0-3  softmax group 0 (heads 0-3), warps 4-7 softmax group 1 (heads
+//              4-7): thread r of a group owns query row r (TMEM lane r).  Per
+//              chunk of 32 KV columns it reads S of its 4 heads from TMEM, gathers
+//              the 4 head biases of each (i, j) with one 16-byte shared load per
+//              bucket byte, exponentiates in base 2, writes P (bf16) to TMEM and
+//              keeps the row sums.  Two warps per SM sub-partition hide latency.
+//   warp 8     MMA issuer: S_h = Q_h K_h^T (M=128, N=32, K=16) into TMEM, then
+//              O_h += P_h V_h (A = P from TMEM, M=128, N=16, two K=16 steps).
+//   warp 9     TMA producer: the bucket tile (128x128 int8, 128B swizzle) and the
 //              K and V column slots (128 x 16 bf16, 32B swizzle) of each KV block,
 //              double-buffered.
-// TMEM (512 columns): O_h at columns 16h; three S/P stages of 8 heads x 16
-// columns each from column 128.  Head dim 8 uses the 16-column MMAs with the
-// neighbouring head's channels riding along: Q is zero-padded per head so the
-// extra K products vanish, and the extra output columns of O are ignored.
+// TMEM (512 columns): O_h at 16h (128 columns), S for 8 heads x 32 columns at
+// 128 (256 columns), P (bf16) for 8 heads x 32 columns at 384 (128 columns).
+// S is read into registers at the start of a chunk, so the next chunk's QK^T
+// starts while this chunk is still being exponentiated.  Head dim 8 uses the
+// 16-wide MMAs with the neighbouring head's channels riding along: Q is
+// zero-padded per head so the extra K products vanish, and the extra output
+// columns of O are ignored.
 //
 // Softmax statistics: the running maximum m is raised lazily.  P = 2^(x - m)
 // is formed against the current m and a chunk is redone against a new maximum
@@ -47,16 +51,21 @@ using namespace sm100;
 constexpr int kH = 8;
 constexpr int kBQ = 128;
 constexpr int kBKV = 128;
-constexpr int kCH = 16;
+constexpr int kCH = 32;                 // KV columns per MMA chunk
 constexpr int kNCH = kBKV / kCH;
 constexpr int kKVST = 2;
-constexpr int kSST = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 192;
+constexpr int kSoftThreads = 256;       // two groups of 128
+constexpr int kThreads = kSoftThreads + 64;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRedoSum = 256.f;   // 2^8: redo a chunk whose row sum exceeds this
+constexpr float kRedoSum = 256.f;       // 2^8: redo a half chunk whose row sum exceeds this
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS = 128;
+constexpr uint32_t kColP = 384;
 
 template <int HD>
 struct Cfg {
@@ -76,19 +85,62 @@ struct Cfg {
 struct Bars {
     uint64_t kv_full[kKVST];
     uint64_t kv_empty[kKVST];
-    uint64_t s_full[kSST];
-    uint64_t p_ready[kSST];
-    uint64_t pv_done[kSST];
+    uint64_t s_full;
+    uint64_t s_free;
+    uint64_t p_ready;
+    uint64_t pv_done;
     uint64_t fin;
     uint32_t tmem_base;
     int abort;
 };
 
-__device__ __forceinline__ uint32_t s_col(int stage) { return 128u + 128u * stage; }
-
 __device__ __forceinline__ void fail(Bars* bars, int* status) {
     *(volatile int*)&bars->abort = 1;
     atomicOr(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// x = s * scale * log2(e) + T[h][code] * log2(e) for 4 heads and the 16 columns of
+// half g of a chunk, in place over the raw S bits; one 16-byte load per code
+// gives the four head biases (tbl: shared address of this head group's half of
+// the first 32-byte table row).
+__device__ __forceinline__ void score16(uint32_t (&sx)[4][16], const uint4 cw, uint32_t tbl,
+                                        float scale_log2) {
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t code = __byte_perm(w[k >> 2], 0u, 0x4440u + (k & 3));
+        const float4 bv = lds_f4(tbl + code * 32u);
+        sx[0][k] = __float_as_uint(fmaf(__uint_as_float(sx[0][k]), scale_log2, bv.x));
+        sx[1][k] = __float_as_uint(fmaf(__uint_as_float(sx[1][k]), scale_log2, bv.y));
+        sx[2][k] = __float_as_uint(fmaf(__uint_as_float(sx[2][k]), scale_log2, bv.z));
+        sx[3][k] = __float_as_uint(fmaf(__uint_as_float(sx[3][k]), scale_log2, bv.w));
+    }
+}
+
+// Columns at or beyond j_end (the tail of the last KV block) get x = -inf.
+__device__ __forceinline__ void mask16(uint32_t (&sx)[4][16], int j, int j_end) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (j + k >= j_end) {
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) sx[hh][k] = __float_as_uint(-INFINITY);
+        }
+}
+
+// p_k = 2^(x_k - m) for one head's 16 columns, packed to bf16 pairs; returns sum p.
+__device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, uint32_t (&pk)[8]) {
+    float2 acc = f2(0.f, 0.f);
+    const float2 mm = f2(-m, -m);
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        const float2 d = __fadd2_rn(f2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), mm);
+        const float2 p = f2(ex2(d.x), ex2(d.y));
+        acc = __fadd2_rn(acc, p);
+        pk[k / 2] = pack_bf16x2(p.x, p.y);
+    }
+    return acc.x + acc.y;
 }
 
 template <int HD>
@@ -112,16 +164,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
     const int nchunks = nblocks * kNCH;
 
-    if (tid == kThreads - 32) {
+    if (tid == kTmaWarp * 32) {
         for (int s = 0; s < kKVST; ++s) {
             mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], kBQ + 1);
+            mbar_init(&bars->kv_empty[s], kSoftThreads + 1);
         }
-        for (int s = 0; s < kSST; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->p_ready[s], kBQ);
-            mbar_init(&bars->pv_done[s], 1);
-        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_free, kSoftThreads);
+        mbar_init(&bars->p_ready, kSoftThreads);
+        mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->fin, 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -129,14 +180,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         tma_prefetch_desc(&mapV);
         tma_prefetch_desc(&mapS);
     }
-    if (warp == 4) tmem_alloc(&bars->tmem_base, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
     // bias table in base-2 units, one 32-byte row of 8 heads per bucket code
     for (int x = tid; x < 256 * kH; x += kThreads) {
         const int code = x / kH, h = x % kH;
         Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
     }
     // per-head Q operands: [128 rows][16] bf16, 32-byte swizzle, K-major
-    if (warp < 4) {
+    if (tid < kBQ) {
         const int row = i0 + tid;
         const uint4* src = reinterpret_cast<const uint4*>(q + (int64_t)(row < n ? row : 0) * kH * HD);
         const uint32_t sw = (uint32_t)((tid >> 2) & 1);
@@ -164,7 +215,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const uint32_t tbase = bars->tmem_base;
     volatile int* abort_flag = &bars->abort;
 
-    if (warp == 5) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int issued = 0;
@@ -195,56 +246,51 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (b >= 0) mbar_wait(&bars->kv_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
-            const uint32_t idQK = idesc_bf16(128, 16, false, false);
+            const uint32_t idQK = idesc_bf16(128, kCH, false, false);
             const uint32_t idPV = idesc_bf16(128, 16, false, true);
             const uint32_t q_base = smem_u32(smem + C::OFF_Q);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
             bool ok = true;
+            // chunk tt covers KV rows 32c .. 32c+31 of block b: 1024 bytes into a slot
             auto issue_qk = [&](int tt) -> bool {
-                const int b = tt / kNCH, c = tt % kNCH, ks = b & 1, ss = tt % kSST;
+                const int b = tt / kNCH, c = tt % kNCH, ks = b & 1;
                 if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
                     return false;
-                if (tt >= kSST &&
-                    !mbar_wait(&bars->pv_done[ss], ((tt / kSST) - 1) & 1, abort_flag, kWaitNs))
+                if (tt > 0 && !mbar_wait(&bars->s_free, (tt - 1) & 1, abort_flag, kWaitNs))
                     return false;
                 tc_fence_after();
-                const uint32_t kbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + c * 512;
+                const uint32_t kbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + c * 1024;
 #pragma unroll
                 for (int h = 0; h < kH; ++h) {
                     const int slot = h * HD / 16;
-                    const uint64_t da = smem_desc(q_base + h * 4096, 16, 256, 6);
-                    const uint64_t db = smem_desc(kbase + slot * C::SLOT_BYTES, 16, 256, 6);
-                    mma_ss(tbase + s_col(ss) + 16 * h, da, db, idQK, 0);
+                    mma_ss(tbase + kColS + kCH * h, smem_desc(q_base + h * 4096, 16, 256, 6),
+                           smem_desc(kbase + slot * C::SLOT_BYTES, 16, 256, 6), idQK, 0);
                 }
-                mma_commit(&bars->s_full[ss]);
+                mma_commit(&bars->s_full);
                 return true;
             };
             ok = issue_qk(0);
-            if (ok && nchunks > 1) ok = issue_qk(1);
             for (int tt = 0; ok && tt < nchunks; ++tt) {
-                const int ss = tt % kSST, b = tt / kNCH, c = tt % kNCH, ks = b & 1;
-                if (!mbar_wait(&bars->p_ready[ss], (tt / kSST) & 1, abort_flag, kWaitNs)) {
-                    ok = false;
-                    break;
-                }
+                const int b = tt / kNCH, c = tt % kNCH, ks = b & 1;
+                if (tt + 1 < nchunks && !issue_qk(tt + 1)) { ok = false; break; }
+                if (!mbar_wait(&bars->p_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t vbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES +
-                                       C::NSLOT * C::SLOT_BYTES + c * 512;
+                                       C::NSLOT * C::SLOT_BYTES + c * 1024;
 #pragma unroll
                 for (int h = 0; h < kH; ++h) {
                     const int slot = h * HD / 16;
-                    const uint64_t db = smem_desc(vbase + slot * C::SLOT_BYTES, 256, 256, 6);
-                    mma_ts(tbase + 16 * h, tbase + s_col(ss) + 16 * h, db, idPV, tt > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int st = 0; st < 2; ++st)
+                        mma_ts(tbase + kColO + 16 * h, tbase + kColP + 16 * h + 8 * st,
+                               smem_desc(vbase + slot * C::SLOT_BYTES + 512 * st, 256, 256, 6), idPV,
+                               (tt > 0 || st > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars->pv_done[ss]);
+                mma_commit(&bars->pv_done);
                 if (c == kNCH - 1) mma_commit(&bars->kv_empty[ks]);
-                if (tt + 2 < nchunks && !issue_qk(tt + 2)) {
-                    ok = false;
-                    break;
-                }
             }
             if (!ok) {
                 fail(bars, status);
@@ -255,90 +301,102 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------- softmax
-        const int r = tid;                       // row within the tile = TMEM lane
-        const uint32_t lrow = tbase + ((uint32_t)(warp * 32) << 16);
-        const float4* T4 = reinterpret_cast<const float4*>(Ts);
-        float m[kH], l[kH];
+        const int grp = warp >> 2;               // head group: heads 4*grp .. 4*grp+3
+        const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
+        const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t tbl = smem_u32(Ts) + 16u * grp;   // 32-byte rows of 8 head biases
+        float m[4], l[4];
 #pragma unroll
-        for (int h = 0; h < kH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+        for (int h = 0; h < 4; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
         int t = 0;
         bool ok = true;
         for (int b = 0; ok && b < nblocks; ++b) {
             const int ks = b & 1;
             if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            const uint8_t* sp = smem + C::OFF_STAGE + ks * C::STAGE_BYTES + r * 128;
+            const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * 128;
             const int j0 = j_begin + b * kBKV;
+            const bool tail_block = j0 + kBKV > j_end;
             for (int c = 0; c < kNCH; ++c, ++t) {
-                const int ss = t % kSST;
-                if (!mbar_wait(&bars->s_full[ss], (t / kSST) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-                const uint4 codes = *reinterpret_cast<const uint4*>(sp + ((c ^ (r & 7)) << 4));
-                const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-                uint32_t raw[kH][16];
-#pragma unroll
-                for (int h = 0; h < kH; ++h) tmem_ld_x16(lrow + s_col(ss) + 16 * h, raw[h]);
-                tmem_wait_ld();
-                float x[kH][16];
+                // codes of the 32 columns: two 16-byte chunks of the swizzled row
+                const uint4 c0 = lds_u4(sp + ((uint32_t)((2 * c) ^ (r & 7)) << 4));
+                const uint4 c1 = lds_u4(sp + ((uint32_t)((2 * c + 1) ^ (r & 7)) << 4));
                 const int jc = j0 + c * kCH;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint32_t code = (cw[k >> 2] >> (8 * (k & 3))) & 0xffu;
-                    const float4 b0 = T4[code * 2], b1 = T4[code * 2 + 1];
-                    const float bias[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                    const bool valid = jc + k < j_end;
-#pragma unroll
-                    for (int h = 0; h < kH; ++h)
-                        x[h][k] = valid ? fmaf(__uint_as_float(raw[h][k]), scale_log2, bias[h]) : -INFINITY;
-                }
                 if (t == 0) {
+                    // the first chunk sets the running maximum exactly (both halves)
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) {
-                        float mx = x[h][0];
+                    for (int g = 0; g < 2; ++g) {
+                        uint32_t sx[4][16];
 #pragma unroll
-                        for (int k = 1; k < 16; ++k) mx = fmaxf(mx, x[h][k]);
-                        m[h] = mx;
+                        for (int hh = 0; hh < 4; ++hh)
+                            tmem_ld_x16(lrow + kColS + kCH * (4 * grp + hh) + 16 * g, sx[hh]);
+                        tmem_wait_ld();
+                        score16(sx, g ? c1 : c0, tbl, scale_log2);
+                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
                     }
                 }
+                // P must not be overwritten before the previous chunk's PV has read it
+                if (t > 0 && !mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+                tc_fence_after();
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t sx[4][16];
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    float p[16], ls = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) { p[k] = ex2(x[h][k] - m[h]); ls += p[k]; }
-                    const bool redo = !(ls <= kRedoSum);
-                    if (__any_sync(0xffffffffu, redo)) {
-                        // new maximum for this head: redo the chunk, rescale l and O
-                        float mx = m[h];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[h][k]);
-                        const float alpha = ex2(m[h] - mx);
-                        m[h] = mx;
-                        l[h] *= alpha;
-                        ls = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) { p[k] = ex2(x[h][k] - mx); ls += p[k]; }
-                        if (t > 0) {
-                            const int tp = t - 1;
-                            if (!mbar_wait(&bars->pv_done[tp % kSST], (tp / kSST) & 1, abort_flag, kWaitNs))
-                                ok = false;
-                            tc_fence_after();
-                            uint32_t ov[16];
-                            tmem_ld_x16(lrow + 16 * h, ov);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                            tmem_st_x16(lrow + 16 * h, ov);
-                            tmem_wait_st();
-                        }
+                    for (int hh = 0; hh < 4; ++hh)
+                        tmem_ld_x16(lrow + kColS + kCH * (4 * grp + hh) + 16 * g, sx[hh]);
+                    tmem_wait_ld();
+                    if (g == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->s_free);      // S is consumed: the next QK^T may start
                     }
-                    l[h] += ls;
-                    uint32_t pk[8];
+                    score16(sx, g ? c1 : c0, tbl, scale_log2);
+                    if (tail_block) mask16(sx, jc + 16 * g, j_end);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(p[2 * k], p[2 * k + 1]);
-                    tmem_st_x8(lrow + s_col(ss) + 16 * h, pk);
+                    for (int hh = 0; hh < 4; ++hh) {
+                        const int h = 4 * grp + hh;
+                        uint32_t pk[8];
+                        float ls = exp_pack16(sx[hh], m[hh], pk);
+                        if (__any_sync(0xffffffffu, !(ls <= kRedoSum))) {
+                            // a new maximum for this head: redo, and rescale l, the P already
+                            // written for this chunk, and O
+                            float mx = m[hh];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) mx = fmaxf(mx, __uint_as_float(sx[hh][k]));
+                            const float alpha = ex2(m[hh] - mx);
+                            m[hh] = mx;
+                            l[hh] *= alpha;
+                            ls = exp_pack16(sx[hh], mx, pk);
+                            if (g == 1) {
+                                uint32_t pw[8];
+                                tmem_ld_x8(lrow + kColP + 16 * h, pw);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 8; ++k)
+                                    pw[k] = pack_bf16x2(__uint_as_float(pw[k] << 16) * alpha,
+                                                        __uint_as_float(pw[k] & 0xffff0000u) * alpha);
+                                tmem_st_x8(lrow + kColP + 16 * h, pw);
+                            }
+                            if (t > 0) {
+                                uint32_t ov[16];
+                                tmem_ld_x16(lrow + kColO + 16 * h, ov);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                                tmem_st_x16(lrow + kColO + 16 * h, ov);
+                            }
+                        }
+                        l[hh] += ls;
+                        tmem_st_x8(lrow + kColP + 16 * h + 8 * g, pk);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars->p_ready[ss]);
+                mbar_arrive(&bars->p_ready);
                 if (!ok) break;
             }
             if (!ok) break;
@@ -348,19 +406,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             fail(bars, status);
         } else {
             // ---------------------------------------------------- epilogue
-            const int tp = nchunks - 1;
-            if (!mbar_wait(&bars->pv_done[tp % kSST], (tp / kSST) & 1, abort_flag, kWaitNs)) {
+            if (!mbar_wait(&bars->pv_done, (nchunks - 1) & 1, abort_flag, kWaitNs)) {
                 fail(bars, status);
             } else {
                 tc_fence_after();
                 const int row = i0 + r;
                 const bool live = row < n;
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
+                for (int hh = 0; hh < 4; ++hh) {
+                    const int h = 4 * grp + hh;
                     uint32_t ov[16];
-                    tmem_ld_x16(lrow + 16 * h, ov);
+                    tmem_ld_x16(lrow + kColO + 16 * h, ov);
                     tmem_wait_ld();
-                    const float inv = 1.f / l[h];
+                    const float inv = 1.f / l[hh];
                     const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
                     if (live) {
                         if (gridDim.y == 1) {
@@ -373,7 +431,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
                             for (int k = 0; k < HD / 8; ++k)
                                 dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                            lse[(int64_t)h * n + row] = (m[h] + log2f(l[h])) * kLn2;
+                            lse[(int64_t)h * n + row] = (m[hh] + log2f(l[hh])) * kLn2;
                         } else {
                             float4* dst = reinterpret_cast<float4*>(
                                 o_part + (((int64_t)split * n + row) * kH + h) * HD);
@@ -383,7 +441,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                                                      __uint_as_float(ov[c0 + 4 * k + 1]) * inv,
                                                      __uint_as_float(ov[c0 + 4 * k + 2]) * inv,
                                                      __uint_as_float(ov[c0 + 4 * k + 3]) * inv);
-                            lse_part[((int64_t)split * kH + h) * n + row] = (m[h] + log2f(l[h])) * kLn2;
+                            lse_part[((int64_t)split * kH + h) * n + row] = (m[hh] + log2f(l[hh])) * kLn2;
                         }
                     }
                 }
@@ -392,11 +450,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
     }
 }
+
+}  // namespace
+}  // namespace gt
+
+namespace gt {
+namespace {
 
 template <int HD>
 int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8_t* spd, int64_t ld,
