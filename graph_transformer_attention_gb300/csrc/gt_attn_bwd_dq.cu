@@ -1,0 +1,453 @@
+// gt_attn_bwd_dq.cu -- tensor-core backward, Q-stationary part: dq and the
+// bias-table gradient dT (bf16 storage, H = 8 heads, head dim 8 or 16).
+//
+// The backward recomputes P = exp(S - lse) blockwise, KV block by KV block with
+// the matching bias slice of the int8 bucket matrix (MegaGraph, Fig. 4), and
+//   dS = P (dO V^T - D),  dq = scale dS K,  dT[h][c] = sum over spd = c of dS.
+//
+// One CTA = one tile of 128 query rows, all 8 heads, 320 threads:
+//   warps 0-3 / 4-7  two groups of four heads; thread r of a group owns query
+//              row r (TMEM lane r), so lse and D are registers.  Per chunk of
+//              16 KV columns: S_h and dP_h from TMEM, one 16-byte shared load of
+//              the 4 head biases per bucket byte, P = 2^(x - lse log2 e),
+//              dS = P (dP - D), dS (bf16) back to TMEM over S, and dS summed per
+//              bucket: in registers while the row's 16 codes are equal, else with
+//              shared-memory reductions into bins [code][head][NCP copies]; lane l
+//              adds into copy l mod NCP, so with NCP = 32 the 32 rows of a warp never
+//              meet on one address or bank, whatever their codes.
+//   warp 8     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
+//              K=16), then dq_h += dS_h K_h (A = dS from TMEM).
+//   warp 9     TMA producer: bucket tile and K / V column slots per KV block.
+// TMEM: dq at columns 0..127 (16 per head), two S/dS stages at 128 and 256,
+// dP at 384.  All waits are bounded (timeout -> device status word, orderly
+// exit, TMEM freed).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gt_common.cuh"
+#include "gt_sm100.cuh"
+#include "gt_tc_common.cuh"
+#include "gt_tma.cuh"
+
+namespace gt {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kBQ = 128;
+constexpr int kCH = 16;
+constexpr int kKVST = 2;
+constexpr int kSoft = 256;
+constexpr int kThreads = kSoft + 64;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColDq = 0;
+constexpr uint32_t kColDp = 384;
+
+__device__ __forceinline__ uint32_t s_col(int stage) { return 128u + 128u * stage; }
+
+template <int HD>
+struct DqCfg {
+    static constexpr int BKV = HD == 8 ? 128 : 64;     // KV rows per TMA block
+    static constexpr int NCH = BKV / kCH;
+    static constexpr int NSLOT = kH * HD / 16;
+    static constexpr uint32_t OP_BYTES = kH * kBQ * 32;
+    static constexpr uint32_t SPD_BYTES = kBQ * BKV;
+    static constexpr uint32_t SLOT_BYTES = BKV * 32;
+    static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_G = OP_BYTES;
+    static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
+    static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
+    static constexpr uint32_t OFF_BIN = OFF_BAR + 256;
+    // bins: [nb][8 heads][ncp] fp32, sized at launch
+    static constexpr uint32_t smem_bytes(int nb, int ncp) { return OFF_BIN + (uint32_t)nb * kH * ncp * 4 + 1024; }
+};
+constexpr uint32_t kSmemLimit = 232448;
+
+struct Bars {
+    uint64_t kv_full[kKVST];
+    uint64_t kv_empty[kKVST];
+    uint64_t s_full[2];
+    uint64_t ds_ready[2];
+    uint64_t dq_done[2];
+    uint64_t dp_full;
+    uint64_t dp_free;
+    uint64_t fin;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int HD, int NCP>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+              const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
+              const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD,
+              const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
+              __nv_bfloat16* __restrict__ dq, double* __restrict__ dT64, int* status) {
+    using C = DqCfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+    float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
+    float* bins = reinterpret_cast<float*>(smem + C::OFF_BIN);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = blockIdx.x * kBQ;
+    const int nblocks = (n + C::BKV - 1) / C::BKV;
+    const int nchunks = nblocks * C::NCH;
+
+    if (tid == kTmaWarp * 32) {
+        for (int s = 0; s < kKVST; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], kSoft + 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->ds_ready[s], kSoft);
+            mbar_init(&bars->dq_done[s], 1);
+        }
+        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->dp_free, kSoft);
+        mbar_init(&bars->fin, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&mapK);
+        tma_prefetch_desc(&mapV);
+        tma_prefetch_desc(&mapS);
+    }
+    if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
+    fill_bias_table(Ts, T, nb, tid, kThreads);
+    for (int x = tid; x < nb * kH * NCP; x += kThreads) bins[x] = 0.f;
+    if (tid < kBQ) {
+        const int row = i0 + tid;
+        const bool live = row < n;
+        const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
+        write_head_operands<HD>(smem + C::OFF_Q, tid, q + off, live);
+        write_head_operands<HD>(smem + C::OFF_G, tid, dO + off, live);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    int* abort_flag = &bars->abort;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int b = 0; b < nblocks; ++b) {
+                const int ks = b & 1;
+                if (b >= kKVST &&
+                    !mbar_wait(&bars->kv_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    fail(abort_flag, status);
+                    break;
+                }
+                uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
+                const int j0 = b * C::BKV;
+                mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
+                tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
+#pragma unroll
+                for (int s = 0; s < C::NSLOT; ++s) {
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * s, j0,
+                                &bars->kv_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV, 16 * s,
+                                j0, &bars->kv_full[ks]);
+                }
+                issued = b + 1;
+            }
+            if (*(volatile int*)abort_flag) {
+                int never = 0;
+                for (int b = issued - kKVST; b < issued; ++b)
+                    if (b >= 0) mbar_wait(&bars->kv_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idKK = idesc_bf16(128, 16, false, false);
+            const uint32_t idKM = idesc_bf16(128, 16, false, true);
+            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+            const uint32_t g_base = smem_u32(smem + C::OFF_G);
+            const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
+            auto kslot = [&](int ks, int c, int h) -> uint32_t {
+                return stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512;
+            };
+            auto issue_s = [&](int tt) -> bool {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
+                if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                if (tt >= 2 && !mbar_wait(&bars->dq_done[ss], ((tt >> 1) - 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    mma_ss(tbase + s_col(ss) + 16 * h, smem_desc(q_base + h * 4096, 16, 256, 6),
+                           smem_desc(kslot(ks, c, h), 16, 256, 6), idKK, 0);
+                mma_commit(&bars->s_full[ss]);
+                return true;
+            };
+            auto issue_dp = [&](int tt) {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    mma_ss(tbase + kColDp + 16 * h, smem_desc(g_base + h * 4096, 16, 256, 6),
+                           smem_desc(kslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
+                mma_commit(&bars->dp_full);
+            };
+            bool ok = issue_s(0);
+            if (ok) issue_dp(0);
+            for (int tt = 0; ok && tt < nchunks; ++tt) {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
+                if (tt + 1 < nchunks) {
+                    if (!issue_s(tt + 1)) { ok = false; break; }
+                    if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_dp(tt + 1);
+                }
+                if (!mbar_wait(&bars->ds_ready[ss], (tt >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    mma_ts(tbase + kColDq + 16 * h, tbase + s_col(ss) + 16 * h,
+                           smem_desc(kslot(ks, c, h), 256, 256, 6), idKM, tt > 0 ? 1u : 0u);
+                mma_commit(&bars->dq_done[ss]);
+                if (c == C::NCH - 1) mma_commit(&bars->kv_empty[ks]);
+            }
+            if (!ok) {
+                fail(abort_flag, status);
+                int never = 0;
+                mma_commit(&bars->fin);
+                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int grp = warp >> 2;
+        const int r = tid & (kBQ - 1);
+        const int row = i0 + r;
+        const bool live = row < n;
+        const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t tbl = smem_u32(Ts) + 16u * grp;
+        // bin address: binb + code * kCodeStride + hh * kHeadStride
+        constexpr uint32_t kHeadStride = 4u * NCP, kCodeStride = kH * kHeadStride;
+        const uint32_t binb = smem_u32(bins) + 4u * (uint32_t)(lane & (NCP - 1)) + 4u * grp * kHeadStride;
+        float L2[4], Dh[4];
+        {
+            const float4* ld4 = reinterpret_cast<const float4*>(LD + (int64_t)(live ? row : 0) * 16);
+            const float4 a = ld4[grp], d = ld4[2 + grp];
+            L2[0] = a.x; L2[1] = a.y; L2[2] = a.z; L2[3] = a.w;
+            Dh[0] = d.x; Dh[1] = d.y; Dh[2] = d.z; Dh[3] = d.w;
+            if (!live) {
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) { L2[hh] = 0.f; Dh[hh] = 0.f; }
+            }
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        int acc_code = -1;
+        int t = 0;
+        bool ok = true;
+        for (int b = 0; ok && b < nblocks; ++b) {
+            const int ks = b & 1;
+            if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * C::BKV;
+            const int j0 = b * C::BKV;
+            const bool tail_block = j0 + C::BKV > n;
+            for (int c = 0; c < C::NCH; ++c, ++t) {
+                const int ss = t & 1;
+                if (!mbar_wait(&bars->s_full[ss], (t >> 1) & 1, abort_flag, kWaitNs) ||
+                    !mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t phys = C::BKV == 128 ? (uint32_t)(c ^ (r & 7)) : (uint32_t)(c ^ ((r >> 1) & 3));
+                const uint4 cv = lds_u4(sp + (phys << 4));
+                const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+                const uint32_t c0 = w[0] & 0xffu;
+                const bool uniform = w[0] == c0 * 0x01010101u && w[1] == w[0] && w[2] == w[0] && w[3] == w[0];
+                if (uniform && (int)c0 != acc_code) {
+                    if (acc_code >= 0 && acc_code < nb) {
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh)
+                            red_shared_add(binb + acc_code * kCodeStride + hh * kHeadStride, acc[hh]);
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) acc[hh] = 0.f;
+                    acc_code = (int)c0;
+                }
+                const int jc = j0 + c * kCH;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t rs[4][8], rd[4][8];
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        tmem_ld_x8(lrow + s_col(ss) + 16 * (4 * grp + hh) + 8 * g, rs[hh]);
+                        tmem_ld_x8(lrow + kColDp + 16 * (4 * grp + hh) + 8 * g, rd[hh]);
+                    }
+                    tmem_wait_ld();
+                    if (g == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->dp_free);
+                    }
+                    // x = s scale log2e + bias (scalar FMA), then packed: x - lse, exp, dS
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int kk = 8 * g + k;
+                        const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
+                        const float4 bv = lds_f4(tbl + code * 32u);
+                        rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
+                        rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
+                        rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
+                        rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                    }
+                    if (tail_block) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (jc + 8 * g + k >= n) {
+#pragma unroll
+                                for (int hh = 0; hh < 4; ++hh) rs[hh][k] = __float_as_uint(-INFINITY);
+                            }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        const float2 ml = make_float2(-L2[hh], -L2[hh]);
+                        const float2 md = make_float2(-Dh[hh], -Dh[hh]);
+                        float2 sum = make_float2(0.f, 0.f);
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2) {
+                            const float2 xv = __fadd2_rn(make_float2(__uint_as_float(rs[hh][k]),
+                                                                     __uint_as_float(rs[hh][k + 1])), ml);
+                            const float2 p = make_float2(ex2(xv.x), ex2(xv.y));
+                            const float2 dv = __fadd2_rn(make_float2(__uint_as_float(rd[hh][k]),
+                                                                     __uint_as_float(rd[hh][k + 1])), md);
+                            const float2 ds = __fmul2_rn(p, dv);
+                            rd[hh][k] = __float_as_uint(ds.x);
+                            rd[hh][k + 1] = __float_as_uint(ds.y);
+                            sum = __fadd2_rn(sum, ds);
+                            pk[k / 2] = pack_bf16x2(ds.x, ds.y);
+                        }
+                        if (uniform) acc[hh] += sum.x + sum.y;
+                        tmem_st_x4(lrow + s_col(ss) + 16 * (4 * grp + hh) + 4 * g, pk);
+                    }
+                    if (!uniform) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int kk = 8 * g + k;
+                            const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
+                            if (code < (uint32_t)nb) {
+#pragma unroll
+                                for (int hh = 0; hh < 4; ++hh)
+                                    red_shared_add(binb + code * kCodeStride + hh * kHeadStride,
+                                                   __uint_as_float(rd[hh][k]));
+                            }
+                        }
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->ds_ready[ss]);
+            }
+            if (!ok) break;
+            mbar_arrive(&bars->kv_empty[ks]);
+        }
+        if (acc_code >= 0 && acc_code < nb) {
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh)
+                red_shared_add(binb + acc_code * kCodeStride + hh * kHeadStride, acc[hh]);
+        }
+        if (!ok) {
+            fail(abort_flag, status);
+        } else {
+            const int tp = nchunks - 1;
+            if (!mbar_wait(&bars->dq_done[tp & 1], (tp >> 1) & 1, abort_flag, kWaitNs)) {
+                fail(abort_flag, status);
+            } else {
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    const int h = 4 * grp + hh;
+                    uint32_t ov[16];
+                    tmem_ld_x16(lrow + kColDq + 16 * h, ov);
+                    tmem_wait_ld();
+                    const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
+                    if (live) {
+                        uint32_t wq[HD / 2];
+#pragma unroll
+                        for (int k = 0; k < HD / 2; ++k)
+                            wq[k] = pack_bf16x2(__uint_as_float(ov[c0h + 2 * k]) * scale,
+                                                __uint_as_float(ov[c0h + 2 * k + 1]) * scale);
+                        uint4* dst = reinterpret_cast<uint4*>(dq + ((int64_t)row * kH + h) * HD);
+#pragma unroll
+                        for (int k = 0; k < HD / 8; ++k)
+                            dst[k] = make_uint4(wq[4 * k], wq[4 * k + 1], wq[4 * k + 2], wq[4 * k + 3]);
+                    }
+                }
+            }
+        }
+        // add the copies of each (code, head) bin to the global table
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory");
+        for (int x = tid; x < nb * kH; x += kSoft) {
+            const float* cp = bins + (int64_t)x * NCP;
+            float s = 0.f;
+#pragma unroll 8
+            for (int l = 0; l < NCP; ++l) s += cp[(l + tid) & (NCP - 1)];
+            const int code = x / kH, h = x % kH;
+            if (s != 0.f) atomicAdd(&dT64[h * nb + code], (double)s);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+template <int HD>
+int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
+           int64_t ld, const float* T, int nb, float scale, const float* LD, void* dq, double* dT64,
+           cudaStream_t s) {
+    using C = DqCfg<HD>;
+    CUtensorMap mk, mv, ms;
+    const uint64_t cols = (uint64_t)kH * HD;
+    if (!make_map_2d(&mk, const_cast<void*>(k), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     C::BKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&mv, const_cast<void*>(v), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     C::BKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, kBQ,
+                     C::BKV, C::BKV == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+        return GT_ERR_CUDA;
+    int* status = device_status_ptr();
+    if (!status) return GT_ERR_CUDA;
+    // 32 bin copies (conflict-free) while they fit, else 8 (nb up to 128 always fits)
+    const bool wide = C::smem_bytes(nb, 32) <= kSmemLimit;
+    auto kern = wide ? bwd_dq_kernel<HD, 32> : bwd_dq_kernel<HD, 8>;
+    const uint32_t smem = C::smem_bytes(nb, wide ? 32 : 8);
+    if (smem > kSmemLimit) return GT_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GT_ERR_CUDA;
+    dim3 grid((n + kBQ - 1) / kBQ);
+    kern<<<grid, kThreads, smem, s>>>(
+        mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
+        T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+    return check_launch();
+}
+
+}  // namespace
+
+int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
+                  const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                  const float* LD, void* dq, double* dT64, cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s);
+}
+
+}  // namespace gt

@@ -10,14 +10,9 @@
 // Kernels:
 //   bwd_prep    D_i per head, and the row table LD[i] = (lse_i log2 e, D_i) for
 //               all 8 heads (64 bytes per node).
-//   bwd_dq      Q-stationary, one CTA per 128 query rows, all heads.  Thread r owns
-//               query row r (TMEM lane r), so lse and D are registers.  Per chunk of
-//               16 KV columns: S_h = Q_h K_h^T and dP_h = dO_h V_h^T on the tensor
-//               cores (M=128, N=16, K=16), P and dS in registers, dS (bf16) back to
-//               TMEM, dq_h += dS_h K_h (A = dS from TMEM).  dT is summed per bucket:
-//               per thread in registers while a row's 16 codes are all equal, else
-//               with shared-memory atomics into per-warp bins.
-// The dk / dv pass follows in a second kernel.
+//   bwd_dq      (gt_attn_bwd_dq.cu) Q-stationary: dq and dT.
+//   bwd_dkdv    KV-stationary: dk and dv (below).
+//   dT_to_f32   the fp64 bucket sums to the fp32 output.
 //
 // All waits are bounded as in the forward kernel (timeout -> device status
 // word, orderly exit, TMEM freed).
@@ -28,21 +23,19 @@
 
 #include "gt_common.cuh"
 #include "gt_sm100.cuh"
+#include "gt_tc_common.cuh"
 #include "gt_tma.cuh"
 
 namespace gt {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
-constexpr int kH = 8;
-constexpr int kBQ = 128;
 constexpr int kCH = 16;
 constexpr int kKVST = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxNb = 128;
 
 // ------------------------------------------------------------------ prep
@@ -68,410 +61,6 @@ __global__ void bwd_prep(int n, int hd, const TE* __restrict__ o, const TE* __re
 __global__ void dT_to_f32(int count, const double* __restrict__ dT64, float* __restrict__ dT) {
     for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < count; x += gridDim.x * blockDim.x)
         dT[x] = (float)dT64[x];
-}
-
-// ----------------------------------------------------------- dq and dT
-
-template <int HD>
-struct DqCfg {
-    static constexpr int BKV = HD == 8 ? 128 : 64;     // KV rows per TMA block
-    static constexpr int NCH = BKV / kCH;
-    static constexpr int NSLOT = kH * HD / 16;
-    static constexpr uint32_t OP_BYTES = kH * kBQ * 32;  // 8 per-head [128][16] bf16 operands
-    static constexpr uint32_t SPD_BYTES = kBQ * BKV;
-    static constexpr uint32_t SLOT_BYTES = BKV * 32;
-    static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_G = OP_BYTES;
-    static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
-    static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
-    static constexpr uint32_t OFF_BIN = OFF_T + 256 * kH * 4;
-    static constexpr uint32_t OFF_BAR = OFF_BIN + 4 * kMaxNb * kH * 4;
-    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
-};
-
-struct DqBars {
-    uint64_t kv_full[kKVST];
-    uint64_t kv_empty[kKVST];
-    uint64_t s_full[2];
-    uint64_t ds_ready[2];
-    uint64_t dq_done[2];
-    uint64_t dp_full;
-    uint64_t dp_free;
-    uint64_t fin;
-    uint32_t tmem_base;
-    int abort;
-};
-
-constexpr uint32_t kColDq = 0;
-__device__ __forceinline__ uint32_t dq_s_col(int stage) { return 128u + 128u * stage; }
-constexpr uint32_t kColDp = 384;
-
-template <typename B>
-__device__ __forceinline__ void fail_bars(B* bars, int* status) {
-    *(volatile int*)&bars->abort = 1;
-    atomicOr(status, kStatusTimeout);
-}
-
-// Writes row r of the 8 per-head K-major [128][16] bf16 operands (32-byte swizzle)
-// from one node's [8][HD] row of x; head dim 8 is zero-padded to 16 per head.
-template <int HD>
-__device__ __forceinline__ void write_head_operands(uint8_t* base, int r, const __nv_bfloat16* src,
-                                                    bool live) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-    const uint32_t sw = (uint32_t)((r >> 2) & 1);
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int h = 0; h < kH; ++h) {
-        uint4 lo, hi;
-        if (HD == 8) {
-            const uint4 v = live ? s[h] : zero;
-            lo = (h & 1) ? zero : v;
-            hi = (h & 1) ? v : zero;
-        } else {
-            lo = live ? s[2 * h] : zero;
-            hi = live ? s[2 * h + 1] : zero;
-        }
-        uint8_t* dst = base + h * 4096 + r * 32;
-        *reinterpret_cast<uint4*>(dst + ((0u ^ sw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + ((1u ^ sw) << 4)) = hi;
-    }
-}
-
-template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
-bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-              const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
-              const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD,
-              const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
-              __nv_bfloat16* __restrict__ dq, double* __restrict__ dT64, int* status) {
-    using C = DqCfg<HD>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    DqBars* bars = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
-    float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
-    float* bins = reinterpret_cast<float*>(smem + C::OFF_BIN);   // [4 warps][kMaxNb][8]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i0 = blockIdx.x * kBQ;
-    const int nblocks = (n + C::BKV - 1) / C::BKV;
-    const int nchunks = nblocks * C::NCH;
-
-    if (tid == kThreads - 32) {
-        for (int s = 0; s < kKVST; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], kBQ + 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->ds_ready[s], kBQ);
-            mbar_init(&bars->dq_done[s], 1);
-        }
-        mbar_init(&bars->dp_full, 1);
-        mbar_init(&bars->dp_free, kBQ);
-        mbar_init(&bars->fin, 1);
-        bars->abort = 0;
-        fence_barrier_init();
-        tma_prefetch_desc(&mapK);
-        tma_prefetch_desc(&mapV);
-        tma_prefetch_desc(&mapS);
-    }
-    if (warp == 4) tmem_alloc(&bars->tmem_base, kTmemCols);
-    for (int x = tid; x < 256 * kH; x += kThreads) {
-        const int code = x / kH, h = x % kH;
-        Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
-    }
-    for (int x = tid; x < 4 * kMaxNb * kH; x += kThreads) bins[x] = 0.f;
-    if (warp < 4) {
-        const int row = i0 + tid;
-        const bool live = row < n;
-        const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
-        write_head_operands<HD>(smem + C::OFF_Q, tid, q + off, live);
-        write_head_operands<HD>(smem + C::OFF_G, tid, dO + off, live);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort;
-
-    if (warp == 5) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int b = 0; b < nblocks; ++b) {
-                const int ks = b & 1;
-                if (b >= kKVST &&
-                    !mbar_wait(&bars->kv_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
-                    fail_bars(bars, status);
-                    break;
-                }
-                uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                const int j0 = b * C::BKV;
-                mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
-                tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
-#pragma unroll
-                for (int s = 0; s < C::NSLOT; ++s) {
-                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * s, j0,
-                                &bars->kv_full[ks]);
-                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV, 16 * s,
-                                j0, &bars->kv_full[ks]);
-                }
-                issued = b + 1;
-            }
-            if (*abort_flag) {
-                int never = 0;
-                for (int b = issued - kKVST; b < issued; ++b)
-                    if (b >= 0) mbar_wait(&bars->kv_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
-            }
-        }
-    } else if (warp == 4) {
-        // ----------------------------------------------------------- MMA
-        if (lane == 0) {
-            const uint32_t idKK = idesc_bf16(128, 16, false, false);
-            const uint32_t idKM = idesc_bf16(128, 16, false, true);
-            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-            const uint32_t g_base = smem_u32(smem + C::OFF_G);
-            const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
-            auto kslot = [&](int ks, int c, int h) -> uint32_t {
-                return stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512;
-            };
-            auto vslot = [&](int ks, int c, int h) -> uint32_t {
-                return kslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES;
-            };
-            auto issue_s = [&](int tt) -> bool {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
-                if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
-                    return false;
-                if (tt >= 2 && !mbar_wait(&bars->dq_done[ss], ((tt >> 1) - 1) & 1, abort_flag, kWaitNs))
-                    return false;
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < kH; ++h)
-                    mma_ss(tbase + dq_s_col(ss) + 16 * h, smem_desc(q_base + h * 4096, 16, 256, 6),
-                           smem_desc(kslot(ks, c, h), 16, 256, 6), idKK, 0);
-                mma_commit(&bars->s_full[ss]);
-                return true;
-            };
-            auto issue_dp = [&](int tt) {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
-#pragma unroll
-                for (int h = 0; h < kH; ++h)
-                    mma_ss(tbase + kColDp + 16 * h, smem_desc(g_base + h * 4096, 16, 256, 6),
-                           smem_desc(vslot(ks, c, h), 16, 256, 6), idKK, 0);
-                mma_commit(&bars->dp_full);
-            };
-            bool ok = issue_s(0);
-            if (ok) issue_dp(0);
-            for (int tt = 0; ok && tt < nchunks; ++tt) {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
-                if (tt + 1 < nchunks) {
-                    if (!issue_s(tt + 1)) { ok = false; break; }
-                    if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_dp(tt + 1);
-                }
-                if (!mbar_wait(&bars->ds_ready[ss], (tt >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < kH; ++h)
-                    mma_ts(tbase + kColDq + 16 * h, tbase + dq_s_col(ss) + 16 * h,
-                           smem_desc(kslot(ks, c, h), 256, 256, 6), idKM, tt > 0 ? 1u : 0u);
-                mma_commit(&bars->dq_done[ss]);
-                if (c == C::NCH - 1) mma_commit(&bars->kv_empty[ks]);
-            }
-            if (!ok) {
-                fail_bars(bars, status);
-                int never = 0;
-                mma_commit(&bars->fin);
-                mbar_wait(&bars->fin, 0, &never, kWaitNs);
-            }
-        }
-    } else {
-        // ------------------------------------------------------- softmax
-        const int r = tid;
-        const int row = i0 + r;
-        const bool live = row < n;
-        const uint32_t lrow = tbase + ((uint32_t)(warp * 32) << 16);
-        const float4* T4 = reinterpret_cast<const float4*>(Ts);
-        float* mybins = bins + warp * kMaxNb * kH;
-        float L2[kH], Dh[kH];
-        {
-            const float4* ld4 = reinterpret_cast<const float4*>(LD + (int64_t)(live ? row : 0) * 16);
-            const float4 a = ld4[0], b2 = ld4[1], c2 = ld4[2], d2 = ld4[3];
-            const float t1[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
-            const float t2[8] = {c2.x, c2.y, c2.z, c2.w, d2.x, d2.y, d2.z, d2.w};
-#pragma unroll
-            for (int h = 0; h < kH; ++h) {
-                L2[h] = live ? t1[h] : 0.f;
-                Dh[h] = live ? t2[h] : 0.f;
-            }
-        }
-        float acc[kH];
-#pragma unroll
-        for (int h = 0; h < kH; ++h) acc[h] = 0.f;
-        int acc_code = -1;
-        int t = 0;
-        bool ok = true;
-        for (int b = 0; ok && b < nblocks; ++b) {
-            const int ks = b & 1;
-            if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            const uint8_t* sp = smem + C::OFF_STAGE + ks * C::STAGE_BYTES + r * C::BKV;
-            const int j0 = b * C::BKV;
-            for (int c = 0; c < C::NCH; ++c, ++t) {
-                const int ss = t & 1;
-                if (!mbar_wait(&bars->s_full[ss], (t >> 1) & 1, abort_flag, kWaitNs) ||
-                    !mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t phys = C::BKV == 128 ? (uint32_t)(c ^ (r & 7)) : (uint32_t)(c ^ ((r >> 1) & 3));
-                const uint4 codes = *reinterpret_cast<const uint4*>(sp + (phys << 4));
-                const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-                const uint32_t c0 = cw[0] & 0xffu;
-                const bool uniform = cw[0] == c0 * 0x01010101u && cw[1] == cw[0] && cw[2] == cw[0] &&
-                                     cw[3] == cw[0];
-                if (uniform && (int)c0 != acc_code) {
-                    if (acc_code >= 0 && acc_code < nb) {
-#pragma unroll
-                        for (int h = 0; h < kH; ++h) atomicAdd(&mybins[acc_code * kH + h], acc[h]);
-                    }
-#pragma unroll
-                    for (int h = 0; h < kH; ++h) acc[h] = 0.f;
-                    acc_code = (int)c0;
-                }
-                const int jc = j0 + c * kCH;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t rs[kH][8], rd[kH][8];
-#pragma unroll
-                    for (int h = 0; h < kH; ++h) {
-                        tmem_ld_x8(lrow + dq_s_col(ss) + 16 * h + 8 * g, rs[h]);
-                        tmem_ld_x8(lrow + kColDp + 16 * h + 8 * g, rd[h]);
-                    }
-                    tmem_wait_ld();
-                    if (g == 1) {
-                        tc_fence_before();
-                        mbar_arrive(&bars->dp_free);
-                    }
-                    float ds[kH][8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int kk = 8 * g + k;
-                        const uint32_t code = (cw[kk >> 2] >> (8 * (kk & 3))) & 0xffu;
-                        const float4 b0 = T4[code * 2], b1 = T4[code * 2 + 1];
-                        const float bias[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                        const bool valid = jc + kk < n;
-#pragma unroll
-                        for (int h = 0; h < kH; ++h) {
-                            const float x = fmaf(__uint_as_float(rs[h][k]), scale_log2, bias[h]) - L2[h];
-                            const float p = valid ? ex2(x) : 0.f;
-                            ds[h][k] = p * (__uint_as_float(rd[h][k]) - Dh[h]);
-                        }
-                        if (!uniform && code < (uint32_t)nb) {
-#pragma unroll
-                            for (int h = 0; h < kH; ++h) atomicAdd(&mybins[code * kH + h], ds[h][k]);
-                        }
-                    }
-                    if (uniform) {
-#pragma unroll
-                        for (int h = 0; h < kH; ++h) {
-                            float s8 = 0.f;
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) s8 += ds[h][k];
-                            acc[h] += s8;
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < kH; ++h) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) pk[k] = pack_bf16x2(ds[h][2 * k], ds[h][2 * k + 1]);
-                        tmem_st_x4(lrow + dq_s_col(ss) + 16 * h + 4 * g, pk);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars->ds_ready[ss]);
-            }
-            if (!ok) break;
-            mbar_arrive(&bars->kv_empty[ks]);
-        }
-        if (acc_code >= 0 && acc_code < nb) {
-#pragma unroll
-            for (int h = 0; h < kH; ++h) atomicAdd(&mybins[acc_code * kH + h], acc[h]);
-        }
-        if (!ok) {
-            fail_bars(bars, status);
-        } else {
-            const int tp = nchunks - 1;
-            if (!mbar_wait(&bars->dq_done[tp & 1], (tp >> 1) & 1, abort_flag, kWaitNs)) {
-                fail_bars(bars, status);
-            } else {
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    uint32_t ov[16];
-                    tmem_ld_x16(lrow + kColDq + 16 * h, ov);
-                    tmem_wait_ld();
-                    const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
-                    if (live) {
-                        uint32_t w[HD / 2];
-#pragma unroll
-                        for (int k = 0; k < HD / 2; ++k)
-                            w[k] = pack_bf16x2(__uint_as_float(ov[c0h + 2 * k]) * scale,
-                                               __uint_as_float(ov[c0h + 2 * k + 1]) * scale);
-                        uint4* dst = reinterpret_cast<uint4*>(dq + ((int64_t)row * kH + h) * HD);
-#pragma unroll
-                        for (int k = 0; k < HD / 8; ++k)
-                            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                    }
-                }
-            }
-        }
-        // sum the four warps' bins and add them to the global table
-        asm volatile("bar.sync 1, %0;" ::"n"(kBQ) : "memory");
-        for (int x = tid; x < nb * kH; x += kBQ) {
-            const float s = bins[x] + bins[kMaxNb * kH + x] + bins[2 * kMaxNb * kH + x] +
-                            bins[3 * kMaxNb * kH + x];
-            const int code = x / kH, h = x % kH;
-            if (s != 0.f) atomicAdd(&dT64[h * nb + code], (double)s);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 4) {
-        tc_fence_after();
-        tmem_dealloc(tbase, kTmemCols);
-    }
-}
-
-template <int HD>
-int launch_dq(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-              int64_t ld, const float* T, int nb, float scale, const float* LD, void* dq,
-              double* dT64, cudaStream_t s) {
-    using C = DqCfg<HD>;
-    CUtensorMap mk, mv, ms;
-    const uint64_t cols = (uint64_t)kH * HD;
-    if (!make_map_2d(&mk, const_cast<void*>(k), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
-                     C::BKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map_2d(&mv, const_cast<void*>(v), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
-                     C::BKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, kBQ,
-                     C::BKV, C::BKV == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-        return GT_ERR_CUDA;
-    if (cudaFuncSetAttribute(bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM) != cudaSuccess)
-        return GT_ERR_CUDA;
-    int* status = device_status_ptr();
-    if (!status) return GT_ERR_CUDA;
-    dim3 grid((n + kBQ - 1) / kBQ);
-    bwd_dq_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-        mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-        T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
-    return check_launch();
 }
 
 // ------------------------------------------------------------- dk and dv
@@ -590,7 +179,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const int ks = b & 1;
                 if (b >= kKVST &&
                     !mbar_wait(&bars->q_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
-                    fail_bars(bars, status);
+                    fail(&bars->abort, status);
                     break;
                 }
                 uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
@@ -671,7 +260,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (ok) {
                 mma_commit(&bars->done);
             } else {
-                fail_bars(bars, status);
+                fail(&bars->abort, status);
                 int never = 0;
                 mma_commit(&bars->fin);
                 mbar_wait(&bars->fin, 0, &never, kWaitNs);
@@ -761,9 +350,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mbar_arrive(&bars->q_empty[ks]);
         }
         if (!ok) {
-            fail_bars(bars, status);
+            fail(&bars->abort, status);
         } else if (!mbar_wait(&bars->done, 0, abort_flag, kWaitNs)) {
-            fail_bars(bars, status);
+            fail(&bars->abort, status);
         } else {
             tc_fence_after();
             const bool live = row < n;
@@ -835,6 +424,10 @@ int launch_dkdv(int n, const void* q, const void* k, const void* v, const void* 
 
 bool bwd_tc_supported(int h, int d, int nb) { return h == kH && (d == 8 || d == 16) && nb <= kMaxNb; }
 
+int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
+                  const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                  const float* LD, void* dq, double* dT64, cudaStream_t s);
+
 int attn_bwd_cols_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                        const void* dO, const float* lse, const float* Dv, const int8_t* spd,
                        int64_t ld, const float* T, int nb, float scale, void* dk, void* dv,
@@ -850,8 +443,7 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     const int pblocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     bwd_prep<__nv_bfloat16><<<pblocks, 256, 0, s>>>(n, d, static_cast<const __nv_bfloat16*>(o),
                                                     static_cast<const __nv_bfloat16*>(dO), lse, LD, Dv);
-    int rc = d == 8 ? launch_dq<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s)
-                    : launch_dq<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s);
+    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s);
     if (rc != GT_OK) return rc;
     rc = d == 8 ? launch_dkdv<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dk, dv, s)
                 : launch_dkdv<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dk, dv, s);

@@ -60,6 +60,10 @@ SMALL = [
     (1000, 8, 8, "bf16", 22, 256, "random"),
     (640, 8, 16, "bf16", 26, 0, "graph"),
     (129, 4, 16, "bf16", 9, 0, "random"),
+    # many buckets: the dT bins of the tensor-core backward shrink to fewer copies
+    (700, 8, 8, "bf16", 100, 0, "random"),
+    (520, 8, 16, "bf16", 60, 0, "random"),
+    (400, 8, 16, "bf16", 128, 0, "random"),
 ]
 
 
