@@ -23,7 +23,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgt.so")
 
 SOURCES = ["gt_abi.cu", "gt_spd.cu", "gt_attn_simt.cu", "gt_noalloc.cu", "gt_attn_fwd_tc.cu",
-           "gt_attn_bwd_tc.cu", "gt_attn_bwd_dq.cu"]
+           "gt_attn_bwd_tc.cu", "gt_attn_bwd_dq.cu",
+           "gt_attn_bwd_dkdv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -92,7 +92,8 @@ size_t bwd_ws(int n, int h, int d, void* base, size_t cap, BwdWs* out) {
     BwdWs w;
     w.Dv = c.take<float>((size_t)h * n);
     w.dT64 = c.take<double>((size_t)h * 128);
-    w.LD = c.take<float>((size_t)n * 16);      // per-node (lse log2 e, D) rows, 8 heads
+    // per-node lse log2 e (rows 0..7) and D (rows 8..15) of the 8 heads, [16][ld_ld]
+    w.LD = c.take<float>((size_t)16 * bwd_ld_ld(n));
     if (out) *out = w;
     return c.off;
 }

@@ -1,0 +1,426 @@
+// gt_attn_bwd_dkdv.cu -- tensor-core backward, KV-stationary part: dk and dv
+// (bf16 storage, H = 8 heads, head dim 8 or 16).
+//
+// With P and dS recomputed as in the Q-stationary pass (MegaGraph, Fig. 4: the
+// bias slice of each block comes from the int8 bucket matrix),
+//   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
+//
+// One CTA = one tile of 128 KV rows, all 8 heads, streaming every Q tile;
+// 320 threads:
+//   warps 0-3 / 4-7  two groups of four heads; thread r of a group owns KV row
+//              j0 + r (TMEM lane r).  Per chunk of 16 query rows i it reads S^T
+//              and dP^T of its heads from TMEM, the bucket code of (i, j) from
+//              column r of the int8 tile, lse_i log2 e and D_i from the staged LD
+//              rows (4 consecutive i per 16-byte load), forms
+//              P^T = 2^(s scale log2 e + b - lse_i log2 e) and dS^T = P^T (dP^T - D_i)
+//              and writes both (bf16) back over S^T.
+//   warp 8     MMA issuer: S^T_h = K_h Q_h^T and dP^T_h = V_h dO_h^T (M=128, N=16,
+//              K=16), then dv_h += P^T_h dO_h and dk_h += dS^T_h Q_h (A from TMEM).
+//   warp 9     TMA producer: per Q tile the bucket tile, the Q and dO column
+//              slots and the LD columns.
+// TMEM: dk at columns 0..127, dv at 128..255, and two 128-column regions whose
+// roles alternate: S^T(t) in X, dP^T(t) in Y; P^T/dS^T(t) go over S^T(t) in X;
+// S^T(t+1) goes into Y once every thread has read dP^T(t); dP^T(t+1) goes into X
+// after the dv/dk products of chunk t (the tensor pipe runs one thread's MMAs in
+// order).  All waits are bounded (timeout -> device status word, orderly exit,
+// TMEM freed).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gt_common.cuh"
+#include "gt_sm100.cuh"
+#include "gt_tc_common.cuh"
+#include "gt_tma.cuh"
+
+namespace gt {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kBKV = 128;
+constexpr int kCH = 16;
+constexpr int kQST = 2;
+constexpr int kSoft = 256;
+constexpr int kThreads = kSoft + 64;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColDk = 0;
+constexpr uint32_t kColDv = 128;
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    return __fadd2_rn(a, make_float2(-b.x, -b.y));
+}
+
+// X_t is region (t & 1), Y_t the other one
+__device__ __forceinline__ uint32_t region(int t, bool x) {
+    const int r = x ? (t & 1) : ((t & 1) ^ 1);
+    return 256u + 128u * r;
+}
+
+template <int HD>
+struct KvCfg {
+    static constexpr int BQ = HD == 8 ? 128 : 64;        // query rows per TMA tile
+    static constexpr int NCH = BQ / kCH;
+    static constexpr int NSLOT = kH * HD / 16;
+    static constexpr uint32_t OP_BYTES = kH * kBKV * 32;  // 8 per-head [128][16] bf16 operands
+    static constexpr uint32_t SPD_BYTES = BQ * kBKV;      // [BQ i][128 j], no swizzle
+    static constexpr uint32_t SLOT_BYTES = BQ * 32;
+    static constexpr uint32_t LD_BYTES = 16 * BQ * 4;     // [16][BQ] fp32
+    static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES + LD_BYTES;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OP_BYTES;
+    static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
+    static constexpr uint32_t OFF_T = OFF_STAGE + kQST * STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+};
+
+struct Bars {
+    uint64_t q_full[kQST];
+    uint64_t q_empty[kQST];
+    uint64_t s_full;
+    uint64_t dp_full;
+    uint64_t dp_free;
+    uint64_t ds_ready;
+    uint64_t done;
+    uint64_t fin;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
+                const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapL,
+                const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
+                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int* status) {
+    using C = KvCfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+    float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = blockIdx.x * kBKV;
+    const int ntiles = (n + C::BQ - 1) / C::BQ;
+    const int nchunks = ntiles * C::NCH;
+
+    if (tid == kTmaWarp * 32) {
+        for (int s = 0; s < kQST; ++s) {
+            mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->q_empty[s], kSoft + 1);
+        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->dp_free, kSoft);
+        mbar_init(&bars->ds_ready, kSoft);
+        mbar_init(&bars->done, 1);
+        mbar_init(&bars->fin, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&mapQ);
+        tma_prefetch_desc(&mapG);
+        tma_prefetch_desc(&mapS);
+        tma_prefetch_desc(&mapL);
+    }
+    if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
+    fill_bias_table(Ts, T, nb, tid, kThreads);
+    if (tid < kBKV) {
+        const int row = j0 + tid;
+        const bool live = row < n;
+        const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
+        write_head_operands<HD>(smem + C::OFF_K, tid, k + off, live);
+        write_head_operands<HD>(smem + C::OFF_V, tid, v + off, live);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bars->tmem_base;
+    int* abort_flag = &bars->abort;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int b = 0; b < ntiles; ++b) {
+                const int ks = b & 1;
+                if (b >= kQST &&
+                    !mbar_wait(&bars->q_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+                    fail(abort_flag, status);
+                    break;
+                }
+                uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
+                const int i0 = b * C::BQ;
+                mbar_arrive_expect_tx(&bars->q_full[ks], C::STAGE_BYTES);
+                tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
+#pragma unroll
+                for (int s = 0; s < C::NSLOT; ++s) {
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapQ, 16 * s, i0,
+                                &bars->q_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG, 16 * s,
+                                i0, &bars->q_full[ks]);
+                }
+                tma_load_2d(st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES, &mapL, i0, 0,
+                            &bars->q_full[ks]);
+                issued = b + 1;
+            }
+            if (*(volatile int*)abort_flag) {
+                int never = 0;
+                for (int b = issued - kQST; b < issued; ++b)
+                    if (b >= 0) mbar_wait(&bars->q_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idKK = idesc_bf16(128, 16, false, false);
+            const uint32_t idKM = idesc_bf16(128, 16, false, true);
+            const uint32_t k_base = smem_u32(smem + C::OFF_K);
+            const uint32_t v_base = smem_u32(smem + C::OFF_V);
+            const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
+            auto qslot = [&](int ks, int c, int h) -> uint32_t {
+                return stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512;
+            };
+            auto issue_s = [&](int tt) -> bool {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+                if (c == 0 && !mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    mma_ss(tbase + region(tt, true) + 16 * h, smem_desc(k_base + h * 4096, 16, 256, 6),
+                           smem_desc(qslot(ks, c, h), 16, 256, 6), idKK, 0);
+                mma_commit(&bars->s_full);
+                return true;
+            };
+            auto issue_dp = [&](int tt) {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+#pragma unroll
+                for (int h = 0; h < kH; ++h)
+                    mma_ss(tbase + region(tt, false) + 16 * h, smem_desc(v_base + h * 4096, 16, 256, 6),
+                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
+                mma_commit(&bars->dp_full);
+            };
+            bool ok = issue_s(0);
+            if (ok) issue_dp(0);
+            for (int tt = 0; ok && tt < nchunks; ++tt) {
+                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+                if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                if (tt + 1 < nchunks && !issue_s(tt + 1)) { ok = false; break; }
+                if (!mbar_wait(&bars->ds_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t x = region(tt, true);
+                const uint32_t acc = tt > 0 ? 1u : 0u;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    mma_ts(tbase + kColDv + 16 * h, tbase + x + 16 * h,
+                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 256, 256, 6), idKM, acc);
+                    mma_ts(tbase + kColDk + 16 * h, tbase + x + 16 * h + 8,
+                           smem_desc(qslot(ks, c, h), 256, 256, 6), idKM, acc);
+                }
+                if (c == C::NCH - 1) mma_commit(&bars->q_empty[ks]);
+                if (tt + 1 < nchunks) issue_dp(tt + 1);
+            }
+            if (ok) {
+                mma_commit(&bars->done);
+            } else {
+                fail(abort_flag, status);
+                int never = 0;
+                mma_commit(&bars->fin);
+                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int grp = warp >> 2;
+        const int r = tid & (kBKV - 1);
+        const int row = j0 + r;
+        const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t tbl = smem_u32(Ts) + 16u * grp;
+        int t = 0;
+        bool ok = true;
+        for (int b = 0; ok && b < ntiles; ++b) {
+            const int ks = b & 1;
+            if (!mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
+            // LD rows of this group's first head: row h is 4 BQ bytes long
+            const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (4 * grp) * C::BQ;
+            const int i0 = b * C::BQ;
+            const bool tail_tile = i0 + C::BQ > n;
+            for (int c = 0; c < C::NCH; ++c, ++t) {
+                if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t x = region(t, true), y = region(t, false);
+                // bucket codes of the 16 (i, j) pairs of this chunk: column r of the tile
+                uint32_t code[16];
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
+                // two passes of two heads over all 16 columns: a head's S^T columns are all
+                // read before its P^T / dS^T overwrite them
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps) {
+                    const int h0 = 4 * grp + 2 * ps;
+                    uint32_t rs[2][16], rd[2][16];
+                    tmem_ld_x16(lrow + x + 16 * h0, rs[0]);
+                    tmem_ld_x16(lrow + x + 16 * (h0 + 1), rs[1]);
+                    tmem_wait_ld();
+                    // x = s scale log2e + b(code) - lse_i log2e
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * ps);
+                        rs[0][kk] = __float_as_uint(fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x));
+                        rs[1][kk] = __float_as_uint(fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t la = ldb + 4u * (2 * ps + e) * C::BQ + 4u * (c * kCH);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const uint4 l = lds_u4(la + 16u * q4);
+                            const float2 xa = fsub2(make_float2(__uint_as_float(rs[e][4 * q4]),
+                                                                __uint_as_float(rs[e][4 * q4 + 1])),
+                                                    make_float2(__uint_as_float(l.x), __uint_as_float(l.y)));
+                            const float2 xb = fsub2(make_float2(__uint_as_float(rs[e][4 * q4 + 2]),
+                                                                __uint_as_float(rs[e][4 * q4 + 3])),
+                                                    make_float2(__uint_as_float(l.z), __uint_as_float(l.w)));
+                            rs[e][4 * q4] = __float_as_uint(ex2(xa.x));
+                            rs[e][4 * q4 + 1] = __float_as_uint(ex2(xa.y));
+                            rs[e][4 * q4 + 2] = __float_as_uint(ex2(xb.x));
+                            rs[e][4 * q4 + 3] = __float_as_uint(ex2(xb.y));
+                        }
+                    }
+                    if (tail_tile) {
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk)
+                            if (i0 + c * kCH + kk >= n) { rs[0][kk] = 0u; rs[1][kk] = 0u; }
+                    }
+                    if (ps == 0) {
+                        if (!mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) ok = false;
+                        tc_fence_after();
+                    }
+                    tmem_ld_x16(lrow + y + 16 * h0, rd[0]);
+                    tmem_ld_x16(lrow + y + 16 * (h0 + 1), rd[1]);
+                    tmem_wait_ld();
+                    if (ps == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->dp_free);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t la = ldb + 4u * (kH + 2 * ps + e) * C::BQ + 4u * (c * kCH);
+                        uint32_t pp[8], pd[8];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const uint4 dd = lds_u4(la + 16u * q4);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int kk = 4 * q4 + 2 * u;
+                                const float2 p = make_float2(__uint_as_float(rs[e][kk]), __uint_as_float(rs[e][kk + 1]));
+                                const float2 dvv = u == 0 ? make_float2(__uint_as_float(dd.x), __uint_as_float(dd.y))
+                                                          : make_float2(__uint_as_float(dd.z), __uint_as_float(dd.w));
+                                const float2 ds = __fmul2_rn(
+                                    p, fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
+                                pp[kk / 2] = pack_bf16x2(p.x, p.y);
+                                pd[kk / 2] = pack_bf16x2(ds.x, ds.y);
+                            }
+                        }
+                        tmem_st_x8(lrow + x + 16 * (h0 + e), pp);
+                        tmem_st_x8(lrow + x + 16 * (h0 + e) + 8, pd);
+                    }
+                }
+                tmem_wait_st();
+                if (!ok) break;
+                tc_fence_before();
+                mbar_arrive(&bars->ds_ready);
+            }
+            if (!ok) break;
+            mbar_arrive(&bars->q_empty[ks]);
+        }
+        if (!ok) {
+            fail(abort_flag, status);
+        } else if (!mbar_wait(&bars->done, 0, abort_flag, kWaitNs)) {
+            fail(abort_flag, status);
+        } else {
+            tc_fence_after();
+            const bool live = row < n;
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                const int h = 4 * grp + hh;
+                uint32_t ok16[16], ov16[16];
+                tmem_ld_x16(lrow + kColDk + 16 * h, ok16);
+                tmem_ld_x16(lrow + kColDv + 16 * h, ov16);
+                tmem_wait_ld();
+                const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
+                if (live) {
+                    uint32_t wk[HD / 2], wv[HD / 2];
+#pragma unroll
+                    for (int q2 = 0; q2 < HD / 2; ++q2) {
+                        wk[q2] = pack_bf16x2(__uint_as_float(ok16[c0h + 2 * q2]) * scale,
+                                             __uint_as_float(ok16[c0h + 2 * q2 + 1]) * scale);
+                        wv[q2] = pack_bf16x2(__uint_as_float(ov16[c0h + 2 * q2]),
+                                             __uint_as_float(ov16[c0h + 2 * q2 + 1]));
+                    }
+                    uint4* dstk = reinterpret_cast<uint4*>(dk + ((int64_t)row * kH + h) * HD);
+                    uint4* dstv = reinterpret_cast<uint4*>(dv + ((int64_t)row * kH + h) * HD);
+#pragma unroll
+                    for (int q2 = 0; q2 < HD / 8; ++q2) {
+                        dstk[q2] = make_uint4(wk[4 * q2], wk[4 * q2 + 1], wk[4 * q2 + 2], wk[4 * q2 + 3]);
+                        dstv[q2] = make_uint4(wv[4 * q2], wv[4 * q2 + 1], wv[4 * q2 + 2], wv[4 * q2 + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+template <int HD>
+int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
+           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, void* dk,
+           void* dv, cudaStream_t s) {
+    using C = KvCfg<HD>;
+    CUtensorMap mq, mg, ms, ml;
+    const uint64_t cols = (uint64_t)kH * HD;
+    if (!make_map_2d(&mq, const_cast<void*>(q), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     C::BQ, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&mg, const_cast<void*>(dO), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
+                     C::BQ, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, C::BQ,
+                     kBKV, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&ml, const_cast<float*>(LD), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 16, n,
+                     (uint64_t)ldl * 4, 16, C::BQ, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GT_ERR_CUDA;
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess)
+        return GT_ERR_CUDA;
+    int* status = device_status_ptr();
+    if (!status) return GT_ERR_CUDA;
+    dim3 grid((n + kBKV - 1) / kBKV);
+    bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
+        mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+        T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dk),
+        static_cast<__nv_bfloat16*>(dv), status);
+    return check_launch();
+}
+
+}  // namespace
+
+int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
+                    const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                    const float* LD, int ldl, void* dk, void* dv, cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s);
+}
+
+}  // namespace gt

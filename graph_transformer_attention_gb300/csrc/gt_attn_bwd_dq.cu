@@ -87,7 +87,7 @@ template <int HD, int NCP>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
-              const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD,
+              const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD, int ldl,
               const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
               __nv_bfloat16* __restrict__ dq, double* __restrict__ dT64, int* status) {
     using C = DqCfg<HD>;
@@ -239,15 +239,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         constexpr uint32_t kHeadStride = 4u * NCP, kCodeStride = kH * kHeadStride;
         const uint32_t binb = smem_u32(bins) + 4u * (uint32_t)(lane & (NCP - 1)) + 4u * grp * kHeadStride;
         float L2[4], Dh[4];
-        {
-            const float4* ld4 = reinterpret_cast<const float4*>(LD + (int64_t)(live ? row : 0) * 16);
-            const float4 a = ld4[grp], d = ld4[2 + grp];
-            L2[0] = a.x; L2[1] = a.y; L2[2] = a.z; L2[3] = a.w;
-            Dh[0] = d.x; Dh[1] = d.y; Dh[2] = d.z; Dh[3] = d.w;
-            if (!live) {
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) { L2[hh] = 0.f; Dh[hh] = 0.f; }
-            }
+        for (int hh = 0; hh < 4; ++hh) {
+            L2[hh] = live ? LD[(int64_t)(4 * grp + hh) * ldl + row] : 0.f;
+            Dh[hh] = live ? LD[(int64_t)(kH + 4 * grp + hh) * ldl + row] : 0.f;
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int acc_code = -1;
@@ -413,8 +408,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-           int64_t ld, const float* T, int nb, float scale, const float* LD, void* dq, double* dT64,
-           cudaStream_t s) {
+           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, void* dq,
+           double* dT64, cudaStream_t s) {
     using C = DqCfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -437,7 +432,7 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     dim3 grid((n + kBQ - 1) / kBQ);
     kern<<<grid, kThreads, smem, s>>>(
         mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-        T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+        ldl, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
     return check_launch();
 }
 
@@ -445,9 +440,9 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, void* dq, double* dT64, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, dq, dT64, s);
+                  const float* LD, int ldl, void* dq, double* dT64, cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s);
 }
 
 }  // namespace gt

@@ -46,6 +46,10 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // Workspace carving: 256-byte aligned sub-buffers.
+// Leading dimension (floats) of the backward's [16][ld] table of per-node
+// lse log2 e and D values: rows padded to 16 bytes for the TMA.
+inline int bwd_ld_ld(int n) { return (n + 3) & ~3; }
+
 struct Carve {
     char* base;
     size_t off;

@@ -95,6 +95,12 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+    float2 v;
+    asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
