@@ -5,20 +5,20 @@
 // bias slice of each block comes from the int8 bucket matrix),
 //   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
 //
-// One CTA = one tile of 128 KV rows, all 8 heads, streaming every Q tile;
-// 320 threads:
-//   warps 0-3 / 4-7  two groups of four heads; thread r of a group owns KV row
-//              j0 + r (TMEM lane r).  Per chunk of 16 query rows i it reads S^T
+// One CTA = one tile of 128 KV rows and one half of the heads (4 of 8: grid.y),
+// streaming every Q tile; two CTAs share an SM, so one's softmax runs while the
+// other waits on its tensor-core products.  192 threads:
+//   warps 0-3  thread r owns KV row j0 + r (TMEM lane r).  Per chunk of 16 query rows i it reads S^T
 //              and dP^T of its heads from TMEM, the bucket code of (i, j) from
 //              column r of the int8 tile, lse_i log2 e and D_i from the staged LD
 //              rows (4 consecutive i per 16-byte load), forms
 //              P^T = 2^(s scale log2 e + b - lse_i log2 e) and dS^T = P^T (dP^T - D_i)
 //              and writes both (bf16) back over S^T.
-//   warp 8     MMA issuer: S^T_h = K_h Q_h^T and dP^T_h = V_h dO_h^T (M=128, N=16,
+//   warp 4     MMA issuer: S^T_h = K_h Q_h^T and dP^T_h = V_h dO_h^T (M=128, N=16,
 //              K=16), then dv_h += P^T_h dO_h and dk_h += dS^T_h Q_h (A from TMEM).
-//   warp 9     TMA producer: per Q tile the bucket tile, the Q and dO column
+//   warp 5     TMA producer: per Q tile the bucket tile, the Q and dO column
 //              slots and the LD columns.
-// TMEM: dk at columns 0..127, dv at 128..255, and two 128-column regions whose
+// TMEM (256 columns): dk at 0..63, dv at 64..127, and two 64-column regions whose
 // roles alternate: S^T(t) in X, dP^T(t) in Y; P^T/dS^T(t) go over S^T(t) in X;
 // S^T(t+1) goes into Y once every thread has read dP^T(t); dP^T(t+1) goes into X
 // after the dv/dk products of chunk t (the tensor pipe runs one thread's MMAs in
@@ -43,13 +43,14 @@ using namespace tc;
 constexpr int kBKV = 128;
 constexpr int kCH = 16;
 constexpr int kQST = 2;
-constexpr int kSoft = 256;
+constexpr int kHC = 4;                     // heads per CTA
+constexpr int kSoft = 128;
 constexpr int kThreads = kSoft + 64;
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColDk = 0;
-constexpr uint32_t kColDv = 128;
+constexpr uint32_t kColDv = 64;
 
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return __fadd2_rn(a, make_float2(-b.x, -b.y));
@@ -58,15 +59,15 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
 // X_t is region (t & 1), Y_t the other one
 __device__ __forceinline__ uint32_t region(int t, bool x) {
     const int r = x ? (t & 1) : ((t & 1) ^ 1);
-    return 256u + 128u * r;
+    return 128u + 64u * r;
 }
 
 template <int HD>
 struct KvCfg {
-    static constexpr int BQ = HD == 8 ? 128 : 64;        // query rows per TMA tile
+    static constexpr int BQ = 64;                         // query rows per TMA tile
     static constexpr int NCH = BQ / kCH;
-    static constexpr int NSLOT = kH * HD / 16;
-    static constexpr uint32_t OP_BYTES = kH * kBKV * 32;  // 8 per-head [128][16] bf16 operands
+    static constexpr int NSLOT = kHC * HD / 16;           // 16-column slots of this CTA's heads
+    static constexpr uint32_t OP_BYTES = kHC * kBKV * 32; // per-head [128][16] bf16 operands
     static constexpr uint32_t SPD_BYTES = BQ * kBKV;      // [BQ i][128 j], no swizzle
     static constexpr uint32_t SLOT_BYTES = BQ * 32;
     static constexpr uint32_t LD_BYTES = 16 * BQ * 4;     // [16][BQ] fp32
@@ -93,7 +94,7 @@ struct Bars {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
                 const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapL,
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
@@ -107,6 +108,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = blockIdx.x * kBKV;
+    const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
     const int ntiles = (n + C::BQ - 1) / C::BQ;
     const int nchunks = ntiles * C::NCH;
 
@@ -134,8 +136,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int row = j0 + tid;
         const bool live = row < n;
         const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
-        write_head_operands<HD>(smem + C::OFF_K, tid, k + off, live);
-        write_head_operands<HD>(smem + C::OFF_V, tid, v + off, live);
+        write_head_operands<HD, kHC>(smem + C::OFF_K, tid, k + off, live, kHC * hb);
+        write_head_operands<HD, kHC>(smem + C::OFF_V, tid, v + off, live, kHC * hb);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before();
@@ -161,10 +163,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
 #pragma unroll
                 for (int s = 0; s < C::NSLOT; ++s) {
-                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapQ, 16 * s, i0,
-                                &bars->q_full[ks]);
-                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG, 16 * s,
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapQ, 16 * (hb * C::NSLOT + s),
                                 i0, &bars->q_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG,
+                                16 * (hb * C::NSLOT + s), i0, &bars->q_full[ks]);
                 }
                 tma_load_2d(st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES, &mapL, i0, 0,
                             &bars->q_full[ks]);
@@ -193,7 +195,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     return false;
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < kH; ++h)
+                for (int h = 0; h < kHC; ++h)
                     mma_ss(tbase + region(tt, true) + 16 * h, smem_desc(k_base + h * 4096, 16, 256, 6),
                            smem_desc(qslot(ks, c, h), 16, 256, 6), idKK, 0);
                 mma_commit(&bars->s_full);
@@ -202,7 +204,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             auto issue_dp = [&](int tt) {
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
 #pragma unroll
-                for (int h = 0; h < kH; ++h)
+                for (int h = 0; h < kHC; ++h)
                     mma_ss(tbase + region(tt, false) + 16 * h, smem_desc(v_base + h * 4096, 16, 256, 6),
                            smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
                 mma_commit(&bars->dp_full);
@@ -218,7 +220,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const uint32_t x = region(tt, true);
                 const uint32_t acc = tt > 0 ? 1u : 0u;
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
+                for (int h = 0; h < kHC; ++h) {
                     mma_ts(tbase + kColDv + 16 * h, tbase + x + 16 * h,
                            smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 256, 256, 6), idKM, acc);
                     mma_ts(tbase + kColDk + 16 * h, tbase + x + 16 * h + 8,
@@ -238,11 +240,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------- softmax
-        const int grp = warp >> 2;
         const int r = tid & (kBKV - 1);
         const int row = j0 + r;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * grp;
+        const uint32_t tbl = smem_u32(Ts) + 16u * hb;
         int t = 0;
         bool ok = true;
         for (int b = 0; ok && b < ntiles; ++b) {
@@ -250,7 +251,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (!mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
             // LD rows of this group's first head: row h is 4 BQ bytes long
-            const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (4 * grp) * C::BQ;
+            const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (kHC * hb) * C::BQ;
             const int i0 = b * C::BQ;
             const bool tail_tile = i0 + C::BQ > n;
             for (int c = 0; c < C::NCH; ++c, ++t) {
@@ -265,7 +266,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 // read before its P^T / dS^T overwrite them
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps) {
-                    const int h0 = 4 * grp + 2 * ps;
+                    const int h0 = 2 * ps;     // local head index (TMEM columns)
                     uint32_t rs[2][16], rd[2][16];
                     tmem_ld_x16(lrow + x + 16 * h0, rs[0]);
                     tmem_ld_x16(lrow + x + 16 * (h0 + 1), rs[1]);
@@ -350,11 +351,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             tc_fence_after();
             const bool live = row < n;
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                const int h = 4 * grp + hh;
+            for (int hh = 0; hh < kHC; ++hh) {
+                const int h = kHC * hb + hh;
                 uint32_t ok16[16], ov16[16];
-                tmem_ld_x16(lrow + kColDk + 16 * h, ok16);
-                tmem_ld_x16(lrow + kColDv + 16 * h, ov16);
+                tmem_ld_x16(lrow + kColDk + 16 * hh, ok16);
+                tmem_ld_x16(lrow + kColDv + 16 * hh, ov16);
                 tmem_wait_ld();
                 const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
                 if (live) {
@@ -406,7 +407,7 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         return GT_ERR_CUDA;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
-    dim3 grid((n + kBKV - 1) / kBKV);
+    dim3 grid((n + kBKV - 1) / kBKV, kH / kHC);
     bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
         mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
         T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dk),

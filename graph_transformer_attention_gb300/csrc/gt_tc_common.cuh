@@ -21,26 +21,27 @@ __device__ __forceinline__ void fail(int* abort_flag, int* status) {
     atomicOr(status, kStatusTimeout);
 }
 
-// Row r of the 8 per-head K-major [128][16] bf16 MMA operands (32-byte swizzle,
-// 4096 bytes per head) from one node's [8][HD] row of x.  Head dim 8 is
-// zero-padded to 16 per head so that products with the neighbouring head's
-// channels vanish; head dim 16 is copied as is.
-template <int HD>
+// Row r of NH per-head K-major [128][16] bf16 MMA operands (32-byte swizzle,
+// 4096 bytes per head) for heads h_first .. h_first + NH - 1 of one node's
+// [8][HD] row of x.  Head dim 8 is zero-padded to 16 per head so that products
+// with the neighbouring head's channels vanish; head dim 16 is copied as is.
+template <int HD, int NH = kH>
 __device__ __forceinline__ void write_head_operands(uint8_t* base, int r, const __nv_bfloat16* src,
-                                                    bool live) {
+                                                    bool live, int h_first = 0) {
     const uint4* s = reinterpret_cast<const uint4*>(src);
     const uint32_t sw = (uint32_t)((r >> 2) & 1);
     const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int h = 0; h < kH; ++h) {
+    for (int h = 0; h < NH; ++h) {
+        const int hg = h_first + h;
         uint4 lo, hi;
         if (HD == 8) {
-            const uint4 v = live ? s[h] : zero;
-            lo = (h & 1) ? zero : v;
-            hi = (h & 1) ? v : zero;
+            const uint4 v = live ? s[hg] : zero;
+            lo = (hg & 1) ? zero : v;
+            hi = (hg & 1) ? v : zero;
         } else {
-            lo = live ? s[2 * h] : zero;
-            hi = live ? s[2 * h + 1] : zero;
+            lo = live ? s[2 * hg] : zero;
+            hi = live ? s[2 * hg + 1] : zero;
         }
         uint8_t* dst = base + h * 4096 + r * 32;
         *reinterpret_cast<uint4*>(dst + ((0u ^ sw) << 4)) = lo;
