@@ -5,9 +5,11 @@
 // the matching bias slice of the int8 bucket matrix (MegaGraph, Fig. 4), and
 //   dS = P (dO V^T - D),  dq = scale dS K,  dT[h][c] = sum over spd = c of dS.
 //
-// One CTA = one tile of 128 query rows, all 8 heads, 320 threads:
-//   warps 0-3 / 4-7  two groups of four heads; thread r of a group owns query
-//              row r (TMEM lane r), so lse and D are registers.  Per chunk of
+// One CTA = one tile of 128 query rows and one half of the heads (4 of 8:
+// grid.y); two CTAs share an SM, so one's softmax runs while the other waits on
+// its tensor-core products.  192 threads:
+//   warps 0-3  thread r owns query row r (TMEM lane r), so lse and D are
+//              registers.  Per chunk of
 //              16 KV columns: S_h and dP_h from TMEM, one 16-byte shared load of
 //              the 4 head biases per bucket byte, P = 2^(x - lse log2 e),
 //              dS = P (dP - D), dS (bf16) back to TMEM over S, and dS summed per
@@ -15,11 +17,11 @@
 //              shared-memory reductions into bins [code][head][NCP copies]; lane l
 //              adds into copy l mod NCP, so with NCP = 32 the 32 rows of a warp never
 //              meet on one address or bank, whatever their codes.
-//   warp 8     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
+//   warp 4     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
 //              K=16), then dq_h += dS_h K_h (A = dS from TMEM).
-//   warp 9     TMA producer: bucket tile and K / V column slots per KV block.
-// TMEM: dq at columns 0..127 (16 per head), two S/dS stages at 128 and 256,
-// dP at 384.  All waits are bounded (timeout -> device status word, orderly
+//   warp 5     TMA producer: bucket tile and K / V column slots per KV block.
+// TMEM (256 columns): dq at 0..63 (16 per head), two S/dS stages at 64 and
+// 128, dP at 192.  All waits are bounded (timeout -> device status word, orderly
 // exit, TMEM freed).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -40,22 +42,23 @@ using namespace tc;
 constexpr int kBQ = 128;
 constexpr int kCH = 16;
 constexpr int kKVST = 2;
-constexpr int kSoft = 256;
+constexpr int kHC = 4;                     // heads per CTA
+constexpr int kSoft = 128;
 constexpr int kThreads = kSoft + 64;
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColDq = 0;
-constexpr uint32_t kColDp = 384;
+constexpr uint32_t kColDp = 192;
 
-__device__ __forceinline__ uint32_t s_col(int stage) { return 128u + 128u * stage; }
+__device__ __forceinline__ uint32_t s_col(int stage) { return 64u + 64u * stage; }
 
 template <int HD>
 struct DqCfg {
-    static constexpr int BKV = HD == 8 ? 128 : 64;     // KV rows per TMA block
+    static constexpr int BKV = 64;                     // KV rows per TMA block
     static constexpr int NCH = BKV / kCH;
-    static constexpr int NSLOT = kH * HD / 16;
-    static constexpr uint32_t OP_BYTES = kH * kBQ * 32;
+    static constexpr int NSLOT = kHC * HD / 16;        // 16-column slots of this CTA's heads
+    static constexpr uint32_t OP_BYTES = kHC * kBQ * 32;
     static constexpr uint32_t SPD_BYTES = kBQ * BKV;
     static constexpr uint32_t SLOT_BYTES = BKV * 32;
     static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
@@ -65,10 +68,11 @@ struct DqCfg {
     static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
     static constexpr uint32_t OFF_BIN = OFF_BAR + 256;
-    // bins: [nb][8 heads][ncp] fp32, sized at launch
-    static constexpr uint32_t smem_bytes(int nb, int ncp) { return OFF_BIN + (uint32_t)nb * kH * ncp * 4 + 1024; }
+    // bins: [nb][4 heads][ncp] fp32, sized at launch
+    static constexpr uint32_t smem_bytes(int nb, int ncp) { return OFF_BIN + (uint32_t)nb * kHC * ncp * 4 + 1024; }
 };
-constexpr uint32_t kSmemLimit = 232448;
+constexpr uint32_t kSmemLimit = 232448;      // one CTA per SM
+constexpr uint32_t kSmemPair = 115712;       // two CTAs per SM
 
 struct Bars {
     uint64_t kv_full[kKVST];
@@ -84,7 +88,7 @@ struct Bars {
 };
 
 template <int HD, int NCP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
               const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD, int ldl,
@@ -99,6 +103,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     float* bins = reinterpret_cast<float*>(smem + C::OFF_BIN);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = blockIdx.x * kBQ;
+    const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
     const int nblocks = (n + C::BKV - 1) / C::BKV;
     const int nchunks = nblocks * C::NCH;
 
@@ -123,13 +128,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
     if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
     fill_bias_table(Ts, T, nb, tid, kThreads);
-    for (int x = tid; x < nb * kH * NCP; x += kThreads) bins[x] = 0.f;
+    for (int x = tid; x < nb * kHC * NCP; x += kThreads) bins[x] = 0.f;
     if (tid < kBQ) {
         const int row = i0 + tid;
         const bool live = row < n;
         const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
-        write_head_operands<HD>(smem + C::OFF_Q, tid, q + off, live);
-        write_head_operands<HD>(smem + C::OFF_G, tid, dO + off, live);
+        write_head_operands<HD, kHC>(smem + C::OFF_Q, tid, q + off, live, kHC * hb);
+        write_head_operands<HD, kHC>(smem + C::OFF_G, tid, dO + off, live, kHC * hb);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before();
@@ -155,10 +160,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
 #pragma unroll
                 for (int s = 0; s < C::NSLOT; ++s) {
-                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * s, j0,
-                                &bars->kv_full[ks]);
-                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV, 16 * s,
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * (hb * C::NSLOT + s),
                                 j0, &bars->kv_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV,
+                                16 * (hb * C::NSLOT + s), j0, &bars->kv_full[ks]);
                 }
                 issued = b + 1;
             }
@@ -187,7 +192,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     return false;
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < kH; ++h)
+                for (int h = 0; h < kHC; ++h)
                     mma_ss(tbase + s_col(ss) + 16 * h, smem_desc(q_base + h * 4096, 16, 256, 6),
                            smem_desc(kslot(ks, c, h), 16, 256, 6), idKK, 0);
                 mma_commit(&bars->s_full[ss]);
@@ -196,7 +201,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             auto issue_dp = [&](int tt) {
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
 #pragma unroll
-                for (int h = 0; h < kH; ++h)
+                for (int h = 0; h < kHC; ++h)
                     mma_ss(tbase + kColDp + 16 * h, smem_desc(g_base + h * 4096, 16, 256, 6),
                            smem_desc(kslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
                 mma_commit(&bars->dp_full);
@@ -214,7 +219,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 if (!mbar_wait(&bars->ds_ready[ss], (tt >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < kH; ++h)
+                for (int h = 0; h < kHC; ++h)
                     mma_ts(tbase + kColDq + 16 * h, tbase + s_col(ss) + 16 * h,
                            smem_desc(kslot(ks, c, h), 256, 256, 6), idKM, tt > 0 ? 1u : 0u);
                 mma_commit(&bars->dq_done[ss]);
@@ -229,20 +234,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------- softmax
-        const int grp = warp >> 2;
         const int r = tid & (kBQ - 1);
         const int row = i0 + r;
         const bool live = row < n;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * grp;
+        const uint32_t tbl = smem_u32(Ts) + 16u * hb;
         // bin address: binb + code * kCodeStride + hh * kHeadStride
-        constexpr uint32_t kHeadStride = 4u * NCP, kCodeStride = kH * kHeadStride;
-        const uint32_t binb = smem_u32(bins) + 4u * (uint32_t)(lane & (NCP - 1)) + 4u * grp * kHeadStride;
+        constexpr uint32_t kHeadStride = 4u * NCP, kCodeStride = kHC * kHeadStride;
+        const uint32_t binb = smem_u32(bins) + 4u * (uint32_t)(lane & (NCP - 1));
         float L2[4], Dh[4];
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
-            L2[hh] = live ? LD[(int64_t)(4 * grp + hh) * ldl + row] : 0.f;
-            Dh[hh] = live ? LD[(int64_t)(kH + 4 * grp + hh) * ldl + row] : 0.f;
+            L2[hh] = live ? LD[(int64_t)(kHC * hb + hh) * ldl + row] : 0.f;
+            Dh[hh] = live ? LD[(int64_t)(kH + kHC * hb + hh) * ldl + row] : 0.f;
         }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int acc_code = -1;
@@ -283,8 +287,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     uint32_t rs[4][8], rd[4][8];
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        tmem_ld_x8(lrow + s_col(ss) + 16 * (4 * grp + hh) + 8 * g, rs[hh]);
-                        tmem_ld_x8(lrow + kColDp + 16 * (4 * grp + hh) + 8 * g, rd[hh]);
+                        tmem_ld_x8(lrow + s_col(ss) + 16 * hh + 8 * g, rs[hh]);
+                        tmem_ld_x8(lrow + kColDp + 16 * hh + 8 * g, rd[hh]);
                     }
                     tmem_wait_ld();
                     if (g == 1) {
@@ -330,7 +334,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             pk[k / 2] = pack_bf16x2(ds.x, ds.y);
                         }
                         if (uniform) acc[hh] += sum.x + sum.y;
-                        tmem_st_x4(lrow + s_col(ss) + 16 * (4 * grp + hh) + 4 * g, pk);
+                        tmem_st_x4(lrow + s_col(ss) + 16 * hh + 4 * g, pk);
                     }
                     if (!uniform) {
 #pragma unroll
@@ -368,9 +372,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
-                    const int h = 4 * grp + hh;
+                    const int h = kHC * hb + hh;
                     uint32_t ov[16];
-                    tmem_ld_x16(lrow + kColDq + 16 * h, ov);
+                    tmem_ld_x16(lrow + kColDq + 16 * hh, ov);
                     tmem_wait_ld();
                     const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
                     if (live) {
@@ -389,12 +393,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
         // add the copies of each (code, head) bin to the global table
         asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory");
-        for (int x = tid; x < nb * kH; x += kSoft) {
+        for (int x = tid; x < nb * kHC; x += kSoft) {
             const float* cp = bins + (int64_t)x * NCP;
             float s = 0.f;
 #pragma unroll 8
             for (int l = 0; l < NCP; ++l) s += cp[(l + tid) & (NCP - 1)];
-            const int code = x / kH, h = x % kH;
+            const int code = x / kHC, h = kHC * hb + x % kHC;
             if (s != 0.f) atomicAdd(&dT64[h * nb + code], (double)s);
         }
     }
@@ -422,14 +426,14 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         return GT_ERR_CUDA;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
-    // 32 bin copies (conflict-free) while they fit, else 8 (nb up to 128 always fits)
-    const bool wide = C::smem_bytes(nb, 32) <= kSmemLimit;
+    // 32 bin copies (conflict-free) while two CTAs still fit on an SM, else 8
+    const bool wide = C::smem_bytes(nb, 32) <= kSmemPair;
     auto kern = wide ? bwd_dq_kernel<HD, 32> : bwd_dq_kernel<HD, 8>;
     const uint32_t smem = C::smem_bytes(nb, wide ? 32 : 8);
     if (smem > kSmemLimit) return GT_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GT_ERR_CUDA;
-    dim3 grid((n + kBQ - 1) / kBQ);
+    dim3 grid((n + kBQ - 1) / kBQ, kH / kHC);
     kern<<<grid, kThreads, smem, s>>>(
         mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
         ldl, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);

@@ -1,25 +1,26 @@
 // gt_attn_fwd_tc.cu -- tensor-core forward of topology-biased graph attention
 // (bf16 storage, H = 8 heads, head dim 8 or 16) for sm_103a.
 //
-// Blockwise form of the MegaGraph paper's Fig. 4: KV blocks of 128 nodes stream
+// Blockwise form of the MegaGraph paper's Fig. 4: KV blocks of 64 nodes stream
 // past a tile of 128 query rows; with each KV block comes the matching
-// 128 x 128 slice of the int8 bucket matrix, and the bias b = T[h][code] is formed
+// 128 x 64 slice of the int8 bucket matrix, and the bias b = T[h][code] is formed
 // in registers from it.  Neither the scores nor the bias are ever stored.
 //
-// One CTA = one tile of 128 query rows, all 8 heads, 320 threads:
-//   warps 0-3  softmax group 0 (heads 0-3), warps 4-7 softmax group 1 (heads
-//              4-7): thread r of a group owns query row r (TMEM lane r).  Per
-//              chunk of 32 KV columns it reads S of its 4 heads from TMEM, gathers
-//              the 4 head biases of each (i, j) with one 16-byte shared load per
-//              bucket byte, exponentiates in base 2, writes P (bf16) to TMEM and
-//              keeps the row sums.  Two warps per SM sub-partition hide latency.
-//   warp 8     MMA issuer: S_h = Q_h K_h^T (M=128, N=32, K=16) into TMEM, then
+// One CTA = one tile of 128 query rows and one half of the heads (4 of 8:
+// grid.z); two CTAs share an SM, so one's softmax runs while the other waits on
+// its tensor-core products.  192 threads:
+//   warps 0-3  thread r owns query row r (TMEM lane r).  Per chunk of 32 KV
+//              columns it reads S of the 4 heads from TMEM, gathers the 4 head
+//              biases of each (i, j) with one 16-byte shared load per bucket byte,
+//              exponentiates in base 2, writes P (bf16) to TMEM and keeps the row
+//              sums.
+//   warp 4     MMA issuer: S_h = Q_h K_h^T (M=128, N=32, K=16) into TMEM, then
 //              O_h += P_h V_h (A = P from TMEM, M=128, N=16, two K=16 steps).
-//   warp 9     TMA producer: the bucket tile (128x128 int8, 128B swizzle) and the
-//              K and V column slots (128 x 16 bf16, 32B swizzle) of each KV block,
+//   warp 5     TMA producer: the bucket tile (128x64 int8, 64B swizzle) and the
+//              K and V column slots (64 x 16 bf16, 32B swizzle) of each KV block,
 //              double-buffered.
-// TMEM (512 columns): O_h at 16h (128 columns), S for 8 heads x 32 columns at
-// 128 (256 columns), P (bf16) for 8 heads x 32 columns at 384 (128 columns).
+// TMEM (256 columns): O_h at 16h (64 columns), S for 4 heads x 32 columns at 64
+// (128 columns), P (bf16) for 4 heads x 32 columns at 192 (64 columns).
 // S is read into registers at the start of a chunk, so the next chunk's QK^T
 // starts while this chunk is still being exponentiated.  Head dim 8 uses the
 // 16-wide MMAs with the neighbouring head's channels riding along: Q is
@@ -41,36 +42,35 @@
 
 #include "gt_common.cuh"
 #include "gt_sm100.cuh"
+#include "gt_tc_common.cuh"
 #include "gt_tma.cuh"
 
 namespace gt {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
-constexpr int kH = 8;
+constexpr int kHC = 4;                  // heads per CTA
 constexpr int kBQ = 128;
-constexpr int kBKV = 128;
+constexpr int kBKV = 64;
 constexpr int kCH = 32;                 // KV columns per MMA chunk
 constexpr int kNCH = kBKV / kCH;
 constexpr int kKVST = 2;
-constexpr uint32_t kTmemCols = 512;
-constexpr int kSoftThreads = 256;       // two groups of 128
+constexpr uint32_t kTmemCols = 256;
+constexpr int kSoftThreads = 128;
 constexpr int kThreads = kSoftThreads + 64;
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
-constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
 constexpr float kRedoSum = 256.f;       // 2^8: redo a half chunk whose row sum exceeds this
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 128;
-constexpr uint32_t kColP = 384;
+constexpr uint32_t kColS = 64;
+constexpr uint32_t kColP = 192;
 
 template <int HD>
 struct Cfg {
-    static constexpr int NSLOT = kH * HD / 16;
-    static constexpr uint32_t Q_BYTES = kH * kBQ * 32;
+    static constexpr int NSLOT = kHC * HD / 16;        // 16-column slots of this CTA's heads
+    static constexpr uint32_t Q_BYTES = kHC * kBQ * 32;
     static constexpr uint32_t SPD_BYTES = kBQ * kBKV;
     static constexpr uint32_t SLOT_BYTES = kBKV * 32;
     static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
@@ -144,7 +144,7 @@ __device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, ui
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
               const float* __restrict__ T, int nb, int n, float scale_log2, int kv_block,
@@ -159,6 +159,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = blockIdx.x * kBQ;
     const int split = blockIdx.y;
+    const int hb = blockIdx.z;                 // heads 4 hb .. 4 hb + 3
     const int j_begin = kv_block > 0 ? split * kv_block : 0;
     const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
     const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
@@ -186,27 +187,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         const int code = x / kH, h = x % kH;
         Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
     }
-    // per-head Q operands: [128 rows][16] bf16, 32-byte swizzle, K-major
+    // per-head Q operands of this CTA's heads: [128 rows][16] bf16, 32-byte swizzle, K-major
     if (tid < kBQ) {
         const int row = i0 + tid;
-        const uint4* src = reinterpret_cast<const uint4*>(q + (int64_t)(row < n ? row : 0) * kH * HD);
-        const uint32_t sw = (uint32_t)((tid >> 2) & 1);
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int h = 0; h < kH; ++h) {
-            uint4 lo, hi;
-            if (HD == 8) {
-                const uint4 v = row < n ? src[h] : zero;
-                lo = (h & 1) ? zero : v;
-                hi = (h & 1) ? v : zero;
-            } else {
-                lo = row < n ? src[2 * h] : zero;
-                hi = row < n ? src[2 * h + 1] : zero;
-            }
-            uint8_t* dst = smem + C::OFF_Q + h * 4096 + tid * 32;
-            *reinterpret_cast<uint4*>(dst + ((0u ^ sw) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dst + ((1u ^ sw) << 4)) = hi;
-        }
+        const bool live = row < n;
+        write_head_operands<HD, kHC>(smem + C::OFF_Q, tid, q + (int64_t)(live ? row : 0) * kH * HD, live,
+                                     kHC * hb);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before();
@@ -232,10 +218,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
 #pragma unroll
                 for (int s = 0; s < C::NSLOT; ++s) {
-                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * s, j0,
-                                &bars->kv_full[ks]);
-                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV, 16 * s,
+                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapK, 16 * (hb * C::NSLOT + s),
                                 j0, &bars->kv_full[ks]);
+                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapV,
+                                16 * (hb * C::NSLOT + s), j0, &bars->kv_full[ks]);
                 }
                 issued = b + 1;
             }
@@ -264,7 +250,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 tc_fence_after();
                 const uint32_t kbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + c * 1024;
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
+                for (int h = 0; h < kHC; ++h) {
                     const int slot = h * HD / 16;
                     mma_ss(tbase + kColS + kCH * h, smem_desc(q_base + h * 4096, 16, 256, 6),
                            smem_desc(kbase + slot * C::SLOT_BYTES, 16, 256, 6), idQK, 0);
@@ -281,7 +267,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const uint32_t vbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES +
                                        C::NSLOT * C::SLOT_BYTES + c * 1024;
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
+                for (int h = 0; h < kHC; ++h) {
                     const int slot = h * HD / 16;
 #pragma unroll
                     for (int st = 0; st < 2; ++st)
@@ -301,10 +287,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------- softmax
-        const int grp = warp >> 2;               // head group: heads 4*grp .. 4*grp+3
         const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * grp;   // 32-byte rows of 8 head biases
+        const uint32_t tbl = smem_u32(Ts) + 16u * hb;    // 32-byte rows of 8 head biases
         float m[4], l[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
@@ -313,15 +298,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         for (int b = 0; ok && b < nblocks; ++b) {
             const int ks = b & 1;
             if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * 128;
+            const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * kBKV;
             const int j0 = j_begin + b * kBKV;
             const bool tail_block = j0 + kBKV > j_end;
             for (int c = 0; c < kNCH; ++c, ++t) {
                 if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-                // codes of the 32 columns: two 16-byte chunks of the swizzled row
-                const uint4 c0 = lds_u4(sp + ((uint32_t)((2 * c) ^ (r & 7)) << 4));
-                const uint4 c1 = lds_u4(sp + ((uint32_t)((2 * c + 1) ^ (r & 7)) << 4));
+                // codes of the 32 columns: two 16-byte chunks of the row (64-byte swizzle)
+                const uint32_t swz = (uint32_t)((r >> 1) & 3);
+                const uint4 c0 = lds_u4(sp + (((uint32_t)(2 * c) ^ swz) << 4));
+                const uint4 c1 = lds_u4(sp + (((uint32_t)(2 * c + 1) ^ swz) << 4));
                 const int jc = j0 + c * kCH;
                 if (t == 0) {
                     // the first chunk sets the running maximum exactly (both halves)
@@ -330,7 +316,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         uint32_t sx[4][16];
 #pragma unroll
                         for (int hh = 0; hh < 4; ++hh)
-                            tmem_ld_x16(lrow + kColS + kCH * (4 * grp + hh) + 16 * g, sx[hh]);
+                            tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
                         tmem_wait_ld();
                         score16(sx, g ? c1 : c0, tbl, scale_log2);
                         if (tail_block) mask16(sx, jc + 16 * g, j_end);
@@ -348,7 +334,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     uint32_t sx[4][16];
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh)
-                        tmem_ld_x16(lrow + kColS + kCH * (4 * grp + hh) + 16 * g, sx[hh]);
+                        tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
                     tmem_wait_ld();
                     if (g == 1) {
                         tc_fence_before();
@@ -358,7 +344,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (tail_block) mask16(sx, jc + 16 * g, j_end);
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        const int h = 4 * grp + hh;
+                        const int h = hh;    // TMEM columns hold this CTA's four heads
                         uint32_t pk[8];
                         float ls = exp_pack16(sx[hh], m[hh], pk);
                         if (__any_sync(0xffffffffu, !(ls <= kRedoSum))) {
@@ -414,9 +400,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const bool live = row < n;
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
-                    const int h = 4 * grp + hh;
+                    const int h = kHC * hb + hh;
                     uint32_t ov[16];
-                    tmem_ld_x16(lrow + kColO + 16 * h, ov);
+                    tmem_ld_x16(lrow + kColO + 16 * hh, ov);
                     tmem_wait_ld();
                     const float inv = 1.f / l[hh];
                     const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
@@ -474,7 +460,7 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
         !make_map_2d(&mv, const_cast<void*>(v), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, cols, cols * 2,
                      kBKV, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, kBQ,
-                     kBKV, CU_TENSOR_MAP_SWIZZLE_128B))
+                     kBKV, CU_TENSOR_MAP_SWIZZLE_64B))
         return GT_ERR_CUDA;
     if (cudaFuncSetAttribute(fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
@@ -482,7 +468,7 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
-    dim3 grid((n + kBQ - 1) / kBQ, nsplit);
+    dim3 grid((n + kBQ - 1) / kBQ, nsplit, kH / kHC);
     fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
         mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e,
         nsplit > 1 ? kv_block : 0, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, status);
