@@ -144,10 +144,32 @@ def measured_peaks() -> dict:
         return {}
 
 
-def kernel_launches_per_step(w: gi.Workload, gt) -> int:
-    """Kernels of libgt launched by one step (memsets are not counted)."""
-    per = gt.launches_per_call(w.dtype, w.heads, w.head_dim, w.n, w.kv_block)
-    return per["spd"] + w.layers * (per["fwd"] + per["bwd"])
+# Exp-bound kernels: one exp per (query, key, head) per launch.
+EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd_cols_simt")
+
+# DRAM bytes (read + write) per launch of a kernel at a workload, from one ncu
+# capture of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
+# the capture summaries live under profiles/.
+DRAM_BYTES = {}
+
+
+def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float) -> dict:
+    """Roofline of one kernel: algorithmic work per launch / measured launch time."""
+    t = ms * 1e-3
+    traffic = DRAM_BYTES.get((name, w.name))
+    if name in EXP_KERNELS:
+        work = float(w.n) * w.n * w.heads            # exps per launch
+        return {"kernel": name, "bound": "alu", "achieved": round(work / t / 1e12, 4),
+                "peak": round(exp_peak / 1e12, 3), "unit": "Texp/s",
+                "frac": round(work / t / exp_peak, 4), "traffic": traffic,
+                "work_per_launch": work, "ms_per_launch": round(ms, 4),
+                "peak_source": f"{SMS} SMs x {EX2_PER_CLK_SM:g} ex2/clk/SM (measured) x max SM clock"}
+    # anything else is taken as bound by HBM on its output (the N^2 bucket bytes)
+    work = float(w.n) * w.n
+    return {"kernel": name, "bound": "hbm", "achieved": round(work / t / 1e9, 2),
+            "peak": round(hbm_peak / 1e9, 1), "unit": "GB/s", "frac": round(work / t / hbm_peak, 4),
+            "traffic": traffic, "work_per_launch": work, "ms_per_launch": round(ms, 4),
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs"}
 
 
 def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
@@ -237,6 +259,7 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     # device-timed region: K steps, per-part events on the launching stream
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gt.gt_kernel_stats_reset(False)          # count the library's launches in the timed region
     with ClockSampler(dev.index) as clk:
         barrier()
         t0.record(stream)
@@ -247,9 +270,22 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     ms_total = t0.elapsed_time(t1)
     clocks = clk.summary()
     gt.gt_check_device_status()
+    launches = sum(c for c, _ in gt.gt_kernel_stats().values())
     part_ms = {"spd": float(np.mean([e[0].elapsed_time(e[1]) for e in evs])),
                "fwd": float(np.mean([e[2].elapsed_time(e[3]) for e in evs])),
                "bwd": float(np.mean([e[4].elapsed_time(e[5]) for e in evs]))}
+
+    # per-kernel device time: a few more steps with every launch bracketed by
+    # CUDA events on its stream (kept out of the timed region above)
+    n_kt = min(args.steps, 3)
+    gt.gt_kernel_stats_reset(True)
+    for _ in range(n_kt):
+        step()
+    torch.cuda.synchronize()
+    kstats = gt.gt_kernel_stats()
+    gt.gt_kernel_stats_reset(False)
+    kernels = {name: {"launches_per_step": c / n_kt, "ms_per_launch": ms / c}
+               for name, (c, ms) in kstats.items()}
 
     # end-to-end through the public API, host buffers in and out
     for _ in range(2):
@@ -281,9 +317,9 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     exp_peak = SMS * EX2_PER_CLK_SM * clk_mhz * 1e6           # exps / s
     tensor_peak = float(peaks.get("bf16_tflops_sustained", 1700.0)) * 1e12
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0)) * 1e9
-    dom = "bwd" if part_ms["bwd"] >= part_ms["fwd"] else "fwd"
-    t_dom = part_ms[dom] * 1e-3
-    achieved = (n * n * H) / t_dom / 1e12 if t_dom > 0 else 0.0
+    # dominant kernel: largest device time per step
+    dom = max(kernels, key=lambda k: kernels[k]["launches_per_step"] * kernels[k]["ms_per_launch"])
+    roof = kernel_roofline(dom, w, kernels[dom]["ms_per_launch"], exp_peak, hbm_peak)
     # whole-path roofline: the slowest of tensor pipe, HBM and exp unit
     t_attn = (part_ms["fwd"] + part_ms["bwd"]) * w.layers * 1e-3
     t_roof = max(flops / tensor_peak, algo_bytes(w) / hbm_peak, exps(w) / exp_peak)
@@ -296,17 +332,15 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
         "parts_ms": {k: round(v, 4) for k, v in part_ms.items()},
         "node_pairs_per_s": {"spd": round(n * n / (part_ms["spd"] * 1e-3), 1),
                              "attn_fwd_bwd": round(n * n * w.layers / t_attn, 1)},
-        "roofline": {"kernel": f"bias_attn_{dom}", "bound": "alu", "achieved": round(achieved, 4),
-                     "peak": round(exp_peak / 1e12, 3), "unit": "Texp/s",
-                     "frac": round(achieved * 1e12 / exp_peak, 4), "traffic": None,
-                     "peak_source": f"{SMS} SMs x {EX2_PER_CLK_SM:g} ex2/clk/SM (measured) x "
-                                    f"{clk_mhz:g} MHz"},
+        "roofline": roof,
+        "kernels_ms": {k: {"launches_per_step": round(v["launches_per_step"], 3),
+                           "ms_per_launch": round(v["ms_per_launch"], 4)} for k, v in kernels.items()},
         "path_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "t_attn_ms": round(t_attn * 1e3, 4),
                           "frac": round(t_roof / t_attn, 4) if t_attn > 0 else None,
                           "bound": "exp unit (MUFU)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": int(kernel_launches_per_step(w, gt) * args.steps),
+        "gpu_launches": int(launches),
         "clocks": clocks,
         "cpu_baseline": None,
     }

@@ -52,6 +52,12 @@ def library_path() -> str:
     return _LIB_PATH
 
 
+class KernelStat(ctypes.Structure):
+    """gt_kernel_stat of the C ABI."""
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
 def load_library():
     """Load libgt.so (build it with graph_transformer_attention_gb300.build first)."""
     global _lib
@@ -80,6 +86,10 @@ def load_library():
         lib.gt_bias_attn_bwd.restype = ctypes.c_int
         lib.gt_check_device_status.argtypes = [P]
         lib.gt_check_device_status.restype = ctypes.c_int
+        lib.gt_kernel_stats_reset.argtypes = [i32]
+        lib.gt_kernel_stats_reset.restype = ctypes.c_int
+        lib.gt_kernel_stats_read.argtypes = [ctypes.POINTER(KernelStat), i32, ctypes.POINTER(i32)]
+        lib.gt_kernel_stats_read.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -211,3 +221,21 @@ def gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T, scale: float | None = None,
 def gt_check_device_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check("gt_check_device_status", load_library().gt_check_device_status(_stream_handle(stream)))
+
+
+def gt_kernel_stats_reset(timing: bool = False) -> None:
+    """Clear the library's launch table; with timing, bracket every launch with
+    CUDA events on its stream from now on."""
+    _check("gt_kernel_stats_reset", load_library().gt_kernel_stats_reset(1 if timing else 0))
+
+
+def gt_kernel_stats() -> dict:
+    """{kernel name: (launches, total device ms or -1 without timing)} since the
+    last reset, in first-launch order."""
+    lib = load_library()
+    count = ctypes.c_int32(0)
+    _check("gt_kernel_stats_read", lib.gt_kernel_stats_read(None, 0, ctypes.byref(count)))
+    arr = (KernelStat * max(1, count.value))()
+    _check("gt_kernel_stats_read", lib.gt_kernel_stats_read(arr, count.value, ctypes.byref(count)))
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(count.value)}

@@ -30,6 +30,7 @@
 #include <stdint.h>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 #include "gt_sm100.cuh"
 #include "gt_tc_common.cuh"
 #include "gt_tma.cuh"
@@ -408,10 +409,13 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     dim3 grid((n + kBKV - 1) / kBKV, kH / kHC);
-    bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-        mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-        T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dk),
-        static_cast<__nv_bfloat16*>(dv), status);
+    {
+        LaunchScope ls("bwd_dkdv", s);
+        bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
+            mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+            T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dk),
+            static_cast<__nv_bfloat16*>(dv), status);
+    }
     return check_launch();
 }
 

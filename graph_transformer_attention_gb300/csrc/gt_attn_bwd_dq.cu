@@ -29,6 +29,7 @@
 #include <stdint.h>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 #include "gt_sm100.cuh"
 #include "gt_tc_common.cuh"
 #include "gt_tma.cuh"
@@ -434,9 +435,12 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GT_ERR_CUDA;
     dim3 grid((n + kBQ - 1) / kBQ, kH / kHC);
-    kern<<<grid, kThreads, smem, s>>>(
-        mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-        ldl, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+    {
+        LaunchScope ls("bwd_dq", s);
+        kern<<<grid, kThreads, smem, s>>>(
+            mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
+            ldl, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+    }
     return check_launch();
 }
 

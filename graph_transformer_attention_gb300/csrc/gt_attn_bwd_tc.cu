@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 #include "gt_tc_common.cuh"
 
 namespace gt {
@@ -73,13 +74,19 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
     const int64_t total = (int64_t)n * kH;
     const int pblocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-    bwd_prep<__nv_bfloat16><<<pblocks, 256, 0, s>>>(n, d, ldl, static_cast<const __nv_bfloat16*>(o),
-                                                    static_cast<const __nv_bfloat16*>(dO), lse, LD, Dv);
+    {
+        LaunchScope ls("bwd_prep", s);
+        bwd_prep<__nv_bfloat16><<<pblocks, 256, 0, s>>>(n, d, ldl, static_cast<const __nv_bfloat16*>(o),
+                                                        static_cast<const __nv_bfloat16*>(dO), lse, LD, Dv);
+    }
     int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s);
     if (rc != GT_OK) return rc;
     rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s);
     if (rc != GT_OK) return rc;
-    dT_to_f32<<<1, 256, 0, s>>>(kH * nb, dT64, dT);
+    {
+        LaunchScope ls("bwd_dT_to_f32", s);
+        dT_to_f32<<<1, 256, 0, s>>>(kH * nb, dT64, dT);
+    }
     return check_launch();
 }
 

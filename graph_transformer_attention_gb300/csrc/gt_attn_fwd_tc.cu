@@ -41,6 +41,7 @@
 #include <stdint.h>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 #include "gt_sm100.cuh"
 #include "gt_tc_common.cuh"
 #include "gt_tma.cuh"
@@ -469,9 +470,12 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
     if (!status) return GT_ERR_CUDA;
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
     dim3 grid((n + kBQ - 1) / kBQ, nsplit, kH / kHC);
-    fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-        mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e,
-        nsplit > 1 ? kv_block : 0, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, status);
+    {
+        LaunchScope ls("fwd_tc", s);
+        fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
+            mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e,
+            nsplit > 1 ? kv_block : 0, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, status);
+    }
     return check_launch();
 }
 

@@ -17,6 +17,7 @@
 #include <type_traits>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 
 namespace gt {
 namespace {
@@ -305,12 +306,18 @@ int fwd_simt_launch(int n, int h, int d, const void* q, const void* k, const voi
                     cudaStream_t s) {
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
     dim3 grid((n + kRows - 1) / kRows, h, nsplit);
-    fwd_simt<TE, DP><<<grid, kRows, 0, s>>>(
-        n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld, T, nb, scale,
-        nsplit > 1 ? kv_block : 0, (TE*)o, lse, o_part, lse_part);
+    {
+        LaunchScope ls("fwd_simt", s);
+        fwd_simt<TE, DP><<<grid, kRows, 0, s>>>(
+            n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld, T, nb, scale,
+            nsplit > 1 ? kv_block : 0, (TE*)o, lse, o_part, lse_part);
+    }
     if (nsplit > 1)
-        merge_splits<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
-                                                                  (TE*)o, lse);
+        {
+            LaunchScope ls("fwd_merge", s);
+            merge_splits<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
+                                                                      (TE*)o, lse);
+        }
     return check_launch();
 }
 
@@ -320,15 +327,27 @@ int bwd_simt_launch(int n, int h, int d, const void* q, const void* k, const voi
                     int64_t ld, const float* T, int nb, float scale, void* dq, void* dk, void* dv,
                     float* dT, float* Dv, double* dT64, cudaStream_t s) {
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)h * nb, s) != cudaSuccess) return GT_ERR_CUDA;
-    bwd_delta<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, (const TE*)o, (const TE*)dO, Dv);
+    {
+        LaunchScope ls("bwd_delta", s);
+        bwd_delta<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, (const TE*)o, (const TE*)dO, Dv);
+    }
     dim3 grid((n + kRows - 1) / kRows, h);
-    bwd_rows_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
-                                                 (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
-                                                 nb, scale, (TE*)dq, dT64);
-    bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
-                                                 (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
-                                                 nb, scale, (TE*)dk, (TE*)dv);
-    dT_finalize<<<1, 256, 0, s>>>(h * nb, dT64, dT);
+    {
+        LaunchScope ls("bwd_rows_simt", s);
+        bwd_rows_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
+                                                     (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
+                                                     nb, scale, (TE*)dq, dT64);
+    }
+    {
+        LaunchScope ls("bwd_cols_simt", s);
+        bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
+                                                     (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
+                                                     nb, scale, (TE*)dk, (TE*)dv);
+    }
+    {
+        LaunchScope ls("bwd_dT_finalize", s);
+        dT_finalize<<<1, 256, 0, s>>>(h * nb, dT64, dT);
+    }
     return check_launch();
 }
 
@@ -367,11 +386,17 @@ int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, 
 int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
                    const float* lse_part, void* o, float* lse, cudaStream_t s) {
     if (dtype == GT_F32)
-        merge_splits<float><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
-                                                                     (float*)o, lse);
+        {
+            LaunchScope ls("fwd_merge", s);
+            merge_splits<float><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
+                                                                         (float*)o, lse);
+        }
     else
-        merge_splits<__nv_bfloat16><<<grid_for((int64_t)n * h), 256, 0, s>>>(
-            n, h, d, nsplit, o_part, lse_part, (__nv_bfloat16*)o, lse);
+        {
+            LaunchScope ls("fwd_merge", s);
+            merge_splits<__nv_bfloat16><<<grid_for((int64_t)n * h), 256, 0, s>>>(
+                n, h, d, nsplit, o_part, lse_part, (__nv_bfloat16*)o, lse);
+        }
     return check_launch();
 }
 
@@ -384,10 +409,13 @@ int attn_bwd_cols_simt(int dtype, int n, int h, int d, const void* q, const void
     auto go = [&](auto tag, auto dp) {
         using TE = decltype(tag);
         constexpr int DP = decltype(dp)::value;
-        bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k,
-                                                     (const TE*)v, (const TE*)dO, lse, Dv,
-                                                     (const uint8_t*)spd, ld, T, nb, scale,
-                                                     (TE*)dk, (TE*)dv);
+        {
+            LaunchScope ls("bwd_cols_simt", s);
+            bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k,
+                                                         (const TE*)v, (const TE*)dO, lse, Dv,
+                                                         (const uint8_t*)spd, ld, T, nb, scale,
+                                                         (TE*)dk, (TE*)dv);
+        }
     };
     using I8 = std::integral_constant<int, 8>;
     using I16 = std::integral_constant<int, 16>;

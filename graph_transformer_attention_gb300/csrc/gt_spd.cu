@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include "gt_common.cuh"
+#include "gt_stats.cuh"
 
 namespace gt {
 namespace {
@@ -283,13 +284,25 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t 
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int sms = num_sms();
-    uf_init<<<sms * 4, 256, 0, stream>>>(comp, n);
-    uf_hook<<<sms * 8, 256, 0, stream>>>(indptr, indices, comp, n, status);
-    uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
+    {
+        LaunchScope ls("spd_uf_init", stream);
+        uf_init<<<sms * 4, 256, 0, stream>>>(comp, n);
+    }
+    {
+        LaunchScope ls("spd_uf_hook", stream);
+        uf_hook<<<sms * 8, 256, 0, stream>>>(indptr, indices, comp, n, status);
+    }
+    {
+        LaunchScope ls("spd_uf_compress", stream);
+        uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
+    }
     // the BFS keeps vis / acc / db zero between batches; start from zero
     if (cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess) return GT_ERR_CUDA;
-    bfs_batches<<<nctas, kSpdThreads, 0, stream>>>(indptr, indices, comp, n, D, nslices, spd, ld,
-                                                   bfs_ws, per);
+    {
+        LaunchScope ls("spd_bfs", stream);
+        bfs_batches<<<nctas, kSpdThreads, 0, stream>>>(indptr, indices, comp, n, D, nslices, spd, ld,
+                                                       bfs_ws, per);
+    }
     return check_launch();
 }
 

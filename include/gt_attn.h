@@ -20,7 +20,8 @@
  *   - Pointers named as device buffers must be device memory of the current
  *     CUDA device.  The caller owns and allocates every buffer, including the
  *     workspace; the library allocates nothing and keeps no state between
- *     calls (apart from one device status word, see gt_check_device_status).
+ *     calls (apart from one device status word, see gt_check_device_status,
+ *     and the launch statistics at the end of this header).
  *   - Layouts are dense row-major: q, k, v, o, dO, dq, dk, dv are [n][h][d]
  *     (node, head, channel); lse is [h][n] fp32; T and dT are [h][nb] fp32;
  *     spd is int8 [n][ld_spd] (row i holds the bucket codes of pairs (i, *)).
@@ -170,6 +171,37 @@ const char* gt_status_string(int status);
  * word is cleared by the call.
  */
 int gt_check_device_status(void* stream);
+
+/*
+ * Launch statistics (a measurement aid; no counterpart in the method).
+ *
+ * The library counts, per kernel name, every kernel it launches.  With timing
+ * on, each launch is also bracketed by two CUDA events recorded on the
+ * launching stream (events come from a pool the library creates on demand and
+ * keeps), so the sum of (end - start) per name is the device time of that
+ * kernel's launches, queueing behind earlier work on the stream excluded.
+ * Timing adds two event records per launch; leave it off while timing whole
+ * steps.  The table is process-wide and guarded by a mutex; with timing on,
+ * use one CUDA device per process.
+ *
+ *   gt_kernel_stats_reset(timing)  clears the table (waiting for events still
+ *       pending) and sets timing on (non-zero) or off.  Returns GT_OK or
+ *       GT_ERR_CUDA.
+ *   gt_kernel_stats_read(out, cap, count)  waits for the recorded events, sets
+ *       *count to the number of distinct kernel names seen since the reset and
+ *       fills min(cap, *count) entries of out (host memory, caller-owned) in
+ *       first-launch order; total_ms is -1 when timing is off.  Returns
+ *       GT_ERR_INVALID_ARG for count == NULL, cap < 0 or out == NULL with
+ *       cap > 0, GT_ERR_CUDA if an event query fails, else GT_OK.
+ */
+typedef struct {
+    char name[40];      /* NUL-terminated kernel name, e.g. "bwd_dq" */
+    int64_t launches;   /* launches since the last reset */
+    double total_ms;    /* summed device time of those launches (timing on) */
+} gt_kernel_stat;
+
+int gt_kernel_stats_reset(int32_t timing);
+int gt_kernel_stats_read(gt_kernel_stat* out, int32_t cap, int32_t* count);
 
 #ifdef __cplusplus
 }

@@ -96,3 +96,14 @@ def test_workspace_sizes(lib):
 def test_spd_ld():
     import graph_transformer_attention_gb300 as gt
     assert [gt.spd_ld(n) for n in (1, 16, 17, 6800)] == [16, 16, 32, 6800]
+
+
+def test_kernel_stats_table_on_host(lib):
+    import graph_transformer_attention_gb300 as gt
+    count = ctypes.c_int32(-7)
+    assert lib.gt_kernel_stats_read(None, -1, ctypes.byref(count)) == -1
+    assert lib.gt_kernel_stats_read(None, 2, ctypes.byref(count)) == -1
+    assert lib.gt_kernel_stats_read(None, 0, None) == -1
+    # nothing launched since the reset: an empty table, no CUDA call needed
+    gt.gt_kernel_stats_reset(False)
+    assert gt.gt_kernel_stats() == {}

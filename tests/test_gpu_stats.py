@@ -1,0 +1,45 @@
+"""Launch statistics of libgt on the GPU: every kernel of a call is counted
+under its name, and with timing on each gets a positive device time."""
+import numpy as np
+import pytest
+import torch
+
+import gt_inputs as gi
+from tests.helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gt():
+    import graph_transformer_attention_gb300 as m
+    from graph_transformer_attention_gb300 import build
+    build.build()
+    m.load_library()
+    return m
+
+
+@pytest.mark.parametrize("timing", [False, True])
+def test_counts_and_times_of_one_layer(gt, timing):
+    n, h, d, nb = 300, 8, 16, 26
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=5)
+    q, k, v, dO = (to_dev(x[a], "bf16") for a in ("q", "k", "v", "dO"))
+    T = torch.from_numpy(x["T"]).cuda()
+    codes = np.random.default_rng(5).integers(0, nb, size=(n, gt.spd_ld(n))).astype(np.int8)
+    spd = torch.from_numpy(codes).cuda()
+    torch.cuda.synchronize()
+    gt.gt_kernel_stats_reset(timing)
+    o, lse = gt.gt_bias_attn_fwd(q, k, v, spd, T)
+    gt.gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T)
+    gt.gt_check_device_status()
+    stats = gt.gt_kernel_stats()
+    gt.gt_kernel_stats_reset(False)
+    assert list(stats) == ["fwd_tc", "bwd_prep", "bwd_dq", "bwd_dkdv", "bwd_dT_to_f32"]
+    per = gt.launches_per_call("bf16", h, d, n)
+    assert sum(c for c, _ in stats.values()) == per["fwd"] + per["bwd"]
+    for name, (launches, ms) in stats.items():
+        assert launches == 1
+        if timing:
+            assert 0.0 < ms < 1000.0, (name, ms)
+        else:
+            assert ms == -1.0
