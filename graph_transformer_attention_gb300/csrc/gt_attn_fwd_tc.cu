@@ -53,20 +53,21 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int kHC = 4;                  // heads per CTA
+constexpr int kCtasPerSm = kH / kHC;
 constexpr int kBQ = 128;
 constexpr int kBKV = 64;
 constexpr int kCH = 32;                 // KV columns per MMA chunk
 constexpr int kNCH = kBKV / kCH;
 constexpr int kKVST = 2;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 64 * kHC;
 constexpr int kSoftThreads = 128;
 constexpr int kThreads = kSoftThreads + 64;
 constexpr int kMmaWarp = 4;
 constexpr int kTmaWarp = 5;
 constexpr float kRedoSum = 256.f;       // 2^8: redo a half chunk whose row sum exceeds this
-constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 64;
-constexpr uint32_t kColP = 192;
+constexpr uint32_t kColO = 0;                       // O: 16 columns per head
+constexpr uint32_t kColS = 16 * kHC;                // S: 32 columns per head
+constexpr uint32_t kColP = 16 * kHC + 32 * kHC;     // P (bf16 pairs): 16 columns per head
 
 template <int HD>
 struct Cfg {
@@ -106,27 +107,40 @@ __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b
 // half g of a chunk, in place over the raw S bits; one 16-byte load per code
 // gives the four head biases (tbl: shared address of this head group's half of
 // the first 32-byte table row).
-__device__ __forceinline__ void score16(uint32_t (&sx)[4][16], const uint4 cw, uint32_t tbl,
+template <int NH>
+__device__ __forceinline__ void load_bias(uint32_t addr, float (&b)[NH]) {
+    if constexpr (NH == 4) {
+        const float4 v = lds_f4(addr);
+        b[0] = v.x; b[1] = v.y; b[2] = v.z; b[3] = v.w;
+    } else {
+        const float2 v = lds_f2(addr);
+        b[0] = v.x; b[1] = v.y;
+    }
+}
+
+template <int NH>
+__device__ __forceinline__ void score16(uint32_t (&sx)[NH][16], const uint4 cw, uint32_t tbl,
                                         float scale_log2) {
     const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const uint32_t code = __byte_perm(w[k >> 2], 0u, 0x4440u + (k & 3));
-        const float4 bv = lds_f4(tbl + code * 32u);
-        sx[0][k] = __float_as_uint(fmaf(__uint_as_float(sx[0][k]), scale_log2, bv.x));
-        sx[1][k] = __float_as_uint(fmaf(__uint_as_float(sx[1][k]), scale_log2, bv.y));
-        sx[2][k] = __float_as_uint(fmaf(__uint_as_float(sx[2][k]), scale_log2, bv.z));
-        sx[3][k] = __float_as_uint(fmaf(__uint_as_float(sx[3][k]), scale_log2, bv.w));
+        float bv[NH];
+        load_bias<NH>(tbl + code * 32u, bv);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh)
+            sx[hh][k] = __float_as_uint(fmaf(__uint_as_float(sx[hh][k]), scale_log2, bv[hh]));
     }
 }
 
 // Columns at or beyond j_end (the tail of the last KV block) get x = -inf.
-__device__ __forceinline__ void mask16(uint32_t (&sx)[4][16], int j, int j_end) {
+template <int NH>
+__device__ __forceinline__ void mask16(uint32_t (&sx)[NH][16], int j, int j_end) {
 #pragma unroll
     for (int k = 0; k < 16; ++k)
         if (j + k >= j_end) {
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) sx[hh][k] = __float_as_uint(-INFINITY);
+            for (int hh = 0; hh < NH; ++hh) sx[hh][k] = __float_as_uint(-INFINITY);
         }
 }
 
@@ -145,7 +159,7 @@ __device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, ui
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
               const float* __restrict__ T, int nb, int n, float scale_log2, int kv_block,
@@ -160,7 +174,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = blockIdx.x * kBQ;
     const int split = blockIdx.y;
-    const int hb = blockIdx.z;                 // heads 4 hb .. 4 hb + 3
+    const int hb = blockIdx.z;                 // heads kHC hb .. kHC hb + kHC - 1
     const int j_begin = kv_block > 0 ? split * kv_block : 0;
     const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
     const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
@@ -290,10 +304,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         // ------------------------------------------------------- softmax
         const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * hb;    // 32-byte rows of 8 head biases
-        float m[4], l[4];
+        const uint32_t tbl = smem_u32(Ts) + 4u * kHC * hb;   // 32-byte rows of 8 head biases
+        float m[kHC], l[kHC];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+        for (int h = 0; h < kHC; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
         int t = 0;
         bool ok = true;
         for (int b = 0; ok && b < nblocks; ++b) {
@@ -314,15 +328,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     // the first chunk sets the running maximum exactly (both halves)
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
-                        uint32_t sx[4][16];
+                        uint32_t sx[kHC][16];
 #pragma unroll
-                        for (int hh = 0; hh < 4; ++hh)
+                        for (int hh = 0; hh < kHC; ++hh)
                             tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
                         tmem_wait_ld();
                         score16(sx, g ? c1 : c0, tbl, scale_log2);
                         if (tail_block) mask16(sx, jc + 16 * g, j_end);
 #pragma unroll
-                        for (int hh = 0; hh < 4; ++hh)
+                        for (int hh = 0; hh < kHC; ++hh)
 #pragma unroll
                             for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
                     }
@@ -332,9 +346,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 tc_fence_after();
 #pragma unroll 1
                 for (int g = 0; g < 2; ++g) {
-                    uint32_t sx[4][16];
+                    uint32_t sx[kHC][16];
 #pragma unroll
-                    for (int hh = 0; hh < 4; ++hh)
+                    for (int hh = 0; hh < kHC; ++hh)
                         tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
                     tmem_wait_ld();
                     if (g == 1) {
@@ -344,7 +358,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     score16(sx, g ? c1 : c0, tbl, scale_log2);
                     if (tail_block) mask16(sx, jc + 16 * g, j_end);
 #pragma unroll
-                    for (int hh = 0; hh < 4; ++hh) {
+                    for (int hh = 0; hh < kHC; ++hh) {
                         const int h = hh;    // TMEM columns hold this CTA's four heads
                         uint32_t pk[8];
                         float ls = exp_pack16(sx[hh], m[hh], pk);
@@ -400,7 +414,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const int row = i0 + r;
                 const bool live = row < n;
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
+                for (int hh = 0; hh < kHC; ++hh) {
                     const int h = kHC * hb + hh;
                     uint32_t ov[16];
                     tmem_ld_x16(lrow + kColO + 16 * hh, ov);
