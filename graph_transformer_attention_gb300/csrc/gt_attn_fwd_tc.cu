@@ -145,16 +145,19 @@ __device__ __forceinline__ void mask16(uint32_t (&sx)[NH][16], int j, int j_end)
 }
 
 // p_k = 2^(x_k - m) for one head's 16 columns, packed to bf16 pairs; returns sum p.
+// (two partial sums keep the dependent chain short)
 __device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, uint32_t (&pk)[8]) {
-    float2 acc = f2(0.f, 0.f);
+    float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
     const float2 mm = f2(-m, -m);
 #pragma unroll
     for (int k = 0; k < 16; k += 2) {
         const float2 d = __fadd2_rn(f2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), mm);
         const float2 p = f2(ex2(d.x), ex2(d.y));
-        acc = __fadd2_rn(acc, p);
+        if (k & 2) acc1 = __fadd2_rn(acc1, p);
+        else acc0 = __fadd2_rn(acc0, p);
         pk[k / 2] = pack_bf16x2(p.x, p.y);
     }
+    const float2 acc = __fadd2_rn(acc0, acc1);
     return acc.x + acc.y;
 }
 
@@ -357,42 +360,54 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     }
                     score16(sx, g ? c1 : c0, tbl, scale_log2);
                     if (tail_block) mask16(sx, jc + 16 * g, j_end);
+                    // exponentials of all heads first (independent chains), one vote on
+                    // whether any head of any row needs a redo against a new maximum
+                    uint32_t pk[kHC][8];
+                    float ls[kHC];
+                    bool need = false;
 #pragma unroll
                     for (int hh = 0; hh < kHC; ++hh) {
-                        const int h = hh;    // TMEM columns hold this CTA's four heads
-                        uint32_t pk[8];
-                        float ls = exp_pack16(sx[hh], m[hh], pk);
-                        if (__any_sync(0xffffffffu, !(ls <= kRedoSum))) {
+                        ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
+                        need |= !(ls[hh] <= kRedoSum);
+                    }
+                    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                        for (int hh = 0; hh < kHC; ++hh) {
+                            if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
                             // a new maximum for this head: redo, and rescale l, the P already
-                            // written for this chunk, and O
+                            // written for this chunk, and O (TMEM columns hold this CTA's heads)
                             float mx = m[hh];
 #pragma unroll
                             for (int k = 0; k < 16; ++k) mx = fmaxf(mx, __uint_as_float(sx[hh][k]));
                             const float alpha = ex2(m[hh] - mx);
                             m[hh] = mx;
                             l[hh] *= alpha;
-                            ls = exp_pack16(sx[hh], mx, pk);
+                            ls[hh] = exp_pack16(sx[hh], mx, pk[hh]);
                             if (g == 1) {
                                 uint32_t pw[8];
-                                tmem_ld_x8(lrow + kColP + 16 * h, pw);
+                                tmem_wait_st();   // the first half's P of this head is written
+                                tmem_ld_x8(lrow + kColP + 16 * hh, pw);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int k = 0; k < 8; ++k)
                                     pw[k] = pack_bf16x2(__uint_as_float(pw[k] << 16) * alpha,
                                                         __uint_as_float(pw[k] & 0xffff0000u) * alpha);
-                                tmem_st_x8(lrow + kColP + 16 * h, pw);
+                                tmem_st_x8(lrow + kColP + 16 * hh, pw);
                             }
                             if (t > 0) {
                                 uint32_t ov[16];
-                                tmem_ld_x16(lrow + kColO + 16 * h, ov);
+                                tmem_ld_x16(lrow + kColO + 16 * hh, ov);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                                tmem_st_x16(lrow + kColO + 16 * h, ov);
+                                tmem_st_x16(lrow + kColO + 16 * hh, ov);
                             }
                         }
-                        l[hh] += ls;
-                        tmem_st_x8(lrow + kColP + 16 * h + 8 * g, pk);
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < kHC; ++hh) {
+                        l[hh] += ls[hh];
+                        tmem_st_x8(lrow + kColP + 16 * hh + 8 * g, pk[hh]);
                     }
                 }
                 tmem_wait_st();
