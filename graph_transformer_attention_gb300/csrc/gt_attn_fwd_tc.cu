@@ -344,9 +344,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
                     }
                 }
-                // P must not be overwritten before the previous chunk's PV has read it
-                if (t > 0 && !mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
-                tc_fence_after();
+                // P and O must not be touched before the previous chunk's PV is done with
+                // them; the wait is put off until the first write, so that the S loads and
+                // the first half's exponentials overlap that PV
+                bool pv_waited = t == 0;
+                auto wait_pv = [&]() {
+                    if (pv_waited) return;
+                    if (!mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+                    tc_fence_after();
+                    pv_waited = true;
+                };
 #pragma unroll 1
                 for (int g = 0; g < 2; ++g) {
                     uint32_t sx[kHC][16];
@@ -371,6 +378,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         need |= !(ls[hh] <= kRedoSum);
                     }
                     if (__any_sync(0xffffffffu, need)) {
+                        wait_pv();
 #pragma unroll
                         for (int hh = 0; hh < kHC; ++hh) {
                             if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
@@ -404,6 +412,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             }
                         }
                     }
+                    wait_pv();
 #pragma unroll
                     for (int hh = 0; hh < kHC; ++hh) {
                         l[hh] += ls[hh];
