@@ -87,6 +87,7 @@ struct Bars {
     uint64_t s_full;
     uint64_t dp_full;
     uint64_t dp_free;
+    uint64_t p_ready;
     uint64_t ds_ready;
     uint64_t done;
     uint64_t fin;
@@ -121,6 +122,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->dp_free, kSoft);
+        mbar_init(&bars->p_ready, kSoft);
         mbar_init(&bars->ds_ready, kSoft);
         mbar_init(&bars->done, 1);
         mbar_init(&bars->fin, 1);
@@ -214,19 +216,24 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (ok) issue_dp(0);
             for (int tt = 0; ok && tt < nchunks; ++tt) {
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+                const uint32_t x = region(tt, true);
+                const uint32_t acc = tt > 0 ? 1u : 0u;
+                // dv as soon as P^T is in TMEM, S^T(t+1) once dP^T(t) is read, dk once
+                // dS^T is in
+                if (!mbar_wait(&bars->p_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < kHC; ++h)
+                    mma_ts(tbase + kColDv + 16 * h, tbase + x + 16 * h,
+                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 256, 256, 6), idKM, acc);
                 if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 if (tt + 1 < nchunks && !issue_s(tt + 1)) { ok = false; break; }
                 if (!mbar_wait(&bars->ds_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t x = region(tt, true);
-                const uint32_t acc = tt > 0 ? 1u : 0u;
 #pragma unroll
-                for (int h = 0; h < kHC; ++h) {
-                    mma_ts(tbase + kColDv + 16 * h, tbase + x + 16 * h,
-                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 256, 256, 6), idKM, acc);
+                for (int h = 0; h < kHC; ++h)
                     mma_ts(tbase + kColDk + 16 * h, tbase + x + 16 * h + 8,
                            smem_desc(qslot(ks, c, h), 256, 256, 6), idKM, acc);
-                }
                 if (c == C::NCH - 1) mma_commit(&bars->q_empty[ks]);
                 if (tt + 1 < nchunks) issue_dp(tt + 1);
             }
@@ -263,12 +270,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 uint32_t code[16];
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
-                // two passes of two heads over all 16 columns: a head's S^T columns are all
-                // read before its P^T / dS^T overwrite them
+                // P^T of all four heads first (S^T of a head pair is read before its P^T
+                // overwrites it), so the exponentials overlap the dP^T products still in
+                // the tensor pipe; then dS^T once dP^T has landed
+                float pf[kHC][16];
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps) {
                     const int h0 = 2 * ps;     // local head index (TMEM columns)
-                    uint32_t rs[2][16], rd[2][16];
+                    uint32_t rs[2][16];
                     tmem_ld_x16(lrow + x + 16 * h0, rs[0]);
                     tmem_ld_x16(lrow + x + 16 * (h0 + 1), rs[1]);
                     tmem_wait_ld();
@@ -276,36 +285,44 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) {
                         const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * ps);
-                        rs[0][kk] = __float_as_uint(fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x));
-                        rs[1][kk] = __float_as_uint(fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y));
+                        pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
+                        pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
                     }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const uint32_t la = ldb + 4u * (2 * ps + e) * C::BQ + 4u * (c * kCH);
+                        const uint32_t la = ldb + 4u * (h0 + e) * C::BQ + 4u * (c * kCH);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const uint4 l = lds_u4(la + 16u * q4);
-                            const float2 xa = fsub2(make_float2(__uint_as_float(rs[e][4 * q4]),
-                                                                __uint_as_float(rs[e][4 * q4 + 1])),
+                            const float2 xa = fsub2(make_float2(pf[h0 + e][4 * q4], pf[h0 + e][4 * q4 + 1]),
                                                     make_float2(__uint_as_float(l.x), __uint_as_float(l.y)));
-                            const float2 xb = fsub2(make_float2(__uint_as_float(rs[e][4 * q4 + 2]),
-                                                                __uint_as_float(rs[e][4 * q4 + 3])),
+                            const float2 xb = fsub2(make_float2(pf[h0 + e][4 * q4 + 2], pf[h0 + e][4 * q4 + 3]),
                                                     make_float2(__uint_as_float(l.z), __uint_as_float(l.w)));
-                            rs[e][4 * q4] = __float_as_uint(ex2(xa.x));
-                            rs[e][4 * q4 + 1] = __float_as_uint(ex2(xa.y));
-                            rs[e][4 * q4 + 2] = __float_as_uint(ex2(xb.x));
-                            rs[e][4 * q4 + 3] = __float_as_uint(ex2(xb.y));
+                            pf[h0 + e][4 * q4] = ex2(xa.x);
+                            pf[h0 + e][4 * q4 + 1] = ex2(xa.y);
+                            pf[h0 + e][4 * q4 + 2] = ex2(xb.x);
+                            pf[h0 + e][4 * q4 + 3] = ex2(xb.y);
                         }
-                    }
-                    if (tail_tile) {
+                        if (tail_tile) {
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk)
-                            if (i0 + c * kCH + kk >= n) { rs[0][kk] = 0u; rs[1][kk] = 0u; }
+                            for (int kk = 0; kk < 16; ++kk)
+                                if (i0 + c * kCH + kk >= n) pf[h0 + e][kk] = 0.f;
+                        }
+                        uint32_t pp[8];
+#pragma unroll
+                        for (int k2 = 0; k2 < 8; ++k2) pp[k2] = pack_bf16x2(pf[h0 + e][2 * k2], pf[h0 + e][2 * k2 + 1]);
+                        tmem_st_x8(lrow + x + 16 * (h0 + e), pp);
                     }
-                    if (ps == 0) {
-                        if (!mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) ok = false;
-                        tc_fence_after();
-                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_ready);
+                if (!mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) ok = false;
+                tc_fence_after();
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps) {
+                    const int h0 = 2 * ps;
+                    uint32_t rd[2][16];
                     tmem_ld_x16(lrow + y + 16 * h0, rd[0]);
                     tmem_ld_x16(lrow + y + 16 * (h0 + 1), rd[1]);
                     tmem_wait_ld();
@@ -315,24 +332,22 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const uint32_t la = ldb + 4u * (kH + 2 * ps + e) * C::BQ + 4u * (c * kCH);
-                        uint32_t pp[8], pd[8];
+                        const uint32_t la = ldb + 4u * (kH + h0 + e) * C::BQ + 4u * (c * kCH);
+                        uint32_t pd[8];
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const uint4 dd = lds_u4(la + 16u * q4);
 #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int kk = 4 * q4 + 2 * u;
-                                const float2 p = make_float2(__uint_as_float(rs[e][kk]), __uint_as_float(rs[e][kk + 1]));
                                 const float2 dvv = u == 0 ? make_float2(__uint_as_float(dd.x), __uint_as_float(dd.y))
                                                           : make_float2(__uint_as_float(dd.z), __uint_as_float(dd.w));
                                 const float2 ds = __fmul2_rn(
-                                    p, fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
-                                pp[kk / 2] = pack_bf16x2(p.x, p.y);
+                                    make_float2(pf[h0 + e][kk], pf[h0 + e][kk + 1]),
+                                    fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
                                 pd[kk / 2] = pack_bf16x2(ds.x, ds.y);
                             }
                         }
-                        tmem_st_x8(lrow + x + 16 * (h0 + e), pp);
                         tmem_st_x8(lrow + x + 16 * (h0 + e) + 8, pd);
                     }
                 }
