@@ -58,6 +58,17 @@ __device__ __forceinline__ void fill_bias_table(float* Ts, const float* T, int n
     }
 }
 
+// Bias table of NH heads h_first .. h_first + NH - 1: 256 rows (every byte
+// code) of NH fp32 biases in base-2 units; codes >= nb get 0.
+template <int NH>
+__device__ __forceinline__ void fill_bias_table_heads(float* Ts, const float* T, int nb, int h_first,
+                                                      int tid, int nthreads) {
+    for (int x = tid; x < 256 * NH; x += nthreads) {
+        const int code = x / NH, h = h_first + x % NH;
+        Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
+    }
+}
+
 __device__ __forceinline__ void red_shared_add(uint32_t addr, float v) {
     asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
