@@ -189,8 +189,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
                 if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
                     return false;
-                if (tt >= 2 && !mbar_wait(&bars->dq_done[ss], ((tt >> 1) - 1) & 1, abort_flag, kWaitNs))
-                    return false;
+                // stage ss last held dS(tt - 2): the dq products that read it were issued
+                // before this point and the tensor pipe runs one thread's MMAs in order,
+                // so no wait is needed before overwriting it
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < kHC; ++h)
