@@ -77,12 +77,17 @@ struct KvCfg {
     static constexpr uint32_t OFF_V = OP_BYTES;
     static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
     static constexpr uint32_t OFF_T = OFF_STAGE + kQST * STAGE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
+    // per stage: one int per (16-row chunk, warp's 32 KV columns): the bucket code
+    // when all 512 codes of that block are equal, else -1
+    static constexpr int NMETA = NCH * 4;
+    static constexpr uint32_t OFF_META = OFF_T + 256 * kH * 4;
+    static constexpr uint32_t OFF_BAR = OFF_META + kQST * NMETA * 4;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 };
 
 struct Bars {
     uint64_t q_full[kQST];
+    uint64_t meta_ready[kQST];   // the stage's bucket summary is written (and its copies landed)
     uint64_t q_empty[kQST];
     uint64_t s_full;
     uint64_t dp_full;
@@ -117,6 +122,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (tid == kTmaWarp * 32) {
         for (int s = 0; s < kQST; ++s) {
             mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->meta_ready[s], 32);
             mbar_init(&bars->q_empty[s], kSoft + 1);
         }
         mbar_init(&bars->s_full, 1);
@@ -151,35 +157,69 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int b = 0; b < ntiles; ++b) {
-                const int ks = b & 1;
-                if (b >= kQST &&
-                    !mbar_wait(&bars->q_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+        // Issues the copies of Q tile b + 2 once tile b is consumed, and summarises
+        // each tile's bucket codes as soon as it lands (one tile ahead of the
+        // softmax): per (16-row chunk, 32-column warp block) the common code or -1.
+        int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
+        int issued = 0;
+        bool ok = true;
+        auto issue = [&](int b) -> bool {
+            const int ks = b & 1;
+            if (lane == 0) {
+                if (b >= kQST && !mbar_wait(&bars->q_empty[ks], ((b >> 1) - 1) & 1, abort_flag, kWaitNs)) {
                     fail(abort_flag, status);
-                    break;
-                }
-                uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                const int i0 = b * C::BQ;
-                mbar_arrive_expect_tx(&bars->q_full[ks], C::STAGE_BYTES);
-                tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
+                } else {
+                    uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
+                    const int i0 = b * C::BQ;
+                    mbar_arrive_expect_tx(&bars->q_full[ks], C::STAGE_BYTES);
+                    tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
 #pragma unroll
-                for (int s = 0; s < C::NSLOT; ++s) {
-                    tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapQ, 16 * (hb * C::NSLOT + s),
-                                i0, &bars->q_full[ks]);
-                    tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG,
-                                16 * (hb * C::NSLOT + s), i0, &bars->q_full[ks]);
+                    for (int s = 0; s < C::NSLOT; ++s) {
+                        tma_load_2d(st + C::SPD_BYTES + s * C::SLOT_BYTES, &mapQ, 16 * (hb * C::NSLOT + s),
+                                    i0, &bars->q_full[ks]);
+                        tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG,
+                                    16 * (hb * C::NSLOT + s), i0, &bars->q_full[ks]);
+                    }
+                    tma_load_2d(st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES, &mapL, i0, 0,
+                                &bars->q_full[ks]);
                 }
-                tma_load_2d(st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES, &mapL, i0, 0,
-                            &bars->q_full[ks]);
-                issued = b + 1;
             }
-            if (*(volatile int*)abort_flag) {
-                int never = 0;
-                for (int b = issued - kQST; b < issued; ++b)
-                    if (b >= 0) mbar_wait(&bars->q_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
+            __syncwarp();
+            if (*(volatile int*)abort_flag) return false;
+            issued = b + 1;
+            return true;
+        };
+        auto summarise = [&](int b) -> bool {
+            const int ks = b & 1;
+            if (!mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) {
+                fail(abort_flag, status);
+                return false;
             }
+            const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
+#pragma unroll 1
+            for (int sb = 0; sb < C::NMETA; ++sb) {
+                const int cc = sb >> 2, w = sb & 3;
+                // lane: row 16 cc + lane / 2, bytes 32 w + 16 (lane & 1) .. + 15
+                const uint4 v = lds_u4(st + (uint32_t)(16 * cc + (lane >> 1)) * kBKV + 32u * w + 16u * (lane & 1));
+                const uint32_t ref = __shfl_sync(0xffffffffu, v.x & 0xffu, 0) * 0x01010101u;
+                const bool same = v.x == ref && v.y == ref && v.z == ref && v.w == ref;
+                const bool all = __all_sync(0xffffffffu, same);
+                if (lane == 0) meta[ks * C::NMETA + sb] = all ? (int)(ref & 0xffu) : -1;
+            }
+            __syncwarp();
+            mbar_arrive(&bars->meta_ready[ks]);
+            return true;
+        };
+        for (int b = 0; ok && b < kQST && b < ntiles; ++b) ok = issue(b);
+        if (ok) ok = summarise(0);
+        for (int b = 0; ok && b < ntiles; ++b) {
+            if (b + 1 < ntiles && !summarise(b + 1)) { ok = false; break; }
+            if (b + kQST < ntiles && !issue(b + kQST)) { ok = false; break; }
+        }
+        if (!ok && lane == 0) {
+            int never = 0;
+            for (int b = issued - kQST; b < issued; ++b)
+                if (b >= 0) mbar_wait(&bars->q_full[b & 1], (b >> 1) & 1, &never, kWaitNs);
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
@@ -256,8 +296,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         bool ok = true;
         for (int b = 0; ok && b < ntiles; ++b) {
             const int ks = b & 1;
-            if (!mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            // (the summary is written after the tile's copies have landed)
+            if (!mbar_wait(&bars->meta_ready[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
+            const int* meta = reinterpret_cast<const int*>(smem + C::OFF_META) + ks * C::NMETA + (warp & 3);
             // LD rows of this group's first head: row h is 4 BQ bytes long
             const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (kHC * hb) * C::BQ;
             const int i0 = b * C::BQ;
@@ -266,10 +308,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t x = region(t, true), y = region(t, false);
-                // bucket codes of the 16 (i, j) pairs of this chunk: column r of the tile
+                // bucket codes of the 16 (i, j) pairs of this chunk: column r of the tile,
+                // unless the warp's whole 16 x 32 block holds one code
+                const int ucode = meta[4 * c];
                 uint32_t code[16];
+                float4 bu = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ucode >= 0) {
+                    bu = lds_f4(tbl + (uint32_t)ucode * 32u);
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
+                    for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
+                }
                 // P^T of all four heads first (S^T of a head pair is read before its P^T
                 // overwrites it), so the exponentials overlap the dP^T products still in
                 // the tensor pipe; then dS^T once dP^T has landed
@@ -282,11 +331,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tmem_ld_x16(lrow + x + 16 * (h0 + 1), rs[1]);
                     tmem_wait_ld();
                     // x = s scale log2e + b(code) - lse_i log2e
+                    if (ucode >= 0) {
+                        const float b0 = ps ? bu.z : bu.x, b1 = ps ? bu.w : bu.y;
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * ps);
-                        pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
-                        pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
+                        for (int kk = 0; kk < 16; ++kk) {
+                            pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
+                            pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * ps);
+                            pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
+                            pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
+                        }
                     }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
