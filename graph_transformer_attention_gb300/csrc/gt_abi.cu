@@ -31,7 +31,7 @@ bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
-                double* dT64, cudaStream_t s);
+                double* dT64, float* aux, cudaStream_t s);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -72,6 +72,7 @@ struct BwdWs {
     float* Dv;
     double* dT64;
     float* LD;
+    float* aux;     // [16]: per head the largest row norm of v (tensor-core path)
 };
 
 size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
@@ -94,6 +95,7 @@ size_t bwd_ws(int n, int h, int d, void* base, size_t cap, BwdWs* out) {
     w.dT64 = c.take<double>((size_t)h * 128);
     // per-node lse log2 e (rows 0..7) and D (rows 8..15) of the 8 heads, [16][ld_ld]
     w.LD = c.take<float>((size_t)16 * bwd_ld_ld(n));
+    w.aux = c.take<float>(16);
     if (out) *out = w;
     return c.off;
 }
@@ -177,7 +179,7 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.Dv, w.dT64, s);
+                               w.LD, w.Dv, w.dT64, w.aux, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

@@ -16,7 +16,12 @@
 //              bucket: in registers while the row's 16 codes are equal, else with
 //              shared-memory reductions into bins [code][head][NCP copies]; lane l
 //              adds into copy l mod NCP, so with NCP = 32 the 32 rows of a warp never
-//              meet on one address or bank, whatever their codes.
+//              meet on one address or bank, whatever their codes.  The bins hold
+//              fixed-point integers (a 32-bit shared-memory add is a single native
+//              operation, a float add is not): a row's dS values satisfy
+//              sum_j |dS_ij| <= |dO_i| max_j |v_j| + |D_i| (the P_ij of a row sum to
+//              1), so one power-of-two scale per CTA keeps every copy's sum below
+//              2^30; the copies are summed exactly in 64 bits at the end.
 //   warp 4     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
 //              K=16), then dq_h += dS_h K_h (A = dS from TMEM).
 //   warp 5     TMA producer: bucket tile and K / V column slots per KV block.
@@ -69,7 +74,7 @@ struct DqCfg {
     static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
     static constexpr uint32_t OFF_BIN = OFF_BAR + 256;
-    // bins: [nb][4 heads][ncp] fp32, sized at launch
+    // bins: [nb][4 heads][ncp] int32 fixed point, sized at launch
     static constexpr uint32_t smem_bytes(int nb, int ncp) { return OFF_BIN + (uint32_t)nb * kHC * ncp * 4 + 1024; }
 };
 constexpr uint32_t kSmemLimit = 232448;      // one CTA per SM
@@ -93,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
               const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD, int ldl,
+              const float* __restrict__ vmax,
               const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
               __nv_bfloat16* __restrict__ dq, double* __restrict__ dT64, int* status) {
     using C = DqCfg<HD>;
@@ -101,7 +107,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                                                ~uintptr_t(1023));
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
-    float* bins = reinterpret_cast<float*>(smem + C::OFF_BIN);
+    int* bins = reinterpret_cast<int*>(smem + C::OFF_BIN);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = blockIdx.x * kBQ;
     const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
@@ -129,7 +135,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
     if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
     fill_bias_table(Ts, T, nb, tid, kThreads);
-    for (int x = tid; x < nb * kHC * NCP; x += kThreads) bins[x] = 0.f;
+    for (int x = tid; x < nb * kHC * NCP; x += kThreads) bins[x] = 0;
     if (tid < kBQ) {
         const int row = i0 + tid;
         const bool live = row < n;
@@ -250,6 +256,42 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             L2[hh] = live ? LD[(int64_t)(kHC * hb + hh) * ldl + row] : 0.f;
             Dh[hh] = live ? LD[(int64_t)(kH + kHC * hb + hh) * ldl + row] : 0.f;
         }
+        // fixed-point scale of the dT bins: 2^e with (rows per copy) * max_i B_i * 2^e
+        // <= 2^30, B_i = |dO_i| max_j |v_j| + |D_i| bounding sum_j |dS_ij| (per head)
+        float bscale;
+        {
+            float bmax = 0.f;
+            if (live) {
+                const uint4* src = reinterpret_cast<const uint4*>(dO + ((int64_t)row * kH + kHC * hb) * HD);
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    float nn = 0.f;
+#pragma unroll
+                    for (int q8 = 0; q8 < HD / 8; ++q8) {
+                        const uint4 u = src[hh * (HD / 8) + q8];
+                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = __uint_as_float(wv[k] << 16), hi = __uint_as_float(wv[k] & 0xffff0000u);
+                            nn = fmaf(lo, lo, fmaf(hi, hi, nn));
+                        }
+                    }
+                    bmax = fmaxf(bmax, sqrtf(nn) * vmax[kHC * hb + hh] + fabsf(Dh[hh]));
+                }
+            }
+            for (int o = 16; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+            float* red = reinterpret_cast<float*>(smem + C::OFF_BAR + sizeof(Bars));
+            if (lane == 0) red[warp] = bmax;
+            asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory");
+            bmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+            const float bound = bmax * (float)(kBQ / NCP);
+            int e = 60;
+            if (bound > 0.f) e = (int)floorf(log2f(1073741824.f / bound));
+            if (!(bound < INFINITY) || e < 0) e = 0;
+            if (e > 60) e = 60;
+            bscale = exp2f((float)e);
+        }
+        auto fx = [&](float v) -> uint32_t { return (uint32_t)__float2int_rn(v * bscale); };
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int acc_code = -1;
         int t = 0;
@@ -277,7 +319,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (acc_code >= 0 && acc_code < nb) {
 #pragma unroll
                         for (int hh = 0; hh < 4; ++hh)
-                            red_shared_add(binb + acc_code * kCodeStride + hh * kHeadStride, acc[hh]);
+                            red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh]));
                     }
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) acc[hh] = 0.f;
@@ -346,8 +388,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             if (code < (uint32_t)nb) {
 #pragma unroll
                                 for (int hh = 0; hh < 4; ++hh)
-                                    red_shared_add(binb + code * kCodeStride + hh * kHeadStride,
-                                                   __uint_as_float(rd[hh][k]));
+                                    red_shared_add_u32(binb + code * kCodeStride + hh * kHeadStride,
+                                                       fx(__uint_as_float(rd[hh][k])));
                             }
                         }
                     }
@@ -362,7 +404,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         if (acc_code >= 0 && acc_code < nb) {
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh)
-                red_shared_add(binb + acc_code * kCodeStride + hh * kHeadStride, acc[hh]);
+                red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh]));
         }
         if (!ok) {
             fail(abort_flag, status);
@@ -396,12 +438,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         // add the copies of each (code, head) bin to the global table
         asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory");
         for (int x = tid; x < nb * kHC; x += kSoft) {
-            const float* cp = bins + (int64_t)x * NCP;
-            float s = 0.f;
+            const int* cp = bins + (int64_t)x * NCP;
+            long long s = 0;
 #pragma unroll 8
             for (int l = 0; l < NCP; ++l) s += cp[(l + tid) & (NCP - 1)];
             const int code = x / kHC, h = kHC * hb + x % kHC;
-            if (s != 0.f) atomicAdd(&dT64[h * nb + code], (double)s);
+            if (s != 0) atomicAdd(&dT64[h * nb + code], (double)s / (double)bscale);
         }
     }
     tc_fence_before();
@@ -414,8 +456,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, void* dq,
-           double* dT64, cudaStream_t s) {
+           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, const float* vmax,
+           void* dq, double* dT64, cudaStream_t s) {
     using C = DqCfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -440,7 +482,7 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         LaunchScope ls("bwd_dq", s);
         kern<<<grid, kThreads, smem, s>>>(
             mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-            ldl, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+            ldl, vmax, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
     }
     return check_launch();
 }
@@ -449,9 +491,9 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, void* dq, double* dT64, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s);
+                  const float* LD, int ldl, const float* vmax, void* dq, double* dT64, cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, dq, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, dq, dT64, s);
 }
 
 }  // namespace gt

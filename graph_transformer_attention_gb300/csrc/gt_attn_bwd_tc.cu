@@ -9,8 +9,9 @@
 // with dS = P (dO V^T - D) and D_i = <dO_i, o_i>.
 //
 // Kernels, in launch order:
-//   bwd_prep    D_i per head, and the table LD [16][ld] fp32: row h holds
-//               lse_i log2 e of head h, row 8 + h holds D_i (one column per node).
+//   bwd_prep    D_i per head, the table LD [16][ld] fp32 (row h holds lse_i log2 e
+//               of head h, row 8 + h holds D_i; one column per node) and per head
+//               the largest row norm of v (bounds the dT sums, see bwd_dq).
 //   bwd_dq      (gt_attn_bwd_dq.cu) Q-stationary: dq and dT.
 //   bwd_dkdv    (gt_attn_bwd_dkdv.cu) KV-stationary: dk and dv.
 //   dT_to_f32   the fp64 bucket sums to the fp32 output.
@@ -32,16 +33,31 @@ constexpr int kMaxNb = 128;
 
 template <typename TE>
 __global__ void bwd_prep(int n, int hd, int ldl, const TE* __restrict__ o, const TE* __restrict__ dO,
-                         const float* __restrict__ lse, float* __restrict__ LD,
-                         float* __restrict__ Dv) {
+                         const TE* __restrict__ v, const float* __restrict__ lse, float* __restrict__ LD,
+                         float* __restrict__ Dv, float* __restrict__ vmax) {
     const int64_t total = (int64_t)n * kH;
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
         const int h = (int)(x / n), i = (int)(x % n);
         const TE* a = o + ((int64_t)i * kH + h) * hd;
         const TE* b = dO + ((int64_t)i * kH + h) * hd;
-        float acc = 0.f;
-        for (int c = 0; c < hd; ++c) acc = fmaf(to_f32(a[c]), to_f32(b[c]), acc);
+        const TE* vv = v + ((int64_t)i * kH + h) * hd;
+        float acc = 0.f, vn = 0.f;
+        for (int c = 0; c < hd; ++c) {
+            acc = fmaf(to_f32(a[c]), to_f32(b[c]), acc);
+            vn = fmaf(to_f32(vv[c]), to_f32(vv[c]), vn);
+        }
+        // one atomic per warp when its lanes share the head (non-negative floats order
+        // like their bit patterns)
+        const unsigned act = __activemask();
+        const int h0 = __shfl_sync(act, h, __ffs(act) - 1);
+        float m = sqrtf(vn);
+        if (__all_sync(act, h == h0) && act == 0xffffffffu) {
+            for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
+            if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(vmax) + h, __float_as_int(m));
+        } else {
+            atomicMax(reinterpret_cast<int*>(vmax) + h, __float_as_int(m));
+        }
         LD[(int64_t)h * ldl + i] = lse[x] * kLog2e;
         LD[(int64_t)(kH + h) * ldl + i] = acc;
         Dv[x] = acc;
@@ -59,27 +75,29 @@ bool bwd_tc_supported(int h, int d, int nb) { return h == kH && (d == 8 || d == 
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, void* dq, double* dT64, cudaStream_t s);
+                  const float* LD, int ldl, const float* vmax, void* dq, double* dT64, cudaStream_t s);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
                     const float* LD, int ldl, void* dk, void* dv, cudaStream_t s);
 
 // Backward on the tensor cores.  Workspace: LD [16][bwd_ld_ld(n)] fp32,
-// Dv [8][n] fp32, dT64 [8][nb] fp64.
+// Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j| of head h).
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
-                double* dT64, cudaStream_t s) {
+                double* dT64, float* aux, cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
+    if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;
     const int64_t total = (int64_t)n * kH;
     const int pblocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     {
         LaunchScope ls("bwd_prep", s);
         bwd_prep<__nv_bfloat16><<<pblocks, 256, 0, s>>>(n, d, ldl, static_cast<const __nv_bfloat16*>(o),
-                                                        static_cast<const __nv_bfloat16*>(dO), lse, LD, Dv);
+                                                        static_cast<const __nv_bfloat16*>(dO),
+                                                        static_cast<const __nv_bfloat16*>(v), lse, LD, Dv, aux);
     }
-    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dq, dT64, s);
+    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, dq, dT64, s);
     if (rc != GT_OK) return rc;
     rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s);
     if (rc != GT_OK) return rc;
