@@ -25,6 +25,7 @@ namespace {
 constexpr int kRows = 128;   // rows (or columns) per thread block, one per thread
 constexpr int kTile = 64;    // streamed tile of the other dimension
 constexpr int kCodes = 256;  // every byte value has a table slot
+constexpr int kHCopies = 8;  // copies of each dT bin (see bwd_rows_simt)
 
 template <typename TE, int DP>
 __device__ __forceinline__ void load_vec(const TE* __restrict__ src, int d, float scale, float* dst) {
@@ -140,13 +141,13 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
     __shared__ float sK[kTile][DP];
     __shared__ float sV[kTile][DP];
     __shared__ float sT[kCodes];
-    __shared__ float sH[kCodes];
+    // dT sums: kHCopies copies per code, lane l adding into copy l % kHCopies, so
+    // rows of a warp that share a code do not all contend for one address
+    __shared__ float sH[kCodes][kHCopies];
     const int head = blockIdx.y;
     const int i = blockIdx.x * kRows + threadIdx.x;
-    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) {
-        sT[c] = c < nb ? T[head * nb + c] : 0.f;
-        sH[c] = 0.f;
-    }
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
+    for (int c = threadIdx.x; c < kCodes * kHCopies; c += blockDim.x) (&sH[0][0])[c] = 0.f;
     const bool live = i < n;
     const int ii = live ? i : 0;
     float qi[DP], gi[DP], acc[DP];
@@ -178,7 +179,7 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
             const float ds = p * (dp - Di);
 #pragma unroll
             for (int c = 0; c < DP; ++c) acc[c] = fmaf(ds, sK[jj][c], acc[c]);
-            atomicAdd(&sH[code], ds);
+            atomicAdd(&sH[code][threadIdx.x % kHCopies], ds);
         }
     }
     if (live) {
@@ -188,8 +189,12 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
             if (c < d) out[c] = from_f32<TE>(acc[c] * scale);
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < nb; c += blockDim.x)
-        if (sH[c] != 0.f) atomicAdd(&dT64[head * nb + c], (double)sH[c]);
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+        double sum = 0.0;
+#pragma unroll
+        for (int k = 0; k < kHCopies; ++k) sum += sH[c][k];
+        if (sum != 0.0) atomicAdd(&dT64[head * nb + c], sum);
+    }
 }
 
 // Column pass: dk_j, dv_j.  grid = (ceil(n/128), h); block = 128.
