@@ -361,11 +361,17 @@ bfs32_smem(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indic
                     heavy[atomicAdd(&s_hlen, 1)] = qi;
                     continue;
                 }
-                for (int64_t e = e0; e < e1; ++e) {
-                    const int v = indices[e];
-                    bool fresh = false;
-                    if ((unsigned)v < (unsigned)n) fresh = atomicOr(&acc[v], w) == 0u;
-                    warp_append(fresh, &s_clen, st.cand, v);
+                // four neighbour loads in flight at a time, then their pushes
+                for (int64_t e = e0; e < e1; e += 4) {
+                    int vv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) vv[k] = e + k < e1 ? __ldg(indices + e + k) : -1;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        bool fresh = false;
+                        if ((unsigned)vv[k] < (unsigned)n) fresh = atomicOr(&acc[vv[k]], w) == 0u;
+                        warp_append(fresh, &s_clen, st.cand, vv[k]);
+                    }
                 }
             }
             __syncthreads();
