@@ -138,6 +138,37 @@ def test_all_unreachable_and_single_bucket(gt, dtype):
     assert np.all(got["dT"][:, np.arange(D + 2) != 3] == 0.0)
 
 
+@pytest.mark.parametrize("d,mag", [(8, 40.0), (16, 40.0), (16, 1e-3)])
+def test_dT_fixed_point_scale_extremes(gt, d, mag):
+    """The bf16 backward sums dT in fixed point with a per-CTA scale derived from
+    |dO_i| max_j |v_j| + |D_i|.  Large dO and v (dS of hundreds) must not
+    overflow; tiny ones must keep their relative accuracy.  Random codes send
+    every chunk through the per-element bins."""
+    n, h, nb = 520, 8, 30
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=31 + d)
+    x["dO"] = gi.round_to_bf16((x["dO"] * mag).astype(np.float32))
+    x["v"] = gi.round_to_bf16((x["v"] * (mag if mag > 1 else 1.0)).astype(np.float32))
+    spd = np.random.default_rng(32).integers(0, nb, size=(n, n)).astype(np.int8)
+    got = _run_gpu(gt, x, spd, "bf16")
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, "bf16")
+
+
+def test_components_not_aligned_to_tiles(gt):
+    """Disjoint graphs of 40 nodes: the 16 x 32 blocks of the bucket matrix mix
+    uniform blocks (pairs in other components, one code) with blocks that cut a
+    component's diagonal block, so both the per-block and per-element paths of
+    the backward run in one launch."""
+    n_comp, size = 25, 40
+    g = gi.disjoint_ba(n_comp, size, 2, seed=41)
+    n, h, d, D = n_comp * size, 8, 16, 12
+    spd = O.spd(n, g.indptr, g.indices, D)
+    x = gi.make_layer_tensors(n, h, d, D + 2, "bf16", seed=42)
+    got = _run_gpu(gt, x, spd, "bf16")
+    ref = O.attn_fwd_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"])
+    _compare_full(got, ref, "bf16")
+
+
 def test_kv_block_matches_single_pass(gt):
     n, h, d, nb = 1100, 8, 8, 34
     x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=8)
