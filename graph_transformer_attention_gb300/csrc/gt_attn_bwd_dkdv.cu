@@ -196,15 +196,26 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 return false;
             }
             const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
+            // per 16-row chunk: lane l checks 16-byte piece l & 7 of rows 4u + l / 8
+            // (u = 0..3), so the eight lanes of a row cover all 32 banks; a warp
+            // block w owns pieces 2w, 2w + 1 of every row
+            const uint32_t piece = (uint32_t)(lane & 7), rsub = (uint32_t)(lane >> 3);
 #pragma unroll 1
-            for (int sb = 0; sb < C::NMETA; ++sb) {
-                const int cc = sb >> 2, w = sb & 3;
-                // lane: row 16 cc + lane / 2, bytes 32 w + 16 (lane & 1) .. + 15
-                const uint4 v = lds_u4(st + (uint32_t)(16 * cc + (lane >> 1)) * kBKV + 32u * w + 16u * (lane & 1));
-                const uint32_t ref = __shfl_sync(0xffffffffu, v.x & 0xffu, 0) * 0x01010101u;
-                const bool same = v.x == ref && v.y == ref && v.z == ref && v.w == ref;
-                const bool all = __all_sync(0xffffffffu, same);
-                if (lane == 0) meta[ks * C::NMETA + sb] = all ? (int)(ref & 0xffu) : -1;
+            for (int cc = 0; cc < C::NCH; ++cc) {
+                const uint32_t row0 = st + (uint32_t)(16 * cc) * kBKV;
+                const uint32_t ref = lds_u8(row0 + 32u * (piece >> 1)) * 0x01010101u;
+                bool same = true;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 v = lds_u4(row0 + (4u * u + rsub) * kBKV + 16u * piece);
+                    same = same && v.x == ref && v.y == ref && v.z == ref && v.w == ref;
+                }
+                const unsigned bal = __ballot_sync(0xffffffffu, same);
+                const uint32_t wref = __shfl_sync(0xffffffffu, ref, 2 * (lane & 3));
+                if (lane < 4) {
+                    const unsigned mask = 0x03030303u << (2 * lane);
+                    meta[ks * C::NMETA + 4 * cc + lane] = (bal & mask) == mask ? (int)(wref & 0xffu) : -1;
+                }
             }
             __syncwarp();
             mbar_arrive(&bars->meta_ready[ks]);
