@@ -86,6 +86,11 @@ def load_library():
         lib.gt_bias_attn_bwd.restype = ctypes.c_int
         lib.gt_check_device_status.argtypes = [P]
         lib.gt_check_device_status.restype = ctypes.c_int
+        lib.gt_bias_attn_fwd_partial.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
+                                                 i32, P, P, P]
+        lib.gt_bias_attn_fwd_partial.restype = ctypes.c_int
+        lib.gt_bias_attn_merge.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P]
+        lib.gt_bias_attn_merge.restype = ctypes.c_int
         lib.gt_kernel_stats_reset.argtypes = [i32]
         lib.gt_kernel_stats_reset.restype = ctypes.c_int
         lib.gt_kernel_stats_read.argtypes = [ctypes.POINTER(KernelStat), i32, ctypes.POINTER(i32)]
@@ -192,6 +197,43 @@ def gt_bias_attn_fwd(q, k, v, spd, T, scale: float | None = None, kv_block: int 
                               _ptr(T), T.shape[1], float(scale), kv_block, _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check("gt_bias_attn_fwd", rc)
+    return out, lse
+
+
+def gt_bias_attn_fwd_partial(q, k, v, spd, T, kv_begin: int, kv_end: int, scale: float | None = None,
+                             o_part=None, lse_part=None, stream=None):
+    """Forward over the KV columns [kv_begin, kv_end) only: fp32 o_part [n][h][d]
+    (normalised over those columns) and lse_part [h][n]."""
+    lib = load_library()
+    _need_cuda(q, k, v, spd, T)
+    n, h, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o_part is None:
+        o_part = torch.empty((n, h, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((h, n), dtype=torch.float32, device=q.device)
+    _need_cuda(o_part, lse_part)
+    rc = lib.gt_bias_attn_fwd_partial(_dtype_code(q), n, h, d, _ptr(q), _ptr(k), _ptr(v), _ptr(spd),
+                                      spd.stride(0), _ptr(T), T.shape[1], float(scale), kv_begin, kv_end,
+                                      _ptr(o_part), _ptr(lse_part), _stream_handle(stream))
+    _check("gt_bias_attn_fwd_partial", rc)
+    return o_part, lse_part
+
+
+def gt_bias_attn_merge(o_parts, lse_parts, dtype=torch.bfloat16, out=None, lse=None, stream=None):
+    """Exact merge of partials: o_parts fp32 [p][n][h][d], lse_parts fp32 [p][h][n]."""
+    lib = load_library()
+    _need_cuda(o_parts, lse_parts)
+    nparts, n, h, d = o_parts.shape
+    if out is None:
+        out = torch.empty((n, h, d), dtype=dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((h, n), dtype=torch.float32, device=o_parts.device)
+    _need_cuda(out, lse)
+    rc = lib.gt_bias_attn_merge(_dtype_code(out), n, h, d, nparts, _ptr(o_parts), _ptr(lse_parts),
+                                _ptr(out), _ptr(lse), _stream_handle(stream))
+    _check("gt_bias_attn_merge", rc)
     return out, lse
 
 

@@ -23,6 +23,14 @@ bool fwd_tc_supported(int h, int d);
 int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
                 int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
                 float* o_part, float* lse_part, cudaStream_t s);
+int attn_fwd_tc_range(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
+                      int64_t ld, const float* T, int nb, float scale, int kv_begin, int kv_end,
+                      float* o_part, float* lse_part, cudaStream_t s);
+int attn_fwd_simt_range(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                        const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                        int kv_begin, int kv_end, float* o_part, float* lse_part, cudaStream_t s);
+int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
+                   const float* lse_part, void* o, float* lse, cudaStream_t s);
 int attn_bwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                   const void* o, const void* dO, const float* lse, const int8_t* spd, int64_t ld,
                   const float* T, int nb, float scale, void* dq, void* dk, void* dv, float* dT,
@@ -159,6 +167,31 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
                                w.lse_part, s);
     return gt::attn_fwd_simt(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb, scale, kv_block, o, lse,
                              w.o_part, w.lse_part, s);
+}
+
+int gt_bias_attn_fwd_partial(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q,
+                             const void* k, const void* v, const int8_t* spd, int64_t ld_spd,
+                             const float* T, int32_t nb, float scale, int32_t kv_begin,
+                             int32_t kv_end, float* o_part, float* lse_part, void* stream) {
+    int rc = gt::check_common(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb);
+    if (rc != GT_OK) return rc;
+    if (!o_part || !lse_part || !gt::aligned16(o_part)) return GT_ERR_INVALID_ARG;
+    if (kv_begin < 0 || kv_begin % 128 != 0 || kv_end <= kv_begin || kv_end > n) return GT_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GT_BF16 && gt::fwd_tc_supported(h, d))
+        return gt::attn_fwd_tc_range(n, d, q, k, v, spd, ld_spd, T, nb, scale, kv_begin, kv_end, o_part,
+                                     lse_part, s);
+    return gt::attn_fwd_simt_range(dtype, n, h, d, q, k, v, spd, ld_spd, T, nb, scale, kv_begin, kv_end,
+                                   o_part, lse_part, s);
+}
+
+int gt_bias_attn_merge(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nparts,
+                       const float* o_parts, const float* lse_parts, void* o, float* lse, void* stream) {
+    if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || nparts < 1) return GT_ERR_INVALID_ARG;
+    if (h > 16 || d > 64) return GT_ERR_UNSUPPORTED;
+    if (!o_parts || !lse_parts || !o || !lse) return GT_ERR_INVALID_ARG;
+    return gt::merge_partials(dtype, n, h, d, nparts, o_parts, lse_parts, o, lse,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,

@@ -165,8 +165,9 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const __grid_constant__ CUtensorMap mapS, const __nv_bfloat16* __restrict__ q,
-              const float* __restrict__ T, int nb, int n, float scale_log2, int kv_block,
-              __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float* __restrict__ o_part,
+              const float* __restrict__ T, int nb, int n, float scale_log2, int kv_begin, int kv_end,
+              int kv_block, int parts, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+              float* __restrict__ o_part,
               float* __restrict__ lse_part, int* status) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -178,8 +179,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const int i0 = blockIdx.x * kBQ;
     const int split = blockIdx.y;
     const int hb = blockIdx.z;                 // heads kHC hb .. kHC hb + kHC - 1
-    const int j_begin = kv_block > 0 ? split * kv_block : 0;
-    const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
+    // KV columns [kv_begin, kv_end), cut into grid.y splits of kv_block columns
+    const int j_begin = kv_begin + (kv_block > 0 ? split * kv_block : 0);
+    const int j_end = kv_block > 0 ? min(kv_end, j_begin + kv_block) : kv_end;
     const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
     const int nchunks = nblocks * kNCH;
 
@@ -446,7 +448,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     const float inv = 1.f / l[hh];
                     const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
                     if (live) {
-                        if (gridDim.y == 1) {
+                        if (!parts) {
                             uint32_t w[HD / 2];
 #pragma unroll
                             for (int k = 0; k < HD / 2; ++k)
@@ -489,8 +491,8 @@ namespace {
 
 template <int HD>
 int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8_t* spd, int64_t ld,
-                  const float* T, int nb, float scale, int kv_block, void* o, float* lse,
-                  float* o_part, float* lse_part, cudaStream_t s) {
+                  const float* T, int nb, float scale, int kv_begin, int kv_end, int kv_block, int parts,
+                  void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s) {
     using C = Cfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -506,13 +508,14 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
         return GT_ERR_CUDA;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
-    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    const int nsplit = kv_block > 0 ? (kv_end - kv_begin + kv_block - 1) / kv_block : 1;
     dim3 grid((n + kBQ - 1) / kBQ, nsplit, kH / kHC);
     {
         LaunchScope ls("fwd_tc", s);
         fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-            mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e,
-            nsplit > 1 ? kv_block : 0, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, status);
+            mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e, kv_begin, kv_end,
+            nsplit > 1 ? kv_block : 0, parts, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part,
+            status);
     }
     return check_launch();
 }
@@ -528,12 +531,24 @@ int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const
                 int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
                 float* o_part, float* lse_part, cudaStream_t s) {
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
-    int rc = d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part,
-                                       lse_part, s)
-                    : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part,
-                                        lse_part, s);
+    const int parts = nsplit > 1;
+    int rc = d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, o, lse,
+                                       o_part, lse_part, s)
+                    : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, o, lse,
+                                        o_part, lse_part, s);
     if (rc != GT_OK || nsplit == 1) return rc;
     return merge_partials(GT_BF16, n, kH, d, nsplit, o_part, lse_part, o, lse, s);
+}
+
+// Attention of every query row over the KV columns [kv_begin, kv_end) only:
+// o_part [n][8][d] fp32 (normalised over those columns) and lse_part [8][n].
+int attn_fwd_tc_range(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
+                      int64_t ld, const float* T, int nb, float scale, int kv_begin, int kv_end,
+                      float* o_part, float* lse_part, cudaStream_t s) {
+    return d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, nullptr,
+                                     nullptr, o_part, lse_part, s)
+                  : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, nullptr,
+                                      nullptr, o_part, lse_part, s);
 }
 
 }  // namespace gt

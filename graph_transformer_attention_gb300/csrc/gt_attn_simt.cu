@@ -44,15 +44,16 @@ __device__ __forceinline__ void stage_tile(float (*dst)[DP], const TE* __restric
     }
 }
 
-// Forward.  grid = (ceil(n/128), h, nsplit); block = 128.
-// nsplit == 1: writes o (TE) and lse.  Otherwise writes fp32 partials
+// Forward over the KV columns [kv_begin, kv_end), cut into nsplit splits of
+// kv_block columns.  grid = (ceil(n/128), h, nsplit); block = 128.
+// parts == 0: writes o (TE) and lse.  Otherwise writes fp32 partials
 // o_part[z][n][h][d] and lse_part[z][h][n] for the KV columns of split z.
 template <typename TE, int DP>
 __global__ void __launch_bounds__(kRows)
 fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
          const TE* __restrict__ v, const uint8_t* __restrict__ spd, int64_t ld,
-         const float* __restrict__ T, int nb, float scale, int kv_block,
-         TE* __restrict__ o, float* __restrict__ lse, float* __restrict__ o_part,
+         const float* __restrict__ T, int nb, float scale, int kv_begin, int kv_end, int kv_block,
+         int parts, TE* __restrict__ o, float* __restrict__ lse, float* __restrict__ o_part,
          float* __restrict__ lse_part) {
     __shared__ float sK[kTile][DP];
     __shared__ float sV[kTile][DP];
@@ -60,8 +61,8 @@ fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k
     const int head = blockIdx.y;
     const int i = blockIdx.x * kRows + threadIdx.x;
     const int split = blockIdx.z;
-    const int j_begin = kv_block > 0 ? split * kv_block : 0;
-    const int j_end = kv_block > 0 ? min(n, j_begin + kv_block) : n;
+    const int j_begin = kv_begin + (kv_block > 0 ? split * kv_block : 0);
+    const int j_end = kv_block > 0 ? min(kv_end, j_begin + kv_block) : kv_end;
     for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
 
     float qi[DP], acc[DP];
@@ -99,7 +100,7 @@ fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k
     }
     if (!live) return;
     const float inv = 1.f / l;
-    if (gridDim.z == 1) {
+    if (!parts) {
         TE* oi = o + ((int64_t)i * h + head) * d;
 #pragma unroll
         for (int c = 0; c < DP; ++c)
@@ -307,22 +308,16 @@ int grid_for(int64_t total) {
 template <typename TE, int DP>
 int fwd_simt_launch(int n, int h, int d, const void* q, const void* k, const void* v,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    int kv_block, void* o, float* lse, float* o_part, float* lse_part,
-                    cudaStream_t s) {
-    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+                    int kv_begin, int kv_end, int kv_block, int parts, void* o, float* lse,
+                    float* o_part, float* lse_part, cudaStream_t s) {
+    const int nsplit = kv_block > 0 ? (kv_end - kv_begin + kv_block - 1) / kv_block : 1;
     dim3 grid((n + kRows - 1) / kRows, h, nsplit);
     {
         LaunchScope ls("fwd_simt", s);
         fwd_simt<TE, DP><<<grid, kRows, 0, s>>>(
             n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld, T, nb, scale,
-            nsplit > 1 ? kv_block : 0, (TE*)o, lse, o_part, lse_part);
+            kv_begin, kv_end, nsplit > 1 ? kv_block : 0, parts, (TE*)o, lse, o_part, lse_part);
     }
-    if (nsplit > 1)
-        {
-            LaunchScope ls("fwd_merge", s);
-            merge_splits<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, nsplit, o_part, lse_part,
-                                                                      (TE*)o, lse);
-        }
     return check_launch();
 }
 
@@ -359,12 +354,15 @@ int bwd_simt_launch(int n, int h, int d, const void* q, const void* k, const voi
 template <typename TE>
 int fwd_simt_dispatch(int n, int h, int d, const void* q, const void* k, const void* v,
                       const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                      int kv_block, void* o, float* lse, float* o_part, float* lse_part,
-                      cudaStream_t s) {
-    if (d <= 8) return fwd_simt_launch<TE, 8>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
-    if (d <= 16) return fwd_simt_launch<TE, 16>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
-    if (d <= 32) return fwd_simt_launch<TE, 32>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
-    return fwd_simt_launch<TE, 64>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+                      int kv_begin, int kv_end, int kv_block, int parts, void* o, float* lse,
+                      float* o_part, float* lse_part, cudaStream_t s) {
+#define GT_FWD_SIMT(DP) fwd_simt_launch<TE, DP>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, \
+                                                kv_block, parts, o, lse, o_part, lse_part, s)
+    if (d <= 8) return GT_FWD_SIMT(8);
+    if (d <= 16) return GT_FWD_SIMT(16);
+    if (d <= 32) return GT_FWD_SIMT(32);
+    return GT_FWD_SIMT(64);
+#undef GT_FWD_SIMT
 }
 
 template <typename TE>
@@ -380,12 +378,32 @@ int bwd_simt_dispatch(int n, int h, int d, const void* q, const void* k, const v
 
 }  // namespace
 
+int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
+                   const float* lse_part, void* o, float* lse, cudaStream_t s);
+
 int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
                   void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s) {
+    const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
+    const int parts = nsplit > 1;
+    const int rc = dtype == GT_F32
+        ? fwd_simt_dispatch<float>(n, h, d, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, o, lse,
+                                   o_part, lse_part, s)
+        : fwd_simt_dispatch<__nv_bfloat16>(n, h, d, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts,
+                                           o, lse, o_part, lse_part, s);
+    if (rc != GT_OK || !parts) return rc;
+    return merge_partials(dtype, n, h, d, nsplit, o_part, lse_part, o, lse, s);
+}
+
+// Attention over the KV columns [kv_begin, kv_end) only (see attn_fwd_tc_range).
+int attn_fwd_simt_range(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
+                        const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
+                        int kv_begin, int kv_end, float* o_part, float* lse_part, cudaStream_t s) {
     if (dtype == GT_F32)
-        return fwd_simt_dispatch<float>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
-    return fwd_simt_dispatch<__nv_bfloat16>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_block, o, lse, o_part, lse_part, s);
+        return fwd_simt_dispatch<float>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1,
+                                        nullptr, nullptr, o_part, lse_part, s);
+    return fwd_simt_dispatch<__nv_bfloat16>(n, h, d, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1,
+                                            nullptr, nullptr, o_part, lse_part, s);
 }
 
 int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,

@@ -115,6 +115,42 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
                      void* o, float* lse, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The forward over one range of KV columns, and the exact merge of such
+ * partials: Fig. 4's ring step on one GPU.  A caller that holds KV blocks
+ * [a_0, a_1), [a_1, a_2), ... in turn (a ring across GPUs, or blocks streamed
+ * from host memory) computes each block's partial with gt_bias_attn_fwd_partial
+ * and combines them with gt_bias_attn_merge; the result equals
+ * gt_bias_attn_fwd over all columns up to rounding.
+ *
+ * gt_bias_attn_fwd_partial: every query row attends only to KV columns
+ * [kv_begin, kv_end), with the bias columns of that range.
+ *   q, k, v, spd, ld_spd, T, nb, scale: as for gt_bias_attn_fwd (k and v hold
+ *            all n rows; only the range's rows are read).
+ *   kv_begin a multiple of 128, 0 <= kv_begin < kv_end <= n.
+ *   o_part   device fp32 [n][h][d] (output, 16-byte aligned): the output
+ *            normalised over the range's columns.
+ *   lse_part device fp32 [h][n] (output): log of the range's softmax
+ *            denominator (natural log, scores include the bias).
+ * Needs no workspace.  Errors as for gt_bias_attn_fwd, plus GT_ERR_INVALID_ARG
+ * for a bad range.
+ *
+ * gt_bias_attn_merge: o = sum_p exp(lse_p - lse) o_p with lse = log sum_p
+ * exp(lse_p), per (node, head).
+ *   o_parts  device fp32 [nparts][n][h][d]; lse_parts device fp32 [nparts][h][n].
+ *   o        device [n][h][d] of `dtype` (output); lse device fp32 [h][n].
+ * Errors: GT_ERR_INVALID_ARG for NULL pointers, n, h, d or nparts < 1;
+ * GT_ERR_UNSUPPORTED for h > 16 or d > 64.
+ */
+int gt_bias_attn_fwd_partial(int32_t dtype, int32_t n, int32_t h, int32_t d,
+                             const void* q, const void* k, const void* v,
+                             const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                             float scale, int32_t kv_begin, int32_t kv_end,
+                             float* o_part, float* lse_part, void* stream);
+int gt_bias_attn_merge(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nparts,
+                       const float* o_parts, const float* lse_parts, void* o, float* lse,
+                       void* stream);
+
+/*
  * gt_bias_attn_bwd: gradients of sum(o * dO) with respect to q, k, v and T.
  *   o, lse   the forward's outputs for the same inputs.
  *   dO       device [n][h][d] of `dtype`, the upstream gradient.

@@ -107,3 +107,18 @@ def test_kernel_stats_table_on_host(lib):
     # nothing launched since the reset: an empty table, no CUDA call needed
     gt.gt_kernel_stats_reset(False)
     assert gt.gt_kernel_stats() == {}
+
+
+def test_partial_and_merge_reject_bad_ranges(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    f32p = ctypes.c_float
+    # kv_begin not a multiple of 128, empty range, range past n, NULL outputs
+    for kb, ke in ((64, 300), (128, 128), (0, 301), (-128, 10)):
+        assert lib.gt_bias_attn_fwd_partial(1, 300, 8, 16, fake, fake, fake, fake, 304, fake, 18,
+                                            f32p(0.25), kb, ke, fake, fake, None) == -1
+    assert lib.gt_bias_attn_fwd_partial(1, 300, 8, 16, fake, fake, fake, fake, 304, fake, 18,
+                                        f32p(0.25), 0, 300, None, fake, None) == -1
+    assert lib.gt_bias_attn_merge(1, 300, 8, 16, 0, fake, fake, fake, fake, None) == -1
+    assert lib.gt_bias_attn_merge(1, 300, 8, 128, 2, fake, fake, fake, fake, None) == -2
+    assert lib.gt_bias_attn_merge(1, 300, 8, 16, 2, None, fake, fake, fake, None) == -1
