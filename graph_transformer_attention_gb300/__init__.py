@@ -27,10 +27,13 @@ __all__ = [
     "GtError", "load_library", "library_path", "gt_spd_build", "gt_bias_attn_fwd",
     "gt_bias_attn_bwd", "gt_spd_workspace_size", "gt_bias_attn_workspace_size",
     "gt_check_device_status", "gt_status_string", "spd_ld", "GT_F32", "GT_BF16",
+    "GT_SPD_AUTO", "GT_SPD_SCAN32", "GT_SPD_SCAN16", "GT_SPD_QUEUE32", "GT_SPD_GLOBAL64",
 ]
 
 GT_F32 = 0
 GT_BF16 = 1
+# search algorithms of gt_spd_build (include/gt_attn.h)
+GT_SPD_AUTO, GT_SPD_SCAN32, GT_SPD_SCAN16, GT_SPD_QUEUE32, GT_SPD_GLOBAL64 = 0, 1, 2, 3, 4
 GT_OK = 0
 _STATUS = {0: "GT_OK", -1: "GT_ERR_INVALID_ARG", -2: "GT_ERR_UNSUPPORTED", -3: "GT_ERR_CUDA",
            -4: "GT_ERR_TIMEOUT", -5: "GT_ERR_WORKSPACE"}
@@ -76,6 +79,10 @@ def load_library():
         lib.gt_spd_workspace_size.restype = sz
         lib.gt_spd_build.argtypes = [P, P, i32, i64, i32, P, i64, P, sz, P]
         lib.gt_spd_build.restype = ctypes.c_int
+        lib.gt_spd_workspace_size_algo.argtypes = [i32, i32, i64, i32]
+        lib.gt_spd_workspace_size_algo.restype = sz
+        lib.gt_spd_build_algo.argtypes = [i32, P, P, i32, i64, i32, P, i64, P, sz, P]
+        lib.gt_spd_build_algo.restype = ctypes.c_int
         lib.gt_bias_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_workspace_size.restype = sz
         lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
@@ -148,8 +155,9 @@ def gt_status_string(status: int) -> str:
     return load_library().gt_status_string(status).decode()
 
 
-def gt_spd_workspace_size(n: int, nnz: int, D: int) -> int:
-    return int(load_library().gt_spd_workspace_size(n, nnz, D))
+def gt_spd_workspace_size(n: int, nnz: int, D: int, algo: int = 0) -> int:
+    """Workspace bytes of gt_spd_build (0 when `algo` cannot take n vertices here)."""
+    return int(load_library().gt_spd_workspace_size_algo(algo, n, nnz, D))
 
 
 def gt_bias_attn_workspace_size(dtype: int, n: int, h: int, d: int, kv_block: int = 0) -> int:
@@ -162,8 +170,10 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 def gt_spd_build(indptr: torch.Tensor, indices: torch.Tensor, n: int, D: int,
                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                 stream=None) -> torch.Tensor:
-    """Clipped shortest-path bucket matrix, int8 [n][spd_ld(n)] (columns >= n unspecified)."""
+                 stream=None, algo: int = 0) -> torch.Tensor:
+    """Clipped shortest-path bucket matrix, int8 [n][spd_ld(n)] (columns >= n unspecified).
+
+    `algo` picks the search (GT_SPD_*; 0 = the first that fits the device)."""
     lib = load_library()
     _need_cuda(indptr, indices)
     if indptr.dtype != torch.int64 or indices.dtype != torch.int32:
@@ -171,9 +181,12 @@ def gt_spd_build(indptr: torch.Tensor, indices: torch.Tensor, n: int, D: int,
     if out is None:
         out = torch.empty((n, spd_ld(n)), dtype=torch.int8, device=indptr.device)
     if workspace is None:
-        workspace = _workspace(lib.gt_spd_workspace_size(n, indices.numel(), D), indptr.device)
-    rc = lib.gt_spd_build(_ptr(indptr), _ptr(indices), n, indices.numel(), D, _ptr(out),
-                          out.stride(0), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+        need = lib.gt_spd_workspace_size_algo(algo, n, indices.numel(), D)
+        if need == 0:
+            raise GtError("gt_spd_build", -2)      # the algorithm cannot take n vertices here
+        workspace = _workspace(need, indptr.device)
+    rc = lib.gt_spd_build_algo(algo, _ptr(indptr), _ptr(indices), n, indices.numel(), D, _ptr(out),
+                               out.stride(0), _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check("gt_spd_build", rc)
     return out
 

@@ -13,9 +13,9 @@ __device__ int g_gt_status = 0;
 namespace gt {
 
 // implemented in the kernel files
-size_t spd_workspace_bytes(int32_t n, int32_t D);
-int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t D, int8_t* spd,
-              int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t spd_workspace_bytes(int32_t n, int64_t nnz, int32_t D, int algo);
+int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t nnz, int32_t D,
+              int8_t* spd, int64_t ld, void* ws, size_t ws_bytes, int algo, cudaStream_t stream);
 int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
                   void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s);
@@ -125,20 +125,33 @@ const char* gt_status_string(int status) {
     }
 }
 
+size_t gt_spd_workspace_size_algo(int32_t algo, int32_t n, int64_t nnz, int32_t D) {
+    if (n < 1 || nnz < 0 || D < 1 || D > GT_MAX_D) return 0;
+    return gt::spd_workspace_bytes(n, nnz, D, algo);
+}
+
 size_t gt_spd_workspace_size(int32_t n, int64_t nnz, int32_t D) {
-    (void)nnz;
-    if (n < 1 || D < 1 || D > GT_MAX_D) return 0;
-    return gt::spd_workspace_bytes(n, D);
+    return gt_spd_workspace_size_algo(GT_SPD_AUTO, n, nnz, D);
+}
+
+int gt_spd_build_algo(int32_t algo, const int64_t* indptr, const int32_t* indices, int32_t n,
+                      int64_t nnz, int32_t D, int8_t* spd, int64_t ld_spd, void* workspace,
+                      size_t ws_bytes, void* stream) {
+    if (!indptr || !spd || n < 1 || nnz < 0 || D < 1 || D > GT_MAX_D) return GT_ERR_INVALID_ARG;
+    if (nnz > 0 && !indices) return GT_ERR_INVALID_ARG;
+    if (ld_spd < n || (ld_spd % 16) != 0 || !gt::aligned16(spd)) return GT_ERR_INVALID_ARG;
+    if (algo < GT_SPD_AUTO || algo > GT_SPD_GLOBAL64) return GT_ERR_INVALID_ARG;
+    const size_t need = gt::spd_workspace_bytes(n, nnz, D, algo);
+    if (need == 0) return GT_ERR_UNSUPPORTED;
+    if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
+    return gt::spd_build(indptr, indices, n, nnz, D, spd, ld_spd, workspace, ws_bytes, algo,
+                         static_cast<cudaStream_t>(stream));
 }
 
 int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t nnz, int32_t D,
                  int8_t* spd, int64_t ld_spd, void* workspace, size_t ws_bytes, void* stream) {
-    if (!indptr || !spd || n < 1 || nnz < 0 || D < 1 || D > GT_MAX_D) return GT_ERR_INVALID_ARG;
-    if (nnz > 0 && !indices) return GT_ERR_INVALID_ARG;
-    if (ld_spd < n || (ld_spd % 16) != 0 || !gt::aligned16(spd)) return GT_ERR_INVALID_ARG;
-    if (!workspace || ws_bytes < gt::spd_workspace_bytes(n, D)) return GT_ERR_WORKSPACE;
-    return gt::spd_build(indptr, indices, n, D, spd, ld_spd, workspace, ws_bytes,
-                         static_cast<cudaStream_t>(stream));
+    return gt_spd_build_algo(GT_SPD_AUTO, indptr, indices, n, nnz, D, spd, ld_spd, workspace, ws_bytes,
+                             stream);
 }
 
 size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {

@@ -23,6 +23,7 @@
 //     the row, then clears only the state it touched.
 // Every loop is bounded: union-find retries and the level loop have hard caps.
 #include <cuda_runtime.h>
+#include <climits>
 #include <stdint.h>
 
 #include "gt_common.cuh"
@@ -112,6 +113,20 @@ __device__ __forceinline__ BfsState bfs_slice(char* base, size_t per_cta, int ct
 
 // Four codes of columns 4c..4c+3 of one output row; the ragged end of the row
 // is written byte by byte so that columns >= n stay untouched.
+// Bits 0..3 of x to the low bit of bytes 0..3 (the four shifted copies of x
+// occupy disjoint bit ranges, so the product has no carries).
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+// store_codes with an evict-first store: the N^2 output streams through L2
+// without displacing the graph and the search state.
+__device__ __forceinline__ void store_codes_cs(int8_t* row, int c, int n, uint32_t word) {
+    if (4 * c + 4 <= n) {
+        __stcs(reinterpret_cast<unsigned int*>(row + 4 * c), word);
+    } else {
+        for (int t = 0; 4 * c + t < n; ++t) row[4 * c + t] = (int8_t)(word >> (8 * t));
+    }
+}
+
 __device__ __forceinline__ void store_codes(int8_t* row, int c, int n, uint32_t word) {
     if (4 * c + 4 <= n) {
         *reinterpret_cast<uint32_t*>(row + 4 * c) = word;
@@ -485,6 +500,359 @@ bfs32_smem(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indic
     }
 }
 
+// ---------------------------------------------------------------------------
+// Batches of W sources with every per-vertex word in shared memory: acc (the
+// bits pushed to a vertex in the current level), vis (the bits that reached it)
+// and fr (the bits new at it in the previous level).  W = 32 keeps one 32-bit
+// word per vertex (12 n bytes of shared memory); W = 16 packs two vertices per
+// word (6 n bytes), for graphs too large for the first.  Only the bit-sliced
+// distances are in global memory: nslices words per vertex word per CTA, small
+// enough to stay in L2.  A level is two passes over all vertices:
+//   push    one warp per block of 32 consecutive vertices that holds a frontier
+//           vertex.  The edges of the block's frontier vertices form one virtual
+//           segment (lane l's edges at positions pre_l .. pre_l + len_l - 1, pre a
+//           prefix sum over the lanes); the warp walks it 32 positions per chunk,
+//           each lane finding its position's vertex by a binary search over the
+//           lanes' pre values, with the index loads of four chunks in flight
+//           before their pushes; the row starts of the warp's next active block
+//           are loaded before the current block is walked.
+//   update  one thread per word keeps the bits not seen before, records them in
+//           the slices of the current level and makes them the next frontier.
+// No queues and no per-level counters: a level costs two scans of the words in
+// shared memory plus the edges of the frontier vertices, and the search ends
+// when an update pass finds no new bit.
+
+constexpr int kScanThreads = 1024;
+constexpr int kPushChunks = 4;     // 32-edge chunks whose index loads a lane has in flight
+constexpr int kUpdateWords = 4;    // words per thread whose slice updates overlap
+
+template <int W>
+struct ScanWords {
+    static constexpr int VPW = 32 / W;                       // vertices per 32-bit word
+    static constexpr uint32_t MASK = W == 32 ? 0xffffffffu : 0xffffu;
+    __device__ static __forceinline__ int word(int v) { return VPW == 1 ? v : v >> 1; }
+    __device__ static __forceinline__ int shift(int v) { return VPW == 1 ? 0 : (v & 1) << 4; }
+};
+
+// words per shared array (and per distance slice): the vertex words rounded up
+// so that the output pass's last group of four columns stays inside
+__host__ __device__ inline int scan_nwp(int n, int W) {
+    const int vpw = 32 / W;
+    const int nwords = (n + vpw - 1) / vpw;
+    return (nwords + 2 + 3) & ~3;
+}
+
+// rows[e] = the vertex whose adjacency list holds CSR entry e (one warp per
+// vertex; entries outside [0, nnz) are never written)
+__global__ void csr_rows(const int64_t* __restrict__ indptr, int n, int64_t nnz, int32_t* __restrict__ rows) {
+    const int lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int v = warp; v < n; v += nwarps) {
+        const int64_t e0 = max(indptr[v], (int64_t)0), e1 = min(indptr[v + 1], nnz);
+        for (int64_t e = e0 + lane; e < e1; e += 32) rows[e] = v;
+    }
+}
+
+template <int W>
+__global__ void __launch_bounds__(kScanThreads)
+bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices,
+         const int32_t* __restrict__ rows, const int* __restrict__ comp, int n, int D, int nslices,
+         int8_t* __restrict__ spd, int64_t ld, uint32_t* __restrict__ db_all) {
+    using SW = ScanWords<W>;
+    extern __shared__ uint32_t sw[];
+    __shared__ int s_comp[32];
+    __shared__ int s_csrc;
+    __shared__ int s_lo, s_hi;     // the vertex ids the batch has pushed to lie in [s_lo, s_hi]
+    const int nwp = scan_nwp(n, W);
+    uint32_t* acc = sw;
+    uint32_t* vis = sw + nwp;
+    uint32_t* fr = sw + 2 * nwp;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int nbatches = (n + W - 1) / W;
+    uint32_t* db = db_all + (size_t)blockIdx.x * nslices * nwp;
+    const unsigned full = 0xffffffffu;
+    const bool comp16 = (reinterpret_cast<uintptr_t>(comp) & 15u) == 0;
+    for (int p = tid; p < 3 * nwp; p += blockDim.x) sw[p] = 0u;
+    __syncthreads();
+
+    for (int batch = blockIdx.x; batch < nbatches; batch += gridDim.x) {
+        const int s0 = batch * W;
+        const int nsrc = min(W, n - s0);
+        if (tid < nsrc) {
+            const int s = s0 + tid;
+            const uint32_t bit = 1u << (SW::shift(s) + tid);
+            atomicOr(&vis[SW::word(s)], bit);
+            atomicOr(&fr[SW::word(s)], bit);
+            s_comp[tid] = comp[s];
+        }
+        if (tid == 0) {
+            s_lo = s0;
+            s_hi = s0 + nsrc - 1;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int c0 = s_comp[0];
+            const bool same = __all_sync(full, lane >= nsrc || s_comp[lane] == c0);
+            if (lane == 0) s_csrc = same ? c0 : -1;
+        }
+        __syncthreads();
+
+        for (int level = 1; level < D; ++level) {
+            // ---- push: each warp walks the active blocks of the touched range; the
+            // row starts of its next active block are loaded before the current
+            // one is walked
+            const int blo = s_lo >> 5, bhi = s_hi >> 5;
+            auto next_block = [&](int b, uint32_t& w, int64_t& st, int64_t& en) -> int {
+                for (; b <= bhi; b += nwarps) {
+                    const int v = b * 32 + lane;
+                    w = v < n ? (fr[SW::word(v)] >> SW::shift(v)) & SW::MASK : 0u;
+                    if (__ballot_sync(full, w != 0u)) {
+                        st = __ldg(indptr + min(v, n));
+                        en = v < n ? __ldg(indptr + v + 1) : st;
+                        return b;
+                    }
+                }
+                w = 0u;
+                return bhi + 1;
+            };
+            int umin = INT_MAX, umax = -1;     // this lane's pushed vertex ids
+            uint32_t w = 0u;
+            int64_t st = 0, en = 0;
+            int blk = next_block(blo + warp, w, st, en);
+            while (blk <= bhi) {
+                uint32_t w2 = 0u;
+                int64_t st2 = 0, en2 = 0;
+                const int blk2 = next_block(blk + nwarps, w2, st2, en2);
+                // the block's active edges as one virtual segment: lane l's edges
+                // (if its vertex is active) at positions pre_l .. pre_l + len_l - 1
+                const int len = w ? (int)(en - st) : 0;
+                int pre = len;
+#pragma unroll
+                for (int dd = 1; dd < 32; dd <<= 1) {
+                    const int t = __shfl_up_sync(full, pre, dd);
+                    if (lane >= dd) pre += t;
+                }
+                const int total = __shfl_sync(full, pre, 31);
+                pre -= len;
+                const int64_t E0 = __shfl_sync(full, st, 0), E1 = __shfl_sync(full, en, 31);
+                if (5 * (int64_t)total >= 2 * (E1 - E0)) {
+                    // mostly active: walk all the block's edges, the owner of each
+                    // from the row array (inactive owners push nothing)
+                    const int vb = blk * 32;
+                    const int seg = (int)(E1 - E0);
+                    const int32_t* ind0 = indices + E0;
+                    const int32_t* row0 = rows + E0;
+                    for (int x = 0; x < seg; x += 32 * kPushChunks) {
+                        int u[kPushChunks], o[kPushChunks];
+#pragma unroll
+                        for (int q = 0; q < kPushChunks; ++q) {
+                            const int off = x + 32 * q + lane;
+                            u[q] = -1;
+                            o[q] = 0;
+                            if (off < seg) {
+                                u[q] = __ldg(ind0 + off);
+                                o[q] = __ldg(row0 + off) - vb;
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < kPushChunks; ++q) {
+                            const uint32_t ww = __shfl_sync(full, w, o[q] & 31);
+                            if (ww && (unsigned)u[q] < (unsigned)n) {
+                                atomicOr(&acc[SW::word(u[q])], ww << SW::shift(u[q]));
+                                umin = min(umin, u[q]);
+                                umax = max(umax, u[q]);
+                            }
+                        }
+                    }
+                } else {
+                    // sparse: only the active edges, each lane finding its position's
+                    // vertex by a binary search over the lanes' pre values
+                    for (int x = 0; x < total; x += 32 * kPushChunks) {
+                        int u[kPushChunks];
+                        uint32_t ww[kPushChunks];
+#pragma unroll
+                        for (int q = 0; q < kPushChunks; ++q) {
+                            const int pos = x + 32 * q + lane;
+                            int lo = 0;
+#pragma unroll
+                            for (int step = 16; step > 0; step >>= 1) {
+                                const int c = lo + step;
+                                if (__shfl_sync(full, pre, c) <= pos) lo = c;
+                            }
+                            ww[q] = __shfl_sync(full, w, lo);
+                            const int64_t so = __shfl_sync(full, st, lo);
+                            const int po = __shfl_sync(full, pre, lo);
+                            u[q] = pos < total ? __ldg(indices + so + (pos - po)) : -1;
+                        }
+#pragma unroll
+                        for (int q = 0; q < kPushChunks; ++q)
+                            if ((unsigned)u[q] < (unsigned)n) {
+                                atomicOr(&acc[SW::word(u[q])], ww[q] << SW::shift(u[q]));
+                                umin = min(umin, u[q]);
+                                umax = max(umax, u[q]);
+                            }
+                    }
+                }
+                blk = blk2;
+                w = w2;
+                st = st2;
+                en = en2;
+            }
+            umin = __reduce_min_sync(full, umin);
+            umax = __reduce_max_sync(full, umax);
+            if (lane == 0 && umax >= 0) {
+                atomicMin(&s_lo, umin);
+                atomicMax(&s_hi, umax);
+            }
+            __syncthreads();
+            // ---- update over the touched words, four per thread at a time so that
+            // their slice read-modify-writes overlap
+            const int wlo = SW::word(s_lo), whi = SW::word(s_hi);
+            uint32_t any = 0u;
+            for (int p0 = wlo + tid; p0 <= whi; p0 += kUpdateWords * blockDim.x) {
+                uint32_t nw[kUpdateWords];
+#pragma unroll
+                for (int r = 0; r < kUpdateWords; ++r) {
+                    const int p = p0 + r * blockDim.x;
+                    nw[r] = 0u;
+                    if (p <= whi) {
+                        const uint32_t a = acc[p];
+                        if (a) {
+                            acc[p] = 0u;
+                            const uint32_t seen = vis[p];
+                            nw[r] = a & ~seen;
+                            vis[p] = seen | nw[r];
+                        }
+                        fr[p] = nw[r];
+                    }
+                    any |= nw[r];
+                }
+                if (nw[0] | nw[1] | nw[2] | nw[3]) {
+                    for (int k = 0; k < nslices; ++k) {
+                        if (!((level >> k) & 1)) continue;
+                        uint32_t* dk = db + (size_t)k * nwp;
+                        uint32_t old[kUpdateWords];
+#pragma unroll
+                        for (int r = 0; r < kUpdateWords; ++r) old[r] = nw[r] ? dk[p0 + r * blockDim.x] : 0u;
+#pragma unroll
+                        for (int r = 0; r < kUpdateWords; ++r)
+                            if (nw[r]) dk[p0 + r * blockDim.x] = old[r] | nw[r];
+                    }
+                }
+            }
+            if (!__syncthreads_or(any != 0u)) break;
+        }
+
+        // ---- rows s0 .. s0+nsrc-1.  Columns outside the touched range (in
+        // 16-column groups) were reached by no source: their codes depend on the
+        // component only and go out as 16-byte stores.  The rest, in groups of four
+        // columns, build codes four rows at a time: each slice's four row bits of a
+        // column are spread to the low bits of four bytes, and a 4 x 4 byte
+        // transpose turns the four columns' words into four rows' words; the same
+        // thread then clears the words of its columns for the next batch.
+        const int csrc = s_csrc;
+        const uint32_t Dc = (uint32_t)D, Dfar = (uint32_t)(D + 1);
+        const int n16 = n >> 4;                     // full 16-column groups
+        const bool fast16 = csrc >= 0 && comp16;
+        const int glo = fast16 ? (s_lo >> 4) : 0;
+        const int ghi = fast16 ? (s_hi >> 4) : n16;
+        if (fast16) {
+            for (int g = tid; g < n16; g += blockDim.x) {
+                if (g >= glo && g <= ghi) continue;
+                const int v0 = 16 * g;
+                uint32_t wd[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int4 c4 = __ldg(reinterpret_cast<const int4*>(comp + v0 + 4 * q));
+                    wd[q] = (c4.x == csrc ? Dc : Dfar) | (c4.y == csrc ? Dc : Dfar) << 8 |
+                            (c4.z == csrc ? Dc : Dfar) << 16 | (c4.w == csrc ? Dc : Dfar) << 24;
+                }
+                const uint4 wv = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                for (int b = 0; b < nsrc; ++b)
+                    __stcs(reinterpret_cast<uint4*>(spd + (int64_t)(s0 + b) * ld + v0), wv);
+            }
+        }
+        // 4-column groups: those of 16-groups glo..ghi, and the ragged tail
+        const int c_lo = 4 * glo, c_hi = min(4 * ghi + 3, (n + 3) / 4 - 1);
+        const int c_tail = 4 * n16;
+        const int nmid = c_hi >= c_lo ? c_hi - c_lo + 1 : 0;
+        const int ntail = max(0, (n + 3) / 4 - max(c_tail, c_hi + 1));
+        for (int i = tid; i < nmid + ntail; i += blockDim.x) {
+            const int c = i < nmid ? c_lo + i : max(c_tail, c_hi + 1) + (i - nmid);
+            const int v0 = 4 * c;
+            uint32_t vw[4];
+            int cp[4];
+            uint32_t anyv = 0u;
+            if (v0 + 4 <= n && comp16) {
+                const int4 c4 = __ldg(reinterpret_cast<const int4*>(comp + v0));
+                cp[0] = c4.x; cp[1] = c4.y; cp[2] = c4.z; cp[3] = c4.w;
+            } else {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) cp[t] = v0 + t < n ? comp[v0 + t] : -1;
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int v = v0 + t;
+                vw[t] = v < n ? (vis[SW::word(v)] >> SW::shift(v)) & SW::MASK : 0u;
+                anyv |= vw[t];
+            }
+            if (!anyv && csrc >= 0) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) word |= (cp[t] == csrc ? Dc : Dfar) << (8 * t);
+                for (int b = 0; b < nsrc; ++b) store_codes_cs(spd + (int64_t)(s0 + b) * ld, c, n, word);
+                continue;
+            }
+            uint32_t dw[4][7];
+#pragma unroll
+            for (int k = 0; k < 7; ++k) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int v = v0 + t;
+                    dw[t][k] = k < nslices ? (db[(size_t)k * nwp + SW::word(v)] >> SW::shift(v)) & SW::MASK : 0u;
+                }
+            }
+            for (int b0 = 0; b0 < nsrc; b0 += 4) {
+                uint32_t col[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    uint32_t code4 = 0u;
+#pragma unroll
+                    for (int k = 0; k < 7; ++k) code4 |= spread4((dw[t][k] >> b0) & 0xfu) << k;
+                    const uint32_t m = spread4((vw[t] >> b0) & 0xfu) * 0xffu;
+                    uint32_t fill4;
+                    if (csrc >= 0) {
+                        fill4 = (cp[t] == csrc ? Dc : Dfar) * 0x01010101u;
+                    } else {
+                        fill4 = 0u;
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            fill4 |= (cp[t] == s_comp[min(b0 + r, nsrc - 1)] ? Dc : Dfar) << (8 * r);
+                    }
+                    col[t] = code4 | (fill4 & ~m);
+                }
+                const uint32_t lo01 = __byte_perm(col[0], col[1], 0x5140), lo23 = __byte_perm(col[2], col[3], 0x5140);
+                const uint32_t hi01 = __byte_perm(col[0], col[1], 0x7362), hi23 = __byte_perm(col[2], col[3], 0x7362);
+                const uint32_t rw[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                        __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (b0 + r < nsrc) store_codes_cs(spd + (int64_t)(s0 + b0 + r) * ld, c, n, rw[r]);
+            }
+            // clear: the words of columns v0 .. v0+3 (inside nwp by construction)
+            const int w0 = SW::word(v0), w1 = SW::word(v0 + 3);
+            for (int p = w0; p <= w1; ++p) {
+                vis[p] = 0u;
+                fr[p] = 0u;
+                for (int k = 0; k < nslices; ++k) db[(size_t)k * nwp + p] = 0u;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // Largest n whose 4 n-byte push words fit the shared memory of one CTA.
 int bfs32_max_n() {
     static int cached = -1;
@@ -514,46 +882,98 @@ int spd_ctas(int n) {
     return nb < sms ? nb : sms;
 }
 
-}  // namespace
+int scan_smem_bytes(int n, int W) { return 3 * scan_nwp(n, W) * 4; }
 
-// The BFS runs in batches of 32 sources with shared-memory pushes when 4 n
-// bytes fit in shared memory, else in batches of 64 with global pushes.
-bool use_bfs32(int n) { return n <= bfs32_max_n(); }
+int optin_smem() {
+    static int cached = -1;
+    if (cached < 0) {
+        int dev = 0, optin = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cached = optin;
+    }
+    return cached;
+}
 
-int spd_ctas32(int n) {
-    int nb = (n + 31) / 32;
-    int sms = num_sms();
+// static shared memory of bfs_scan and some slack
+constexpr int kScanStaticSmem = 1024;
+
+bool scan_fits(int n, int W) { return scan_smem_bytes(n, W) + kScanStaticSmem <= optin_smem(); }
+
+// The algorithm used for a graph of n vertices: the first that fits of
+// shared-memory words with 32 sources, with 16, the queue-based search with
+// shared-memory pushes, the global-memory search.  -1: the requested one
+// does not fit.
+int resolve_algo(int algo, int n) {
+    switch (algo) {
+        case GT_SPD_AUTO:
+            if (scan_fits(n, 32)) return GT_SPD_SCAN32;
+            if (scan_fits(n, 16)) return GT_SPD_SCAN16;
+            if (n <= bfs32_max_n()) return GT_SPD_QUEUE32;
+            return GT_SPD_GLOBAL64;
+        case GT_SPD_SCAN32: return scan_fits(n, 32) ? algo : -1;
+        case GT_SPD_SCAN16: return scan_fits(n, 16) ? algo : -1;
+        case GT_SPD_QUEUE32: return n <= bfs32_max_n() ? algo : -1;
+        case GT_SPD_GLOBAL64: return algo;
+        default: return -1;
+    }
+}
+
+int nctas_for(int n, int per_batch) {
+    const int nb = (n + per_batch - 1) / per_batch;
+    const int sms = num_sms();
     return nb < sms ? nb : sms;
 }
 
-size_t bfs_state_bytes(int n, int nslices, size_t* per, int* nctas) {
-    if (use_bfs32(n)) {
-        *per = per_cta_bytes32(n, nslices);
-        *nctas = spd_ctas32(n);
-    } else {
-        *per = per_cta_bytes(n, nslices);
-        *nctas = spd_ctas(n);
+// Bytes of the search state for a resolved algorithm.
+size_t bfs_state_bytes(int algo, int n, int nslices, size_t* per, int* nctas) {
+    switch (algo) {
+        case GT_SPD_SCAN32:
+        case GT_SPD_SCAN16: {
+            const int W = algo == GT_SPD_SCAN32 ? 32 : 16;
+            *per = (size_t)nslices * scan_nwp(n, W) * 4;
+            *nctas = nctas_for(n, W);
+            break;
+        }
+        case GT_SPD_QUEUE32:
+            *per = per_cta_bytes32(n, nslices);
+            *nctas = nctas_for(n, 32);
+            break;
+        default:
+            *per = per_cta_bytes(n, nslices);
+            *nctas = spd_ctas(n);
+            break;
     }
     return *per * (size_t)*nctas;
 }
 
-size_t spd_workspace_bytes(int32_t n, int32_t D) {
+}  // namespace
+
+bool is_scan(int a) { return a == GT_SPD_SCAN32 || a == GT_SPD_SCAN16; }
+
+size_t spd_workspace_bytes(int32_t n, int64_t nnz, int32_t D, int algo) {
+    const int a = resolve_algo(algo, n);
+    if (a < 0) return 0;
     Carve c(nullptr, 0);
     c.take<int>((size_t)n);
+    if (is_scan(a)) c.take<int32_t>((size_t)(nnz > 0 ? nnz : 1));
     size_t per = 0;
     int nctas = 0;
-    c.take<char>(bfs_state_bytes(n, slices_for(D), &per, &nctas));
+    c.take<char>(bfs_state_bytes(a, n, slices_for(D), &per, &nctas));
     return c.off + 256;
 }
 
-int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t D,
-              int8_t* spd, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
+int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t nnz, int32_t D,
+              int8_t* spd, int64_t ld, void* ws, size_t ws_bytes, int algo, cudaStream_t stream) {
+    const int a = resolve_algo(algo, n);
+    if (a < 0) return GT_ERR_UNSUPPORTED;
     Carve c(ws, ws_bytes);
     int* comp = c.take<int>((size_t)n);
+    int32_t* rows = is_scan(a) ? c.take<int32_t>((size_t)(nnz > 0 ? nnz : 1)) : nullptr;
     const int nslices = slices_for(D);
     size_t per = 0;
     int nctas = 0;
-    char* bfs_ws = c.take<char>(bfs_state_bytes(n, nslices, &per, &nctas));
+    char* bfs_ws = c.take<char>(bfs_state_bytes(a, n, nslices, &per, &nctas));
     if (!c.fits()) return GT_ERR_WORKSPACE;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
@@ -570,9 +990,23 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int32_t 
         LaunchScope ls("spd_uf_compress", stream);
         uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
     }
-    // the BFS keeps vis / acc / db zero between batches; start from zero
-    if (cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess) return GT_ERR_CUDA;
-    if (use_bfs32(n)) {
+    // every search keeps its global state zero between batches; start from zero
+    if (per * (size_t)nctas > 0 && cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess)
+        return GT_ERR_CUDA;
+    if (is_scan(a)) {
+        if (nnz > 0) {
+            LaunchScope ls("spd_rows", stream);
+            csr_rows<<<sms * 8, 256, 0, stream>>>(indptr, n, nnz, rows);
+        }
+        const int W = a == GT_SPD_SCAN32 ? 32 : 16;
+        const int smem = scan_smem_bytes(n, W);
+        auto kern = W == 32 ? bfs_scan<32> : bfs_scan<16>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return GT_ERR_CUDA;
+        LaunchScope ls("spd_bfs", stream);
+        kern<<<nctas, kScanThreads, smem, stream>>>(indptr, indices, rows, comp, n, D, nslices, spd, ld,
+                                                   reinterpret_cast<uint32_t*>(bfs_ws));
+    } else if (a == GT_SPD_QUEUE32) {
         const size_t smem = (size_t)n * 4;
         if (cudaFuncSetAttribute(bfs32_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)

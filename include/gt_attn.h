@@ -86,6 +86,37 @@ int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64
                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Search algorithms of gt_spd_build.  All give the same codes; they differ in
+ * where the per-vertex state lives, which bounds the graph size they take:
+ *   GT_SPD_SCAN32    32 sources per batch, every per-vertex word in shared
+ *                    memory (12 bytes per vertex): the fastest, n up to ~18.8K
+ *                    on a GB300.
+ *   GT_SPD_SCAN16    16 sources per batch, two vertices per word (6 bytes per
+ *                    vertex), n up to ~37K.
+ *   GT_SPD_QUEUE32   32 sources per batch, frontier queues in global memory,
+ *                    pushes into shared memory (4 bytes per vertex), n up to ~58K.
+ *   GT_SPD_GLOBAL64  64 sources per batch, all state in global memory: any n.
+ *   GT_SPD_AUTO      the first of these that fits (what gt_spd_build uses).
+ */
+enum { GT_SPD_AUTO = 0, GT_SPD_SCAN32 = 1, GT_SPD_SCAN16 = 2, GT_SPD_QUEUE32 = 3, GT_SPD_GLOBAL64 = 4 };
+
+/*
+ * Workspace bytes of gt_spd_build_algo for this algorithm, or 0 when the
+ * algorithm cannot take n vertices on the current device (or the arguments are
+ * out of range).
+ */
+size_t gt_spd_workspace_size_algo(int32_t algo, int32_t n, int64_t nnz, int32_t D);
+
+/*
+ * gt_spd_build with an explicit search algorithm (same arguments and result).
+ * Errors as gt_spd_build, plus GT_ERR_INVALID_ARG for an unknown algo and
+ * GT_ERR_UNSUPPORTED when the algorithm cannot take n vertices on this device.
+ */
+int gt_spd_build_algo(int32_t algo, const int64_t* indptr, const int32_t* indices, int32_t n,
+                      int64_t nnz, int32_t D, int8_t* spd, int64_t ld_spd,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Bytes of device workspace needed by gt_bias_attn_fwd (with this kv_block)
  * and by gt_bias_attn_bwd for these sizes; one buffer of this size serves both.
  */

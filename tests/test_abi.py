@@ -58,6 +58,9 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, fake, 8, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 20, 2, 3, fake, 24, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, P(0x1001), 16, fake, 1 << 20, None) == -1
+    # unknown search algorithm
+    assert lib.gt_spd_build_algo(9, fake, fake, 4, 2, 3, fake, 16, fake, 1 << 20, None) == -1
+    assert lib.gt_spd_build_algo(-1, fake, fake, 4, 2, 3, fake, 16, fake, 1 << 20, None) == -1
     # forward: bad dtype, NULL q, misaligned q, bad ld, nb too large, bad kv_block
     args = lambda **kw: [kw.get("dt", 1), kw.get("n", 64), kw.get("h", 8), kw.get("d", 8),
                          kw.get("q", fake), fake, fake, fake, kw.get("ld", 64), fake,
@@ -91,6 +94,9 @@ def test_workspace_sizes(lib):
     assert gt.gt_bias_attn_workspace_size(9, 4096, 8, 8, 0) == 0
     assert gt.gt_spd_workspace_size(0, 0, 16) == 0
     assert gt.gt_spd_workspace_size(512, 4000, 16) > 0
+    # the global-memory search takes any n; an unknown algorithm takes none
+    assert gt.gt_spd_workspace_size(512, 4000, 16, algo=gt.GT_SPD_GLOBAL64) > 0
+    assert gt.gt_spd_workspace_size(512, 4000, 16, algo=9) == 0
 
 
 def test_spd_ld():

@@ -19,9 +19,12 @@ def gt():
     return m
 
 
-def _gpu_spd(gt, g, D):
+ALGOS = [0, 1, 2, 3, 4]     # auto, scan32, scan16, queue32, global64
+
+
+def _gpu_spd(gt, g, D, algo=0):
     ip, ix = graph_to_dev(g)
-    out = gt.gt_spd_build(ip, ix, g.n, D)
+    out = gt.gt_spd_build(ip, ix, g.n, D, algo=algo)
     gt.gt_check_device_status()
     return out[:, :g.n].cpu().numpy()
 
@@ -57,10 +60,39 @@ def _empty(n):
     ("dba_5x70", gi.disjoint_ba(5, 70, 2, seed=3), 24),
     ("ba_1000_tree", gi.barabasi_albert(1000, 1, seed=9), 32),
 ])
-def test_spd_edge_cases(gt, name, g, D):
-    got = _gpu_spd(gt, g, D)
+@pytest.mark.parametrize("algo", ALGOS)
+def test_spd_edge_cases(gt, name, g, D, algo):
+    got = _gpu_spd(gt, g, D, algo)
     ref = O.spd(g.n, g.indptr, g.indices, D)
-    assert np.array_equal(got, ref), f"{name}: {int((got != ref).sum())} codes differ"
+    assert np.array_equal(got, ref), f"{name}, algo {algo}: {int((got != ref).sum())} codes differ"
+
+
+@pytest.mark.parametrize("name,g,D", [
+    ("cm_3001", gi.configuration_model(3001, 2.1, 2, 300, seed=11), 32),
+    ("rgg_2500", gi.random_geometric(2500, 0.03, seed=12), 16),
+    ("dba_9x333", gi.disjoint_ba(9, 333, 3, seed=13), 24),
+    ("ba_4095", gi.barabasi_albert(4095, 4, seed=14), 20),
+])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_spd_every_algorithm_mid_size(gt, name, g, D, algo):
+    """Every search algorithm on graphs of a few thousand vertices (several
+    batches per CTA, blocks of hubs and of leaves, odd n for the packed words)."""
+    got = _gpu_spd(gt, g, D, algo)
+    ref = O.spd(g.n, g.indptr, g.indices, D)
+    assert np.array_equal(got, ref), f"{name}, algo {algo}: {int((got != ref).sum())} codes differ"
+
+
+def test_spd_algorithm_limits(gt):
+    """Each algorithm takes the sizes it documents; asking for more is refused."""
+    assert gt.gt_spd_workspace_size(18000, 10, 8, algo=1) > 0
+    assert gt.gt_spd_workspace_size(20000, 10, 8, algo=1) == 0
+    assert gt.gt_spd_workspace_size(36000, 10, 8, algo=2) > 0
+    assert gt.gt_spd_workspace_size(40000, 10, 8, algo=2) == 0
+    assert gt.gt_spd_workspace_size(1 << 20, 10, 8, algo=4) > 0
+    g = _path(300)
+    ip, ix = graph_to_dev(g)
+    with pytest.raises(gt.GtError):
+        gt.gt_spd_build(ip, ix, 20000, 8, algo=1)
 
 
 def test_spd_tolerates_self_loops_and_repeats(gt):
