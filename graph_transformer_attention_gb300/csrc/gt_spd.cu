@@ -524,6 +524,7 @@ bfs32_smem(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indic
 
 constexpr int kScanThreads = 1024;
 constexpr int kPushChunks = 4;     // 32-edge chunks whose index loads a lane has in flight
+constexpr int kFlatChunks = 8;     // the same for the flat push
 constexpr int kUpdateWords = 4;    // words per thread whose slice updates overlap
 
 template <int W>
@@ -542,28 +543,38 @@ __host__ __device__ inline int scan_nwp(int n, int W) {
     return (nwords + 2 + 3) & ~3;
 }
 
-// rows[e] = the vertex whose adjacency list holds CSR entry e (one warp per
-// vertex; entries outside [0, nnz) are never written)
-__global__ void csr_rows(const int64_t* __restrict__ indptr, int n, int64_t nnz, int32_t* __restrict__ rows) {
+// pairs[e] = indices[e] | (the vertex whose adjacency list holds CSR entry e) << 16:
+// one 4-byte load gives a push's target and source (vertex ids of the
+// shared-memory searches fit 16 bits; an entry outside 0..n-1 is stored as
+// 0xffff, which is >= n and so never pushed).  One warp per vertex; entries
+// outside [0, nnz) are never written.
+__global__ void csr_pairs(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices, int n,
+                          int64_t nnz, uint32_t* __restrict__ pairs) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int v = warp; v < n; v += nwarps) {
         const int64_t e0 = max(indptr[v], (int64_t)0), e1 = min(indptr[v + 1], nnz);
-        for (int64_t e = e0 + lane; e < e1; e += 32) rows[e] = v;
+        for (int64_t e = e0 + lane; e < e1; e += 32) {
+            const int u = indices[e];
+            const uint32_t uu = (unsigned)u < (unsigned)n ? (uint32_t)u : 0xffffu;
+            pairs[e] = uu | ((uint32_t)v << 16);
+        }
     }
 }
 
 template <int W>
 __global__ void __launch_bounds__(kScanThreads)
 bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices,
-         const int32_t* __restrict__ rows, const int* __restrict__ comp, int n, int D, int nslices,
+         const uint32_t* __restrict__ pairs, const int* __restrict__ comp, int n, int D, int nslices,
          int8_t* __restrict__ spd, int64_t ld, uint32_t* __restrict__ db_all) {
     using SW = ScanWords<W>;
     extern __shared__ uint32_t sw[];
     __shared__ int s_comp[32];
     __shared__ int s_csrc;
     __shared__ int s_lo, s_hi;     // the vertex ids the batch has pushed to lie in [s_lo, s_hi]
+    __shared__ int s_nfront[2];    // frontier vertices after the update pass of an odd / even level
+    __shared__ int s_nopen[2];     // vertices not reached by every source, the same way
     const int nwp = scan_nwp(n, W);
     uint32_t* acc = sw;
     uint32_t* vis = sw + nwp;
@@ -590,6 +601,8 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
         if (tid == 0) {
             s_lo = s0;
             s_hi = s0 + nsrc - 1;
+            s_nfront[0] = nsrc;
+            s_nopen[0] = n;
         }
         __syncthreads();
         if (warp == 0) {
@@ -599,11 +612,78 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
         }
         __syncthreads();
 
+        // a vertex is open while some source of the batch has not reached it
+        const uint32_t fmask = nsrc == 32 ? 0xffffffffu : (1u << nsrc) - 1u;
         for (int level = 1; level < D; ++level) {
-            // ---- push: each warp walks the active blocks of the touched range; the
-            // row starts of its next active block are loaded before the current
-            // one is walked
-            const int blo = s_lo >> 5, bhi = s_hi >> 5;
+            const int lo = s_lo, hi = s_hi;
+            const int nfront = s_nfront[(level - 1) & 1];
+            const int nopen = s_nopen[(level - 1) & 1];
+            if (tid == 0) {
+                s_nfront[level & 1] = 0;
+                s_nopen[level & 1] = 0;
+            }
+            const bool whole = lo == 0 && hi == n - 1;
+            int umin = INT_MAX, umax = -1;     // this lane's pushed vertex ids
+            if (whole && level > 1 && nopen < nfront) {
+            // ---- pull, few open vertices left (the batch has reached every vertex
+            // id, so no vertex outside the scanned range can gain bits): each open
+            // vertex ORs the frontier bits of its neighbours, stopping once it has
+            // every bit it lacks; a thread owns its words, so no atomics
+            for (int p = tid; p < (n + SW::VPW - 1) / SW::VPW; p += blockDim.x) {
+                const uint32_t seen = vis[p];
+                uint32_t got = 0u;
+#pragma unroll
+                for (int h = 0; h < SW::VPW; ++h) {
+                    const int v = p * SW::VPW + h;
+                    const uint32_t miss = v < n ? fmask & ~((seen >> SW::shift(v)) & SW::MASK) : 0u;
+                    if (!miss) continue;
+                    uint32_t g = 0u;
+                    const int64_t e1 = __ldg(indptr + v + 1);
+                    for (int64_t e = __ldg(indptr + v); e < e1 && (g & miss) != miss; e += 4) {
+                        int uu[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) uu[k] = e + k < e1 ? __ldg(indices + e + k) : -1;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if ((unsigned)uu[k] < (unsigned)n) g |= (fr[SW::word(uu[k])] >> SW::shift(uu[k])) & SW::MASK;
+                    }
+                    got |= (g & miss) << SW::shift(v);
+                }
+                if (got) acc[p] = got;
+            }
+            } else if (8 * nfront >= hi - lo + 1) {
+            // ---- push, large frontier: the edges of the touched range split evenly
+            // over the warps; each edge's source is checked against the frontier
+            const int64_t Elo = __ldg(indptr + lo), Ehi = __ldg(indptr + hi + 1);
+            const int64_t per = ((Ehi - Elo + nwarps - 1) / nwarps + 31) & ~(int64_t)31;
+            const int64_t my0 = min(Elo + warp * per, Ehi);
+            const int seg = (int)(min(my0 + per, Ehi) - my0);
+            const uint32_t* pr = pairs + my0;
+            for (int x = 0; x < seg; x += 32 * kFlatChunks) {
+                uint32_t ed[kFlatChunks];
+#pragma unroll
+                for (int q = 0; q < kFlatChunks; ++q) {
+                    const int off = x + 32 * q + lane;
+                    ed[q] = off < seg ? __ldg(pr + off) : 0xffffffffu;
+                }
+#pragma unroll
+                for (int q = 0; q < kFlatChunks; ++q) {
+                    const int u = (int)(ed[q] & 0xffffu), r = (int)(ed[q] >> 16);
+                    if (u < n && r < n) {
+                        const uint32_t ww = (fr[SW::word(r)] >> SW::shift(r)) & SW::MASK;
+                        if (ww) {
+                            atomicOr(&acc[SW::word(u)], ww << SW::shift(u));
+                            umin = min(umin, u);
+                            umax = max(umax, u);
+                        }
+                    }
+                }
+            }
+            } else {
+            // ---- push, small frontier: each warp walks the active blocks of the
+            // touched range; the row starts of its next active block are loaded
+            // before the current one is walked
+            const int blo = lo >> 5, bhi = hi >> 5;
             auto next_block = [&](int b, uint32_t& w, int64_t& st, int64_t& en) -> int {
                 for (; b <= bhi; b += nwarps) {
                     const int v = b * 32 + lane;
@@ -617,7 +697,6 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                 w = 0u;
                 return bhi + 1;
             };
-            int umin = INT_MAX, umax = -1;     // this lane's pushed vertex ids
             uint32_t w = 0u;
             int64_t st = 0, en = 0;
             int blk = next_block(blo + warp, w, st, en);
@@ -642,8 +721,7 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                     // from the row array (inactive owners push nothing)
                     const int vb = blk * 32;
                     const int seg = (int)(E1 - E0);
-                    const int32_t* ind0 = indices + E0;
-                    const int32_t* row0 = rows + E0;
+                    const uint32_t* pr0 = pairs + E0;
                     for (int x = 0; x < seg; x += 32 * kPushChunks) {
                         int u[kPushChunks], o[kPushChunks];
 #pragma unroll
@@ -652,8 +730,9 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                             u[q] = -1;
                             o[q] = 0;
                             if (off < seg) {
-                                u[q] = __ldg(ind0 + off);
-                                o[q] = __ldg(row0 + off) - vb;
+                                const uint32_t ed = __ldg(pr0 + off);
+                                u[q] = (int)(ed & 0xffffu);
+                                o[q] = (int)(ed >> 16) - vb;
                             }
                         }
 #pragma unroll
@@ -700,6 +779,7 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                 st = st2;
                 en = en2;
             }
+            }
             umin = __reduce_min_sync(full, umin);
             umax = __reduce_max_sync(full, umax);
             if (lane == 0 && umax >= 0) {
@@ -711,6 +791,7 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
             // their slice read-modify-writes overlap
             const int wlo = SW::word(s_lo), whi = SW::word(s_hi);
             uint32_t any = 0u;
+            int nfv = 0, nov = 0;     // this thread's frontier and open vertices
             for (int p0 = wlo + tid; p0 <= whi; p0 += kUpdateWords * blockDim.x) {
                 uint32_t nw[kUpdateWords];
 #pragma unroll
@@ -719,13 +800,22 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                     nw[r] = 0u;
                     if (p <= whi) {
                         const uint32_t a = acc[p];
+                        uint32_t seen = vis[p];
                         if (a) {
                             acc[p] = 0u;
-                            const uint32_t seen = vis[p];
                             nw[r] = a & ~seen;
-                            vis[p] = seen | nw[r];
+                            seen |= nw[r];
+                            vis[p] = seen;
                         }
                         fr[p] = nw[r];
+#pragma unroll
+                        for (int h = 0; h < SW::VPW; ++h) {
+                            const int v = p * SW::VPW + h;
+                            if (v < n) {
+                                nfv += ((nw[r] >> SW::shift(v)) & SW::MASK) != 0u;
+                                nov += ((seen >> SW::shift(v)) & SW::MASK) != fmask;
+                            }
+                        }
                     }
                     any |= nw[r];
                 }
@@ -741,6 +831,12 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                             if (nw[r]) dk[p0 + r * blockDim.x] = old[r] | nw[r];
                     }
                 }
+            }
+            nfv = __reduce_add_sync(full, nfv);
+            nov = __reduce_add_sync(full, nov);
+            if (lane == 0) {
+                if (nfv) atomicAdd(&s_nfront[level & 1], nfv);
+                if (nov) atomicAdd(&s_nopen[level & 1], nov);
             }
             if (!__syncthreads_or(any != 0u)) break;
         }
@@ -820,7 +916,8 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                 for (int t = 0; t < 4; ++t) {
                     uint32_t code4 = 0u;
 #pragma unroll
-                    for (int k = 0; k < 7; ++k) code4 |= spread4((dw[t][k] >> b0) & 0xfu) << k;
+                    for (int k = 0; k < 7; ++k)
+                        if (k < nslices) code4 |= spread4((dw[t][k] >> b0) & 0xfu) << k;
                     const uint32_t m = spread4((vw[t] >> b0) & 0xfu) * 0xffu;
                     uint32_t fill4;
                     if (csrc >= 0) {
@@ -898,7 +995,8 @@ int optin_smem() {
 // static shared memory of bfs_scan and some slack
 constexpr int kScanStaticSmem = 1024;
 
-bool scan_fits(int n, int W) { return scan_smem_bytes(n, W) + kScanStaticSmem <= optin_smem(); }
+// (vertex ids of the scan searches travel as 16-bit fields of the edge pairs)
+bool scan_fits(int n, int W) { return n < 65535 && scan_smem_bytes(n, W) + kScanStaticSmem <= optin_smem(); }
 
 // The algorithm used for a graph of n vertices: the first that fits of
 // shared-memory words with 32 sources, with 16, the queue-based search with
@@ -956,7 +1054,7 @@ size_t spd_workspace_bytes(int32_t n, int64_t nnz, int32_t D, int algo) {
     if (a < 0) return 0;
     Carve c(nullptr, 0);
     c.take<int>((size_t)n);
-    if (is_scan(a)) c.take<int32_t>((size_t)(nnz > 0 ? nnz : 1));
+    if (is_scan(a)) c.take<uint32_t>((size_t)(nnz > 0 ? nnz : 1));
     size_t per = 0;
     int nctas = 0;
     c.take<char>(bfs_state_bytes(a, n, slices_for(D), &per, &nctas));
@@ -969,7 +1067,7 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
     if (a < 0) return GT_ERR_UNSUPPORTED;
     Carve c(ws, ws_bytes);
     int* comp = c.take<int>((size_t)n);
-    int32_t* rows = is_scan(a) ? c.take<int32_t>((size_t)(nnz > 0 ? nnz : 1)) : nullptr;
+    uint32_t* pairs = is_scan(a) ? c.take<uint32_t>((size_t)(nnz > 0 ? nnz : 1)) : nullptr;
     const int nslices = slices_for(D);
     size_t per = 0;
     int nctas = 0;
@@ -995,8 +1093,8 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         return GT_ERR_CUDA;
     if (is_scan(a)) {
         if (nnz > 0) {
-            LaunchScope ls("spd_rows", stream);
-            csr_rows<<<sms * 8, 256, 0, stream>>>(indptr, n, nnz, rows);
+            LaunchScope ls("spd_pairs", stream);
+            csr_pairs<<<sms * 8, 256, 0, stream>>>(indptr, indices, n, nnz, pairs);
         }
         const int W = a == GT_SPD_SCAN32 ? 32 : 16;
         const int smem = scan_smem_bytes(n, W);
@@ -1004,7 +1102,7 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return GT_ERR_CUDA;
         LaunchScope ls("spd_bfs", stream);
-        kern<<<nctas, kScanThreads, smem, stream>>>(indptr, indices, rows, comp, n, D, nslices, spd, ld,
+        kern<<<nctas, kScanThreads, smem, stream>>>(indptr, indices, pairs, comp, n, D, nslices, spd, ld,
                                                    reinterpret_cast<uint32_t*>(bfs_ws));
     } else if (a == GT_SPD_QUEUE32) {
         const size_t smem = (size_t)n * 4;
