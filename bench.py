@@ -343,8 +343,21 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches),
         "clocks": clocks,
+        "memory": memory_line(w, dev),
         "cpu_baseline": None,
     }
+
+
+def memory_line(w: gi.Workload, dev) -> dict:
+    """Model bytes of one layer's forward + backward, blockwise (this library) and
+    materialised (N x N per head), and the process's measured peak."""
+    import torch
+    from graph_transformer_attention_gb300 import memory as M
+    blk = M.blockwise_layer_bytes(w.n, w.heads, w.head_dim, w.nb, w.dtype, w.kv_block)
+    mat = M.materialised_layer_bytes(w.n, w.heads, w.head_dim, w.dtype)
+    return {"model_blockwise_layer_bytes": int(blk["peak"]),
+            "model_materialised_layer_bytes_min": int(mat["peak_min"]),
+            "process_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(dev))}
 
 
 # --------------------------------------------------------- CPU oracle arm
