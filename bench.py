@@ -173,6 +173,22 @@ def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_p
             "peak_source": "MEASURED_PEAKS.json hbm_gbs"}
 
 
+def max_over_ranks(values, world: int, device) -> list:
+    """Each rank's times -> their maximum over the ranks (the job lasts as long as
+    its slowest replica); a no-op on one rank."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, ms: float, world: int) -> float:
+    """Replicas only: every rank runs the whole workload, so the job's work is
+    world x the per-rank work, over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     import torch
     import graph_transformer_attention_gb300 as gt
@@ -302,17 +318,14 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
                                                     for hl in h_layers for t in hl.values())
     d2h = sum(t.numel() * t.element_size() for ho in h_outs for t in ho.values())
 
-    ms = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
-    ms_total, e2e_ms = float(ms[0]), float(ms[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], world, dev)
     if rank != 0:
         return None
 
     ms_step = ms_total / args.steps
     flops = attn_flops(w)
-    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
-    e2e_value = world * flops * args.steps / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, ms_total, world)
+    e2e_value = whole_job_tflops(flops, args.steps, e2e_ms, world)
     peaks = measured_peaks()
     clk_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     exp_peak = SMS * EX2_PER_CLK_SM * clk_mhz * 1e6           # exps / s

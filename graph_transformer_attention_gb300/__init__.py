@@ -93,6 +93,8 @@ def load_library():
         lib.gt_bias_attn_bwd.restype = ctypes.c_int
         lib.gt_check_device_status.argtypes = [P]
         lib.gt_check_device_status.restype = ctypes.c_int
+        lib.gt_selftest_wait_timeout.argtypes = [i64, P]
+        lib.gt_selftest_wait_timeout.restype = ctypes.c_int
         lib.gt_bias_attn_fwd_partial.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
                                                  i32, P, P, P]
         lib.gt_bias_attn_fwd_partial.restype = ctypes.c_int
@@ -276,6 +278,13 @@ def gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T, scale: float | None = None,
 def gt_check_device_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check("gt_check_device_status", load_library().gt_check_device_status(_stream_handle(stream)))
+
+
+def gt_selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
+    """Launch the library's bounded-wait self-test: a wait that nothing ends, which
+    gives up after limit_ns; the next gt_check_device_status reports GT_ERR_TIMEOUT."""
+    _check("gt_selftest_wait_timeout",
+           load_library().gt_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
 
 
 def gt_kernel_stats_reset(timing: bool = False) -> None:

@@ -240,6 +240,15 @@ const char* gt_status_string(int status);
 int gt_check_device_status(void* stream);
 
 /*
+ * Self-test of the bounded waits (no counterpart in the method): launches one
+ * CTA on `stream` whose wait on a barrier that nothing arrives at gives up after
+ * limit_ns nanoseconds of wall time, exactly as a kernel's wait would; the next
+ * gt_check_device_status then reports GT_ERR_TIMEOUT and the context stays
+ * usable.  1e6 <= limit_ns <= 1e9, else GT_ERR_INVALID_ARG.
+ */
+int gt_selftest_wait_timeout(int64_t limit_ns, void* stream);
+
+/*
  * Launch statistics (a measurement aid; no counterpart in the method).
  *
  * The library counts, per kernel name, every kernel it launches.  With timing

@@ -58,6 +58,9 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, fake, 8, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 20, 2, 3, fake, 24, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, P(0x1001), 16, fake, 1 << 20, None) == -1
+    # bounded-wait self-test: limits out of range
+    assert lib.gt_selftest_wait_timeout(ctypes.c_int64(10), None) == -1
+    assert lib.gt_selftest_wait_timeout(ctypes.c_int64(2_000_000_000), None) == -1
     # unknown search algorithm
     assert lib.gt_spd_build_algo(9, fake, fake, 4, 2, 3, fake, 16, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build_algo(-1, fake, fake, 4, 2, 3, fake, 16, fake, 1 << 20, None) == -1
