@@ -23,7 +23,8 @@ import numpy as np
 __all__ = [
     "Graph", "Workload", "CONFIGS", "make_graph", "make_layer_tensors",
     "erdos_renyi", "random_geometric", "barabasi_albert", "disjoint_ba",
-    "configuration_model", "csr_from_edges", "round_to_bf16",
+    "configuration_model", "csr_from_edges", "round_to_bf16", "make_gt_layer_params",
+    "make_gt_layer_io",
 ]
 
 
@@ -227,3 +228,46 @@ def make_layer_tensors(n: int, heads: int, head_dim: int, nb: int, dtype: str, s
 def config_layer_tensors(cfg: Workload, layer: int = 0) -> dict:
     return make_layer_tensors(cfg.n, cfg.heads, cfg.head_dim, cfg.nb, cfg.dtype,
                               cfg.tensor_seed(layer))
+
+
+def make_gt_layer_params(width: int, ffn: int, nb: int, heads: int, seed: int) -> dict:
+    """Weights of one GT encoder layer around the biased attention, drawn from
+    PCG64(seed) in this order: LayerNorm 1 (gain, shift), W_qkv, b_qkv, W_o, b_o,
+    LayerNorm 2, W_1, b_1, W_2, b_2, T.  Matrices ~ N(0, 1/fan_in) (a unit-variance
+    input keeps a unit-variance output), biases and shifts ~ N(0, 0.02^2), gains
+    ~ 1 + N(0, 0.1^2), T ~ N(0, 0.1^2).  All float32.  W_qkv is [width][3 width]
+    (columns: q | k | v, each in (head, channel) order), W_o [width][width],
+    W_1 [width][ffn], W_2 [ffn][width]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    f32 = np.float32
+
+    def mat(r, c):
+        return (rng.standard_normal((r, c)) / math.sqrt(r)).astype(f32)
+
+    def vec(m, std=0.02):
+        return (std * rng.standard_normal(m)).astype(f32)
+
+    p = {}
+    p["ln1_g"] = (1.0 + vec(width, 0.1)).astype(f32)
+    p["ln1_b"] = vec(width)
+    p["w_qkv"] = mat(width, 3 * width)
+    p["b_qkv"] = vec(3 * width)
+    p["w_o"] = mat(width, width)
+    p["b_o"] = vec(width)
+    p["ln2_g"] = (1.0 + vec(width, 0.1)).astype(f32)
+    p["ln2_b"] = vec(width)
+    p["w_1"] = mat(width, ffn)
+    p["b_1"] = vec(ffn)
+    p["w_2"] = mat(ffn, width)
+    p["b_2"] = vec(width)
+    p["T"] = (0.1 * rng.standard_normal((heads, nb))).astype(f32)
+    return p
+
+
+def make_gt_layer_io(n: int, width: int, seed: int) -> dict:
+    """Layer input x and the gradient dy of the layer output, both N(0, 1)
+    float32 [n][width], drawn from PCG64(seed) in that order."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((n, width), dtype=np.float32)
+    dy = rng.standard_normal((n, width), dtype=np.float32)
+    return dict(x=x, dy=dy)
