@@ -95,6 +95,13 @@ def load_library():
         lib.gt_check_device_status.restype = ctypes.c_int
         lib.gt_selftest_wait_timeout.argtypes = [i64, P]
         lib.gt_selftest_wait_timeout.restype = ctypes.c_int
+        lib.gt_layer_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.gt_layer_workspace_size.restype = sz
+        lib.gt_layer_fwd.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, i32, P, P, P, P, P, P, P, sz, P]
+        lib.gt_layer_fwd.restype = ctypes.c_int
+        lib.gt_layer_bwd.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, i32, P, P, P, P, P, P, P, P, P,
+                                     P, sz, P]
+        lib.gt_layer_bwd.restype = ctypes.c_int
         lib.gt_bias_attn_fwd_partial.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
                                                  i32, P, P, P]
         lib.gt_bias_attn_fwd_partial.restype = ctypes.c_int
@@ -273,6 +280,66 @@ def gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T, scale: float | None = None,
                               workspace.numel(), _stream_handle(stream))
     _check("gt_bias_attn_bwd", rc)
     return dq, dk, dv, dT
+
+
+LAYER_PARAMS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_1", "b_1", "w_2", "b_2")
+
+
+class _LayerPtrs(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in LAYER_PARAMS]
+
+
+def _layer_ptrs(tensors: dict) -> _LayerPtrs:
+    for name in LAYER_PARAMS:
+        t = tensors[name]
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"layer tensor {name} must be contiguous fp32 on the GPU")
+    return _LayerPtrs(*[_ptr(tensors[name]) for name in LAYER_PARAMS])
+
+
+def gt_layer_workspace_size(n: int, h: int = 8, d: int = 8, f: int = 64) -> int:
+    return int(load_library().gt_layer_workspace_size(n, h, d, f))
+
+
+def gt_layer_fwd(x, params: dict, spd, T, workspace=None, stream=None):
+    """GT encoder layer forward: y fp32 [n][64] from x fp32 [n][64], and the saved
+    tensors of the backward {q, k, v, o (bf16 [n][8][8]), lse}."""
+    lib = load_library()
+    _need_cuda(x, spd, T)
+    n = x.shape[0]
+    dev = x.device
+    saved = {name: torch.empty((n, 8, 8), dtype=torch.bfloat16, device=dev) for name in ("q", "k", "v", "o")}
+    saved["lse"] = torch.empty((8, n), dtype=torch.float32, device=dev)
+    y = torch.empty_like(x)
+    if workspace is None:
+        workspace = _workspace(lib.gt_layer_workspace_size(n, 8, 8, 64), dev)
+    w = _layer_ptrs(params)
+    rc = lib.gt_layer_fwd(n, 8, 8, 64, _ptr(x), ctypes.byref(w), _ptr(spd), spd.stride(0), _ptr(T), T.shape[1],
+                          _ptr(saved["q"]), _ptr(saved["k"]), _ptr(saved["v"]), _ptr(saved["o"]),
+                          _ptr(saved["lse"]), _ptr(y), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check("gt_layer_fwd", rc)
+    return y, saved
+
+
+def gt_layer_bwd(x, params: dict, spd, T, saved: dict, dy, workspace=None, stream=None):
+    """GT encoder layer backward: (dx, {weight name: gradient}, dT)."""
+    lib = load_library()
+    _need_cuda(x, spd, T, dy)
+    n = x.shape[0]
+    dev = x.device
+    grads = {name: torch.empty_like(params[name]) for name in LAYER_PARAMS}
+    dx = torch.empty_like(x)
+    dT = torch.empty_like(T)
+    if workspace is None:
+        workspace = _workspace(lib.gt_layer_workspace_size(n, 8, 8, 64), dev)
+    w = _layer_ptrs(params)
+    g = _layer_ptrs(grads)
+    rc = lib.gt_layer_bwd(n, 8, 8, 64, _ptr(x), ctypes.byref(w), _ptr(spd), spd.stride(0), _ptr(T), T.shape[1],
+                          _ptr(saved["q"]), _ptr(saved["k"]), _ptr(saved["v"]), _ptr(saved["o"]),
+                          _ptr(saved["lse"]), _ptr(dy), _ptr(dx), ctypes.byref(g), _ptr(dT), _ptr(workspace),
+                          workspace.numel(), _stream_handle(stream))
+    _check("gt_layer_bwd", rc)
+    return dx, grads, dT
 
 
 def gt_check_device_status(stream=None) -> None:

@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libgt.so")
 
 SOURCES = ["gt_abi.cu", "gt_spd.cu", "gt_attn_simt.cu", "gt_noalloc.cu", "gt_attn_fwd_tc.cu",
            "gt_attn_bwd_tc.cu", "gt_attn_bwd_dq.cu",
-           "gt_attn_bwd_dkdv.cu", "gt_stats.cu", "gt_selftest.cu"]
+           "gt_attn_bwd_dkdv.cu", "gt_stats.cu", "gt_selftest.cu", "gt_layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

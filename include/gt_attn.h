@@ -227,6 +227,60 @@ int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
                              const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
                              float scale, void* dq, void* dk, void* dv, float* dT, void* stream);
 
+/*
+ * The GT encoder layer around the biased attention (MegaGraph, Fig. 8: 8 heads,
+ * hidden and FFN width 64).  The pages give the widths, not the order of the
+ * steps; this is the pre-LayerNorm (Graphormer) encoder layer:
+ *
+ *   u = LN1(x); [q|k|v] = u W_qkv + b_qkv; o = biased attention(q, k, v);
+ *   hh = x + o W_o + b_o; z = LN2(hh); y = hh + GELU(z W_1 + b_1) W_2 + b_2
+ *
+ * with LN(v) = gain (v - mean v) / sqrt(var v + 1e-5) + shift over the 64
+ * features of a node, GELU(a) = a Phi(a) (Phi the normal CDF), the attention
+ * scale 1/sqrt(8), and q, k, v split into heads as [n][8][8] (feature = head * 8
+ * + channel).  Supported: h = 8, d = 8, f = 64 (else GT_ERR_UNSUPPORTED); the
+ * attention runs in bf16 on the tensor cores.
+ *
+ * All weights are device fp32, row-major: ln*_g / ln*_b [64]; w_qkv [64][192]
+ * (columns q | k | v); b_qkv [192]; w_o [64][64]; b_o [64]; w_1 [64][64] (in x
+ * out); b_1 [64]; w_2 [64][64]; b_2 [64].  gt_layer_grads has the same shapes
+ * and receives dL/d(weight) (overwritten).
+ */
+typedef struct {
+    const float *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_g, *ln2_b, *w_1, *b_1, *w_2, *b_2;
+} gt_layer_weights;
+
+typedef struct {
+    float *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_g, *ln2_b, *w_1, *b_1, *w_2, *b_2;
+} gt_layer_grads;
+
+/* Workspace bytes of gt_layer_fwd and gt_layer_bwd (one buffer serves both);
+ * 0 for unsupported sizes. */
+size_t gt_layer_workspace_size(int32_t n, int32_t h, int32_t d, int32_t f);
+
+/*
+ * gt_layer_fwd: y (device fp32 [n][64]) from x (device fp32 [n][64]).  Also
+ * writes what the backward needs: q, k, v, o (device bf16 [n][8][8]) and lse
+ * (fp32 [8][n]).  spd, ld_spd, T, nb as for gt_bias_attn_fwd.
+ * Errors: GT_ERR_UNSUPPORTED for other sizes, GT_ERR_INVALID_ARG for NULL
+ * pointers (any weight included), the attention's own checks, GT_ERR_WORKSPACE.
+ */
+int gt_layer_fwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, const gt_layer_weights* w,
+                 const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                 void* q, void* k, void* v, void* o, float* lse, float* y,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gt_layer_bwd: given dy = dL/dy (device fp32 [n][64]) and the forward's x, q,
+ * k, v, o, lse: dx (device fp32 [n][64], overwritten), every weight gradient
+ * (overwritten) and dT (fp32 [8][nb], overwritten).  Errors as gt_layer_fwd.
+ */
+int gt_layer_bwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, const gt_layer_weights* w,
+                 const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
+                 const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const float* dy, float* dx, const gt_layer_grads* g, float* dT,
+                 void* workspace, size_t ws_bytes, void* stream);
+
 /* Static English text for a gt_status value. */
 const char* gt_status_string(int status);
 

@@ -58,6 +58,12 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, fake, 8, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 20, 2, 3, fake, 24, fake, 1 << 20, None) == -1
     assert lib.gt_spd_build(fake, fake, 4, 2, 3, P(0x1001), 16, fake, 1 << 20, None) == -1
+    # GT layer: unsupported widths, NULL weights
+    assert lib.gt_layer_fwd(100, 4, 8, 64, fake, fake, fake, 112, fake, 8, fake, fake, fake, fake, fake, fake,
+                            fake, 1 << 20, None) == -2
+    assert lib.gt_layer_fwd(100, 8, 8, 64, fake, None, fake, 112, fake, 8, fake, fake, fake, fake, fake, fake,
+                            fake, 1 << 20, None) == -1
+    assert lib.gt_layer_workspace_size(100, 8, 16, 64) == 0 and lib.gt_layer_workspace_size(100, 8, 8, 64) > 0
     # bounded-wait self-test: limits out of range
     assert lib.gt_selftest_wait_timeout(ctypes.c_int64(10), None) == -1
     assert lib.gt_selftest_wait_timeout(ctypes.c_int64(2_000_000_000), None) == -1
