@@ -373,6 +373,95 @@ def memory_line(w: gi.Workload, dev) -> dict:
             "process_peak_allocated_bytes": int(torch.cuda.max_memory_allocated(dev))}
 
 
+# ------------------------------------------------- the GT layer stack (Fig. 8)
+
+LAYER_METRIC = "GT layer stack (pre-LN, QKV/O projections, GELU FFN, biased attention) fwd+bwd TFLOP/s on 1 GB300"
+LAYER_DENSE_FLOPS_PER_ROW = 3 * 2 * 64 * (3 * 64 + 64 + 64 + 64)   # fwd + bwd (dx and dW) of the four matmuls
+
+
+def run_layer(args, w: gi.Workload, rank: int, world: int) -> dict | None:
+    """One step = SPD build + every layer's forward and backward (gt_layer_fwd /
+    gt_layer_bwd), layers independent (each with its own seeded weights, x, dy)."""
+    import torch
+    import graph_transformer_attention_gb300 as gt
+    from graph_transformer_attention_gb300 import build as gtb
+
+    if w.heads != 8 or w.head_dim != 8 or w.dtype != "bf16":
+        raise SystemExit(f"--model gt-layer needs a bf16 workload with 8 heads of width 8 (not {w.name})")
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(gt.library_path()):
+        gtb.build()
+    if world > 1:
+        torch.distributed.barrier()
+    gt.load_library()
+    stream = torch.cuda.current_stream()
+    g = gi.config_graph(w)
+    n = w.n
+    d_ip, d_ix = torch.from_numpy(g.indptr).to(dev), torch.from_numpy(g.indices).to(dev)
+    spd = torch.empty((n, gt.spd_ld(n)), dtype=torch.int8, device=dev)
+    ws_spd = torch.empty(gt.gt_spd_workspace_size(n, g.nnz, w.D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(gt.gt_layer_workspace_size(n), dtype=torch.uint8, device=dev)
+    layers = []
+    for li in range(w.layers):
+        p = gi.make_gt_layer_params(64, 64, w.nb, 8, seed=w.tensor_seed(li))
+        io = gi.make_gt_layer_io(n, 64, seed=w.tensor_seed(li) + 50)
+        layers.append(dict(params={k: torch.from_numpy(v).to(dev) for k, v in p.items() if k != "T"},
+                           T=torch.from_numpy(p["T"]).to(dev), x=torch.from_numpy(io["x"]).to(dev),
+                           dy=torch.from_numpy(io["dy"]).to(dev)))
+
+    def step():
+        gt.gt_spd_build(d_ip, d_ix, n, w.D, out=spd, workspace=ws_spd)
+        for L in layers:
+            y, saved = gt.gt_layer_fwd(L["x"], L["params"], spd, L["T"], workspace=ws)
+            gt.gt_layer_bwd(L["x"], L["params"], spd, L["T"], saved, L["dy"], workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    gt.gt_check_device_status()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gt.gt_kernel_stats_reset(False)
+    with ClockSampler(dev.index) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    gt.gt_check_device_status()
+    launches = sum(c for c, _ in gt.gt_kernel_stats().values())
+    gt.gt_kernel_stats_reset(True)
+    for _ in range(min(args.steps, 3)):
+        step()
+    torch.cuda.synchronize()
+    kst = gt.gt_kernel_stats()
+    gt.gt_kernel_stats_reset(False)
+    nk = min(args.steps, 3)
+    kernels = {k: {"launches_per_step": c / nk, "ms_per_launch": t / c} for k, (c, t) in kst.items() if c}
+    (ms_total,) = max_over_ranks([ms_total], world, dev)
+    if rank != 0:
+        return None
+    flops = w.layers * (14.0 * n * n * 8 * 8 + LAYER_DENSE_FLOPS_PER_ROW * n)
+    around = ("layer_ln_qkv", "layer_out_ffn", "layer_ffn_bwd", "layer_qkv_bwd", "layer_grad_sum")
+    per_step = {k: v["launches_per_step"] * v["ms_per_launch"] for k, v in kernels.items()}
+    return {
+        "metric": LAYER_METRIC, "value": round(whole_job_tflops(flops, args.steps, ms_total, world), 3),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 attention, fp32 around it",
+        "data": "synthetic (seeded random graph, weights, x and dy)",
+        "config": {**workload_config(w), "model": "GT encoder layer, 8 heads, hidden 64, FFN 64"},
+        "kernels_ms": {k: {"launches_per_step": round(v["launches_per_step"], 3),
+                           "ms_per_launch": round(v["ms_per_launch"], 4)} for k, v in kernels.items()},
+        "around_attention_ms_per_step": round(sum(per_step.get(k, 0.0) for k in around), 4),
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+    }
+
+
 # --------------------------------------------------------- CPU oracle arm
 
 def oracle_sample(w: gi.Workload, rows_per_step: int, seed: int = 0):
@@ -437,7 +526,12 @@ def main(argv=None) -> int:
                     help="rows (and columns) the CPU oracle processes per sample "
                          "(default: N/2 for the baseline line, N/8 per reference step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--model", choices=["attention", "gt-layer"], default="attention",
+                    help="attention: the biased-attention path (default); gt-layer: the whole encoder "
+                         "layer around it (default workload then ba6800x16)")
     args = ap.parse_args(argv)
+    if args.model == "gt-layer" and "--config" not in (argv if argv is not None else sys.argv):
+        args.config = 3
     w = gi.CONFIGS[args.config]
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -450,6 +544,14 @@ def main(argv=None) -> int:
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if args.model == "gt-layer":
+        line = run_layer(args, w, rank, world)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return 0
     line = run_gpu(args, w, rank, world)
     if rank == 0 and line is not None:
         if world == 1 and not args.no_cpu_baseline:

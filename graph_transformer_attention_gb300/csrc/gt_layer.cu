@@ -21,9 +21,10 @@
 //                   db_qkv, dLN1
 // Weight gradients: the 8 warps of a CTA each leave one row's vectors in shared
 // memory; then every thread adds the 8 rows' outer products into its own
-// registers (16 or 48 entries of each matrix); at the end one atomicAdd per entry
-// into the fp32 gradient.  The attention itself is the library's tensor-core
-// forward and backward.
+// registers (16 or 48 entries of each matrix); at the end each CTA stores its
+// sums in its own row of a partials buffer, which reduce_partials adds up in a
+// fixed order (deterministic, no atomics).  The attention itself is the
+// library's tensor-core forward and backward.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -54,9 +55,29 @@ __device__ __forceinline__ float gelu_grad(float a) {
     return 0.5f * (1.0f + erff(a * 0.70710678118654752f)) + a * 0.39894228040143268f * expf(-0.5f * a * a);
 }
 
-// Copy a [rows][cols] fp32 matrix into shared memory with row stride `stride`.
-__device__ __forceinline__ void load_mat(float* dst, const float* src, int rows, int cols, int stride) {
-    for (int i = threadIdx.x; i < rows * cols; i += blockDim.x) dst[(i / cols) * stride + (i % cols)] = src[i];
+// Copy a [ROWS][COLS] fp32 matrix (16-byte aligned, COLS % 4 == 0) into shared
+// memory with row stride `stride`: 16-byte loads, all of a thread's in flight
+// before its stores.
+template <int ROWS, int COLS>
+__device__ __forceinline__ void load_mat(float* dst, const float* src, int stride) {
+    constexpr int kN4 = ROWS * COLS / 4;
+    constexpr int kPer = (kN4 + kThreads - 1) / kThreads;
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = threadIdx.x + u * kThreads;
+        if (i < kN4) v[u] = __ldg(s4 + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i = threadIdx.x + u * kThreads;
+        if (i < kN4) {
+            const int r = i / (COLS / 4), c = 4 * (i % (COLS / 4));
+            float* d = dst + r * stride + c;
+            d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+        }
+    }
 }
 
 // out[j] for j = lane + 32 i (i < NO): b[j] + sum_k in[k] W[k][j]; `in` in shared memory.
@@ -126,11 +147,49 @@ __device__ __forceinline__ void outer_acc(const float* A, int astride, const flo
     }
 }
 
+// This thread's entries of a [64][ncols] partial sum, stored (the CTA's own copy).
 template <int E>
-__device__ __forceinline__ void flush_outer(float* g, int ncols, const float (&acc)[E]) {
+__device__ __forceinline__ void store_outer(float* g, int ncols, const float (&acc)[E]) {
     const int f = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * E;
 #pragma unroll
-    for (int i = 0; i < E; ++i) atomicAdd(g + f * ncols + c0 + i, acc[i]);
+    for (int i = 0; i < E; i += 4)
+        *reinterpret_cast<float4*>(g + f * ncols + c0 + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+}
+
+// Per-CTA partial weight gradients: each CTA stores its sums in its own row of
+// `part` ([nparts][kPartStride]); reduce_partials adds the rows in a fixed
+// order (no atomics: no contention on the few thousand gradient entries, and
+// the same result on every run) into the gradient arrays.
+constexpr int kPartStride = kC * 3 * kC + 5 * kC;   // the larger of the two kernels' layouts (12608)
+
+struct PartSegs {
+    float* dst[8];
+    int off[8];
+    int nseg;
+};
+
+// One CTA per 32 consecutive entries: warp w adds partial rows w, w + 8, ...
+// (coalesced along the entries), then warp 0 adds the 8 warp sums.
+__global__ void __launch_bounds__(256) reduce_partials(const float* __restrict__ part, int nparts, PartSegs sg,
+                                                       int total) {
+    __shared__ float red[8][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int i = blockIdx.x * 32 + tx;
+    float acc = 0.f;
+    if (i < total) {
+#pragma unroll 4
+        for (int p = ty; p < nparts; p += 8) acc += part[(size_t)p * kPartStride + i];
+    }
+    red[ty][tx] = acc;
+    __syncthreads();
+    if (ty == 0 && i < total) {
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) sum += red[r][tx];
+        int seg = 0;
+        while (seg + 1 < sg.nseg && i >= sg.off[seg + 1]) ++seg;
+        sg.dst[seg][i - sg.off[seg]] = sum;
+    }
 }
 
 // ------------------------------------------------------------------ forward
@@ -148,7 +207,7 @@ layer_ln_qkv(int n, const float* __restrict__ x, const float* __restrict__ ln_g,
              __nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ v) {
     extern __shared__ float4 smem_f4[];
     SmemQkv& S = *reinterpret_cast<SmemQkv*>(smem_f4);
-    load_mat(S.w, w_qkv, kC, 3 * kC, kS3);
+    load_mat<kC, 3 * kC>(S.w, w_qkv, kS3);
     for (int i = threadIdx.x; i < 3 * kC; i += blockDim.x) S.b[i] = b_qkv[i];
     for (int i = threadIdx.x; i < kC; i += blockDim.x) { S.g1[i] = ln_g[i]; S.b1[i] = ln_b[i]; }
     __syncthreads();
@@ -183,9 +242,9 @@ layer_out_ffn(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
               const float* __restrict__ w_2, const float* __restrict__ b_2, float* __restrict__ y) {
     extern __shared__ float4 smem_f4[];
     SmemFfn& S = *reinterpret_cast<SmemFfn*>(smem_f4);
-    load_mat(S.wo, w_o, kC, kC, kS);
-    load_mat(S.w1, w_1, kC, kF, kS);
-    load_mat(S.w2, w_2, kF, kC, kS);
+    load_mat<kC, kC>(S.wo, w_o, kS);
+    load_mat<kC, kF>(S.w1, w_1, kS);
+    load_mat<kF, kC>(S.w2, w_2, kS);
     for (int i = threadIdx.x; i < kC; i += blockDim.x) {
         S.bo[i] = b_o[i]; S.b1[i] = b_1[i]; S.b2[i] = b_2[i]; S.g2[i] = ln_g[i]; S.s2[i] = ln_b[i];
     }
@@ -236,14 +295,12 @@ layer_ffn_bwd(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
               const float* __restrict__ dy, const float* __restrict__ w_o, const float* __restrict__ b_o,
               const float* __restrict__ ln_g, const float* __restrict__ ln_b, const float* __restrict__ w_1,
               const float* __restrict__ b_1, const float* __restrict__ w_2, __nv_bfloat16* __restrict__ dO,
-              float* __restrict__ dh, float* __restrict__ g_w2, float* __restrict__ g_b2,
-              float* __restrict__ g_w1, float* __restrict__ g_b1, float* __restrict__ g_wo,
-              float* __restrict__ g_bo, float* __restrict__ g_ln2g, float* __restrict__ g_ln2b) {
+              float* __restrict__ dh, float* __restrict__ part) {
     extern __shared__ float4 smem_f4[];
     SmemFfnBwd& S = *reinterpret_cast<SmemFfnBwd*>(smem_f4);
-    load_mat(S.wo, w_o, kC, kC, kS);
-    load_mat(S.w1, w_1, kC, kF, kS);
-    load_mat(S.w2, w_2, kF, kC, kS);
+    load_mat<kC, kC>(S.wo, w_o, kS);
+    load_mat<kC, kF>(S.w1, w_1, kS);
+    load_mat<kF, kC>(S.w2, w_2, kS);
     for (int i = threadIdx.x; i < kC; i += blockDim.x) {
         S.bo[i] = b_o[i]; S.b1[i] = b_1[i]; S.g2[i] = ln_g[i]; S.s2[i] = ln_b[i];
     }
@@ -318,16 +375,13 @@ layer_ffn_bwd(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
         }
         __syncthreads();
     }
-    flush_outer<16>(g_w2, kC, aw2);
-    flush_outer<16>(g_w1, kF, aw1);
-    flush_outer<16>(g_wo, kC, awo);
-    if (tid < kC) {
-        atomicAdd(g_b2 + tid, avec[0]);
-        atomicAdd(g_b1 + tid, avec[1]);
-        atomicAdd(g_bo + tid, avec[2]);
-        atomicAdd(g_ln2g + tid, avec[3]);
-        atomicAdd(g_ln2b + tid, avec[4]);
-    }
+    // partial layout: dW_2, dW_1, dW_o (4096 each), then db_2, db_1, db_o, dLN2 gain, shift
+    float* pp = part + (size_t)blockIdx.x * kPartStride;
+    store_outer<16>(pp, kC, aw2);
+    store_outer<16>(pp + kF * kC, kF, aw1);
+    store_outer<16>(pp + 2 * kC * kC, kC, awo);
+    if (tid < kC)
+        for (int i = 0; i < 5; ++i) pp[3 * kC * kC + i * kC + tid] = avec[i];
 }
 
 enum { kQu = 0, kQduh = 64, kQdu = 128, kQdqkv = 192, kQvec = 384 };
@@ -342,11 +396,10 @@ __global__ void __launch_bounds__(kThreads)
 layer_qkv_bwd(int n, const float* __restrict__ x, const float* __restrict__ ln_g, const float* __restrict__ ln_b,
               const float* __restrict__ w_qkv, const __nv_bfloat16* __restrict__ dq,
               const __nv_bfloat16* __restrict__ dk, const __nv_bfloat16* __restrict__ dv,
-              const float* __restrict__ dh, float* __restrict__ dx, float* __restrict__ g_wqkv,
-              float* __restrict__ g_bqkv, float* __restrict__ g_ln1g, float* __restrict__ g_ln1b) {
+              const float* __restrict__ dh, float* __restrict__ dx, float* __restrict__ part) {
     extern __shared__ float4 smem_f4[];
     SmemQkvBwd& S = *reinterpret_cast<SmemQkvBwd*>(smem_f4);
-    load_mat(S.w, w_qkv, kC, 3 * kC, kS3);
+    load_mat<kC, 3 * kC>(S.w, w_qkv, kS3);
     for (int i = threadIdx.x; i < kC; i += blockDim.x) { S.g1[i] = ln_g[i]; S.b1[i] = ln_b[i]; }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     float aw[48] = {};
@@ -388,14 +441,19 @@ layer_qkv_bwd(int n, const float* __restrict__ x, const float* __restrict__ ln_g
             for (int r = 0; r < kWarps; ++r) { ag += S.rowv[r][kQduh + tid]; as += S.rowv[r][kQdu + tid]; }
         __syncthreads();
     }
-    flush_outer<48>(g_wqkv, 3 * kC, aw);
-    if (tid < 3 * kC) atomicAdd(g_bqkv + tid, ab);
-    if (tid < kC) { atomicAdd(g_ln1g + tid, ag); atomicAdd(g_ln1b + tid, as); }
+    // partial layout: dW_qkv (64 x 192), db_qkv (192), dLN1 gain, shift
+    float* pp = part + (size_t)blockIdx.x * kPartStride;
+    store_outer<48>(pp, 3 * kC, aw);
+    if (tid < 3 * kC) pp[3 * kC * kC + tid] = ab;
+    if (tid < kC) { pp[3 * kC * kC + 3 * kC + tid] = ag; pp[3 * kC * kC + 4 * kC + tid] = as; }
 }
 
-int row_grid(int n) {
+// one row per warp while the rows last, at most `per_sm` CTAs per SM (what the
+// kernel's shared memory lets an SM hold): more warps in flight hide the
+// shared-memory latency of the row products
+int row_grid(int n, int per_sm) {
     const int want = (n + kWarps - 1) / kWarps;
-    const int cap = 2 * num_sms();
+    const int cap = per_sm * num_sms();
     return want < cap ? want : cap;
 }
 
@@ -406,7 +464,8 @@ bool set_smem(K kern, size_t bytes) {
 
 bool weights_ok(const gt_layer_weights* w) {
     return w && w->ln1_g && w->ln1_b && w->w_qkv && w->b_qkv && w->w_o && w->b_o && w->ln2_g && w->ln2_b &&
-           w->w_1 && w->b_1 && w->w_2 && w->b_2;
+           w->w_1 && w->b_1 && w->w_2 && w->b_2 && aligned16(w->w_qkv) && aligned16(w->w_o) &&
+           aligned16(w->w_1) && aligned16(w->w_2);
 }
 
 bool grads_ok(const gt_layer_grads* g) {
@@ -419,6 +478,7 @@ bool grads_ok(const gt_layer_grads* g) {
 struct LayerBwdWs {
     __nv_bfloat16* dO;
     float* dh;
+    float* part;
     __nv_bfloat16 *dq, *dk, *dv;
     void* attn;
     size_t attn_bytes;
@@ -430,6 +490,7 @@ size_t layer_bwd_carve(int n, void* ws, size_t bytes, LayerBwdWs* out) {
     LayerBwdWs w;
     w.dO = c.take<__nv_bfloat16>(e);
     w.dh = c.take<float>(e);
+    w.part = c.take<float>((size_t)row_grid(n, 2) * kPartStride);
     w.dq = c.take<__nv_bfloat16>(e);
     w.dk = c.take<__nv_bfloat16>(e);
     w.dv = c.take<__nv_bfloat16>(e);
@@ -459,11 +520,10 @@ int gt_layer_fwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     if (h != 8 || d != 8 || f != kF) return GT_ERR_UNSUPPORTED;
     if (n < 1 || !x || !gt::weights_ok(w) || !q || !k || !v || !o || !lse || !y) return GT_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = row_grid(n);
     if (!set_smem(layer_ln_qkv, sizeof(SmemQkv)) || !set_smem(layer_out_ffn, sizeof(SmemFfn))) return GT_ERR_CUDA;
     {
         LaunchScope ls("layer_ln_qkv", s);
-        layer_ln_qkv<<<grid, kThreads, sizeof(SmemQkv), s>>>(
+        layer_ln_qkv<<<row_grid(n, 2), kThreads, sizeof(SmemQkv), s>>>(
             n, x, w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, static_cast<__nv_bfloat16*>(q),
             static_cast<__nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(v));
     }
@@ -474,7 +534,7 @@ int gt_layer_fwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     if (rc != GT_OK) return rc;
     {
         LaunchScope ls("layer_out_ffn", s);
-        layer_out_ffn<<<grid, kThreads, sizeof(SmemFfn), s>>>(
+        layer_out_ffn<<<row_grid(n, 2), kThreads, sizeof(SmemFfn), s>>>(
             n, x, static_cast<const __nv_bfloat16*>(o), w->w_o, w->b_o, w->ln2_g, w->ln2_b, w->w_1, w->b_1,
             w->w_2, w->b_2, y);
     }
@@ -494,21 +554,23 @@ int gt_layer_bwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     const size_t need = layer_bwd_carve(n, workspace, ws_bytes, &ws);
     if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the weight gradients accumulate atomically: start from zero
-    const struct { float* p; size_t count; } zero[] = {
-        {g->ln1_g, kC}, {g->ln1_b, kC}, {g->w_qkv, (size_t)kC * 3 * kC}, {g->b_qkv, 3 * kC},
-        {g->w_o, kC * kC}, {g->b_o, kC}, {g->ln2_g, kC}, {g->ln2_b, kC}, {g->w_1, kC * kF}, {g->b_1, kF},
-        {g->w_2, kF * kC}, {g->b_2, kC}};
-    for (const auto& z : zero)
-        if (cudaMemsetAsync(z.p, 0, z.count * sizeof(float), s) != cudaSuccess) return GT_ERR_CUDA;
-    const int grid = row_grid(n);
     if (!set_smem(layer_ffn_bwd, sizeof(SmemFfnBwd)) || !set_smem(layer_qkv_bwd, sizeof(SmemQkvBwd)))
         return GT_ERR_CUDA;
+    const int grid = row_grid(n, 2);
+    const int rgrid = (kPartStride + 31) / 32;
     {
         LaunchScope ls("layer_ffn_bwd", s);
         layer_ffn_bwd<<<grid, kThreads, sizeof(SmemFfnBwd), s>>>(
             n, x, static_cast<const __nv_bfloat16*>(o), dy, w->w_o, w->b_o, w->ln2_g, w->ln2_b, w->w_1, w->b_1,
-            w->w_2, ws.dO, ws.dh, g->w_2, g->b_2, g->w_1, g->b_1, g->w_o, g->b_o, g->ln2_g, g->ln2_b);
+            w->w_2, ws.dO, ws.dh, ws.part);
+    }
+    {
+        PartSegs sg = {{g->w_2, g->w_1, g->w_o, g->b_2, g->b_1, g->b_o, g->ln2_g, g->ln2_b},
+                       {0, kF * kC, 2 * kC * kC, 3 * kC * kC, 3 * kC * kC + kC, 3 * kC * kC + 2 * kC,
+                        3 * kC * kC + 3 * kC, 3 * kC * kC + 4 * kC},
+                       8};
+        LaunchScope ls("layer_grad_sum", s);
+        reduce_partials<<<rgrid, 256, 0, s>>>(ws.part, grid, sg, 3 * kC * kC + 5 * kC);
     }
     if (check_launch() != GT_OK) return GT_ERR_CUDA;
     const float scale = 0.35355339059327373f;
@@ -518,8 +580,14 @@ int gt_layer_bwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     {
         LaunchScope ls("layer_qkv_bwd", s);
         layer_qkv_bwd<<<grid, kThreads, sizeof(SmemQkvBwd), s>>>(n, x, w->ln1_g, w->ln1_b, w->w_qkv, ws.dq, ws.dk,
-                                                                  ws.dv, ws.dh, dx, g->w_qkv, g->b_qkv, g->ln1_g,
-                                                                  g->ln1_b);
+                                                                 ws.dv, ws.dh, dx, ws.part);
+    }
+    {
+        PartSegs sg = {{g->w_qkv, g->b_qkv, g->ln1_g, g->ln1_b},
+                       {0, 3 * kC * kC, 3 * kC * kC + 3 * kC, 3 * kC * kC + 4 * kC},
+                       4};
+        LaunchScope ls("layer_grad_sum", s);
+        reduce_partials<<<rgrid, 256, 0, s>>>(ws.part, grid, sg, 3 * kC * kC + 5 * kC);
     }
     return check_launch();
 }

@@ -243,8 +243,8 @@ int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
  *
  * All weights are device fp32, row-major: ln*_g / ln*_b [64]; w_qkv [64][192]
  * (columns q | k | v); b_qkv [192]; w_o [64][64]; b_o [64]; w_1 [64][64] (in x
- * out); b_1 [64]; w_2 [64][64]; b_2 [64].  gt_layer_grads has the same shapes
- * and receives dL/d(weight) (overwritten).
+ * out); b_1 [64]; w_2 [64][64]; b_2 [64]; the four matrices 16-byte aligned.
+ * gt_layer_grads has the same shapes and receives dL/d(weight) (overwritten).
  */
 typedef struct {
     const float *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o, *ln2_g, *ln2_b, *w_1, *b_1, *w_2, *b_2;
@@ -263,7 +263,8 @@ size_t gt_layer_workspace_size(int32_t n, int32_t h, int32_t d, int32_t f);
  * writes what the backward needs: q, k, v, o (device bf16 [n][8][8]) and lse
  * (fp32 [8][n]).  spd, ld_spd, T, nb as for gt_bias_attn_fwd.
  * Errors: GT_ERR_UNSUPPORTED for other sizes, GT_ERR_INVALID_ARG for NULL
- * pointers (any weight included), the attention's own checks, GT_ERR_WORKSPACE.
+ * pointers (any weight included) or unaligned matrices, the attention's own
+ * checks, GT_ERR_WORKSPACE.
  */
 int gt_layer_fwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, const gt_layer_weights* w,
                  const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,

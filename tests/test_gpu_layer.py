@@ -61,6 +61,7 @@ def test_layer_forward_and_backward_match_the_oracle(gt, n, graph, D):
             "dx": _rel(dx, gr["x"]), "dT": _rel(dT, gr["T"])}
     for name in L_PARAMS:
         errs["d" + name] = _rel(grads[name], gr[name])
+    print(f"layer n={n}: " + ", ".join(f"{k} {v:.1e}" for k, v in errs.items()))
     bad = {k: v for k, v in errs.items() if not v <= TOL}
     assert not bad, f"relative L2 above {TOL}: {bad} (all: {errs})"
 
