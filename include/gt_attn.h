@@ -19,9 +19,12 @@
  * Conventions for every call below
  *   - Pointers named as device buffers must be device memory of the current
  *     CUDA device.  The caller owns and allocates every buffer, including the
- *     workspace; the library allocates nothing and keeps no state between
- *     calls (apart from one device status word, see gt_check_device_status,
- *     and the launch statistics at the end of this header).
+ *     workspace; the library allocates no device memory and keeps no state
+ *     between calls (apart from one device status word, see
+ *     gt_check_device_status, the launch statistics at the end of this header,
+ *     and, per device, one internal stream and two events that the tensor-core
+ *     backward creates on first use to run two of its kernels side by side,
+ *     forked from and joined back into the caller's stream).
  *   - Layouts are dense row-major: q, k, v, o, dO, dq, dk, dv are [n][h][d]
  *     (node, head, channel); lse is [h][n] fp32; T and dT are [h][nb] fp32;
  *     spd is int8 [n][ld_spd] (row i holds the bucket codes of pairs (i, *)).

@@ -22,7 +22,16 @@ import torch
 
 from oracle import oracle as O
 
-torch.set_default_dtype(torch.float64)
+
+
+@pytest.fixture(autouse=True)
+def _fp64_default():
+    """fp64 as torch's default dtype inside this module's tests only (set at
+    import it would leak into every test collected after it)."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def _case(n, h, d, nb, seed, t_std=1.0, sym=False):
