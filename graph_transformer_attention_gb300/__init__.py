@@ -85,6 +85,8 @@ def load_library():
         lib.gt_spd_build_algo.restype = ctypes.c_int
         lib.gt_bias_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_workspace_size.restype = sz
+        lib.gt_bias_attn_fwd_kv_block.argtypes = [i32, i32, i32, i32, i32]
+        lib.gt_bias_attn_fwd_kv_block.restype = i32
         lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
                                          P, P, P, sz, P]
         lib.gt_bias_attn_fwd.restype = ctypes.c_int
@@ -152,12 +154,12 @@ def spd_ld(n: int) -> int:
 
 
 def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0) -> dict:
-    """Number of libgt kernels each entry point launches for these sizes (memsets
-    not counted), mirroring the dispatch in gt_abi.cu."""
-    nsplit = -(-n // kv_block) if kv_block and kv_block < n else 1
-    fwd = 1 + (1 if nsplit > 1 else 0)
-    bwd = 4
-    return {"spd": 4, "fwd": fwd, "bwd": bwd}
+    """Number of libgt kernels gt_bias_attn_fwd and gt_bias_attn_bwd launch for
+    these sizes on the current device (memsets not counted)."""
+    code = GT_F32 if dtype == "f32" else GT_BF16
+    kvb = int(load_library().gt_bias_attn_fwd_kv_block(code, n, h, d, kv_block))
+    nsplit = -(-n // kvb) if kvb > 0 else 1
+    return {"fwd": 1 + (1 if nsplit > 1 else 0), "bwd": 4}
 
 
 def gt_status_string(status: int) -> str:

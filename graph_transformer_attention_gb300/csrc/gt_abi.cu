@@ -83,6 +83,21 @@ struct BwdWs {
     float* aux;     // [16]: per head the largest row norm of v (tensor-core path)
 };
 
+// The KV block the forward uses.  An explicit kv_block is kept; with 0 the
+// tensor-core path splits the KV columns itself when the graph has too few
+// 128-row tiles to give every SM two CTAs (grid = tiles x 2 head halves x
+// splits), and merges the partials exactly: up to 4 splits, each a multiple of
+// 128 columns.
+int effective_kv_block(int dtype, int n, int h, int d, int kv_block) {
+    if (kv_block > 0 || dtype != GT_BF16 || !fwd_tc_supported(h, d)) return kv_block;
+    const int ctas = 2 * ((n + 127) / 128);
+    int nsplit = 2 * num_sms() / ctas;
+    if (nsplit > 4) nsplit = 4;
+    if (nsplit < 2) return 0;
+    const int per = ((n + nsplit - 1) / nsplit + 127) / 128 * 128;
+    return per >= n ? 0 : per;
+}
+
 size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
     Carve c(base, cap);
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
@@ -156,9 +171,16 @@ int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64
 
 size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
-    size_t a = gt::fwd_ws(n, h, d, kv_block, nullptr, 0, nullptr);
+    if (kv_block >= n) kv_block = 0;
+    size_t a = gt::fwd_ws(n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
     size_t b = gt::bwd_ws(n, h, d, nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
+}
+
+int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
+    if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return -1;
+    if (kv_block >= n) kv_block = 0;
+    return gt::effective_kv_block(dtype, n, h, d, kv_block);
 }
 
 int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,
@@ -170,6 +192,7 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     if (!o || !lse || !gt::aligned16(o)) return GT_ERR_INVALID_ARG;
     if (kv_block < 0 || (kv_block > 0 && kv_block % 128 != 0)) return GT_ERR_INVALID_ARG;
     if (kv_block >= n) kv_block = 0;
+    kv_block = gt::effective_kv_block(dtype, n, h, d, kv_block);
     const size_t need = gt::fwd_ws(n, h, d, kv_block, nullptr, 0, nullptr);
     if (need > 0 && (!workspace || ws_bytes < need)) return GT_ERR_WORKSPACE;
     gt::FwdWs w;

@@ -120,6 +120,16 @@ int gt_spd_build_algo(int32_t algo, const int64_t* indptr, const int32_t* indice
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The KV block gt_bias_attn_fwd uses for these arguments on the current device
+ * (0 = one pass over all columns; -1 for invalid arguments).  An explicit
+ * kv_block (< n) is used as given.  With kv_block = 0 the bf16 tensor-core path
+ * splits the columns itself when the graph has too few 128-row tiles to give
+ * every SM two CTAs (up to 4 splits of a multiple of 128 columns, merged
+ * exactly, as with an explicit kv_block).
+ */
+int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block);
+
+/*
  * Bytes of device workspace needed by gt_bias_attn_fwd (with this kv_block)
  * and by gt_bias_attn_bwd for these sizes; one buffer of this size serves both.
  */
