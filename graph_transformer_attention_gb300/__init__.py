@@ -87,6 +87,8 @@ def load_library():
         lib.gt_bias_attn_workspace_size.restype = sz
         lib.gt_bias_attn_fwd_kv_block.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_fwd_kv_block.restype = i32
+        lib.gt_bias_attn_bwd_split.argtypes = [i32, i32, i32, i32, i32]
+        lib.gt_bias_attn_bwd_split.restype = i32
         lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
                                          P, P, P, sz, P]
         lib.gt_bias_attn_fwd.restype = ctypes.c_int
@@ -153,13 +155,15 @@ def spd_ld(n: int) -> int:
     return (n + 15) // 16 * 16
 
 
-def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0) -> dict:
+def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0, nb: int = 18) -> dict:
     """Number of libgt kernels gt_bias_attn_fwd and gt_bias_attn_bwd launch for
     these sizes on the current device (memsets not counted)."""
+    lib = load_library()
     code = GT_F32 if dtype == "f32" else GT_BF16
-    kvb = int(load_library().gt_bias_attn_fwd_kv_block(code, n, h, d, kv_block))
+    kvb = int(lib.gt_bias_attn_fwd_kv_block(code, n, h, d, kv_block))
     nsplit = -(-n // kvb) if kvb > 0 else 1
-    return {"fwd": 1 + (1 if nsplit > 1 else 0), "bwd": 4}
+    split = int(lib.gt_bias_attn_bwd_split(code, n, h, d, nb))
+    return {"fwd": 1 + (1 if nsplit > 1 else 0), "bwd": 4 + (1 if split > 1 else 0)}
 
 
 def gt_status_string(status: int) -> str:

@@ -39,7 +39,7 @@ bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
-                double* dT64, float* aux, cudaStream_t s);
+                double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -81,6 +81,7 @@ struct BwdWs {
     double* dT64;
     float* LD;
     float* aux;     // [16]: per head the largest row norm of v (tensor-core path)
+    float* acc;     // split backward: fp32 dq, dk, dv accumulators, else null
 };
 
 // The KV block the forward uses.  An explicit kv_block is kept; with 0 the
@@ -110,10 +111,22 @@ size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* 
     return c.off;
 }
 
-size_t bwd_ws(int n, int h, int d, void* base, size_t cap, BwdWs* out) {
-    (void)d;
+// Splits of the streamed dimension of the tensor-core backward kernels: with too
+// few 128-row tiles to give every SM two CTAs, each kernel's tiles also split
+// their KV blocks (dq) or query tiles (dk, dv) over up to 4 CTAs, which sum into
+// fp32 accumulators (workspace `acc`, 3 [n][h][d] arrays) turned into bf16 at
+// the end.  1 = no split.
+int bwd_split(int dtype, int n, int h, int d, int nb) {
+    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb)) return 1;
+    const int ctas = 2 * ((n + 127) / 128);
+    int s = 2 * num_sms() / ctas;
+    return s > 4 ? 4 : (s < 2 ? 1 : s);
+}
+
+size_t bwd_ws(int n, int h, int d, int nsplit, void* base, size_t cap, BwdWs* out) {
     Carve c(base, cap);
     BwdWs w;
+    w.acc = nsplit > 1 ? c.take<float>((size_t)3 * n * h * d) : nullptr;
     w.Dv = c.take<float>((size_t)h * n);
     w.dT64 = c.take<double>((size_t)h * 128);
     // per-node lse log2 e (rows 0..7) and D (rows 8..15) of the 8 heads, [16][ld_ld]
@@ -173,8 +186,13 @@ size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t 
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
     size_t a = gt::fwd_ws(n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
-    size_t b = gt::bwd_ws(n, h, d, nullptr, 0, nullptr);
+    size_t b = gt::bwd_ws(n, h, d, gt::bwd_split(dtype, n, h, d, 128), nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
+}
+
+int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb) {
+    if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || nb < 1) return -1;
+    return gt::bwd_split(dtype, n, h, d, nb);
 }
 
 int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
@@ -241,14 +259,18 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     if (!gt::aligned16(o) || !gt::aligned16(dO) || !gt::aligned16(dq) || !gt::aligned16(dk) ||
         !gt::aligned16(dv))
         return GT_ERR_INVALID_ARG;
-    const size_t need = gt::bwd_ws(n, h, d, nullptr, 0, nullptr);
+    // the split needs its accumulators; a workspace sized for the unsplit pass
+    // (a caller's fixed scratch) runs unsplit
+    int nsplit = gt::bwd_split(dtype, n, h, d, nb);
+    if (nsplit > 1 && ws_bytes < gt::bwd_ws(n, h, d, nsplit, nullptr, 0, nullptr)) nsplit = 1;
+    const size_t need = gt::bwd_ws(n, h, d, nsplit, nullptr, 0, nullptr);
     if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
     gt::BwdWs w;
-    gt::bwd_ws(n, h, d, workspace, ws_bytes, &w);
+    gt::bwd_ws(n, h, d, nsplit, workspace, ws_bytes, &w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.Dv, w.dT64, w.aux, s);
+                               w.LD, w.Dv, w.dT64, w.aux, nsplit, w.acc, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

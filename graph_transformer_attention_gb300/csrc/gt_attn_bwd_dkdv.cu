@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
                 const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapL,
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
-                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int* status) {
+                const float* __restrict__ T, int nb, int n, float scale, float scale_log2, int split_tiles,
+                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dk_acc,
+                float* __restrict__ dv_acc, int* status) {
     using C = KvCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -116,7 +117,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = blockIdx.x * kBKV;
     const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
-    const int ntiles = (n + C::BQ - 1) / C::BQ;
+    // Q tiles qt0 .. qt0 + ntiles - 1 (all of them unless the rows are split over
+    // grid.z, in which case dk and dv are summed into dk_acc / dv_acc in fp32)
+    const int total_tiles = (n + C::BQ - 1) / C::BQ;
+    const int qt0 = split_tiles > 0 ? blockIdx.z * split_tiles : 0;
+    const int ntiles = split_tiles > 0 ? min(split_tiles, total_tiles - qt0) : total_tiles;
     const int nchunks = ntiles * C::NCH;
 
     if (tid == kTmaWarp * 32) {
@@ -170,7 +175,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     fail(abort_flag, status);
                 } else {
                     uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                    const int i0 = b * C::BQ;
+                    const int i0 = (qt0 + b) * C::BQ;
                     mbar_arrive_expect_tx(&bars->q_full[ks], C::STAGE_BYTES);
                     tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
 #pragma unroll
@@ -313,7 +318,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const int* meta = reinterpret_cast<const int*>(smem + C::OFF_META) + ks * C::NMETA + (warp & 3);
             // LD rows of this group's first head: row h is 4 BQ bytes long
             const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (kHC * hb) * C::BQ;
-            const int i0 = b * C::BQ;
+            const int i0 = (qt0 + b) * C::BQ;
             const bool tail_tile = i0 + C::BQ > n;
             for (int c = 0; c < C::NCH; ++c, ++t) {
                 if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -443,7 +448,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 tmem_ld_x16(lrow + kColDv + 16 * hh, ov16);
                 tmem_wait_ld();
                 const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
-                if (live) {
+                if (live && dk_acc) {
+                    float* gk = dk_acc + ((int64_t)row * kH + h) * HD;
+                    float* gv = dv_acc + ((int64_t)row * kH + h) * HD;
+#pragma unroll
+                    for (int q2 = 0; q2 < HD; ++q2) {
+                        atomicAdd(gk + q2, __uint_as_float(ok16[c0h + q2]) * scale);
+                        atomicAdd(gv + q2, __uint_as_float(ov16[c0h + q2]));
+                    }
+                } else if (live) {
                     uint32_t wk[HD / 2], wv[HD / 2];
 #pragma unroll
                     for (int q2 = 0; q2 < HD / 2; ++q2) {
@@ -473,8 +486,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, void* dk,
-           void* dv, cudaStream_t s) {
+           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, int nsplit, void* dk,
+           void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
     using C = KvCfg<HD>;
     CUtensorMap mq, mg, ms, ml;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -492,13 +505,16 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         return GT_ERR_CUDA;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
-    dim3 grid((n + kBKV - 1) / kBKV, kH / kHC);
+    const int total_tiles = (n + C::BQ - 1) / C::BQ;
+    const int per = nsplit > 1 ? (total_tiles + nsplit - 1) / nsplit : 0;
+    const int nz = per > 0 ? (total_tiles + per - 1) / per : 1;
+    dim3 grid((n + kBKV - 1) / kBKV, kH / kHC, nz);
     {
         LaunchScope ls("bwd_dkdv", s);
         bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
             mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-            T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dk),
-            static_cast<__nv_bfloat16*>(dv), status);
+            T, nb, n, scale, scale * kLog2e, per, static_cast<__nv_bfloat16*>(dk),
+            static_cast<__nv_bfloat16*>(dv), per > 0 ? dk_acc : nullptr, per > 0 ? dv_acc : nullptr, status);
     }
     return check_launch();
 }
@@ -507,9 +523,10 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const float* LD, int ldl, void* dk, void* dv, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s);
+                    const float* LD, int ldl, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, nsplit, dk, dv, dk_acc, dv_acc, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, nsplit, dk, dv, dk_acc, dv_acc, s);
 }
 
 }  // namespace gt

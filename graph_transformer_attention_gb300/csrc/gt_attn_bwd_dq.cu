@@ -100,7 +100,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD, int ldl,
               const float* __restrict__ vmax,
               const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
-              __nv_bfloat16* __restrict__ dq, double* __restrict__ dT64, int* status) {
+              int split_blocks, __nv_bfloat16* __restrict__ dq, float* __restrict__ dq_acc,
+              double* __restrict__ dT64, int* status) {
     using C = DqCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -111,7 +112,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i0 = blockIdx.x * kBQ;
     const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
-    const int nblocks = (n + C::BKV - 1) / C::BKV;
+    // KV blocks kb0 .. kb0 + nblocks - 1 (all of them unless the columns are split
+    // over grid.z, in which case dq is summed into dq_acc in fp32)
+    const int total_blocks = (n + C::BKV - 1) / C::BKV;
+    const int kb0 = split_blocks > 0 ? blockIdx.z * split_blocks : 0;
+    const int nblocks = split_blocks > 0 ? min(split_blocks, total_blocks - kb0) : total_blocks;
     const int nchunks = nblocks * C::NCH;
 
     if (tid == kTmaWarp * 32) {
@@ -162,7 +167,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     break;
                 }
                 uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                const int j0 = b * C::BKV;
+                const int j0 = (kb0 + b) * C::BKV;
                 mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
                 tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
 #pragma unroll
@@ -300,7 +305,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             const int ks = b & 1;
             if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * C::BKV;
-            const int j0 = b * C::BKV;
+            const int j0 = (kb0 + b) * C::BKV;
             const bool tail_block = j0 + C::BKV > n;
             for (int c = 0; c < C::NCH; ++c, ++t) {
                 const int ss = t & 1;
@@ -421,7 +426,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     tmem_ld_x16(lrow + kColDq + 16 * hh, ov);
                     tmem_wait_ld();
                     const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
-                    if (live) {
+                    if (live && dq_acc) {
+                        float* dst = dq_acc + ((int64_t)row * kH + h) * HD;
+#pragma unroll
+                        for (int k = 0; k < HD; ++k) atomicAdd(dst + k, __uint_as_float(ov[c0h + k]) * scale);
+                    } else if (live) {
                         uint32_t wq[HD / 2];
 #pragma unroll
                         for (int k = 0; k < HD / 2; ++k)
@@ -457,7 +466,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
            int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, const float* vmax,
-           void* dq, double* dT64, cudaStream_t s) {
+           int nsplit, void* dq, float* dq_acc, double* dT64, cudaStream_t s) {
     using C = DqCfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -477,12 +486,16 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     if (smem > kSmemLimit) return GT_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GT_ERR_CUDA;
-    dim3 grid((n + kBQ - 1) / kBQ, kH / kHC);
+    const int total_blocks = (n + C::BKV - 1) / C::BKV;
+    const int per = nsplit > 1 ? (total_blocks + nsplit - 1) / nsplit : 0;
+    const int nz = per > 0 ? (total_blocks + per - 1) / per : 1;
+    dim3 grid((n + kBQ - 1) / kBQ, kH / kHC, nz);
     {
         LaunchScope ls("bwd_dq", s);
         kern<<<grid, kThreads, smem, s>>>(
             mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-            ldl, vmax, T, nb, n, scale, scale * kLog2e, static_cast<__nv_bfloat16*>(dq), dT64, status);
+            ldl, vmax, T, nb, n, scale, scale * kLog2e, per, static_cast<__nv_bfloat16*>(dq),
+            per > 0 ? dq_acc : nullptr, dT64, status);
     }
     return check_launch();
 }
@@ -491,9 +504,10 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, void* dq, double* dT64, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, dq, dT64, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, dq, dT64, s);
+                  const float* LD, int ldl, const float* vmax, int nsplit, void* dq, float* dq_acc,
+                  double* dT64, cudaStream_t s) {
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, dq, dq_acc, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, dq, dq_acc, dT64, s);
 }
 
 }  // namespace gt

@@ -70,6 +70,16 @@ __global__ void bwd_prep(int n, int hd, int ldl, const TE* __restrict__ o, const
     }
 }
 
+// the split backward's fp32 sums [3][elems] (dq, dk, dv) to the bf16 outputs
+__global__ void acc_to_bf16(size_t elems, const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                            __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv) {
+    for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < elems; x += (size_t)gridDim.x * blockDim.x) {
+        dq[x] = __float2bfloat16_rn(acc[x]);
+        dk[x] = __float2bfloat16_rn(acc[elems + x]);
+        dv[x] = __float2bfloat16_rn(acc[2 * elems + x]);
+    }
+}
+
 __global__ void dT_to_f32(int count, const double* __restrict__ dT64, float* __restrict__ dT) {
     for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < count; x += gridDim.x * blockDim.x)
         dT[x] = (float)dT64[x];
@@ -106,17 +116,19 @@ bool bwd_tc_supported(int h, int d, int nb) { return h == kH && (d == 8 || d == 
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, void* dq, double* dT64, cudaStream_t s);
+                  const float* LD, int ldl, const float* vmax, int nsplit, void* dq, float* dq_acc,
+                  double* dT64, cudaStream_t s);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const float* LD, int ldl, void* dk, void* dv, cudaStream_t s);
+                    const float* LD, int ldl, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    cudaStream_t s);
 
 // Backward on the tensor cores.  Workspace: LD [16][bwd_ld_ld(n)] fp32,
 // Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j| of head h).
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
-                double* dT64, float* aux, cudaStream_t s) {
+                double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
     if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;
@@ -134,10 +146,25 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     // N = 16384 backward 2.41 ms in sequence, 2.68 ms side by side; N = 4096
     // 0.74 ms in sequence, 0.44 ms side by side)
     const int ctas = 2 * ((n + 127) / 128);
-    if (2 * ctas > 3 * num_sms() / 2) {
-        int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, dq, dT64, s);
+    const size_t elems = (size_t)n * kH * d;
+    if (nsplit > 1 && acc) {
+        // split streams: fp32 sums, then bf16
+        if (cudaMemsetAsync(acc, 0, sizeof(float) * 3 * elems, s) != cudaSuccess) return GT_ERR_CUDA;
+        int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, nsplit, dq, acc, dT64, s);
         if (rc != GT_OK) return rc;
-        rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, s);
+        rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, nsplit, dk, dv, acc + elems,
+                             acc + 2 * elems, s);
+        if (rc != GT_OK) return rc;
+        {
+            LaunchScope ls("bwd_acc_to_bf16", s);
+            acc_to_bf16<<<2 * num_sms(), 256, 0, s>>>(elems, acc, static_cast<__nv_bfloat16*>(dq),
+                                                     static_cast<__nv_bfloat16*>(dk),
+                                                     static_cast<__nv_bfloat16*>(dv));
+        }
+    } else if (2 * ctas > 3 * num_sms() / 2) {
+        int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, 1, dq, nullptr, dT64, s);
+        if (rc != GT_OK) return rc;
+        rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, 1, dk, dv, nullptr, nullptr, s);
         if (rc != GT_OK) return rc;
     } else {
         std::lock_guard<std::mutex> lock(side_mu);
@@ -145,8 +172,10 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
         if (!side_for_device(&sd)) return GT_ERR_CUDA;
         if (cudaEventRecord(sd.fork, s) != cudaSuccess || cudaStreamWaitEvent(sd.s2, sd.fork, 0) != cudaSuccess)
             return GT_ERR_CUDA;
-        const int rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, dk, dv, sd.s2);
-        const int rc2 = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, dq, dT64, s);
+        const int rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, 1, dk, dv, nullptr,
+                                       nullptr, sd.s2);
+        const int rc2 = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, 1, dq, nullptr, dT64,
+                                      s);
         // join even when a launch failed, so the caller's stream never runs ahead
         if (cudaEventRecord(sd.join, sd.s2) != cudaSuccess || cudaStreamWaitEvent(s, sd.join, 0) != cudaSuccess)
             return GT_ERR_CUDA;

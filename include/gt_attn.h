@@ -130,6 +130,16 @@ int gt_spd_build_algo(int32_t algo, const int64_t* indptr, const int32_t* indice
 int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block);
 
 /*
+ * How many CTAs share each 128-row tile's streamed dimension in the bf16
+ * tensor-core backward for these sizes on the current device (1 = none; -1 for
+ * invalid arguments).  With too few tiles to give every SM two CTAs, the dq
+ * kernel splits its KV blocks and the dk/dv kernel its query tiles over up to 4
+ * CTAs each, which sum in fp32 (workspace included in
+ * gt_bias_attn_workspace_size; a workspace too small for the sums runs unsplit).
+ */
+int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb);
+
+/*
  * Bytes of device workspace needed by gt_bias_attn_fwd (with this kv_block)
  * and by gt_bias_attn_bwd for these sizes; one buffer of this size serves both.
  */

@@ -35,12 +35,14 @@ def test_counts_and_times_of_one_layer(gt, timing):
     stats = gt.gt_kernel_stats()
     gt.gt_kernel_stats_reset(False)
     # first-launch order (the forward may split its KV columns on a small graph
-    # and merge; bwd_dq and bwd_dkdv may run side by side, in either order)
-    names = [m for m in stats if m != "fwd_merge"]
+    # and merge; the backward may split its streams and convert fp32 sums; bwd_dq
+    # and bwd_dkdv may run side by side, in either order)
+    per = gt.launches_per_call("bf16", h, d, n, nb=nb)
+    names = [m for m in stats if m not in ("fwd_merge", "bwd_acc_to_bf16")]
     assert names[:2] == ["fwd_tc", "bwd_prep"] and names[-1] == "bwd_dT_to_f32"
     assert sorted(names[2:4]) == ["bwd_dkdv", "bwd_dq"]
-    assert ("fwd_merge" in stats) == (gt.launches_per_call("bf16", h, d, n)["fwd"] == 2)
-    per = gt.launches_per_call("bf16", h, d, n)
+    assert ("fwd_merge" in stats) == (per["fwd"] == 2)
+    assert ("bwd_acc_to_bf16" in stats) == (per["bwd"] == 5)
     assert sum(c for c, _ in stats.values()) == per["fwd"] + per["bwd"]
     for name, (launches, ms) in stats.items():
         assert launches == 1
