@@ -20,8 +20,10 @@
 //              fixed-point integers (a 32-bit shared-memory add is a single native
 //              operation, a float add is not): a row's dS values satisfy
 //              sum_j |dS_ij| <= |dO_i| max_j |v_j| + |D_i| (the P_ij of a row sum to
-//              1), so one power-of-two scale per CTA keeps every copy's sum below
-//              2^30; the copies are summed exactly in 64 bits at the end.
+//              1), so one power-of-two scale 2^e per CTA keeps every copy's sum below
+//              2^30; the copies are summed exactly in 64 bits at the end.  The
+//              scale is folded into the exponent (P 2^e = 2^(x - lse log2 e + e)),
+//              so dS is formed in fixed-point units; dq drops the 2^e at the end.
 //   warp 4     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
 //              K=16), then dq_h += dS_h K_h (A = dS from TMEM).
 //   warp 5     TMA producer: bucket tile and K / V column slots per KV block.
@@ -295,8 +297,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             if (!(bound < INFINITY) || e < 0) e = 0;
             if (e > 60) e = 60;
             bscale = exp2f((float)e);
+            // the scale rides in the exponent: P 2^e = 2^(x - (lse log2 e - e)), so
+            // dS comes out already in fixed-point units (and dq carries 2^e, taken
+            // out in the epilogue)
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) L2[hh] -= (float)e;
         }
-        auto fx = [&](float v) -> uint32_t { return (uint32_t)__float2int_rn(v * bscale); };
+        auto fx = [&](float v) -> uint32_t { return (uint32_t)__float2int_rn(v); };
+        const float qscale = scale / bscale;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         int acc_code = -1;
         int t = 0;
@@ -429,13 +437,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (live && dq_acc) {
                         float* dst = dq_acc + ((int64_t)row * kH + h) * HD;
 #pragma unroll
-                        for (int k = 0; k < HD; ++k) atomicAdd(dst + k, __uint_as_float(ov[c0h + k]) * scale);
+                        for (int k = 0; k < HD; ++k) atomicAdd(dst + k, __uint_as_float(ov[c0h + k]) * qscale);
                     } else if (live) {
                         uint32_t wq[HD / 2];
 #pragma unroll
                         for (int k = 0; k < HD / 2; ++k)
-                            wq[k] = pack_bf16x2(__uint_as_float(ov[c0h + 2 * k]) * scale,
-                                                __uint_as_float(ov[c0h + 2 * k + 1]) * scale);
+                            wq[k] = pack_bf16x2(__uint_as_float(ov[c0h + 2 * k]) * qscale,
+                                                __uint_as_float(ov[c0h + 2 * k + 1]) * qscale);
                         uint4* dst = reinterpret_cast<uint4*>(dq + ((int64_t)row * kH + h) * HD);
 #pragma unroll
                         for (int k = 0; k < HD / 8; ++k)
