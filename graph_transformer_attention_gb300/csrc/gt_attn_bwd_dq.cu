@@ -328,6 +328,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
                 const uint32_t c0 = w[0] & 0xffu;
                 const bool uniform = w[0] == c0 * 0x01010101u && w[1] == w[0] && w[2] == w[0] && w[3] == w[0];
+                const bool wuni = __all_sync(0xffffffffu, uniform);
                 if (uniform && (int)c0 != acc_code) {
                     if (acc_code >= 0 && acc_code < nb) {
 #pragma unroll
@@ -352,16 +353,29 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         tc_fence_before();
                         mbar_arrive(&bars->dp_free);
                     }
-                    // x = s scale log2e + bias (scalar FMA), then packed: x - lse, exp, dS
+                    // x = s scale log2e + bias (scalar FMA), then packed: x - lse, exp, dS;
+                    // when each of the warp's 32 rows has 16 equal codes (a warp vote, so
+                    // the warp never splits), a row takes its 4 head biases once
+                    if (wuni) {
+                        const float4 bv = lds_f4(tbl + c0 * 32u);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int kk = 8 * g + k;
-                        const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
-                        const float4 bv = lds_f4(tbl + code * 32u);
-                        rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
-                        rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
-                        rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
-                        rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                        for (int k = 0; k < 8; ++k) {
+                            rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
+                            rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
+                            rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
+                            rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int kk = 8 * g + k;
+                            const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
+                            const float4 bv = lds_f4(tbl + code * 32u);
+                            rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
+                            rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
+                            rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
+                            rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                        }
                     }
                     if (tail_block) {
 #pragma unroll
