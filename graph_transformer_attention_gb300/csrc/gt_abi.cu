@@ -137,6 +137,10 @@ size_t bwd_ws(int n, int h, int d, int nsplit, void* base, size_t cap, BwdWs* ou
 }
 
 }  // namespace
+
+// Workspace of the backward run unsplit: the least a backward call accepts.
+size_t bwd_ws_unsplit(int n, int h, int d) { return bwd_ws(n, h, d, 1, nullptr, 0, nullptr); }
+
 }  // namespace gt
 
 extern "C" {

@@ -21,6 +21,10 @@
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GT_NOALLOC_SCRATCH_BYTES];
 
+namespace gt {
+size_t bwd_ws_unsplit(int n, int h, int d);   // gt_abi.cu
+}  // namespace gt
+
 namespace {
 
 // Device address of g_noalloc_scratch on the current device, looked up on the
@@ -47,9 +51,9 @@ extern "C" int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int
                                         const int8_t* spd, int64_t ld_spd, const float* T,
                                         int32_t nb, float scale, void* dq, void* dk, void* dv,
                                         float* dT, void* stream) {
-    const size_t need = gt_bias_attn_workspace_size(dtype, n, h, d, 0);
-    if (need == 0) return GT_ERR_INVALID_ARG;
-    if (need > (size_t)GT_NOALLOC_SCRATCH_BYTES) return GT_ERR_WORKSPACE;
+    if (gt_bias_attn_workspace_size(dtype, n, h, d, 0) == 0) return GT_ERR_INVALID_ARG;
+    // the backward run unsplit is what has to fit; with room to spare it splits
+    if (gt::bwd_ws_unsplit(n, h, d) > (size_t)GT_NOALLOC_SCRATCH_BYTES) return GT_ERR_WORKSPACE;
     void* scratch = noalloc_scratch_ptr();
     if (!scratch) return GT_ERR_CUDA;
     return gt_bias_attn_bwd(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
