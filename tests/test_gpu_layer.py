@@ -28,9 +28,14 @@ def _rel(a, b):
     return float(np.linalg.norm(a.ravel() - b.ravel()) / max(np.linalg.norm(b.ravel()), 1e-30))
 
 
-@pytest.mark.parametrize("n,graph,D", [(300, "ba", 6), (1000, "dba", 12), (2049, "er", 5)])
+@pytest.mark.parametrize("n,graph,D", [(300, "ba", 6), (1000, "dba", 12), (2049, "er", 5), (1, "empty", 3),
+                                       (129, "path", 4)])
 def test_layer_forward_and_backward_match_the_oracle(gt, n, graph, D):
-    if graph == "ba":
+    if graph == "empty":
+        g = gi.csr_from_edges(n, np.zeros(0, np.int64), np.zeros(0, np.int64))
+    elif graph == "path":
+        g = gi.csr_from_edges(n, np.arange(n - 1), np.arange(1, n))
+    elif graph == "ba":
         g = gi.barabasi_albert(n, 3, seed=21)
     elif graph == "dba":
         g = gi.disjoint_ba(4, n // 4, 2, seed=22)
