@@ -95,6 +95,24 @@ struct Bars {
     int abort;
 };
 
+// round(v) for a pair of floats with |v| < 2^29, on the FP32 and integer pipes
+// instead of the conversion unit (which shares its throughput with ex2 and
+// runs at half its rate).  v = a + b with a the nearest multiple of 128 (the
+// sum v + 1.5 * 2^30 has a unit in the last place of 128, so its low mantissa
+// bits hold a / 128) and b = v - a, |b| <= 64, exact; b + 1.5 * 2^23 holds
+// round(b) in its low mantissa bits.  a + round(b) = round(v) exactly.
+__device__ __forceinline__ uint2 round_fixed2(float x, float y) {
+    constexpr float kC1 = 1610612736.f;   // 1.5 * 2^30
+    constexpr float kC2 = 12582912.f;     // 1.5 * 2^23
+    const float2 v = make_float2(x, y);
+    const float2 h = __fadd2_rn(v, make_float2(kC1, kC1));
+    const float2 na = __fadd2_rn(make_float2(kC1, kC1), make_float2(-h.x, -h.y));   // -a, exact
+    const float2 b = __fadd2_rn(__fadd2_rn(v, na), make_float2(kC2, kC2));
+    constexpr uint32_t kBias = (0x4EC00000u << 7) + 0x4B400000u;   // bits(kC1) * 128 + bits(kC2)
+    return make_uint2((__float_as_uint(h.x) << 7) + __float_as_uint(b.x) - kBias,
+                      (__float_as_uint(h.y) << 7) + __float_as_uint(b.y) - kBias);
+}
+
 template <int HD, int NCP>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -408,6 +426,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         tmem_st_x4(lrow + s_col(ss) + 16 * hh + 4 * g, pk);
                     }
                     if (!uniform) {
+                        // dS in fixed point (|dS| < 2^29 by the choice of the scale)
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+                            for (int k = 0; k < 8; k += 2) {
+                                const uint2 fv = round_fixed2(__uint_as_float(rd[hh][k]), __uint_as_float(rd[hh][k + 1]));
+                                rd[hh][k] = fv.x;
+                                rd[hh][k + 1] = fv.y;
+                            }
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int kk = 8 * g + k;
@@ -415,8 +442,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             if (code < (uint32_t)nb) {
 #pragma unroll
                                 for (int hh = 0; hh < 4; ++hh)
-                                    red_shared_add_u32(binb + code * kCodeStride + hh * kHeadStride,
-                                                       fx(__uint_as_float(rd[hh][k])));
+                                    red_shared_add_u32(binb + code * kCodeStride + hh * kHeadStride, rd[hh][k]);
                             }
                         }
                     }
