@@ -998,6 +998,20 @@ constexpr int kScanStaticSmem = 1024;
 // (vertex ids of the scan searches travel as 16-bit fields of the edge pairs)
 bool scan_fits(int n, int W) { return n < 65535 && scan_smem_bytes(n, W) + kScanStaticSmem <= optin_smem(); }
 
+// CTAs of the search per SM: two of half the threads when two fit the SM's shared
+// memory and there are more batches than SMs (one CTA's output pass then runs
+// while the other waits at its per-level barriers), else one.
+int scan_per_sm(int n, int W) {
+    static int per_sm_smem = -1;
+    if (per_sm_smem < 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    }
+    const int nb = (n + W - 1) / W;
+    return 2 * (scan_smem_bytes(n, W) + kScanStaticSmem + 1024) <= per_sm_smem && nb > num_sms() ? 2 : 1;
+}
+
 // The algorithm used for a graph of n vertices: the first that fits of
 // shared-memory words with 32 sources, with 16, the queue-based search with
 // shared-memory pushes, the global-memory search.  -1: the requested one
@@ -1005,6 +1019,11 @@ bool scan_fits(int n, int W) { return n < 65535 && scan_smem_bytes(n, W) + kScan
 int resolve_algo(int algo, int n) {
     switch (algo) {
         case GT_SPD_AUTO:
+            // two CTAs per SM when they fit, with 16 sources per batch if 32 do not fit
+            // twice and 32-source batches would fill the SMs anyway
+            if (scan_fits(n, 32) && scan_per_sm(n, 32) == 2) return GT_SPD_SCAN32;
+            if (scan_fits(n, 16) && scan_per_sm(n, 16) == 2 && (n + 31) / 32 >= num_sms())
+                return GT_SPD_SCAN16;
             if (scan_fits(n, 32)) return GT_SPD_SCAN32;
             if (scan_fits(n, 16)) return GT_SPD_SCAN16;
             if (n <= bfs32_max_n()) return GT_SPD_QUEUE32;
@@ -1031,6 +1050,10 @@ size_t bfs_state_bytes(int algo, int n, int nslices, size_t* per, int* nctas) {
             const int W = algo == GT_SPD_SCAN32 ? 32 : 16;
             *per = (size_t)nslices * scan_nwp(n, W) * 4;
             *nctas = nctas_for(n, W);
+            if (scan_per_sm(n, W) == 2) {
+                const int nb = (n + W - 1) / W;
+                *nctas = nb < 2 * num_sms() ? nb : 2 * num_sms();
+            }
             break;
         }
         case GT_SPD_QUEUE32:
@@ -1102,7 +1125,7 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return GT_ERR_CUDA;
         LaunchScope ls("spd_bfs", stream);
-        kern<<<nctas, kScanThreads, smem, stream>>>(indptr, indices, pairs, comp, n, D, nslices, spd, ld,
+        kern<<<nctas, kScanThreads / scan_per_sm(n, W), smem, stream>>>(indptr, indices, pairs, comp, n, D, nslices, spd, ld,
                                                    reinterpret_cast<uint32_t*>(bfs_ws));
     } else if (a == GT_SPD_QUEUE32) {
         const size_t smem = (size_t)n * 4;
