@@ -356,7 +356,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     tc_fence_after();
                     pv_waited = true;
                 };
-#pragma unroll 1
+#pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     uint32_t sx[kHC][16];
 #pragma unroll
