@@ -375,13 +375,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     // when each of the warp's 32 rows has 16 equal codes (a warp vote, so
                     // the warp never splits), a row takes its 4 head biases once
                     if (wuni) {
+                        // x - lse log2 e = s scale log2 e + (b - lse log2 e): one packed FMA
+                        // per two columns (the subtraction below then takes 0)
                         const float4 bv = lds_f4(tbl + c0 * 32u);
+                        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
-                            rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
-                            rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
-                            rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                        for (int hh = 0; hh < 4; ++hh) {
+                            const float2 bl = make_float2(bb[hh] - L2[hh], bb[hh] - L2[hh]);
+#pragma unroll
+                            for (int k = 0; k < 8; k += 2) {
+                                const float2 x = __ffma2_rn(
+                                    make_float2(__uint_as_float(rs[hh][k]), __uint_as_float(rs[hh][k + 1])),
+                                    make_float2(scale_log2, scale_log2), bl);
+                                rs[hh][k] = __float_as_uint(x.x);
+                                rs[hh][k + 1] = __float_as_uint(x.y);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -405,7 +413,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     }
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        const float2 ml = make_float2(-L2[hh], -L2[hh]);
+                        const float2 ml = wuni ? make_float2(0.f, 0.f) : make_float2(-L2[hh], -L2[hh]);
                         const float2 md = make_float2(-Dh[hh], -Dh[hh]);
                         float2 sum = make_float2(0.f, 0.f);
                         uint32_t pk[4];

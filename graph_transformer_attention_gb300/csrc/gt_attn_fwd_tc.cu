@@ -13,7 +13,9 @@
 //              columns it reads S of the 4 heads from TMEM, gathers the 4 head
 //              biases of each (i, j) with one 16-byte shared load per bucket byte,
 //              exponentiates in base 2, writes P (bf16) to TMEM and keeps the row
-//              sums.
+//              sums.  When every row of the warp has 16 equal codes in a half chunk
+//              (a warp vote), each head takes one bias and x - m is formed with one
+//              packed fused multiply-add per two columns.
 //   warp 4     MMA issuer: S_h = Q_h K_h^T (M=128, N=32, K=16) into TMEM, then
 //              O_h += P_h V_h (A = P from TMEM, M=128, N=16, two K=16 steps).
 //   warp 5     TMA producer: the bucket tile (128x64 int8, 64B swizzle) and the
@@ -153,6 +155,40 @@ __device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, ui
     for (int k = 0; k < 16; k += 2) {
         const float2 d = __fadd2_rn(f2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), mm);
         const float2 p = f2(ex2(d.x), ex2(d.y));
+        if (k & 2) acc1 = __fadd2_rn(acc1, p);
+        else acc0 = __fadd2_rn(acc0, p);
+        pk[k / 2] = pack_bf16x2(p.x, p.y);
+    }
+    const float2 acc = __fadd2_rn(acc0, acc1);
+    return acc.x + acc.y;
+}
+
+// Rows whose 16 codes of a half chunk are all equal (in every row of the warp):
+// x - m = s * scale * log2(e) + (b - m) in one packed fused multiply-add per two
+// columns, the head's bias minus its running maximum taken once.
+__device__ __forceinline__ void score16_shifted(uint32_t (&sx)[kHC][16], const float4 b4, const float (&m)[kHC],
+                                                float scale_log2) {
+    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+    const float2 cc = f2(scale_log2, scale_log2);
+#pragma unroll
+    for (int hh = 0; hh < kHC; ++hh) {
+        const float bm = bb[hh] - m[hh];
+        const float2 bm2 = f2(bm, bm);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            const float2 x = __ffma2_rn(f2(__uint_as_float(sx[hh][k]), __uint_as_float(sx[hh][k + 1])), cc, bm2);
+            sx[hh][k] = __float_as_uint(x.x);
+            sx[hh][k + 1] = __float_as_uint(x.y);
+        }
+    }
+}
+
+// p_k = 2^(x_k) for x already shifted by the running maximum; returns sum p.
+__device__ __forceinline__ float exp_pack16_shifted(const uint32_t (&x)[16], uint32_t (&pk)[8]) {
+    float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        const float2 p = f2(ex2(__uint_as_float(x[k])), ex2(__uint_as_float(x[k + 1])));
         if (k & 2) acc1 = __fadd2_rn(acc1, p);
         else acc0 = __fadd2_rn(acc0, p);
         pk[k / 2] = pack_bf16x2(p.x, p.y);
@@ -315,6 +351,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         for (int h = 0; h < kHC; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
         int t = 0;
         bool ok = true;
+        int uni_skip = 0;   // half chunks left before the next uniformity vote (warp-uniform)
         for (int b = 0; ok && b < nblocks; ++b) {
             const int ks = b & 1;
             if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -367,17 +404,40 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         tc_fence_before();
                         mbar_arrive(&bars->s_free);      // S is consumed: the next QK^T may start
                     }
-                    score16(sx, g ? c1 : c0, tbl, scale_log2);
-                    if (tail_block) mask16(sx, jc + 16 * g, j_end);
                     // exponentials of all heads first (independent chains), one vote on
                     // whether any head of any row needs a redo against a new maximum
                     uint32_t pk[kHC][8];
                     float ls[kHC];
                     bool need = false;
+                    const uint4 cw = g ? c1 : c0;
+                    const uint32_t code0 = cw.x & 0xffu;
+                    bool wuni = false;
+                    if (uni_skip > 0) {
+                        --uni_skip;
+                    } else if (t > 0) {
+                        const bool uni = cw.x == code0 * 0x01010101u && cw.y == cw.x && cw.z == cw.x && cw.w == cw.x;
+                        wuni = __all_sync(0xffffffffu, uni);
+                        // after a failed vote the warp votes again 16 half chunks (256
+                        // columns) later: where codes are mixed the vote seldom succeeds, and
+                        // the mixed columns of a graph of small components come in runs
+                        if (!wuni) uni_skip = 16;
+                    }
+                    if (wuni) {
+                        score16_shifted(sx, lds_f4(tbl + code0 * 32u), m, scale_log2);
+                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
 #pragma unroll
-                    for (int hh = 0; hh < kHC; ++hh) {
-                        ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
-                        need |= !(ls[hh] <= kRedoSum);
+                        for (int hh = 0; hh < kHC; ++hh) {
+                            ls[hh] = exp_pack16_shifted(sx[hh], pk[hh]);
+                            need |= !(ls[hh] <= kRedoSum);
+                        }
+                    } else {
+                        score16(sx, g ? c1 : c0, tbl, scale_log2);
+                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
+#pragma unroll
+                        for (int hh = 0; hh < kHC; ++hh) {
+                            ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
+                            need |= !(ls[hh] <= kRedoSum);
+                        }
                     }
                     if (__any_sync(0xffffffffu, need)) {
                         wait_pv();
@@ -386,11 +446,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
                             // a new maximum for this head: redo, and rescale l, the P already
                             // written for this chunk, and O (TMEM columns hold this CTA's heads)
-                            float mx = m[hh];
+                            // (x of a uniform step is already shifted by m: its new maximum is
+                            // m + the largest shifted x above 0)
+                            float mx = wuni ? 0.f : m[hh];
 #pragma unroll
                             for (int k = 0; k < 16; ++k) mx = fmaxf(mx, __uint_as_float(sx[hh][k]));
-                            const float alpha = ex2(m[hh] - mx);
-                            m[hh] = mx;
+                            const float alpha = wuni ? ex2(-mx) : ex2(m[hh] - mx);
+                            m[hh] = wuni ? m[hh] + mx : mx;
                             l[hh] *= alpha;
                             ls[hh] = exp_pack16(sx[hh], mx, pk[hh]);
                             if (g == 1) {
