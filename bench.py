@@ -151,7 +151,7 @@ EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd
 # capture of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
 # the capture summaries live under profiles/.
 DRAM_BYTES = {("fwd_tc", "ba64x256"): 284.806e6, ("bwd_dq", "ba64x256"): 290.329e6,
-              ("bwd_dkdv", "ba64x256"): 289.759e6, ("spd_bfs", "ba64x256"): 215.059e6}
+              ("bwd_dkdv", "ba64x256"): 289.543e6, ("spd_bfs", "ba64x256"): 215.059e6}
 
 
 def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float) -> dict:

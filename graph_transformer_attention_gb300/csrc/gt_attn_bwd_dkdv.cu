@@ -349,10 +349,29 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     // x = s scale log2e + b(code) - lse_i log2e
                     if (ucode >= 0) {
                         const float b0 = ps ? bu.z : bu.x, b1 = ps ? bu.w : bu.y;
+                        if constexpr (HD == 16) {
+                            // packed FMAs, two rows i at a time (the same results; measured
+                            // faster at head dim 16 and not at 8)
+                            const float2 cc = make_float2(scale_log2, scale_log2);
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
-                            pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
+                            for (int kk = 0; kk < 16; kk += 2) {
+                                const float2 xa = __ffma2_rn(
+                                    make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
+                                    make_float2(b0, b0));
+                                const float2 xb = __ffma2_rn(
+                                    make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
+                                    make_float2(b1, b1));
+                                pf[h0][kk] = xa.x;
+                                pf[h0][kk + 1] = xa.y;
+                                pf[h0 + 1][kk] = xb.x;
+                                pf[h0 + 1][kk + 1] = xb.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 16; ++kk) {
+                                pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
+                                pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
+                            }
                         }
                     } else {
 #pragma unroll
