@@ -19,8 +19,11 @@
 //     lives in one small component touches only that component), then keeps the
 //     bits not seen before.  Distances are stored bit-sliced: slice k holds bit k
 //     of the level at which each source reached the vertex.
-//  3. The same CTA writes its 64 output rows, 4 bytes per store, coalesced along
-//     the row, then clears only the state it touched.
+//  3. The same CTA writes its output rows, coalesced along the row, then clears
+//     only the state it touched.
+//  The default search (bfs_scan, below) keeps all per-vertex words of a batch of
+//  32 or 16 sources in shared memory and works on the range of vertex ids the
+//  batch has touched; bfs32_smem and bfs_batches take graphs too large for it.
 // Every loop is bounded: union-find retries and the level loop have hard caps.
 #include <cuda_runtime.h>
 #include <climits>
@@ -507,20 +510,31 @@ bfs32_smem(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indic
 // word per vertex (12 n bytes of shared memory); W = 16 packs two vertices per
 // word (6 n bytes), for graphs too large for the first.  Only the bit-sliced
 // distances are in global memory: nslices words per vertex word per CTA, small
-// enough to stay in L2.  A level is two passes over all vertices:
-//   push    one warp per block of 32 consecutive vertices that holds a frontier
-//           vertex.  The edges of the block's frontier vertices form one virtual
-//           segment (lane l's edges at positions pre_l .. pre_l + len_l - 1, pre a
-//           prefix sum over the lanes); the warp walks it 32 positions per chunk,
-//           each lane finding its position's vertex by a binary search over the
-//           lanes' pre values, with the index loads of four chunks in flight
-//           before their pushes; the row starts of the warp's next active block
-//           are loaded before the current block is walked.
-//   update  one thread per word keeps the bits not seen before, records them in
-//           the slices of the current level and makes them the next frontier.
-// No queues and no per-level counters: a level costs two scans of the words in
-// shared memory plus the edges of the frontier vertices, and the search ends
-// when an update pass finds no new bit.
+// enough to stay in L2.  A level works on the range of vertex ids the batch has
+// touched so far ([s_lo, s_hi]) and is a push or a pull, then an update:
+//   push, flat   (frontier at least 1/8 of the range) the range's CSR entries,
+//                as 32-bit pairs target | source << 16, split evenly over the
+//                warps; frontier bits of the source from shared memory, atomicOr
+//                into the target's acc; eight 32-entry chunks of loads in flight.
+//   push, block  (small frontier) one warp per block of 32 consecutive vertices
+//                that holds a frontier vertex: a mostly active block walks its
+//                whole CSR segment; a sparse one walks only the edges of its
+//                frontier vertices as one virtual segment (lane l's edges at
+//                pre_l .. pre_l + len_l - 1), each lane finding its position's
+//                vertex by a binary search over the lanes' pre values; the next
+//                active block's row starts are loaded while one is walked.
+//   pull         (the range is the whole graph and fewer vertices are open than
+//                in the frontier) each open vertex ORs its neighbours' frontier
+//                bits and stops once it has every bit it lacks; no atomics.
+//   update       one thread per word keeps the bits not seen before, records them
+//                in the slices of the level, makes them the next frontier, and
+//                counts frontier and open vertices for the next level's choice.
+// The search ends when an update finds no new bit, or at level D - 1.  The batch's
+// rows then go out: 16-column groups outside the touched range by component only,
+// 16-byte evict-first stores; the others four rows at a time from the slices.
+// One CTA of 1024 threads per SM, or two of 512 when two fit the SM's shared
+// memory and the batches outnumber the SMs (a level ends at a CTA-wide barrier, and
+// the other CTA's output pass fills that wait).
 
 constexpr int kScanThreads = 1024;
 constexpr int kPushChunks = 4;     // 32-edge chunks whose index loads a lane has in flight
