@@ -37,36 +37,51 @@ using tc::kLog2e;
 
 constexpr int kMaxNb = 128;
 
-template <typename TE>
-__global__ void bwd_prep(int n, int hd, int ldl, const TE* __restrict__ o, const TE* __restrict__ dO,
-                         const TE* __restrict__ v, const float* __restrict__ lse, float* __restrict__ LD,
-                         float* __restrict__ Dv, float* __restrict__ vmax) {
+// One thread per (node, head), node-major (x = 8 i + h), so a warp reads 32
+// consecutive rows of HD bf16 of o, dO and v with 16-byte loads.
+template <int HD>
+__global__ void bwd_prep(int n, int ldl, const __nv_bfloat16* __restrict__ o,
+                         const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ v,
+                         const float* __restrict__ lse, float* __restrict__ LD, float* __restrict__ Dv,
+                         float* __restrict__ vmax) {
     const int64_t total = (int64_t)n * kH;
-    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
-         x += (int64_t)gridDim.x * blockDim.x) {
-        const int h = (int)(x / n), i = (int)(x % n);
-        const TE* a = o + ((int64_t)i * kH + h) * hd;
-        const TE* b = dO + ((int64_t)i * kH + h) * hd;
-        const TE* vv = v + ((int64_t)i * kH + h) * hd;
+    // the loop bound is the same for the whole block, so every lane reaches the shuffles
+    for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t x = base + threadIdx.x;
+        const bool live = x < total;
+        const int h = (int)(x & (kH - 1));
+        const int64_t i = x / kH;
         float acc = 0.f, vn = 0.f;
-        for (int c = 0; c < hd; ++c) {
-            acc = fmaf(to_f32(a[c]), to_f32(b[c]), acc);
-            vn = fmaf(to_f32(vv[c]), to_f32(vv[c]), vn);
+        if (live) {
+            const uint4* a = reinterpret_cast<const uint4*>(o + x * HD);
+            const uint4* b = reinterpret_cast<const uint4*>(dO + x * HD);
+            const uint4* c = reinterpret_cast<const uint4*>(v + x * HD);
+#pragma unroll
+            for (int q = 0; q < HD / 8; ++q) {
+                const uint4 ua = a[q], ub = b[q], uc = c[q];
+                const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w},
+                               wc[4] = {uc.x, uc.y, uc.z, uc.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc = fmaf(__uint_as_float(wa[k] << 16), __uint_as_float(wb[k] << 16), acc);
+                    acc = fmaf(__uint_as_float(wa[k] & 0xffff0000u), __uint_as_float(wb[k] & 0xffff0000u), acc);
+                    vn = fmaf(__uint_as_float(wc[k] << 16), __uint_as_float(wc[k] << 16), vn);
+                    vn = fmaf(__uint_as_float(wc[k] & 0xffff0000u), __uint_as_float(wc[k] & 0xffff0000u), vn);
+                }
+            }
         }
-        // one atomic per warp when its lanes share the head (non-negative floats order
-        // like their bit patterns)
-        const unsigned act = __activemask();
-        const int h0 = __shfl_sync(act, h, __ffs(act) - 1);
+        // lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same head (the warp's first x is a
+        // multiple of 32); lanes 0..7 then add their head's maximum (non-negative
+        // floats order like their bit patterns)
         float m = sqrtf(vn);
-        if (__all_sync(act, h == h0) && act == 0xffffffffu) {
-            for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
-            if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(vmax) + h, __float_as_int(m));
-        } else {
-            atomicMax(reinterpret_cast<int*>(vmax) + h, __float_as_int(m));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if ((threadIdx.x & 31) < kH && m > 0.f) atomicMax(reinterpret_cast<int*>(vmax) + h, __float_as_int(m));
+        if (live) {
+            LD[(int64_t)h * ldl + i] = lse[(int64_t)h * n + i] * kLog2e;
+            LD[(int64_t)(kH + h) * ldl + i] = acc;
+            Dv[(int64_t)h * n + i] = acc;
         }
-        LD[(int64_t)h * ldl + i] = lse[x] * kLog2e;
-        LD[(int64_t)(kH + h) * ldl + i] = acc;
-        Dv[x] = acc;
     }
 }
 
@@ -136,9 +151,10 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     const int pblocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     {
         LaunchScope ls("bwd_prep", s);
-        bwd_prep<__nv_bfloat16><<<pblocks, 256, 0, s>>>(n, d, ldl, static_cast<const __nv_bfloat16*>(o),
-                                                        static_cast<const __nv_bfloat16*>(dO),
-                                                        static_cast<const __nv_bfloat16*>(v), lse, LD, Dv, aux);
+        auto prep = d == 8 ? bwd_prep<8> : bwd_prep<16>;
+        prep<<<pblocks, 256, 0, s>>>(n, ldl, static_cast<const __nv_bfloat16*>(o),
+                                     static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(v),
+                                     lse, LD, Dv, aux);
     }
     // side by side only while the two kernels' CTAs (one per 128-row tile and
     // head half each) fit about one per SM: two co-resident CTAs of different
