@@ -92,14 +92,19 @@ int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64
  * Search algorithms of gt_spd_build.  All give the same codes; they differ in
  * where the per-vertex state lives, which bounds the graph size they take:
  *   GT_SPD_SCAN32    32 sources per batch, every per-vertex word in shared
- *                    memory (12 bytes per vertex): the fastest, n up to ~18.8K
- *                    on a GB300.
+ *                    memory (12 bytes per vertex), n up to ~18.8K on a GB300.
  *   GT_SPD_SCAN16    16 sources per batch, two vertices per word (6 bytes per
  *                    vertex), n up to ~37K.
  *   GT_SPD_QUEUE32   32 sources per batch, frontier queues in global memory,
  *                    pushes into shared memory (4 bytes per vertex), n up to ~58K.
  *   GT_SPD_GLOBAL64  64 sources per batch, all state in global memory: any n.
- *   GT_SPD_AUTO      the first of these that fits (what gt_spd_build uses).
+ *   GT_SPD_AUTO      what gt_spd_build uses: a scan search that runs two CTAs
+ *                    per SM when its state fits twice in an SM's shared memory
+ *                    and the batches outnumber the SMs (SCAN32 if it does so,
+ *                    else SCAN16 when 32-source batches would fill the SMs
+ *                    anyway), otherwise the first of these that fits.
+ * The scan searches run one CTA of 1024 threads per SM, or two of 512 under the
+ * condition above.
  */
 enum { GT_SPD_AUTO = 0, GT_SPD_SCAN32 = 1, GT_SPD_SCAN16 = 2, GT_SPD_QUEUE32 = 3, GT_SPD_GLOBAL64 = 4 };
 
