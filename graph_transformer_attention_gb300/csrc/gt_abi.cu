@@ -149,7 +149,7 @@ const char* gt_status_string(int status) {
     switch (status) {
         case GT_OK: return "ok";
         case GT_ERR_INVALID_ARG: return "invalid argument (NULL pointer, size, alignment or layout)";
-        case GT_ERR_UNSUPPORTED: return "shape not supported by this build";
+        case GT_ERR_UNSUPPORTED: return "shape not supported by this library";
         case GT_ERR_CUDA: return "CUDA runtime error";
         case GT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
         case GT_ERR_WORKSPACE: return "workspace missing or too small";

@@ -1,6 +1,6 @@
 // gt_attn_bwd_tc.cu -- tensor-core backward of topology-biased graph attention
-// (bf16 storage, H = 8 heads, head dim 8 or 16) for sm_103a: the driver of the
-// backward kernels.
+// (bf16 storage, H = 8 heads, head dim 8 or 16) for sm_103a: the host side that
+// launches the backward kernels.
 //
 // The backward pass recomputes P = exp(S - lse) blockwise, as the forward forms
 // it (MegaGraph paper, Fig. 4: KV blocks stream past a Q tile, the bias column

@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     GT_OK = 0,
     GT_ERR_INVALID_ARG = -1,  /* NULL, size, alignment or layout check failed */
-    GT_ERR_UNSUPPORTED = -2,  /* shape valid but not handled by this build */
+    GT_ERR_UNSUPPORTED = -2,  /* shape valid but not handled by this library */
     GT_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
     GT_ERR_TIMEOUT = -4,      /* a kernel gave up a bounded wait (see below) */
     GT_ERR_WORKSPACE = -5     /* workspace NULL or smaller than the size query */
