@@ -24,6 +24,11 @@
  * over KV, no fusion and no reordering beyond splitting independent rows or
  * columns over threads.
  *
+ * Bucket bytes are read as unsigned codes 0..255.  The pages define only the
+ * codes a shortest-path build produces (0..D+1, i.e. below nb); a byte at or
+ * above nb is read as "no bias": it adds 0 to the score and belongs to no
+ * column of T, so it adds nothing to dT.
+ *
  * Layouts (row-major): q, k, v, o, dO, dq, dk, dv are [n][h][d] doubles;
  * lse and D are [h][n]; T and dT are [h][nb]; spd is int8 [n][ld].
  */
@@ -152,8 +157,9 @@ static double score(const attn_ctx* c, int32_t i, int32_t j, int32_t hh) {
     const double* kj = c->k + ((int64_t)j * c->h + hh) * c->d;
     double dot = 0.0;
     for (int32_t t = 0; t < c->d; ++t) dot += qi[t] * kj[t];
-    int code = (int)c->spd[(int64_t)i * c->ld + j];
-    return c->scale * dot + c->T[(int64_t)hh * c->nb + code];
+    int code = (int)(uint8_t)c->spd[(int64_t)i * c->ld + j];
+    double bias = code < c->nb ? c->T[(int64_t)hh * c->nb + code] : 0.0;
+    return c->scale * dot + bias;
 }
 
 static void fwd_rows(void* vctx, int64_t lo, int64_t hi, int tid) {
@@ -245,7 +251,8 @@ static void bwd_rows(void* vctx, int64_t lo, int64_t hi, int tid) {
                     const double* kj = c->k + ((int64_t)j * c->h + hh) * c->d;
                     for (int32_t t = 0; t < c->d; ++t) dqi[t] += c->scale * ds * kj[t];
                 }
-                if (dT) dT[(int64_t)hh * c->nb + c->spd[(int64_t)i * c->ld + j]] += ds;
+                int code = (int)(uint8_t)c->spd[(int64_t)i * c->ld + j];
+                if (dT && code < c->nb) dT[(int64_t)hh * c->nb + code] += ds;
             }
         }
     }

@@ -34,26 +34,33 @@ def _fp64_default():
     torch.set_default_dtype(old)
 
 
-def _case(n, h, d, nb, seed, t_std=1.0, sym=False):
+def _case(n, h, d, nb, seed, t_std=1.0, sym=False, code_hi=None):
+    """Random inputs; bucket codes uniform on [0, nb), or on [0, code_hi) when
+    given (code_hi up to 256: bytes at or above nb, above 127 included)."""
     rng = np.random.default_rng(seed)
     q = rng.standard_normal((n, h, d))
     k = rng.standard_normal((n, h, d))
     v = rng.standard_normal((n, h, d))
     dO = rng.standard_normal((n, h, d))
     T = t_std * rng.standard_normal((h, nb))
-    spd = rng.integers(0, nb, size=(n, n)).astype(np.int8)
+    spd = rng.integers(0, code_hi or nb, size=(n, n)).astype(np.uint8).view(np.int8)
     if sym:
         spd = np.triu(spd) + np.triu(spd, 1).T
     return q, k, v, dO, T, spd
 
 
 def _torch_ref(q, k, v, dO, T, spd, scale):
-    """SDPA + autograd reference: returns o, lse, dq, dk, dv, dT (numpy fp64)."""
+    """SDPA + autograd reference: returns o, lse, dq, dk, dv, dT (numpy fp64).
+    The bias of a pair is column `code` of T padded with zero columns to 256
+    (every byte value), so a code at or above nb adds 0 and, the padding being a
+    constant, receives no gradient."""
     qt = torch.tensor(q).permute(1, 0, 2).contiguous().requires_grad_(True)   # [h][n][d]
     kt = torch.tensor(k).permute(1, 0, 2).contiguous().requires_grad_(True)
     vt = torch.tensor(v).permute(1, 0, 2).contiguous().requires_grad_(True)
     Tt = torch.tensor(T).requires_grad_(True)
-    bias = Tt[:, torch.tensor(spd.astype(np.int64))]                          # [h][n][n]
+    Tpad = torch.cat([Tt, torch.zeros(T.shape[0], 256 - T.shape[1])], dim=1)
+    codes = torch.tensor(np.asarray(spd).view(np.uint8).astype(np.int64))
+    bias = Tpad[:, codes]                                                     # [h][n][n]
     o = torch.nn.functional.scaled_dot_product_attention(
         qt[None], kt[None], vt[None], attn_mask=bias[None], scale=scale)[0]
     o.backward(torch.tensor(dO).permute(1, 0, 2))
@@ -87,6 +94,31 @@ def test_backward_matches_autograd(n, h, d, nb):
     got = O.attn_fwd_bwd(q, k, v, dO, spd, T, scale)
     for name in ("o", "lse", "dq", "dk", "dv", "dT"):
         np.testing.assert_allclose(got[name], ref[name], rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+@pytest.mark.parametrize("n,h,d,nb", [(40, 3, 8, 7), (70, 8, 16, 26), (33, 2, 4, 1)])
+def test_codes_at_or_above_nb_match_autograd(n, h, d, nb):
+    """Bytes 0..255, most of them at or above nb (and above 127): zero bias,
+    nothing in dT -- against SDPA + autograd over T padded with zero columns."""
+    q, k, v, dO, T, spd = _case(n, h, d, nb, seed=n * 13 + nb, code_hi=256)
+    assert (spd.view(np.uint8) >= nb).mean() > 0.5 and (spd.view(np.uint8) > 127).any()
+    scale = 1.0 / np.sqrt(d)
+    ref = _torch_ref(q, k, v, dO, T, spd, scale)
+    got = O.attn_fwd_bwd(q, k, v, dO, spd, T, scale)
+    for name in ("o", "lse", "dq", "dk", "dv", "dT"):
+        np.testing.assert_allclose(got[name], ref[name], rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_codes_at_or_above_nb_all_pairs():
+    """Every pair's code at or above nb: plain softmax attention (SDPA without a
+    mask) and dT = 0 exactly."""
+    q, k, v, dO, T, _ = _case(25, 4, 8, 9, seed=77)
+    spd = np.random.default_rng(78).integers(9, 256, size=(25, 25)).astype(np.uint8).view(np.int8)
+    g = O.attn_fwd_bwd(q, k, v, dO, spd, T)
+    qt, kt, vt = (torch.tensor(a).permute(1, 0, 2) for a in (q, k, v))
+    plain = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(g["o"], plain, rtol=1e-10, atol=1e-12)
+    assert np.all(g["dT"] == 0.0)
 
 
 def test_forward_row_subset_matches_full():
@@ -197,19 +229,22 @@ def test_partial_rows_cols_match_full():
 # ----------------------------------------------------------- planted mistakes
 
 MUTATIONS = {
-    "drop_bias": ("return c->scale * dot + c->T[(int64_t)hh * c->nb + code];",
-                  "return c->scale * dot;"),
-    "transpose_spd": ("int code = (int)c->spd[(int64_t)i * c->ld + j];",
-                      "int code = (int)c->spd[(int64_t)j * c->ld + i];"),
-    "bias_head_index": ("return c->scale * dot + c->T[(int64_t)hh * c->nb + code];",
-                        "return c->scale * dot + c->T[code];"),
-    "scale_dropped": ("return c->scale * dot + c->T", "return dot + c->T"),
+    "drop_bias": ("return c->scale * dot + bias;", "return c->scale * dot;"),
+    "transpose_spd": ("int code = (int)(uint8_t)c->spd[(int64_t)i * c->ld + j];\n    double bias",
+                      "int code = (int)(uint8_t)c->spd[(int64_t)j * c->ld + i];\n    double bias"),
+    "bias_head_index": ("double bias = code < c->nb ? c->T[(int64_t)hh * c->nb + code] : 0.0;",
+                        "double bias = code < c->nb ? c->T[code] : 0.0;"),
+    "scale_dropped": ("return c->scale * dot + bias;", "return dot + bias;"),
+    "high_code_clamped": ("double bias = code < c->nb ? c->T[(int64_t)hh * c->nb + code] : 0.0;",
+                          "double bias = c->T[(int64_t)hh * c->nb + (code < c->nb ? code : c->nb - 1)];"),
+    "high_code_in_dT": ("if (dT && code < c->nb) dT[(int64_t)hh * c->nb + code] += ds;",
+                        "if (dT) dT[(int64_t)hh * c->nb + (code < c->nb ? code : c->nb - 1)] += ds;"),
     "ds_sign": ("double ds = p * (dprob(c, i, j, hh) - Di);",
                 "double ds = p * (dprob(c, i, j, hh) + Di);"),
     "dk_uses_k": ("dkj[t] += c->scale * ds * qi[t];", "dkj[t] += c->scale * ds * c->k[((int64_t)j * c->h + hh) * c->d + t];"),
     "dv_drops_p": ("dvj[t] += p * gi[t];", "dvj[t] += gi[t];"),
-    "dT_wrong_bucket": ("if (dT) dT[(int64_t)hh * c->nb + c->spd[(int64_t)i * c->ld + j]] += ds;",
-                        "if (dT) dT[(int64_t)hh * c->nb + c->spd[(int64_t)j * c->ld + i]] += ds;"),
+    "dT_wrong_bucket": ("int code = (int)(uint8_t)c->spd[(int64_t)i * c->ld + j];\n                if (dT",
+                        "int code = (int)(uint8_t)c->spd[(int64_t)j * c->ld + i];\n                if (dT"),
     "lse_no_max": ("c->lse_out[(int64_t)hh * c->nrows + r] = m + log(l);",
                    "c->lse_out[(int64_t)hh * c->nrows + r] = log(l);"),
     "spd_no_clip": ("(dist[v] < c->D ? dist[v] : c->D)", "dist[v]"),
@@ -228,8 +263,8 @@ def mutant_dir():
 def _pins_pass() -> bool:
     """Run a compact set of the pins above against whatever library is loaded."""
     try:
-        for (n, h, d, nb) in [(33, 3, 8, 7), (12, 2, 4, 5)]:
-            q, k, v, dO, T, spd = _case(n, h, d, nb, seed=n + d)
+        for (n, h, d, nb, hi) in [(33, 3, 8, 7, None), (12, 2, 4, 5, None), (20, 2, 4, 5, 256)]:
+            q, k, v, dO, T, spd = _case(n, h, d, nb, seed=n + d, code_hi=hi)
             ref = _torch_ref(q, k, v, dO, T, spd, 0.45)
             got = O.attn_fwd_bwd(q, k, v, dO, spd, T, 0.45)
             for name in ("o", "lse", "dq", "dk", "dv", "dT"):
