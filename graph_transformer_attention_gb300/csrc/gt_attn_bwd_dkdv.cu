@@ -6,24 +6,26 @@
 //   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
 //
 // One CTA = one tile of 128 KV rows and one half of the heads (4 of 8: grid.y),
-// streaming every Q tile; two CTAs share an SM, so one's softmax runs while the
-// other waits on its tensor-core products.  192 threads:
-//   warps 0-3  thread r owns KV row j0 + r (TMEM lane r).  Per chunk of 16 query rows i it reads S^T
-//              and dP^T of its heads from TMEM, the bucket code of (i, j) from
-//              column r of the int8 tile, lse_i log2 e and D_i from the staged LD
-//              rows (4 consecutive i per 16-byte load), forms
+// streaming every Q tile; two CTAs share an SM.  The work is cut into steps of
+// one head pair and 16 query rows, and the tensor core runs two steps ahead of
+// the softmax warps, so that they never wait on their products.  192 threads:
+//   warps 0-3  thread r owns KV row j0 + r (TMEM lane r).  Per step it reads S^T
+//              and dP^T of its two heads from TMEM, the bucket code of (i, j) from
+//              column r of the int8 tile (once per 16 query rows), lse_i log2 e and
+//              D_i from the staged LD rows (4 consecutive i per 16-byte load), forms
 //              P^T = 2^(s scale log2 e + b - lse_i log2 e) and dS^T = P^T (dP^T - D_i)
 //              and writes both (bf16) back over S^T.
-//   warp 4     MMA issuer: S^T_h = K_h Q_h^T and dP^T_h = V_h dO_h^T (M=128, N=16,
-//              K=16), then dv_h += P^T_h dO_h and dk_h += dS^T_h Q_h (A from TMEM).
+//   warp 4     MMA issuer: per step, once its P^T and dS^T are in, dv_h += P^T_h dO_h
+//              and dk_h += dS^T_h Q_h (A from TMEM), then S^T_h = K_h Q_h^T and
+//              dP^T_h = V_h dO_h^T (M=128, N=16, K=16) of the step two ahead into the
+//              same buffer (the tensor pipe runs one thread's MMAs in order, so they
+//              land after the products that read the buffer).
 //   warp 5     TMA producer: per Q tile the bucket tile, the Q and dO column
 //              slots and the LD columns.
-// TMEM (256 columns): dk at 0..63, dv at 64..127, and two 64-column regions whose
-// roles alternate: S^T(t) in X, dP^T(t) in Y; P^T/dS^T(t) go over S^T(t) in X;
-// S^T(t+1) goes into Y once every thread has read dP^T(t); dP^T(t+1) goes into X
-// after the dv/dk products of chunk t (the tensor pipe runs one thread's MMAs in
-// order).  All waits are bounded (timeout -> device status word, orderly exit,
-// TMEM freed).
+// TMEM (256 columns): dk at 0..63, dv at 64..127, and one 64-column buffer per
+// head pair at 128 and 192: head e of the pair holds S^T (then P^T | dS^T in
+// bf16) at +16e and dP^T at +32 + 16e.  All waits are bounded (timeout ->
+// device status word, orderly exit, TMEM freed).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,11 +59,8 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return __fadd2_rn(a, make_float2(-b.x, -b.y));
 }
 
-// X_t is region (t & 1), Y_t the other one
-__device__ __forceinline__ uint32_t region(int t, bool x) {
-    const int r = x ? (t & 1) : ((t & 1) ^ 1);
-    return 128u + 64u * r;
-}
+// TMEM buffer of head pair p
+__device__ __forceinline__ uint32_t pair_buf(int p) { return 128u + 64u * (uint32_t)p; }
 
 template <int HD>
 struct KvCfg {
@@ -89,11 +88,8 @@ struct Bars {
     uint64_t q_full[kQST];
     uint64_t meta_ready[kQST];   // the stage's bucket summary is written (and its copies landed)
     uint64_t q_empty[kQST];
-    uint64_t s_full;
-    uint64_t dp_full;
-    uint64_t dp_free;
-    uint64_t p_ready;
-    uint64_t ds_ready;
+    uint64_t sd_full[2];         // S^T and dP^T of a step are in its head pair's buffer
+    uint64_t ds_ready[2];        // P^T and dS^T of a step are in (dP^T read)
     uint64_t done;
     uint64_t fin;
     uint32_t tmem_base;
@@ -130,11 +126,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mbar_init(&bars->meta_ready[s], 32);
             mbar_init(&bars->q_empty[s], kSoft + 1);
         }
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->dp_full, 1);
-        mbar_init(&bars->dp_free, kSoft);
-        mbar_init(&bars->p_ready, kSoft);
-        mbar_init(&bars->ds_ready, kSoft);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(&bars->sd_full[p], 1);
+            mbar_init(&bars->ds_ready[p], kSoft);
+        }
         mbar_init(&bars->done, 1);
         mbar_init(&bars->fin, 1);
         bars->abort = 0;
@@ -239,67 +234,73 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
-        if (lane == 0) {
+        // Step s = 2 t + p: chunk t of 16 query rows, head pair p (heads 2p, 2p + 1
+        // of this CTA), TMEM buffer p.  The whole warp runs the loop and waits; the
+        // elected lane issues (an MMA from a converged warp through elect.sync costs
+        // a fraction of one from a lane-0 branch), and descriptors are precomputed
+        // so that an MMA costs one add.
+        {
             const uint32_t idKK = idesc_bf16(128, 16, false, false);
             const uint32_t idKM = idesc_bf16(128, 16, false, true);
-            const uint32_t k_base = smem_u32(smem + C::OFF_K);
-            const uint32_t v_base = smem_u32(smem + C::OFF_V);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
-            auto qslot = [&](int ks, int c, int h) -> uint32_t {
-                return stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512;
+            const SmemDesc dK = smem_desc_split(smem_u32(smem + C::OFF_K), 16, 256, 6);
+            const SmemDesc dV = smem_desc_split(smem_u32(smem + C::OFF_V), 16, 256, 6);
+            const SmemDesc dQk = smem_desc_split(stage_base + C::SPD_BYTES, 16, 256, 6);     // K-major Q
+            const SmemDesc dQm = smem_desc_split(stage_base + C::SPD_BYTES, 256, 256, 6);    // MN-major Q
+            constexpr uint32_t kG = C::NSLOT * C::SLOT_BYTES;                                 // dO after Q
+            const int nsteps = 2 * nchunks;
+            // offset of (stage, chunk, head) in the Q / dO column slots
+            auto qoff = [&](int t, int h) -> uint32_t {
+                const int b = t / C::NCH, c = t % C::NCH;
+                return (uint32_t)((b & 1) * C::STAGE_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512);
             };
-            auto issue_s = [&](int tt) -> bool {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
-                if (c == 0 && !mbar_wait(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+            auto issue_sd = [&](int st) -> bool {
+                const int t = st >> 1, p = st & 1, b = t / C::NCH, c = t % C::NCH, ks = b & 1;
+                if (c == 0 && p == 0 && !mbar_wait_all(&bars->q_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
                     return false;
                 tc_fence_after();
+                const uint32_t d = tbase + pair_buf(p);
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ss(tbase + region(tt, true) + 16 * h, smem_desc(k_base + h * 4096, 16, 256, 6),
-                           smem_desc(qslot(ks, c, h), 16, 256, 6), idKK, 0);
-                mma_commit(&bars->s_full);
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = 2 * p + e;
+                        mma_ss(d + 16 * e, desc_at(dK, h * 4096), desc_at(dQk, qoff(t, h)), idKK, 0);
+                        mma_ss(d + 32 + 16 * e, desc_at(dV, h * 4096), desc_at(dQk, qoff(t, h) + kG), idKK, 0);
+                    }
+                    mma_commit(&bars->sd_full[p]);
+                }
+                __syncwarp();
                 return true;
             };
-            auto issue_dp = [&](int tt) {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
-#pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ss(tbase + region(tt, false) + 16 * h, smem_desc(v_base + h * 4096, 16, 256, 6),
-                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
-                mma_commit(&bars->dp_full);
-            };
-            bool ok = issue_s(0);
-            if (ok) issue_dp(0);
-            for (int tt = 0; ok && tt < nchunks; ++tt) {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
-                const uint32_t x = region(tt, true);
-                const uint32_t acc = tt > 0 ? 1u : 0u;
-                // dv as soon as P^T is in TMEM, S^T(t+1) once dP^T(t) is read, dk once
-                // dS^T is in
-                if (!mbar_wait(&bars->p_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            bool ok = issue_sd(0);
+            if (ok && nsteps > 1) ok = issue_sd(1);
+            for (int st = 0; ok && st < nsteps; ++st) {
+                const int t = st >> 1, p = st & 1, b = t / C::NCH, c = t % C::NCH, ks = b & 1;
+                if (!mbar_wait_all(&bars->ds_ready[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t x = tbase + pair_buf(p);
+                const uint32_t acc = t > 0 ? 1u : 0u;
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ts(tbase + kColDv + 16 * h, tbase + x + 16 * h,
-                           smem_desc(qslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 256, 256, 6), idKM, acc);
-                if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                if (tt + 1 < nchunks && !issue_s(tt + 1)) { ok = false; break; }
-                if (!mbar_wait(&bars->ds_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ts(tbase + kColDk + 16 * h, tbase + x + 16 * h + 8,
-                           smem_desc(qslot(ks, c, h), 256, 256, 6), idKM, acc);
-                if (c == C::NCH - 1) mma_commit(&bars->q_empty[ks]);
-                if (tt + 1 < nchunks) issue_dp(tt + 1);
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = 2 * p + e;
+                        mma_ts(tbase + kColDv + 16 * h, x + 16 * e, desc_at(dQm, qoff(t, h) + kG), idKM, acc);
+                        mma_ts(tbase + kColDk + 16 * h, x + 16 * e + 8, desc_at(dQm, qoff(t, h)), idKM, acc);
+                    }
+                    if (c == C::NCH - 1 && p == 1) mma_commit(&bars->q_empty[ks]);
+                }
+                __syncwarp();
+                if (st + 2 < nsteps && !issue_sd(st + 2)) { ok = false; break; }
             }
             if (ok) {
-                mma_commit(&bars->done);
+                if (elect_one()) mma_commit(&bars->done);
+                __syncwarp();
             } else {
                 fail(abort_flag, status);
                 int never = 0;
-                mma_commit(&bars->fin);
-                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+                if (elect_one()) mma_commit(&bars->fin);
+                __syncwarp();
+                mbar_wait_all(&bars->fin, 0, &never, kWaitNs);
             }
         }
     } else {
@@ -320,10 +321,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (kHC * hb) * C::BQ;
             const int i0 = (qt0 + b) * C::BQ;
             const bool tail_tile = i0 + C::BQ > n;
-            for (int c = 0; c < C::NCH; ++c, ++t) {
-                if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t x = region(t, true), y = region(t, false);
+            for (int c = 0; ok && c < C::NCH; ++c, ++t) {
                 // bucket codes of the 16 (i, j) pairs of this chunk: column r of the tile,
                 // unless the warp's whole 16 x 32 block holds one code
                 const int ucode = meta[4 * c];
@@ -335,50 +333,52 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
                 }
-                // P^T of all four heads first (S^T of a head pair is read before its P^T
-                // overwrites it), so the exponentials overlap the dP^T products still in
-                // the tensor pipe; then dS^T once dP^T has landed
-                float pf[kHC][16];
 #pragma unroll
-                for (int ps = 0; ps < 2; ++ps) {
-                    const int h0 = 2 * ps;     // local head index (TMEM columns)
-                    uint32_t rs[2][16];
-                    tmem_ld_x16(lrow + x + 16 * h0, rs[0]);
-                    tmem_ld_x16(lrow + x + 16 * (h0 + 1), rs[1]);
-                    tmem_wait_ld();
-                    // x = s scale log2e + b(code) - lse_i log2e
-                    if (ucode >= 0) {
-                        const float b0 = ps ? bu.z : bu.x, b1 = ps ? bu.w : bu.y;
-                        if constexpr (HD == 16) {
-                            // packed FMAs, two rows i at a time (the same results; measured
-                            // faster at head dim 16 and not at 8)
-                            const float2 cc = make_float2(scale_log2, scale_log2);
+                for (int p = 0; p < 2; ++p) {
+                    if (!mbar_wait(&bars->sd_full[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t x = lrow + pair_buf(p);
+                    const int h0 = 2 * p;     // local head index of the pair's first head
+                    float pf[2][16];
+                    {
+                        uint32_t rs[2][16];
+                        tmem_ld_x16(x, rs[0]);
+                        tmem_ld_x16(x + 16, rs[1]);
+                        tmem_wait_ld();
+                        // x = s scale log2e + b(code) - lse_i log2e
+                        if (ucode >= 0) {
+                            const float b0 = p ? bu.z : bu.x, b1 = p ? bu.w : bu.y;
+                            if constexpr (HD == 16) {
+                                // packed FMAs, two rows i at a time (the same results; measured
+                                // faster at head dim 16 and not at 8)
+                                const float2 cc = make_float2(scale_log2, scale_log2);
 #pragma unroll
-                            for (int kk = 0; kk < 16; kk += 2) {
-                                const float2 xa = __ffma2_rn(
-                                    make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
-                                    make_float2(b0, b0));
-                                const float2 xb = __ffma2_rn(
-                                    make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
-                                    make_float2(b1, b1));
-                                pf[h0][kk] = xa.x;
-                                pf[h0][kk + 1] = xa.y;
-                                pf[h0 + 1][kk] = xb.x;
-                                pf[h0 + 1][kk + 1] = xb.y;
+                                for (int kk = 0; kk < 16; kk += 2) {
+                                    const float2 xa = __ffma2_rn(
+                                        make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
+                                        make_float2(b0, b0));
+                                    const float2 xb = __ffma2_rn(
+                                        make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
+                                        make_float2(b1, b1));
+                                    pf[0][kk] = xa.x;
+                                    pf[0][kk + 1] = xa.y;
+                                    pf[1][kk] = xb.x;
+                                    pf[1][kk + 1] = xb.y;
+                                }
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < 16; ++kk) {
+                                    pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
+                                    pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
+                                }
                             }
                         } else {
 #pragma unroll
                             for (int kk = 0; kk < 16; ++kk) {
-                                pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
-                                pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
+                                const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * p);
+                                pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
+                                pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
                             }
-                        }
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * ps);
-                            pf[h0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
-                            pf[h0 + 1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
                         }
                     }
 #pragma unroll
@@ -387,67 +387,55 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const uint4 l = lds_u4(la + 16u * q4);
-                            const float2 xa = fsub2(make_float2(pf[h0 + e][4 * q4], pf[h0 + e][4 * q4 + 1]),
+                            const float2 xa = fsub2(make_float2(pf[e][4 * q4], pf[e][4 * q4 + 1]),
                                                     make_float2(__uint_as_float(l.x), __uint_as_float(l.y)));
-                            const float2 xb = fsub2(make_float2(pf[h0 + e][4 * q4 + 2], pf[h0 + e][4 * q4 + 3]),
+                            const float2 xb = fsub2(make_float2(pf[e][4 * q4 + 2], pf[e][4 * q4 + 3]),
                                                     make_float2(__uint_as_float(l.z), __uint_as_float(l.w)));
-                            pf[h0 + e][4 * q4] = ex2(xa.x);
-                            pf[h0 + e][4 * q4 + 1] = ex2(xa.y);
-                            pf[h0 + e][4 * q4 + 2] = ex2(xb.x);
-                            pf[h0 + e][4 * q4 + 3] = ex2(xb.y);
+                            pf[e][4 * q4] = ex2(xa.x);
+                            pf[e][4 * q4 + 1] = ex2(xa.y);
+                            pf[e][4 * q4 + 2] = ex2(xb.x);
+                            pf[e][4 * q4 + 3] = ex2(xb.y);
                         }
                         if (tail_tile) {
 #pragma unroll
                             for (int kk = 0; kk < 16; ++kk)
-                                if (i0 + c * kCH + kk >= n) pf[h0 + e][kk] = 0.f;
+                                if (i0 + c * kCH + kk >= n) pf[e][kk] = 0.f;
                         }
                         uint32_t pp[8];
 #pragma unroll
-                        for (int k2 = 0; k2 < 8; ++k2) pp[k2] = pack_bf16x2(pf[h0 + e][2 * k2], pf[h0 + e][2 * k2 + 1]);
-                        tmem_st_x8(lrow + x + 16 * (h0 + e), pp);
+                        for (int k2 = 0; k2 < 8; ++k2) pp[k2] = pack_bf16x2(pf[e][2 * k2], pf[e][2 * k2 + 1]);
+                        tmem_st_x8(x + 16 * e, pp);
                     }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars->p_ready);
-                if (!mbar_wait(&bars->dp_full, t & 1, abort_flag, kWaitNs)) ok = false;
-                tc_fence_after();
+                    {
+                        uint32_t rd[2][16];
+                        tmem_ld_x16(x + 32, rd[0]);
+                        tmem_ld_x16(x + 48, rd[1]);
+                        tmem_wait_ld();
 #pragma unroll
-                for (int ps = 0; ps < 2; ++ps) {
-                    const int h0 = 2 * ps;
-                    uint32_t rd[2][16];
-                    tmem_ld_x16(lrow + y + 16 * h0, rd[0]);
-                    tmem_ld_x16(lrow + y + 16 * (h0 + 1), rd[1]);
-                    tmem_wait_ld();
-                    if (ps == 1) {
-                        tc_fence_before();
-                        mbar_arrive(&bars->dp_free);
-                    }
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t la = ldb + 4u * (kH + h0 + e) * C::BQ + 4u * (c * kCH);
+                            uint32_t pd[8];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint32_t la = ldb + 4u * (kH + h0 + e) * C::BQ + 4u * (c * kCH);
-                        uint32_t pd[8];
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const uint4 dd = lds_u4(la + 16u * q4);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint4 dd = lds_u4(la + 16u * q4);
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int kk = 4 * q4 + 2 * u;
-                                const float2 dvv = u == 0 ? make_float2(__uint_as_float(dd.x), __uint_as_float(dd.y))
-                                                          : make_float2(__uint_as_float(dd.z), __uint_as_float(dd.w));
-                                const float2 ds = __fmul2_rn(
-                                    make_float2(pf[h0 + e][kk], pf[h0 + e][kk + 1]),
-                                    fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
-                                pd[kk / 2] = pack_bf16x2(ds.x, ds.y);
+                                for (int u = 0; u < 2; ++u) {
+                                    const int kk = 4 * q4 + 2 * u;
+                                    const float2 dvv = u == 0 ? make_float2(__uint_as_float(dd.x), __uint_as_float(dd.y))
+                                                              : make_float2(__uint_as_float(dd.z), __uint_as_float(dd.w));
+                                    const float2 ds = __fmul2_rn(
+                                        make_float2(pf[e][kk], pf[e][kk + 1]),
+                                        fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
+                                    pd[kk / 2] = pack_bf16x2(ds.x, ds.y);
+                                }
                             }
+                            tmem_st_x8(x + 16 * e + 8, pd);
                         }
-                        tmem_st_x8(lrow + x + 16 * (h0 + e) + 8, pd);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars->ds_ready[p]);
                 }
-                tmem_wait_st();
-                if (!ok) break;
-                tc_fence_before();
-                mbar_arrive(&bars->ds_ready);
             }
             if (!ok) break;
             mbar_arrive(&bars->q_empty[ks]);

@@ -207,37 +207,48 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
-        if (lane == 0) {
+        // The whole warp runs the loop and waits; the elected lane issues (an MMA
+        // from a converged warp through elect.sync costs a fraction of one from a
+        // lane-0 branch), and descriptors are precomputed so that an MMA costs one add.
+        {
             const uint32_t idKK = idesc_bf16(128, 16, false, false);
             const uint32_t idKM = idesc_bf16(128, 16, false, true);
-            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-            const uint32_t g_base = smem_u32(smem + C::OFF_G);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
-            auto kslot = [&](int ks, int c, int h) -> uint32_t {
-                return stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512;
+            const SmemDesc dQ = smem_desc_split(smem_u32(smem + C::OFF_Q), 16, 256, 6);
+            const SmemDesc dG = smem_desc_split(smem_u32(smem + C::OFF_G), 16, 256, 6);
+            const SmemDesc dKk = smem_desc_split(stage_base + C::SPD_BYTES, 16, 256, 6);    // K-major K, V
+            const SmemDesc dKm = smem_desc_split(stage_base + C::SPD_BYTES, 256, 256, 6);   // MN-major K
+            constexpr uint32_t kVoff = C::NSLOT * C::SLOT_BYTES;                             // V after K
+            auto koff = [&](int tt, int h) -> uint32_t {
+                const int b = tt / C::NCH, c = tt % C::NCH;
+                return (uint32_t)((b & 1) * C::STAGE_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512);
             };
             auto issue_s = [&](int tt) -> bool {
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
-                if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+                if (c == 0 && !mbar_wait_all(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
                     return false;
                 // stage ss last held dS(tt - 2): the dq products that read it were issued
                 // before this point and the tensor pipe runs one thread's MMAs in order,
                 // so no wait is needed before overwriting it
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ss(tbase + s_col(ss) + 16 * h, smem_desc(q_base + h * 4096, 16, 256, 6),
-                           smem_desc(kslot(ks, c, h), 16, 256, 6), idKK, 0);
-                mma_commit(&bars->s_full[ss]);
+                    for (int h = 0; h < kHC; ++h)
+                        mma_ss(tbase + s_col(ss) + 16 * h, desc_at(dQ, h * 4096), desc_at(dKk, koff(tt, h)), idKK, 0);
+                    mma_commit(&bars->s_full[ss]);
+                }
+                __syncwarp();
                 return true;
             };
             auto issue_dp = [&](int tt) {
-                const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1;
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ss(tbase + kColDp + 16 * h, smem_desc(g_base + h * 4096, 16, 256, 6),
-                           smem_desc(kslot(ks, c, h) + C::NSLOT * C::SLOT_BYTES, 16, 256, 6), idKK, 0);
-                mma_commit(&bars->dp_full);
+                    for (int h = 0; h < kHC; ++h)
+                        mma_ss(tbase + kColDp + 16 * h, desc_at(dG, h * 4096), desc_at(dKk, koff(tt, h) + kVoff),
+                               idKK, 0);
+                    mma_commit(&bars->dp_full);
+                }
+                __syncwarp();
             };
             bool ok = issue_s(0);
             if (ok) issue_dp(0);
@@ -245,24 +256,28 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const int b = tt / C::NCH, c = tt % C::NCH, ks = b & 1, ss = tt & 1;
                 if (tt + 1 < nchunks) {
                     if (!issue_s(tt + 1)) { ok = false; break; }
-                    if (!mbar_wait(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    if (!mbar_wait_all(&bars->dp_free, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
                     issue_dp(tt + 1);
                 }
-                if (!mbar_wait(&bars->ds_ready[ss], (tt >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                if (!mbar_wait_all(&bars->ds_ready[ss], (tt >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h)
-                    mma_ts(tbase + kColDq + 16 * h, tbase + s_col(ss) + 16 * h,
-                           smem_desc(kslot(ks, c, h), 256, 256, 6), idKM, tt > 0 ? 1u : 0u);
-                mma_commit(&bars->dq_done[ss]);
-                if (c == C::NCH - 1) mma_commit(&bars->kv_empty[ks]);
+                    for (int h = 0; h < kHC; ++h)
+                        mma_ts(tbase + kColDq + 16 * h, tbase + s_col(ss) + 16 * h, desc_at(dKm, koff(tt, h)), idKM,
+                               tt > 0 ? 1u : 0u);
+                    mma_commit(&bars->dq_done[ss]);
+                    if (c == C::NCH - 1) mma_commit(&bars->kv_empty[ks]);
+                }
+                __syncwarp();
             }
             if (!ok) {
                 fail(abort_flag, status);
                 int never = 0;
-                mma_commit(&bars->fin);
-                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+                if (elect_one()) mma_commit(&bars->fin);
+                __syncwarp();
+                mbar_wait_all(&bars->fin, 0, &never, kWaitNs);
             }
         }
     } else {

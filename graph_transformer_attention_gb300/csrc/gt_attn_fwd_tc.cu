@@ -290,55 +290,69 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
-        if (lane == 0) {
+        // The whole warp runs the loop and waits; the elected lane issues (an MMA
+        // from a converged warp through elect.sync costs a fraction of one from a
+        // lane-0 branch), and descriptors are precomputed so that an MMA costs one add.
+        {
             const uint32_t idQK = idesc_bf16(128, kCH, false, false);
             const uint32_t idPV = idesc_bf16(128, 16, false, true);
-            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
+            const SmemDesc dQ = smem_desc_split(smem_u32(smem + C::OFF_Q), 16, 256, 6);
+            const SmemDesc dKk = smem_desc_split(stage_base + C::SPD_BYTES, 16, 256, 6);     // K-major K
+            const SmemDesc dVm = smem_desc_split(stage_base + C::SPD_BYTES, 256, 256, 6);    // MN-major V
             bool ok = true;
             // chunk tt covers KV rows 32c .. 32c+31 of block b: 1024 bytes into a slot
+            auto koff = [&](int tt) -> uint32_t {
+                const int b = tt / kNCH, c = tt % kNCH;
+                return (uint32_t)((b & 1) * C::STAGE_BYTES + c * 1024);
+            };
             auto issue_qk = [&](int tt) -> bool {
                 const int b = tt / kNCH, c = tt % kNCH, ks = b & 1;
-                if (c == 0 && !mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
+                if (c == 0 && !mbar_wait_all(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs))
                     return false;
-                if (tt > 0 && !mbar_wait(&bars->s_free, (tt - 1) & 1, abort_flag, kWaitNs))
+                if (tt > 0 && !mbar_wait_all(&bars->s_free, (tt - 1) & 1, abort_flag, kWaitNs))
                     return false;
                 tc_fence_after();
-                const uint32_t kbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES + c * 1024;
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h) {
-                    const int slot = h * HD / 16;
-                    mma_ss(tbase + kColS + kCH * h, smem_desc(q_base + h * 4096, 16, 256, 6),
-                           smem_desc(kbase + slot * C::SLOT_BYTES, 16, 256, 6), idQK, 0);
+                    for (int h = 0; h < kHC; ++h) {
+                        const int slot = h * HD / 16;
+                        mma_ss(tbase + kColS + kCH * h, desc_at(dQ, h * 4096),
+                               desc_at(dKk, koff(tt) + slot * C::SLOT_BYTES), idQK, 0);
+                    }
+                    mma_commit(&bars->s_full);
                 }
-                mma_commit(&bars->s_full);
+                __syncwarp();
                 return true;
             };
             ok = issue_qk(0);
             for (int tt = 0; ok && tt < nchunks; ++tt) {
                 const int b = tt / kNCH, c = tt % kNCH, ks = b & 1;
                 if (tt + 1 < nchunks && !issue_qk(tt + 1)) { ok = false; break; }
-                if (!mbar_wait(&bars->p_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                if (!mbar_wait_all(&bars->p_ready, tt & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t vbase = stage_base + ks * C::STAGE_BYTES + C::SPD_BYTES +
-                                       C::NSLOT * C::SLOT_BYTES + c * 1024;
+                const uint32_t voff = koff(tt) + C::NSLOT * C::SLOT_BYTES;
+                if (elect_one()) {
 #pragma unroll
-                for (int h = 0; h < kHC; ++h) {
-                    const int slot = h * HD / 16;
+                    for (int h = 0; h < kHC; ++h) {
+                        const int slot = h * HD / 16;
 #pragma unroll
-                    for (int st = 0; st < 2; ++st)
-                        mma_ts(tbase + kColO + 16 * h, tbase + kColP + 16 * h + 8 * st,
-                               smem_desc(vbase + slot * C::SLOT_BYTES + 512 * st, 256, 256, 6), idPV,
-                               (tt > 0 || st > 0) ? 1u : 0u);
+                        for (int st = 0; st < 2; ++st)
+                            mma_ts(tbase + kColO + 16 * h, tbase + kColP + 16 * h + 8 * st,
+                                   desc_at(dVm, voff + slot * C::SLOT_BYTES + 512 * st), idPV,
+                                   (tt > 0 || st > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars->pv_done);
+                    if (c == kNCH - 1) mma_commit(&bars->kv_empty[ks]);
                 }
-                mma_commit(&bars->pv_done);
-                if (c == kNCH - 1) mma_commit(&bars->kv_empty[ks]);
+                __syncwarp();
             }
             if (!ok) {
                 fail(bars, status);
                 int never = 0;
-                mma_commit(&bars->fin);
-                mbar_wait(&bars->fin, 0, &never, kWaitNs);
+                if (elect_one()) mma_commit(&bars->fin);
+                __syncwarp();
+                mbar_wait_all(&bars->fin, 0, &never, kWaitNs);
             }
         }
     } else {

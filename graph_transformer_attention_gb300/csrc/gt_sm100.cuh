@@ -84,6 +84,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// One lane of a converged warp (the lowest active one, so the same lane each
+// time the whole warp executes it): the lane that issues a warp's tcgen05.mma
+// and tcgen05.commit instructions.  Measured on GB300 (M=128, N=16, K=16, bf16):
+// from a converged warp through elect.sync an MMA with A in TMEM costs about 11
+// cycles and one with both operands in shared memory 39 (the 4 KB A operand at
+// 128 B per clock); from a lane-0 branch of a diverged warp, or behind a plain
+// lane test, every MMA costs 45-55 cycles whatever its operands.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// mbar_wait by every lane of a warp, which leaves the warp converged (the lanes
+// read the same barrier; the vote only rejoins lanes that gave up at different
+// polls).
+__device__ __forceinline__ bool mbar_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // 16-byte shared-memory loads through a 32-bit shared-window address.  lds_f4
 // is for tables that do not change while the kernel runs (the compiler may
 // schedule it freely); the others are ordered like ordinary memory accesses.
@@ -180,6 +206,24 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)1u << 46;                 // descriptor version for sm_100
     d |= (uint64_t)(layout & 7u) << 61;
     return d;
+}
+
+// The same descriptor as two 32-bit halves.  The start address lives in the
+// low half only (bits 0-13, in 16-byte units; shared addresses stay below 2^18
+// bytes), so a descriptor for base + off is (lo + (off >> 4), hi): the issuing
+// thread adds one 32-bit offset per MMA instead of rebuilding 64 bits.
+struct SmemDesc {
+    uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SmemDesc smem_desc_split(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    const uint64_t d = smem_desc(saddr, lbo, sbo, layout);
+    return SmemDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
+// Descriptor of (base + off bytes); off a multiple of 16.
+__device__ __forceinline__ uint64_t desc_at(SmemDesc d, uint32_t off) {
+    return ((uint64_t)d.hi << 32) | (uint64_t)(d.lo + (off >> 4));
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
