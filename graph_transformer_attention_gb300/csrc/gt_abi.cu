@@ -38,8 +38,8 @@ int attn_bwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, 
 bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
-                int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, float* Dv,
-                double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s);
+                int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
+                float* Dv, double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -80,6 +80,7 @@ struct BwdWs {
     float* Dv;
     double* dT64;
     float* LD;
+    uint16_t* LB;   // bf16 [n][8][16]: per node and head -lse / scale and -D in three parts (dk/dv)
     float* aux;     // [16]: per head the largest row norm of v (tensor-core path)
     float* acc;     // split backward: fp32 dq, dk, dv accumulators, else null
 };
@@ -131,6 +132,7 @@ size_t bwd_ws(int n, int h, int d, int nsplit, void* base, size_t cap, BwdWs* ou
     w.dT64 = c.take<double>((size_t)h * 128);
     // per-node lse log2 e (rows 0..7) and D (rows 8..15) of the 8 heads, [16][ld_ld]
     w.LD = c.take<float>((size_t)16 * bwd_ld_ld(n));
+    w.LB = c.take<uint16_t>((size_t)n * 8 * 16);
     w.aux = c.take<float>(16);
     if (out) *out = w;
     return c.off;
@@ -274,7 +276,7 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.Dv, w.dT64, w.aux, nsplit, w.acc, s);
+                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, w.acc, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

@@ -5,30 +5,41 @@
 // bias slice of each block comes from the int8 bucket matrix),
 //   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
 //
-// One CTA = one tile of 128 KV rows and one half of the heads (4 of 8: grid.y),
-// streaming every Q tile; two CTAs share an SM.  The work is cut into steps of
-// one head pair and 16 query rows, and the tensor core runs two steps ahead of
-// the softmax warps, so that they never wait on their products.  192 threads:
-//   warps 0-3  thread r owns KV row j0 + r (TMEM lane r).  Per step it reads S^T
-//              and dP^T of its two heads from TMEM, the bucket code of (i, j) from
-//              column r of the int8 tile (once per 16 query rows), lse_i log2 e and
-//              D_i from the staged LD rows (4 consecutive i per 16-byte load), forms
-//              P^T = 2^(s scale log2 e + b - lse_i log2 e) and dS^T = P^T (dP^T - D_i)
-//              and writes both (bf16) back over S^T.
-//   warp 4     MMA issuer: per step, once its P^T and dS^T are in, dv_h += P^T_h dO_h
-//              and dk_h += dS^T_h Q_h (A from TMEM), then S^T_h = K_h Q_h^T and
-//              dP^T_h = V_h dO_h^T (M=128, N=16, K=16) of the step two ahead into the
-//              same buffer (the tensor pipe runs one thread's MMAs in order, so they
-//              land after the products that read the buffer).
-//   warp 5     TMA producer: per Q tile the bucket tile, the Q and dO column
-//              slots and the LD columns.
-// TMEM (256 columns): dk at 0..63, dv at 64..127, and one 64-column buffer per
-// head pair at 128 and 192: head e of the pair holds S^T (then P^T | dS^T in
-// bf16) at +16e and dP^T at +32 + 16e.  All waits are bounded (timeout ->
-// device status word, orderly exit, TMEM freed).
+// One CTA per SM = one tile of 128 KV rows and one half of the heads (4 of 8:
+// grid.y), streaming every Q tile.  The CTA owns all 512 TMEM columns, so K and
+// V sit in TMEM as the A operands of S^T = K Q^T and dP^T = V dO^T: every
+// product reads only its small B operand from shared memory (an MMA with A in
+// shared memory reads 4 KB of it, which both costs ~4x the tensor time and
+// delays the softmax warps' own shared loads).  The work is cut into steps of
+// one head pair and 32 query rows; the tensor core runs two steps ahead of the
+// softmax warps.  320 threads:
+//   warps 0-7  warp w owns KV rows 32 (w mod 4) .. + 31 (TMEM lanes) and query
+//              rows 16 (w / 4) .. + 15 of each step, for both heads of the pair: it
+//              reads S'^T and dP'^T from TMEM, the bucket codes from column r of the
+//              int8 tile, forms P^T = 2^(s' scale log2 e + b) and dS^T = P^T dP'^T
+//              and writes both (bf16) back over S'^T.  The tensor core has already
+//              taken lse_i and D_i out: S'^T = K Q^T + 1 (-lse_i / scale) and
+//              dP'^T = V dO^T + 1 (-D_i), the second product of each with a constant
+//              A operand of ones in TMEM and B = the per-row values as three bf16
+//              parts (exact to fp32 rounding), so the softmax warps load neither.
+//   warp 8     MMA issuer (the whole warp waits, the elected lane issues): per
+//              step, once its P^T and dS^T are in, dv_h += P^T_h dO_h and
+//              dk_h += dS^T_h Q_h (A from TMEM), then S^T and dP^T of the step two
+//              ahead into the same buffer (the tensor pipe runs one thread's MMAs
+//              in order, so they land after the products that read the buffer).
+//   warp 9     TMA producer: per Q tile the bucket tile and the Q, dO and LB
+//              column slots (LB: -lse_i / scale and -D_i per head in three bf16
+//              parts each); it also summarises each tile's codes.
+// TMEM (512 columns): dk at 0, dv at 64, K at 128 and V at 160 (8 columns of
+// bf16 pairs per head), the two ones operands at 192 and 200, and one
+// 128-column buffer per head pair at 256 and 384: head e of the pair holds S'^T
+// at +32e and dP'^T at +64 + 32e; the 16 columns of query rows 16u .. 16u + 15
+// take P^T (columns +16u .. +7) and dS^T (+16u + 8 .. +15) over S'^T.  All waits are bounded (timeout -> device status word, orderly
+// exit, TMEM freed).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "gt_common.cuh"
@@ -44,44 +55,47 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int kBKV = 128;
-constexpr int kCH = 16;
+constexpr int kCH = 32;                    // query rows per step
 constexpr int kQST = 2;
 constexpr int kHC = 4;                     // heads per CTA
-constexpr int kSoft = 128;
+constexpr int kSoft = 256;                 // softmax threads: 128 KV rows x 2 heads of a pair
 constexpr int kThreads = kSoft + 64;
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDk = 0;
 constexpr uint32_t kColDv = 64;
+constexpr uint32_t kColKA = 128;
+constexpr uint32_t kColVA = 160;
+constexpr uint32_t kColOnesL = 192;        // A = [1 1 1 0 ...]: picks -lse / scale from LB
+constexpr uint32_t kColOnesD = 200;        // A = [0 0 0 1 1 1 0 ...]: picks -D
+constexpr uint32_t kSmemOneCta = 120 * 1024;   // more than half an SM's shared memory: one CTA per SM
 
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return __fadd2_rn(a, make_float2(-b.x, -b.y));
 }
 
 // TMEM buffer of head pair p
-__device__ __forceinline__ uint32_t pair_buf(int p) { return 128u + 64u * (uint32_t)p; }
+__device__ __forceinline__ uint32_t pair_buf(int p) { return 256u + 128u * (uint32_t)p; }
 
 template <int HD>
 struct KvCfg {
     static constexpr int BQ = 64;                         // query rows per TMA tile
-    static constexpr int NCH = BQ / kCH;
+    static constexpr int NCH = BQ / kCH;                  // steps of one head pair per tile
     static constexpr int NSLOT = kHC * HD / 16;           // 16-column slots of this CTA's heads
-    static constexpr uint32_t OP_BYTES = kHC * kBKV * 32; // per-head [128][16] bf16 operands
     static constexpr uint32_t SPD_BYTES = BQ * kBKV;      // [BQ i][128 j], no swizzle
     static constexpr uint32_t SLOT_BYTES = BQ * 32;
-    static constexpr uint32_t LD_BYTES = 16 * BQ * 4;     // [16][BQ] fp32
-    static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES + LD_BYTES;
-    static constexpr uint32_t OFF_K = 0;
-    static constexpr uint32_t OFF_V = OP_BYTES;
-    static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
+    static constexpr uint32_t LB_OFF = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;   // one LB slot per head
+    static constexpr uint32_t STAGE_BYTES = LB_OFF + kHC * SLOT_BYTES;
+    static constexpr uint32_t OFF_STAGE = 0;
     static constexpr uint32_t OFF_T = OFF_STAGE + kQST * STAGE_BYTES;
-    // per stage: one int per (16-row chunk, warp's 32 KV columns): the bucket code
-    // when all 512 codes of that block are equal, else -1
+    // per stage: one int per (32-row chunk, warp's 32 KV columns): the bucket code
+    // when all 1024 codes of that block are equal, else -1
     static constexpr int NMETA = NCH * 4;
     static constexpr uint32_t OFF_META = OFF_T + 256 * kH * 4;
     static constexpr uint32_t OFF_BAR = OFF_META + kQST * NMETA * 4;
-    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t SMEM_USED = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t SMEM = SMEM_USED > kSmemOneCta ? SMEM_USED : kSmemOneCta;
 };
 
 struct Bars {
@@ -96,18 +110,39 @@ struct Bars {
     int abort;
 };
 
+// A-operand row r of head h (this CTA's local head index) of the per-head
+// products with K = 16: the head's channels as bf16 pairs; head dim 8 sits in
+// the half of the 16-column slot it shares with its neighbour head (the other
+// half zero, so the neighbour's channels of the B operand drop out of the sum).
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void head_a_row(const __nv_bfloat16* src, int hg, bool live, uint32_t (&a)[8]) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    if (HD == 16) {
+        const uint4 lo = live ? s4[2 * hg] : make_uint4(0, 0, 0, 0);
+        const uint4 hi = live ? s4[2 * hg + 1] : make_uint4(0, 0, 0, 0);
+        a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
+        a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+    } else {
+        const uint4 v = live ? s4[hg] : make_uint4(0, 0, 0, 0);
+        const bool odd = hg & 1;
+        a[0] = odd ? 0u : v.x; a[1] = odd ? 0u : v.y; a[2] = odd ? 0u : v.z; a[3] = odd ? 0u : v.w;
+        a[4] = odd ? v.x : 0u; a[5] = odd ? v.y : 0u; a[6] = odd ? v.z : 0u; a[7] = odd ? v.w : 0u;
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
-                const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapL,
+                const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapB,
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                 const float* __restrict__ T, int nb, int n, float scale, float scale_log2, int split_tiles,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dk_acc,
                 float* __restrict__ dv_acc, int* status) {
     using C = KvCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array, so that the
+    // compiler still knows plain accesses through it are shared-memory accesses
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -137,29 +172,45 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         tma_prefetch_desc(&mapQ);
         tma_prefetch_desc(&mapG);
         tma_prefetch_desc(&mapS);
-        tma_prefetch_desc(&mapL);
+        tma_prefetch_desc(&mapB);
     }
     if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
     fill_bias_table(Ts, T, nb, tid, kThreads);
-    if (tid < kBKV) {
-        const int row = j0 + tid;
-        const bool live = row < n;
-        const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
-        write_head_operands<HD, kHC>(smem + C::OFF_K, tid, k + off, live, kHC * hb);
-        write_head_operands<HD, kHC>(smem + C::OFF_V, tid, v + off, live, kHC * hb);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = bars->tmem_base;
     int* abort_flag = &bars->abort;
+    // K and V rows of this CTA's heads into TMEM (A operands), one row per lane
+    if (tid < kBKV) {
+        const int row = j0 + tid;
+        const bool live = row < n;
+        const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
+        const uint32_t lr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+#pragma unroll
+        for (int hh = 0; hh < kHC; ++hh) {
+            uint32_t a[8];
+            head_a_row<HD>(k + off, kHC * hb + hh, live, a);
+            tmem_st_x8(lr + kColKA + 8 * hh, a);
+            head_a_row<HD>(v + off, kHC * hb + hh, live, a);
+            tmem_st_x8(lr + kColVA + 8 * hh, a);
+        }
+        // ones operands (bf16 1.0 = 0x3f80; element 2c in the low half of column c)
+        const uint32_t onesL[8] = {0x3f803f80u, 0x00003f80u, 0u, 0u, 0u, 0u, 0u, 0u};
+        const uint32_t onesD[8] = {0u, 0x3f800000u, 0x3f803f80u, 0u, 0u, 0u, 0u, 0u};
+        tmem_st_x8(lr + kColOnesL, onesL);
+        tmem_st_x8(lr + kColOnesD, onesD);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------ TMA producer
         // Issues the copies of Q tile b + 2 once tile b is consumed, and summarises
         // each tile's bucket codes as soon as it lands (one tile ahead of the
-        // softmax): per (16-row chunk, 32-column warp block) the common code or -1.
+        // softmax): per (32-row chunk, 32-column warp block) the common code or -1.
         int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
         int issued = 0;
         bool ok = true;
@@ -180,8 +231,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         tma_load_2d(st + C::SPD_BYTES + (C::NSLOT + s) * C::SLOT_BYTES, &mapG,
                                     16 * (hb * C::NSLOT + s), i0, &bars->q_full[ks]);
                     }
-                    tma_load_2d(st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES, &mapL, i0, 0,
-                                &bars->q_full[ks]);
+#pragma unroll
+                    for (int hh = 0; hh < kHC; ++hh)
+                        tma_load_2d(st + C::LB_OFF + hh * C::SLOT_BYTES, &mapB, 16 * (kHC * hb + hh), i0,
+                                    &bars->q_full[ks]);
                 }
             }
             __syncwarp();
@@ -196,19 +249,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 return false;
             }
             const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
-            // per 16-row chunk: lane l checks 16-byte piece l & 7 of rows 4u + l / 8
-            // (u = 0..3), so the eight lanes of a row cover all 32 banks; a warp
+            // per 32-row chunk: lane l checks 16-byte piece l & 7 of rows 4u + l / 8
+            // (u = 0..7), so the eight lanes of a row cover all 32 banks; a warp
             // block w owns pieces 2w, 2w + 1 of every row
             const uint32_t piece = (uint32_t)(lane & 7), rsub = (uint32_t)(lane >> 3);
 #pragma unroll 1
             for (int cc = 0; cc < C::NCH; ++cc) {
-                const uint32_t row0 = st + (uint32_t)(16 * cc) * kBKV;
+                const uint32_t row0 = st + (uint32_t)(kCH * cc) * kBKV;
                 const uint32_t ref = lds_u8(row0 + 32u * (piece >> 1)) * 0x01010101u;
                 bool same = true;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint4 v = lds_u4(row0 + (4u * u + rsub) * kBKV + 16u * piece);
-                    same = same && v.x == ref && v.y == ref && v.z == ref && v.w == ref;
+                for (int u = 0; u < kCH / 4; ++u) {
+                    const uint4 vv = lds_u4(row0 + (4u * u + rsub) * kBKV + 16u * piece);
+                    same = same && vv.x == ref && vv.y == ref && vv.z == ref && vv.w == ref;
                 }
                 const unsigned bal = __ballot_sync(0xffffffffu, same);
                 const uint32_t wref = __shfl_sync(0xffffffffu, ref, 2 * (lane & 3));
@@ -234,25 +287,28 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
-        // Step s = 2 t + p: chunk t of 16 query rows, head pair p (heads 2p, 2p + 1
+        // Step s = 2 t + p: chunk t of 32 query rows, head pair p (heads 2p, 2p + 1
         // of this CTA), TMEM buffer p.  The whole warp runs the loop and waits; the
         // elected lane issues (an MMA from a converged warp through elect.sync costs
         // a fraction of one from a lane-0 branch), and descriptors are precomputed
         // so that an MMA costs one add.
         {
-            const uint32_t idKK = idesc_bf16(128, 16, false, false);
+            const uint32_t idS = idesc_bf16(128, kCH, false, false);
             const uint32_t idKM = idesc_bf16(128, 16, false, true);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
-            const SmemDesc dK = smem_desc_split(smem_u32(smem + C::OFF_K), 16, 256, 6);
-            const SmemDesc dV = smem_desc_split(smem_u32(smem + C::OFF_V), 16, 256, 6);
             const SmemDesc dQk = smem_desc_split(stage_base + C::SPD_BYTES, 16, 256, 6);     // K-major Q
             const SmemDesc dQm = smem_desc_split(stage_base + C::SPD_BYTES, 256, 256, 6);    // MN-major Q
             constexpr uint32_t kG = C::NSLOT * C::SLOT_BYTES;                                 // dO after Q
             const int nsteps = 2 * nchunks;
-            // offset of (stage, chunk, head) in the Q / dO column slots
+            // offset of (stage, chunk, head) in the Q / dO column slots (32 rows = 1 KB)
             auto qoff = [&](int t, int h) -> uint32_t {
                 const int b = t / C::NCH, c = t % C::NCH;
-                return (uint32_t)((b & 1) * C::STAGE_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 512);
+                return (uint32_t)((b & 1) * C::STAGE_BYTES + (h * HD / 16) * C::SLOT_BYTES + c * 1024);
+            };
+            // offset of (stage, chunk, head) in the LB slots
+            auto boff = [&](int t, int h) -> uint32_t {
+                const int b = t / C::NCH, c = t % C::NCH;
+                return (uint32_t)((b & 1) * C::STAGE_BYTES + (C::LB_OFF - C::SPD_BYTES) + h * C::SLOT_BYTES + c * 1024);
             };
             auto issue_sd = [&](int st) -> bool {
                 const int t = st >> 1, p = st & 1, b = t / C::NCH, c = t % C::NCH, ks = b & 1;
@@ -264,8 +320,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = 2 * p + e;
-                        mma_ss(d + 16 * e, desc_at(dK, h * 4096), desc_at(dQk, qoff(t, h)), idKK, 0);
-                        mma_ss(d + 32 + 16 * e, desc_at(dV, h * 4096), desc_at(dQk, qoff(t, h) + kG), idKK, 0);
+                        const uint32_t lb = boff(t, h);
+                        mma_ts(d + 32 * e, tbase + kColKA + 8 * h, desc_at(dQk, qoff(t, h)), idS, 0);
+                        mma_ts(d + 32 * e, tbase + kColOnesL, desc_at(dQk, lb), idS, 1);
+                        mma_ts(d + 64 + 32 * e, tbase + kColVA + 8 * h, desc_at(dQk, qoff(t, h) + kG), idS, 0);
+                        mma_ts(d + 64 + 32 * e, tbase + kColOnesD, desc_at(dQk, lb), idS, 1);
                     }
                     mma_commit(&bars->sd_full[p]);
                 }
@@ -279,13 +338,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!mbar_wait_all(&bars->ds_ready[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t x = tbase + pair_buf(p);
-                const uint32_t acc = t > 0 ? 1u : 0u;
                 if (elect_one()) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = 2 * p + e;
-                        mma_ts(tbase + kColDv + 16 * h, x + 16 * e, desc_at(dQm, qoff(t, h) + kG), idKM, acc);
-                        mma_ts(tbase + kColDk + 16 * h, x + 16 * e + 8, desc_at(dQm, qoff(t, h)), idKM, acc);
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const uint32_t acc = (t > 0 || k2 > 0) ? 1u : 0u;
+                            mma_ts(tbase + kColDv + 16 * h, x + 32 * e + 16 * k2,
+                                   desc_at(dQm, qoff(t, h) + kG + 512 * k2), idKM, acc);
+                            mma_ts(tbase + kColDk + 16 * h, x + 32 * e + 16 * k2 + 8,
+                                   desc_at(dQm, qoff(t, h) + 512 * k2), idKM, acc);
+                        }
                     }
                     if (c == C::NCH - 1 && p == 1) mma_commit(&bars->q_empty[ks]);
                 }
@@ -305,7 +369,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------- softmax
+        // Warps w and w + 4 own the same 32 KV rows (TMEM lanes): thread (r, half)
+        // takes query rows 16 half .. 16 half + 15 of every step, both heads.
         const int r = tid & (kBKV - 1);
+        const int half = tid >> 7;
         const int row = j0 + r;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t tbl = smem_u32(Ts) + 16u * hb;
@@ -315,15 +382,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const int ks = b & 1;
             // (the summary is written after the tile's copies have landed)
             if (!mbar_wait(&bars->meta_ready[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            const uint32_t st = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES);
+            const uint8_t* stp = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
             const int* meta = reinterpret_cast<const int*>(smem + C::OFF_META) + ks * C::NMETA + (warp & 3);
-            // LD rows of this group's first head: row h is 4 BQ bytes long
-            const uint32_t ldb = st + C::SPD_BYTES + 2 * C::NSLOT * C::SLOT_BYTES + 4u * (kHC * hb) * C::BQ;
             const int i0 = (qt0 + b) * C::BQ;
             const bool tail_tile = i0 + C::BQ > n;
             for (int c = 0; ok && c < C::NCH; ++c, ++t) {
-                // bucket codes of the 16 (i, j) pairs of this chunk: column r of the tile,
-                // unless the warp's whole 16 x 32 block holds one code
+                const int ir = c * kCH + 16 * half;       // this thread's first query row in the tile
+                // bucket codes of the 16 (i, j) pairs: column r of the tile, unless the
+                // warp's whole 32 x 32 block holds one code
                 const int ucode = meta[4 * c];
                 uint32_t code[16];
                 float4 bu = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -331,106 +397,65 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     bu = lds_f4(tbl + (uint32_t)ucode * 32u);
                 } else {
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) code[kk] = lds_u8(st + (uint32_t)(c * kCH + kk) * kBKV + r);
+                    for (int kk = 0; kk < 16; ++kk) code[kk] = stp[(ir + kk) * kBKV + r];
                 }
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
                     if (!mbar_wait(&bars->sd_full[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t x = lrow + pair_buf(p);
-                    const int h0 = 2 * p;     // local head index of the pair's first head
+                    const uint32_t x = lrow + pair_buf(p) + 16 * half;
+                    uint32_t rs[2][16], rd[2][16];
+                    tmem_ld_x16(x, rs[0]);
+                    tmem_ld_x16(x + 32, rs[1]);
+                    tmem_ld_x16(x + 64, rd[0]);
+                    tmem_ld_x16(x + 96, rd[1]);
+                    tmem_wait_ld();
+                    // x = s' scale log2e + b(code); P = 2^x
                     float pf[2][16];
-                    {
-                        uint32_t rs[2][16];
-                        tmem_ld_x16(x, rs[0]);
-                        tmem_ld_x16(x + 16, rs[1]);
-                        tmem_wait_ld();
-                        // x = s scale log2e + b(code) - lse_i log2e
-                        if (ucode >= 0) {
-                            const float b0 = p ? bu.z : bu.x, b1 = p ? bu.w : bu.y;
-                            if constexpr (HD == 16) {
-                                // packed FMAs, two rows i at a time (the same results; measured
-                                // faster at head dim 16 and not at 8)
-                                const float2 cc = make_float2(scale_log2, scale_log2);
+                    if (ucode >= 0) {
+                        const float b0 = p ? bu.z : bu.x, b1 = p ? bu.w : bu.y;
+                        const float2 cc = make_float2(scale_log2, scale_log2);
 #pragma unroll
-                                for (int kk = 0; kk < 16; kk += 2) {
-                                    const float2 xa = __ffma2_rn(
-                                        make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
-                                        make_float2(b0, b0));
-                                    const float2 xb = __ffma2_rn(
-                                        make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
-                                        make_float2(b1, b1));
-                                    pf[0][kk] = xa.x;
-                                    pf[0][kk + 1] = xa.y;
-                                    pf[1][kk] = xb.x;
-                                    pf[1][kk + 1] = xb.y;
-                                }
-                            } else {
+                        for (int kk = 0; kk < 16; kk += 2) {
+                            const float2 xa = __ffma2_rn(
+                                make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
+                                make_float2(b0, b0));
+                            const float2 xb = __ffma2_rn(
+                                make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
+                                make_float2(b1, b1));
+                            pf[0][kk] = xa.x;
+                            pf[0][kk + 1] = xa.y;
+                            pf[1][kk] = xb.x;
+                            pf[1][kk + 1] = xb.y;
+                        }
+                    } else {
 #pragma unroll
-                                for (int kk = 0; kk < 16; ++kk) {
-                                    pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, b0);
-                                    pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, b1);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 16; ++kk) {
-                                const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * p);
-                                pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
-                                pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
-                            }
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * p);
+                            pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
+                            pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
                         }
                     }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const uint32_t la = ldb + 4u * (h0 + e) * C::BQ + 4u * (c * kCH);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint4 l = lds_u4(la + 16u * q4);
-                            const float2 xa = fsub2(make_float2(pf[e][4 * q4], pf[e][4 * q4 + 1]),
-                                                    make_float2(__uint_as_float(l.x), __uint_as_float(l.y)));
-                            const float2 xb = fsub2(make_float2(pf[e][4 * q4 + 2], pf[e][4 * q4 + 3]),
-                                                    make_float2(__uint_as_float(l.z), __uint_as_float(l.w)));
-                            pf[e][4 * q4] = ex2(xa.x);
-                            pf[e][4 * q4 + 1] = ex2(xa.y);
-                            pf[e][4 * q4 + 2] = ex2(xb.x);
-                            pf[e][4 * q4 + 3] = ex2(xb.y);
-                        }
+                        for (int kk = 0; kk < 16; ++kk) pf[e][kk] = ex2(pf[e][kk]);
                         if (tail_tile) {
 #pragma unroll
                             for (int kk = 0; kk < 16; ++kk)
-                                if (i0 + c * kCH + kk >= n) pf[e][kk] = 0.f;
+                                if (i0 + ir + kk >= n) pf[e][kk] = 0.f;
                         }
-                        uint32_t pp[8];
+                        uint32_t pp[8], pd[8];
 #pragma unroll
-                        for (int k2 = 0; k2 < 8; ++k2) pp[k2] = pack_bf16x2(pf[e][2 * k2], pf[e][2 * k2 + 1]);
-                        tmem_st_x8(x + 16 * e, pp);
-                    }
-                    {
-                        uint32_t rd[2][16];
-                        tmem_ld_x16(x + 32, rd[0]);
-                        tmem_ld_x16(x + 48, rd[1]);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const uint32_t la = ldb + 4u * (kH + h0 + e) * C::BQ + 4u * (c * kCH);
-                            uint32_t pd[8];
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                const uint4 dd = lds_u4(la + 16u * q4);
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const int kk = 4 * q4 + 2 * u;
-                                    const float2 dvv = u == 0 ? make_float2(__uint_as_float(dd.x), __uint_as_float(dd.y))
-                                                              : make_float2(__uint_as_float(dd.z), __uint_as_float(dd.w));
-                                    const float2 ds = __fmul2_rn(
-                                        make_float2(pf[e][kk], pf[e][kk + 1]),
-                                        fsub2(make_float2(__uint_as_float(rd[e][kk]), __uint_as_float(rd[e][kk + 1])), dvv));
-                                    pd[kk / 2] = pack_bf16x2(ds.x, ds.y);
-                                }
-                            }
-                            tmem_st_x8(x + 16 * e + 8, pd);
+                        for (int k2 = 0; k2 < 8; ++k2) {
+                            pp[k2] = pack_bf16x2(pf[e][2 * k2], pf[e][2 * k2 + 1]);
+                            const float2 ds = __fmul2_rn(
+                                make_float2(pf[e][2 * k2], pf[e][2 * k2 + 1]),
+                                make_float2(__uint_as_float(rd[e][2 * k2]), __uint_as_float(rd[e][2 * k2 + 1])));
+                            pd[k2] = pack_bf16x2(ds.x, ds.y);
                         }
+                        tmem_st_x8(x + 32 * e, pp);
+                        tmem_st_x8(x + 32 * e + 8, pd);
                     }
                     tmem_wait_st();
                     tc_fence_before();
@@ -448,7 +473,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             tc_fence_after();
             const bool live = row < n;
 #pragma unroll
-            for (int hh = 0; hh < kHC; ++hh) {
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int hh = 2 * half + h2;
                 const int h = kHC * hb + hh;
                 uint32_t ok16[16], ov16[16];
                 tmem_ld_x16(lrow + kColDk + 16 * hh, ok16);
@@ -493,8 +519,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-           int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, int nsplit, void* dk,
-           void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
+           int64_t ld, const float* T, int nb, float scale, float fold_scale, const uint16_t* LB, int nsplit,
+           void* dk, void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
     using C = KvCfg<HD>;
     CUtensorMap mq, mg, ms, ml;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -504,8 +530,8 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
                      C::BQ, 16, CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_map_2d(&ms, const_cast<int8_t*>(spd), CU_TENSOR_MAP_DATA_TYPE_UINT8, n, n, ld, C::BQ,
                      kBKV, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&ml, const_cast<float*>(LD), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 16, n,
-                     (uint64_t)ldl * 4, 16, C::BQ, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map_2d(&ml, const_cast<uint16_t*>(LB), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, (uint64_t)kH * 16,
+                     (uint64_t)kH * 16 * 2, C::BQ, 16, CU_TENSOR_MAP_SWIZZLE_32B))
         return GT_ERR_CUDA;
     if (cudaFuncSetAttribute(bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
@@ -520,7 +546,7 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         LaunchScope ls("bwd_dkdv", s);
         bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
             mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-            T, nb, n, scale, scale * kLog2e, per, static_cast<__nv_bfloat16*>(dk),
+            T, nb, n, scale, fold_scale * kLog2e, per, static_cast<__nv_bfloat16*>(dk),
             static_cast<__nv_bfloat16*>(dv), per > 0 ? dk_acc : nullptr, per > 0 ? dv_acc : nullptr, status);
     }
     return check_launch();
@@ -530,10 +556,13 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const float* LD, int ldl, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    const uint16_t* LB, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
                     cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, nsplit, dk, dv, dk_acc, dv_acc, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, nsplit, dk, dv, dk_acc, dv_acc, s);
+    // LB holds -lse / fold_scale with fold_scale = scale, or a tiny stand-in for a
+    // zero scale; dk takes the true scale
+    const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, dk, dv, dk_acc, dv_acc, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, dk, dv, dk_acc, dv_acc, s);
 }
 
 }  // namespace gt

@@ -20,11 +20,13 @@
  *   - Pointers named as device buffers must be device memory of the current
  *     CUDA device.  The caller owns and allocates every buffer, including the
  *     workspace; the library allocates no device memory and keeps no state
- *     between calls (apart from one device status word, see
- *     gt_check_device_status, the launch statistics at the end of this header,
- *     and, per device, one internal stream and two events that the tensor-core
- *     backward creates on first use to run two of its kernels side by side,
- *     forked from and joined back into the caller's stream).
+ *     between calls apart from one device status word per device (see
+ *     gt_check_device_status) and the launch statistics at the end of this
+ *     header.  Every kernel runs on the caller's stream.
+ *   - The library caches per-device addresses (the status word; the scratch
+ *     array of gt_bias_attn_bwd_noalloc).  Do not reset a device
+ *     (cudaDeviceReset) while the library is loaded in the process: the cached
+ *     addresses would outlive the context they belong to.
  *   - Layouts are dense row-major: q, k, v, o, dO, dq, dk, dv are [n][h][d]
  *     (node, head, channel); lse is [h][n] fp32; T and dT are [h][nb] fp32;
  *     spd is int8 [n][ld_spd] (row i holds the bucket codes of pairs (i, *)).
@@ -243,10 +245,15 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d,
  *     clears what must start at zero).  Calls whose GPU work overlaps, on
  *     different streams or host threads of one device, race on the array and
  *     corrupt each other's results: serialise them.
- *   - Returns GT_ERR_WORKSPACE, with nothing launched, when the problem needs
- *     more scratch than GT_NOALLOC_SCRATCH_BYTES, i.e. when
- *     gt_bias_attn_workspace_size(dtype, n, h, d, 0) exceeds it (with H = 8 the
- *     limit is N of about 43,000 nodes).
+ *   - Returns GT_ERR_WORKSPACE, with nothing launched, when the backward run
+ *     without its split (the split's fp32 sums are left out when they do not
+ *     fit) needs more than GT_NOALLOC_SCRATCH_BYTES.  That scratch is, in bytes,
+ *     with 256-byte alignment of each part: 4 h n (D) + 1024 (dT sums)
+ *     + 64 * ((n + 3) / 4 * 4) (per-node lse and D rows) + 256 n (the bf16 lse / D
+ *     operand of the dk/dv products) + 64; with H = 8 about 352 bytes per node,
+ *     so N up to about 11,900 nodes.  gt_bias_attn_workspace_size may report
+ *     more than this for small graphs (it includes the split's sums); such calls
+ *     still succeed, unsplit.
  */
 #define GT_NOALLOC_SCRATCH_BYTES (4u << 20)
 int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
