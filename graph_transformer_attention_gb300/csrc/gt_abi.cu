@@ -39,7 +39,8 @@ bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s);
+                float* Dv, double* dT64, float* aux, int nsplit, int tail, float* acc, cudaStream_t s);
+int bwd_dkdv_tail_split(int n);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -124,10 +125,17 @@ int bwd_split(int dtype, int n, int h, int d, int nb) {
     return s > 4 ? 4 : (s < 2 ? 1 : s);
 }
 
-size_t bwd_ws(int n, int h, int d, int nsplit, void* base, size_t cap, BwdWs* out) {
+// Query-range split of the last, partial wave of the tensor-core dk/dv groups
+// (1 = none); its sums share `acc` with the small-graph split.
+int bwd_tail(int dtype, int n, int h, int d, int nb) {
+    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb) || bwd_split(dtype, n, h, d, nb) > 1) return 1;
+    return bwd_dkdv_tail_split(n);
+}
+
+size_t bwd_ws(int n, int h, int d, bool with_acc, void* base, size_t cap, BwdWs* out) {
     Carve c(base, cap);
     BwdWs w;
-    w.acc = nsplit > 1 ? c.take<float>((size_t)3 * n * h * d) : nullptr;
+    w.acc = with_acc ? c.take<float>((size_t)3 * n * h * d) : nullptr;
     w.Dv = c.take<float>((size_t)h * n);
     w.dT64 = c.take<double>((size_t)h * 128);
     // per-node lse log2 e (rows 0..7) and D (rows 8..15) of the 8 heads, [16][ld_ld]
@@ -141,7 +149,7 @@ size_t bwd_ws(int n, int h, int d, int nsplit, void* base, size_t cap, BwdWs* ou
 }  // namespace
 
 // Workspace of the backward run unsplit: the least a backward call accepts.
-size_t bwd_ws_unsplit(int n, int h, int d) { return bwd_ws(n, h, d, 1, nullptr, 0, nullptr); }
+size_t bwd_ws_unsplit(int n, int h, int d) { return bwd_ws(n, h, d, false, nullptr, 0, nullptr); }
 
 }  // namespace gt
 
@@ -192,7 +200,8 @@ size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t 
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
     size_t a = gt::fwd_ws(n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
-    size_t b = gt::bwd_ws(n, h, d, gt::bwd_split(dtype, n, h, d, 128), nullptr, 0, nullptr);
+    const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1;
+    size_t b = gt::bwd_ws(n, h, d, acc, nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
 }
 
@@ -268,15 +277,20 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     // the split needs its accumulators; a workspace sized for the unsplit pass
     // (a caller's fixed scratch) runs unsplit
     int nsplit = gt::bwd_split(dtype, n, h, d, nb);
-    if (nsplit > 1 && ws_bytes < gt::bwd_ws(n, h, d, nsplit, nullptr, 0, nullptr)) nsplit = 1;
-    const size_t need = gt::bwd_ws(n, h, d, nsplit, nullptr, 0, nullptr);
+    int tail = gt::bwd_tail(dtype, n, h, d, nb);
+    bool with_acc = nsplit > 1 || tail > 1;
+    if (with_acc && ws_bytes < gt::bwd_ws(n, h, d, true, nullptr, 0, nullptr)) {
+        with_acc = false;
+        nsplit = tail = 1;
+    }
+    const size_t need = gt::bwd_ws(n, h, d, with_acc, nullptr, 0, nullptr);
     if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
     gt::BwdWs w;
-    gt::bwd_ws(n, h, d, nsplit, workspace, ws_bytes, &w);
+    gt::bwd_ws(n, h, d, with_acc, workspace, ws_bytes, &w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, w.acc, s);
+                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, tail, w.acc, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

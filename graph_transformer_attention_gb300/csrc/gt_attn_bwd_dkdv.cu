@@ -5,8 +5,8 @@
 // bias slice of each block comes from the int8 bucket matrix),
 //   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
 //
-// One CTA per SM = one tile of 128 KV rows and one half of the heads (4 of 8:
-// grid.y), streaming every Q tile.  The CTA owns all 512 TMEM columns, so K and
+// One CTA per SM = one group: a tile of 128 KV rows and one half of the heads
+// (4 of 8), streaming every Q tile (or, for split groups, a range of them).  The CTA owns all 512 TMEM columns, so K and
 // V sit in TMEM as the A operands of S^T = K Q^T and dP^T = V dO^T: every
 // product reads only its small B operand from shared memory (an MMA with A in
 // shared memory reads 4 KB of it, which both costs ~4x the tensor time and
@@ -110,32 +110,12 @@ struct Bars {
     int abort;
 };
 
-// A-operand row r of head h (this CTA's local head index) of the per-head
-// products with K = 16: the head's channels as bf16 pairs; head dim 8 sits in
-// the half of the 16-column slot it shares with its neighbour head (the other
-// half zero, so the neighbour's channels of the B operand drop out of the sum).
-template <int HD>
-__device__ __forceinline__ void head_a_row(const __nv_bfloat16* src, int hg, bool live, uint32_t (&a)[8]) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    if (HD == 16) {
-        const uint4 lo = live ? s4[2 * hg] : make_uint4(0, 0, 0, 0);
-        const uint4 hi = live ? s4[2 * hg + 1] : make_uint4(0, 0, 0, 0);
-        a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
-        a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
-    } else {
-        const uint4 v = live ? s4[hg] : make_uint4(0, 0, 0, 0);
-        const bool odd = hg & 1;
-        a[0] = odd ? 0u : v.x; a[1] = odd ? 0u : v.y; a[2] = odd ? 0u : v.z; a[3] = odd ? 0u : v.w;
-        a[4] = odd ? v.x : 0u; a[5] = odd ? v.y : 0u; a[6] = odd ? v.z : 0u; a[7] = odd ? v.w : 0u;
-    }
-}
-
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
                 const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapB,
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                const float* __restrict__ T, int nb, int n, float scale, float scale_log2, int split_tiles,
+                const float* __restrict__ T, int nb, int n, float scale, float scale_log2, int g0, int split_tiles,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dk_acc,
                 float* __restrict__ dv_acc, int* status) {
     using C = KvCfg<HD>;
@@ -146,8 +126,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j0 = blockIdx.x * kBKV;
-    const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
+    const int g = g0 + (int)blockIdx.x;        // group: KV tile g / 2, head half g % 2
+    const int j0 = (g >> 1) * kBKV;
+    const int hb = g & 1;                      // heads 4 hb .. 4 hb + 3
     // Q tiles qt0 .. qt0 + ntiles - 1 (all of them unless the rows are split over
     // grid.z, in which case dk and dv are summed into dk_acc / dv_acc in fp32)
     const int total_tiles = (n + C::BQ - 1) / C::BQ;
@@ -517,10 +498,43 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     }
 }
 
+// the tail groups' fp32 sums to bf16: one thread per (row, head) of rows row0 ..
+// n - 1, converting the head's HD values when its group (KV tile row / 128, head
+// half) is one of the split groups >= g1
+template <int HD>
+__global__ void dkdv_tail_to_bf16(int n, int row0, int g1, const float* __restrict__ dk_acc,
+                                  const float* __restrict__ dv_acc, __nv_bfloat16* __restrict__ dk,
+                                  __nv_bfloat16* __restrict__ dv) {
+    const int total = (n - row0) * kH;
+    for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < total; x += gridDim.x * blockDim.x) {
+        const int row = row0 + x / kH, h = x % kH;
+        if ((row / kBKV) * 2 + h / kHC < g1) continue;
+        const int64_t e = ((int64_t)row * kH + h) * HD;
+        const float4* sk = reinterpret_cast<const float4*>(dk_acc + e);
+        const float4* sv = reinterpret_cast<const float4*>(dv_acc + e);
+        uint32_t wk[HD / 2], wv[HD / 2];
+#pragma unroll
+        for (int q = 0; q < HD / 4; ++q) {
+            const float4 a = sk[q], b = sv[q];
+            wk[2 * q] = pack_bf16x2(a.x, a.y);
+            wk[2 * q + 1] = pack_bf16x2(a.z, a.w);
+            wv[2 * q] = pack_bf16x2(b.x, b.y);
+            wv[2 * q + 1] = pack_bf16x2(b.z, b.w);
+        }
+        uint4* dk4 = reinterpret_cast<uint4*>(dk + e);
+        uint4* dv4 = reinterpret_cast<uint4*>(dv + e);
+#pragma unroll
+        for (int q = 0; q < HD / 8; ++q) {
+            dk4[q] = make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+            dv4[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+        }
+    }
+}
+
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
            int64_t ld, const float* T, int nb, float scale, float fold_scale, const uint16_t* LB, int nsplit,
-           void* dk, void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
+           int tail, void* dk, void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
     using C = KvCfg<HD>;
     CUtensorMap mq, mg, ms, ml;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -539,30 +553,73 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int total_tiles = (n + C::BQ - 1) / C::BQ;
-    const int per = nsplit > 1 ? (total_tiles + nsplit - 1) / nsplit : 0;
-    const int nz = per > 0 ? (total_tiles + per - 1) / per : 1;
-    dim3 grid((n + kBKV - 1) / kBKV, kH / kHC, nz);
-    {
+    const int groups = 2 * ((n + kBKV - 1) / kBKV);
+    auto run = [&](int g_first, int g_count, int per, bool sums) -> int {
+        const int nz = per > 0 ? (total_tiles + per - 1) / per : 1;
+        dim3 grid(g_count, 1, nz);
         LaunchScope ls("bwd_dkdv", s);
         bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-            mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-            T, nb, n, scale, fold_scale * kLog2e, per, static_cast<__nv_bfloat16*>(dk),
-            static_cast<__nv_bfloat16*>(dv), per > 0 ? dk_acc : nullptr, per > 0 ? dv_acc : nullptr, status);
+            mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T, nb,
+            n, scale, fold_scale * kLog2e, g_first, per, static_cast<__nv_bfloat16*>(dk),
+            static_cast<__nv_bfloat16*>(dv), sums ? dk_acc : nullptr, sums ? dv_acc : nullptr, status);
+        return check_launch();
+    };
+    if (nsplit > 1 && dk_acc) {
+        // every group split over nsplit CTAs (graphs with fewer groups than SMs)
+        return run(0, groups, (total_tiles + nsplit - 1) / nsplit, true);
     }
-    return check_launch();
+    const int sms = num_sms();
+    if (tail > 1 && dk_acc && groups > sms && groups % sms != 0) {
+        // full waves of whole groups, then the remaining groups split tail ways so
+        // that the last wave fills the SMs; their fp32 sums become bf16 at the end
+        const int g1 = groups / sms * sms;
+        int rc = run(0, g1, 0, false);
+        if (rc != GT_OK) return rc;
+        const int row0 = (g1 >> 1) * kBKV;
+        const size_t bytes = sizeof(float) * (size_t)(n - row0) * kH * HD;
+        if (cudaMemsetAsync(dk_acc + (size_t)row0 * kH * HD, 0, bytes, s) != cudaSuccess ||
+            cudaMemsetAsync(dv_acc + (size_t)row0 * kH * HD, 0, bytes, s) != cudaSuccess)
+            return GT_ERR_CUDA;
+        rc = run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
+        if (rc != GT_OK) return rc;
+        LaunchScope ls("bwd_dkdv_tail_to_bf16", s);
+        dkdv_tail_to_bf16<HD><<<sms, 256, 0, s>>>(n, row0, g1, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
+                                                  static_cast<__nv_bfloat16*>(dv));
+        return check_launch();
+    }
+    return run(0, groups, 0, false);
 }
 
 }  // namespace
 
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const uint16_t* LB, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    const uint16_t* LB, int nsplit, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
                     cudaStream_t s) {
     // LB holds -lse / fold_scale with fold_scale = scale, or a tiny stand-in for a
     // zero scale; dk takes the true scale
     const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, dk, dv, dk_acc, dv_acc, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, dk, dv, dk_acc, dv_acc, s);
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, tail, dk, dv, dk_acc,
+                              dv_acc, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, tail, dk, dv, dk_acc,
+                               dv_acc, s);
+}
+
+// Query-range split of the tail groups (see launch): the k in [2, 8] that makes
+// the last wave of whole-group CTAs plus the split tail the shortest, in units of
+// one group's time, or 1 when the groups fill whole waves (or do not fill one).
+int bwd_dkdv_tail_split(int n) {
+    const int sms = num_sms();
+    const int groups = 2 * ((n + kBKV - 1) / kBKV);
+    if (groups <= sms || groups % sms == 0) return 1;
+    const int rem = groups % sms;
+    int best = 1;
+    double best_t = 1.0;                        // the tail unsplit: one more wave of whole groups
+    for (int k = 2; k <= 8; ++k) {
+        const double t = (double)((rem * k + sms - 1) / sms) / k;
+        if (t < best_t - 1e-9) { best_t = t; best = k; }
+    }
+    return best;
 }
 
 }  // namespace gt

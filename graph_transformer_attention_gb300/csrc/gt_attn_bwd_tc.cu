@@ -32,22 +32,9 @@ namespace {
 
 using tc::kH;
 using tc::kLog2e;
+using tc::split3_bf16;
 
 constexpr int kMaxNb = 128;
-
-// bf16 round-to-nearest-even bits of a float (finite inputs)
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-// Three bf16 parts of v whose fp32 sum is v to about 2^-24 relative: hi = bf16(v),
-// mid = bf16(v - hi), lo = bf16(v - hi - mid) (both differences are exact in fp32).
-__device__ __forceinline__ void split3(float v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-    hi = bf16_bits(v);
-    const float r1 = v - __uint_as_float(hi << 16);
-    mid = bf16_bits(r1);
-    lo = bf16_bits(r1 - __uint_as_float(mid << 16));
-}
 
 // One thread per (node, head), node-major (x = 8 i + h), so a warp reads 32
 // consecutive rows of HD bf16 of o, dO and v with 16-byte loads.
@@ -95,8 +82,8 @@ __global__ void bwd_prep(int n, int ldl, float inv_scale, const __nv_bfloat16* _
             LD[(int64_t)(kH + h) * ldl + i] = acc;
             Dv[(int64_t)h * n + i] = acc;
             uint32_t a0, a1, a2, b0, b1, b2;
-            split3(-l * inv_scale, a0, a1, a2);
-            split3(-acc, b0, b1, b2);
+            split3_bf16(-l * inv_scale, a0, a1, a2);
+            split3_bf16(-acc, b0, b1, b2);
             uint4* dst = reinterpret_cast<uint4*>(LB + x * 16);
             dst[0] = make_uint4(a0 | (a1 << 16), a2 | (b0 << 16), b1 | (b2 << 16), 0u);
             dst[1] = make_uint4(0u, 0u, 0u, 0u);
@@ -129,16 +116,18 @@ int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, con
                   double* dT64, cudaStream_t s);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const uint16_t* LB, int nsplit, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    const uint16_t* LB, int nsplit, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
                     cudaStream_t s);
 
 // Backward on the tensor cores.  Workspace: LD [16][bwd_ld_ld(n)] fp32, LB bf16
 // [n][8][16], Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j|
-// of head h), and with nsplit > 1 the fp32 sums acc [3][n][8][d].
+// of head h), and the fp32 sums acc [3][n][8][d] when either split applies
+// (nsplit > 1: every tile's streamed dimension split; tail > 1: the dk/dv groups
+// of the last, partial wave split), else null.
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, float* acc, cudaStream_t s) {
+                float* Dv, double* dT64, float* aux, int nsplit, int tail, float* acc, cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
     if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;
@@ -163,8 +152,8 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1, dq,
                            split ? acc : nullptr, dT64, s);
     if (rc != GT_OK) return rc;
-    rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, split ? nsplit : 1, dk, dv,
-                         split ? acc + elems : nullptr, split ? acc + 2 * elems : nullptr, s);
+    rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, split ? nsplit : 1, acc ? tail : 1, dk, dv,
+                         acc ? acc + elems : nullptr, acc ? acc + 2 * elems : nullptr, s);
     if (rc != GT_OK) return rc;
     if (split) {
         LaunchScope ls("bwd_acc_to_bf16", s);

@@ -69,6 +69,36 @@ __device__ __forceinline__ void fill_bias_table_heads(float* Ts, const float* T,
     }
 }
 
+// One TMEM row (lane) of the A operand of a per-head product with K = 16, for
+// global head hg of a node's [8][HD] row src: the head's channels as bf16 pairs; head dim 8 sits in
+// the half of the 16-column slot it shares with its neighbour head (the other
+// half zero, so the neighbour's channels of the B operand drop out of the sum).
+template <int HD>
+__device__ __forceinline__ void head_a_row(const __nv_bfloat16* src, int hg, bool live, uint32_t (&a)[8]) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    if (HD == 16) {
+        const uint4 lo = live ? s4[2 * hg] : make_uint4(0, 0, 0, 0);
+        const uint4 hi = live ? s4[2 * hg + 1] : make_uint4(0, 0, 0, 0);
+        a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
+        a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+    } else {
+        const uint4 v = live ? s4[hg] : make_uint4(0, 0, 0, 0);
+        const bool odd = hg & 1;
+        a[0] = odd ? 0u : v.x; a[1] = odd ? 0u : v.y; a[2] = odd ? 0u : v.z; a[3] = odd ? 0u : v.w;
+        a[4] = odd ? v.x : 0u; a[5] = odd ? v.y : 0u; a[6] = odd ? v.z : 0u; a[7] = odd ? v.w : 0u;
+    }
+}
+
+// Three bf16 parts (bits) of v whose fp32 sum is v to about 2^-24 relative:
+// hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid); both differences
+// are exact in fp32.
+__device__ __forceinline__ void split3_bf16(float v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+    hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+    const float r1 = v - __uint_as_float(hi << 16);
+    mid = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(r1));
+    lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(r1 - __uint_as_float(mid << 16)));
+}
+
 __device__ __forceinline__ void red_shared_add_u32(uint32_t addr, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
