@@ -35,11 +35,15 @@ import gt_inputs as gi  # noqa: E402
 
 METRIC = "biased-attention fwd+bwd TFLOP/s and % of roofline on 1 GB300"
 
-# Exp throughput of one GB300 SM: 32 ex2.approx.f32 results per clock, measured
-# with a dependent-chain-free ex2 loop on 152 SMs (packed f16x2/bf16x2 ex2 gives
-# the same 32 results per clock).  152 SMs at the 2070 MHz maximum clock.
+# Exp throughput of one GB300 SM: 32 ex2.approx.f32 results per clock (measured
+# on this GPU with a throughput loop of independent ex2 chains, 16 warps per SM
+# on all 152 SMs: 31.8 per clock per SM; packed f16x2/bf16x2 ex2 give the same 32
+# results per clock).  MEASURED_PEAKS.json has no exp entry, so this figure is
+# the denominator of the exp-unit roofline, at the maximum SM clock.
 EX2_PER_CLK_SM = 32.0
 SMS = 152
+EXP_PEAK_SOURCE = ("152 SMs x 32 ex2.approx.f32 results/clk/SM (this library's throughput probe on a GB300: "
+                   "31.8/clk/SM) x max SM clock from MEASURED_PEAKS.json")
 
 
 def attn_flops(w: gi.Workload) -> float:
@@ -149,22 +153,29 @@ EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd
 
 # DRAM bytes (read + write) per launch of a kernel at a workload, from one ncu
 # capture of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
-# the capture summaries live under profiles/.
-DRAM_BYTES = {("fwd_tc", "ba64x256"): 284.806e6, ("bwd_dq", "ba64x256"): 290.329e6,
-              ("bwd_dkdv", "ba64x256"): 289.543e6, ("spd_bfs", "ba64x256"): 215.059e6}
+# the capture summaries live under profiles/.  A kernel changed since its capture
+# has no entry (its traffic is reported as null).
+DRAM_BYTES = {("fwd_tc", "ba64x256"): 284.962e6, ("bwd_dq", "ba64x256"): 307.238e6,
+              ("spd_bfs", "ba64x256"): 215.059e6}
 
 
-def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float) -> dict:
-    """Roofline of one kernel: algorithmic work per launch / measured launch time."""
+def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float,
+                    launches_per_layer: float = 1.0) -> dict:
+    """Roofline of one kernel: algorithmic work per launch / measured launch time.
+
+    An exp-bound kernel evaluates one exp per (query, key, head) of a layer; when
+    it takes several launches per layer (the dk/dv kernel's full waves and split
+    tail) the work per launch is the layer's N^2 H over its launches, and `ms` the
+    mean launch time, so work / time is the layer's exps over the kernel's time."""
     t = ms * 1e-3
-    traffic = DRAM_BYTES.get((name, w.name))
+    traffic = DRAM_BYTES.get((name, w.name)) if launches_per_layer == 1.0 else None
     if name in EXP_KERNELS:
-        work = float(w.n) * w.n * w.heads            # exps per launch
-        return {"kernel": name, "bound": "alu", "achieved": round(work / t / 1e12, 4),
+        work = float(w.n) * w.n * w.heads / launches_per_layer     # exps per launch
+        return {"kernel": name, "bound": "exp", "achieved": round(work / t / 1e12, 4),
                 "peak": round(exp_peak / 1e12, 3), "unit": "Texp/s",
                 "frac": round(work / t / exp_peak, 4), "traffic": traffic,
                 "work_per_launch": work, "ms_per_launch": round(ms, 4),
-                "peak_source": f"{SMS} SMs x {EX2_PER_CLK_SM:g} ex2/clk/SM (measured) x max SM clock"}
+                "launches_per_layer": launches_per_layer, "peak_source": EXP_PEAK_SOURCE}
     # anything else is taken as bound by HBM on its output (the N^2 bucket bytes)
     work = float(w.n) * w.n
     return {"kernel": name, "bound": "hbm", "achieved": round(work / t / 1e9, 2),
@@ -343,6 +354,25 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     barrier()
     e2e_ms = (time.perf_counter() - e0) * 1e3
 
+    # the same, one step at a time with nothing overlapped: inputs in, the step,
+    # results out, synchronised (the latency of one step through the API)
+    lat = []
+    S0 = sets[0]
+    for _ in range(args.steps):
+        barrier()
+        l0 = time.perf_counter()
+        S0["ip"].copy_(h_ip, non_blocking=True)
+        S0["ix"].copy_(h_ix, non_blocking=True)
+        for li in range(w.layers):
+            for k in S0["layers"][li]:
+                S0["layers"][li][k].copy_(h_layers[li][k], non_blocking=True)
+        step(S=S0)
+        for li in range(w.layers):
+            for k, t in h_outs[li].items():
+                t.copy_(S0["outs"][li][k], non_blocking=True)
+        torch.cuda.synchronize()
+        lat.append((time.perf_counter() - l0) * 1e3)
+
     h2d = h_ip.numel() * 8 + h_ix.numel() * 4 + sum(t.numel() * t.element_size()
                                                     for hl in h_layers for t in hl.values())
     d2h = sum(t.numel() * t.element_size() for ho in h_outs for t in ho.values())
@@ -362,7 +392,8 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0)) * 1e9
     # dominant kernel: largest device time per step
     dom = max(kernels, key=lambda k: kernels[k]["launches_per_step"] * kernels[k]["ms_per_launch"])
-    roof = kernel_roofline(dom, w, kernels[dom]["ms_per_launch"], exp_peak, hbm_peak)
+    roof = kernel_roofline(dom, w, kernels[dom]["ms_per_launch"], exp_peak, hbm_peak,
+                           launches_per_layer=kernels[dom]["launches_per_step"] / w.layers)
     # whole-path roofline: the slowest of tensor pipe, HBM and exp unit
     t_attn = (part_ms["fwd"] + part_ms["bwd"]) * w.layers * 1e-3
     t_roof = max(flops / tensor_peak, algo_bytes(w) / hbm_peak, exps(w) / exp_peak)
@@ -382,12 +413,99 @@ def run_gpu(args, w: gi.Workload, rank: int, world: int) -> dict | None:
                           "frac": round(t_roof / t_attn, 4) if t_attn > 0 else None,
                           "bound": "exp unit (MUFU)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "pipelined": "step k's copies overlap steps k - 1 and k + 1 (two buffer sets)",
+                "latency_ms_per_step": round(float(np.median(lat)), 4),
+                "latency_note": "one step alone: copies in, SPD build, fwd, bwd, copies out, synchronised "
+                                "(median of the timed steps, host clock)"},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "memory": memory_line(w, dev),
         "cpu_baseline": None,
+        "configs": extra_configs(args, w, dev, world, exp_peak, tensor_peak, hbm_peak),
     }
+
+
+def extra_configs(args, w: gi.Workload, dev, world: int, exp_peak: float, tensor_peak: float,
+                  hbm_peak: float) -> dict | None:
+    """Every other workload timed the same way after the headline (one GPU only;
+    --no-extra-configs skips them)."""
+    if world > 1 or args.no_extra_configs:
+        return None
+    out = {}
+    for ci, wc in sorted(gi.CONFIGS.items()):
+        if wc.name == w.name:
+            continue
+        steps = 3 if wc.layers > 1 or wc.n >= 32768 else 10
+        out[wc.name] = measure_config(wc, dev, steps, 2, exp_peak, tensor_peak, hbm_peak)
+    return out
+
+
+def measure_config(w: gi.Workload, dev, steps: int, warmup: int, exp_peak: float, tensor_peak: float,
+                   hbm_peak: float) -> dict:
+    """Device time of one step (SPD build + fwd + bwd of every layer, inputs
+    resident) of another workload, with per-part CUDA events on the stream."""
+    import torch
+    import graph_transformer_attention_gb300 as gt
+    stream = torch.cuda.current_stream()
+    g = gi.config_graph(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ip, ix = torch.from_numpy(g.indptr).to(dev), torch.from_numpy(g.indices).to(dev)
+    layers = []
+    for li in range(w.layers):
+        x = gi.config_layer_tensors(w, li)
+        layers.append({k: torch.from_numpy(x[k]).to(dev).to(tdt if k != "T" else torch.float32)
+                       for k in ("q", "k", "v", "dO", "T")})
+    n, H, d = w.n, w.heads, w.head_dim
+    code = gt.GT_BF16 if w.dtype == "bf16" else gt.GT_F32
+    spd = torch.empty((n, gt.spd_ld(n)), dtype=torch.int8, device=dev)
+    ws_spd = torch.empty(gt.gt_spd_workspace_size(n, g.nnz, w.D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(256, gt.gt_bias_attn_workspace_size(code, n, H, d, w.kv_block)), dtype=torch.uint8,
+                     device=dev)
+    outs = [dict(o=torch.empty((n, H, d), dtype=tdt, device=dev), lse=torch.empty((H, n), device=dev),
+                 dq=torch.empty((n, H, d), dtype=tdt, device=dev), dk=torch.empty((n, H, d), dtype=tdt, device=dev),
+                 dv=torch.empty((n, H, d), dtype=tdt, device=dev), dT=torch.empty((H, w.nb), device=dev))
+            for _ in range(w.layers)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+
+    def step(e=None):
+        if e:
+            e[0].record(stream)
+        gt.gt_spd_build(ip, ix, n, w.D, out=spd, workspace=ws_spd)
+        if e:
+            e[1].record(stream)
+        for li, x in enumerate(layers):
+            oo = outs[li]
+            gt.gt_bias_attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], kv_block=w.kv_block, out=oo["o"],
+                                lse=oo["lse"], workspace=ws)
+            if e and li == 0:
+                e[2].record(stream)
+            gt.gt_bias_attn_bwd(x["q"], x["k"], x["v"], oo["o"], x["dO"], oo["lse"], spd, x["T"], dq=oo["dq"],
+                                dk=oo["dk"], dv=oo["dv"], dT=oo["dT"], workspace=ws)
+        if e:
+            e[3].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for sidx in range(steps):
+        step(ev[sidx])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    gt.gt_check_device_status()
+    ms_step = t0.elapsed_time(t1) / steps
+    spd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    attn_ms = float(np.mean([e[1].elapsed_time(e[3]) for e in ev]))
+    flops = attn_flops(w)
+    t_roof = max(flops / tensor_peak, algo_bytes(w) / hbm_peak, exps(w) / exp_peak)
+    return {"workload": workload_config(w)["workload"], "ms_per_step": round(ms_step, 4),
+            "tflops": round(flops / (ms_step * 1e-3) / 1e12, 3), "spd_ms": round(spd_ms, 4),
+            "attn_fwd_bwd_ms": round(attn_ms, 4),
+            "path_frac": round(t_roof / (attn_ms * 1e-3), 4) if attn_ms > 0 else None,
+            "path_bound": "exp unit" if w.dtype == "bf16" else "exp unit (fp32 CUDA-core path: not its bound)",
+            "steps": steps, "warmup": warmup}
 
 
 def memory_line(w: gi.Workload, dev) -> dict:
@@ -555,6 +673,8 @@ def main(argv=None) -> int:
                     help="rows (and columns) the CPU oracle processes per sample "
                          "(default: N/2 for the baseline line, N/8 per reference step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only the chosen workload (by default the others follow it, in 'configs')")
     ap.add_argument("--model", choices=["attention", "gt-layer"], default="attention",
                     help="attention: the biased-attention path (default); gt-layer: the whole encoder "
                          "layer around it (default workload then ba6800x16)")

@@ -26,16 +26,20 @@ def test_credited_work_per_step():
 def test_exp_kernel_roofline_is_work_over_time_over_peak():
     w = gi.CONFIGS[4]
     peak = 152 * 32.0 * 2.07e9              # ex2 results per second
-    r = bench.kernel_roofline("bwd_dkdv", w, 1.25, peak, 6693.5e9)
+    r = bench.kernel_roofline("fwd_tc", w, 1.25, peak, 6693.5e9)
     work = 16384.0 ** 2 * 8                 # one exp per (query, key, head) per launch
-    assert r["bound"] == "alu" and r["unit"] == "Texp/s"
+    assert r["bound"] == "exp" and r["unit"] == "Texp/s"
     assert r["work_per_launch"] == work
     assert r["achieved"] == pytest.approx(work / 1.25e-3 / 1e12, abs=1e-4)
     assert r["peak"] == pytest.approx(peak / 1e12, abs=1e-3)
     assert r["frac"] == pytest.approx(work / 1.25e-3 / peak, abs=1e-4)
-    assert r["traffic"] == bench.DRAM_BYTES[("bwd_dkdv", "ba64x256")]
+    assert r["traffic"] == bench.DRAM_BYTES[("fwd_tc", "ba64x256")]
     # a workload without a capture reports no traffic rather than another's
-    assert bench.kernel_roofline("bwd_dkdv", gi.CONFIGS[2], 1.0, peak, 6693.5e9)["traffic"] is None
+    assert bench.kernel_roofline("fwd_tc", gi.CONFIGS[2], 1.0, peak, 6693.5e9)["traffic"] is None
+    # a kernel with several launches per layer: the layer's exps over its launches
+    r2 = bench.kernel_roofline("bwd_dkdv", w, 0.5, peak, 6693.5e9, launches_per_layer=2.0)
+    assert r2["work_per_launch"] == work / 2 and r2["traffic"] is None
+    assert r2["frac"] == pytest.approx(work / 2 / 0.5e-3 / peak, abs=1e-4)
 
 
 def test_hbm_kernel_roofline_counts_the_bucket_bytes():
