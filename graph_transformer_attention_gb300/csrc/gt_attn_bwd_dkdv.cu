@@ -58,10 +58,10 @@ constexpr int kBKV = 128;
 constexpr int kCH = 32;                    // query rows per step
 constexpr int kQST = 2;
 constexpr int kHC = 4;                     // heads per CTA
-constexpr int kSoft = 256;                 // softmax threads: 128 KV rows x 2 heads of a pair
+constexpr int kSoft = 512;                 // softmax threads: 128 KV rows x (2 heads x 2 row halves)
 constexpr int kThreads = kSoft + 64;
-constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
+constexpr int kMmaWarp = 16;
+constexpr int kTmaWarp = 17;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDk = 0;
 constexpr uint32_t kColDv = 64;
@@ -350,10 +350,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------- softmax
-        // Warps w and w + 4 own the same 32 KV rows (TMEM lanes): thread (r, half)
-        // takes query rows 16 half .. 16 half + 15 of every step, both heads.
+        // Warps w, w + 4, w + 8, w + 12 own the same 32 KV rows (TMEM lanes):
+        // thread (r, e, half) takes head e of the pair and query rows 16 half ..
+        // 16 half + 15 of every step.
         const int r = tid & (kBKV - 1);
-        const int half = tid >> 7;
+        const int e = (tid >> 7) & 1;
+        const int half = tid >> 8;
         const int row = j0 + r;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t tbl = smem_u32(Ts) + 16u * hb;
@@ -384,60 +386,50 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int p = 0; p < 2; ++p) {
                     if (!mbar_wait(&bars->sd_full[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t x = lrow + pair_buf(p) + 16 * half;
-                    uint32_t rs[2][16], rd[2][16];
-                    tmem_ld_x16(x, rs[0]);
-                    tmem_ld_x16(x + 32, rs[1]);
-                    tmem_ld_x16(x + 64, rd[0]);
-                    tmem_ld_x16(x + 96, rd[1]);
+                    const uint32_t x = lrow + pair_buf(p) + 32 * e + 16 * half;
+                    uint32_t rs[16], rd[16];
+                    tmem_ld_x16(x, rs);
+                    tmem_ld_x16(x + 64, rd);
                     tmem_wait_ld();
                     // x = s' scale log2e + b(code); P = 2^x
-                    float pf[2][16];
+                    float pf[16];
                     if (ucode >= 0) {
-                        const float b0 = p ? bu.z : bu.x, b1 = p ? bu.w : bu.y;
+                        const float bh = p ? (e ? bu.w : bu.z) : (e ? bu.y : bu.x);
                         const float2 cc = make_float2(scale_log2, scale_log2);
 #pragma unroll
                         for (int kk = 0; kk < 16; kk += 2) {
                             const float2 xa = __ffma2_rn(
-                                make_float2(__uint_as_float(rs[0][kk]), __uint_as_float(rs[0][kk + 1])), cc,
-                                make_float2(b0, b0));
-                            const float2 xb = __ffma2_rn(
-                                make_float2(__uint_as_float(rs[1][kk]), __uint_as_float(rs[1][kk + 1])), cc,
-                                make_float2(b1, b1));
-                            pf[0][kk] = xa.x;
-                            pf[0][kk + 1] = xa.y;
-                            pf[1][kk] = xb.x;
-                            pf[1][kk + 1] = xb.y;
+                                make_float2(__uint_as_float(rs[kk]), __uint_as_float(rs[kk + 1])), cc,
+                                make_float2(bh, bh));
+                            pf[kk] = xa.x;
+                            pf[kk + 1] = xa.y;
                         }
                     } else {
+                        const uint32_t hofs = 4u * (uint32_t)(2 * p + e);
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk) {
-                            const float2 bv = lds_f2(tbl + code[kk] * 32u + 8u * p);
-                            pf[0][kk] = fmaf(__uint_as_float(rs[0][kk]), scale_log2, bv.x);
-                            pf[1][kk] = fmaf(__uint_as_float(rs[1][kk]), scale_log2, bv.y);
+                            const float bv = __uint_as_float(lds_u32(tbl + code[kk] * 32u + hofs));
+                            pf[kk] = fmaf(__uint_as_float(rs[kk]), scale_log2, bv);
                         }
                     }
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
+                    for (int kk = 0; kk < 16; ++kk) pf[kk] = ex2(pf[kk]);
+                    if (tail_tile) {
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) pf[e][kk] = ex2(pf[e][kk]);
-                        if (tail_tile) {
-#pragma unroll
-                            for (int kk = 0; kk < 16; ++kk)
-                                if (i0 + ir + kk >= n) pf[e][kk] = 0.f;
-                        }
-                        uint32_t pp[8], pd[8];
-#pragma unroll
-                        for (int k2 = 0; k2 < 8; ++k2) {
-                            pp[k2] = pack_bf16x2(pf[e][2 * k2], pf[e][2 * k2 + 1]);
-                            const float2 ds = __fmul2_rn(
-                                make_float2(pf[e][2 * k2], pf[e][2 * k2 + 1]),
-                                make_float2(__uint_as_float(rd[e][2 * k2]), __uint_as_float(rd[e][2 * k2 + 1])));
-                            pd[k2] = pack_bf16x2(ds.x, ds.y);
-                        }
-                        tmem_st_x8(x + 32 * e, pp);
-                        tmem_st_x8(x + 32 * e + 8, pd);
+                        for (int kk = 0; kk < 16; ++kk)
+                            if (i0 + ir + kk >= n) pf[kk] = 0.f;
                     }
+                    uint32_t pp[8], pd[8];
+#pragma unroll
+                    for (int k2 = 0; k2 < 8; ++k2) {
+                        pp[k2] = pack_bf16x2(pf[2 * k2], pf[2 * k2 + 1]);
+                        const float2 ds = __fmul2_rn(
+                            make_float2(pf[2 * k2], pf[2 * k2 + 1]),
+                            make_float2(__uint_as_float(rd[2 * k2]), __uint_as_float(rd[2 * k2 + 1])));
+                        pd[k2] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    tmem_st_x8(x, pp);
+                    tmem_st_x8(x + 8, pd);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(&bars->ds_ready[p]);
@@ -453,15 +445,23 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         } else {
             tc_fence_after();
             const bool live = row < n;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int hh = 2 * half + h2;
+            {
+                const int hh = 2 * half + e;
                 const int h = kHC * hb + hh;
                 uint32_t ok16[16], ov16[16];
                 tmem_ld_x16(lrow + kColDk + 16 * hh, ok16);
                 tmem_ld_x16(lrow + kColDv + 16 * hh, ov16);
                 tmem_wait_ld();
-                const int c0h = (HD == 8) ? (h & 1) * 8 : 0;
+                // head dim 8: the head's channels are columns 8 (h & 1) .. of the 16;
+                // shift them down with constant register indices
+                if (HD == 8 && (h & 1)) {
+#pragma unroll
+                    for (int q2 = 0; q2 < 8; ++q2) {
+                        ok16[q2] = ok16[q2 + 8];
+                        ov16[q2] = ov16[q2 + 8];
+                    }
+                }
+                constexpr int c0h = 0;
                 if (live && dk_acc) {
                     float* gk = dk_acc + ((int64_t)row * kH + h) * HD;
                     float* gv = dv_acc + ((int64_t)row * kH + h) * HD;

@@ -136,6 +136,13 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
     return v;
 }
 
+// 4-byte load of a table that does not change while the kernel runs (scheduled freely)
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
