@@ -62,10 +62,11 @@ constexpr int kCH = 32;                 // KV columns per MMA chunk
 constexpr int kNCH = kBKV / kCH;
 constexpr int kKVST = 2;
 constexpr uint32_t kTmemCols = 64 * kHC;
-constexpr int kSoftThreads = 128;
+constexpr int kNH = 2;                  // heads per softmax thread
+constexpr int kSoftThreads = 128 * kHC / kNH;
 constexpr int kThreads = kSoftThreads + 64;
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
+constexpr int kMmaWarp = kSoftThreads / 32;
+constexpr int kTmaWarp = kMmaWarp + 1;
 constexpr float kRedoSum = 256.f;       // 2^8: redo a half chunk whose row sum exceeds this
 constexpr uint32_t kColO = 0;                       // O: 16 columns per head
 constexpr uint32_t kColS = 16 * kHC;                // S: 32 columns per head
@@ -166,12 +167,12 @@ __device__ __forceinline__ float exp_pack16(const uint32_t (&x)[16], float m, ui
 // Rows whose 16 codes of a half chunk are all equal (in every row of the warp):
 // x - m = s * scale * log2(e) + (b - m) in one packed fused multiply-add per two
 // columns, the head's bias minus its running maximum taken once.
-__device__ __forceinline__ void score16_shifted(uint32_t (&sx)[kHC][16], const float4 b4, const float (&m)[kHC],
+template <int NH>
+__device__ __forceinline__ void score16_shifted(uint32_t (&sx)[NH][16], const float (&bb)[NH], const float (&m)[NH],
                                                 float scale_log2) {
-    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
     const float2 cc = f2(scale_log2, scale_log2);
 #pragma unroll
-    for (int hh = 0; hh < kHC; ++hh) {
+    for (int hh = 0; hh < NH; ++hh) {
         const float bm = bb[hh] - m[hh];
         const float2 bm2 = f2(bm, bm);
 #pragma unroll
@@ -357,12 +358,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------- softmax
+        // warps w and w + 4 own the same 32 query rows (TMEM lanes) and split the
+        // CTA's heads: thread (r, half) takes heads 2 half, 2 half + 1
         const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
+        const int hl0 = kNH * (tid >> 7);        // this thread's first head among the CTA's
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 4u * kHC * hb;   // 32-byte rows of 8 head biases
-        float m[kHC], l[kHC];
+        const uint32_t tbl = smem_u32(Ts) + 4u * (kHC * hb + hl0);   // 32-byte rows of 8 head biases
+        float m[kNH], l[kNH];
 #pragma unroll
-        for (int h = 0; h < kHC; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+        for (int h = 0; h < kNH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
         int t = 0;
         bool ok = true;
         int uni_skip = 0;   // half chunks left before the next uniformity vote (warp-uniform)
@@ -384,15 +388,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     // the first chunk sets the running maximum exactly (both halves)
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
-                        uint32_t sx[kHC][16];
+                        uint32_t sx[kNH][16];
 #pragma unroll
-                        for (int hh = 0; hh < kHC; ++hh)
-                            tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
+                        for (int hh = 0; hh < kNH; ++hh)
+                            tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
                         tmem_wait_ld();
-                        score16(sx, g ? c1 : c0, tbl, scale_log2);
-                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
+                        score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
+                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
 #pragma unroll
-                        for (int hh = 0; hh < kHC; ++hh)
+                        for (int hh = 0; hh < kNH; ++hh)
 #pragma unroll
                             for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
                     }
@@ -409,10 +413,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 };
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
-                    uint32_t sx[kHC][16];
+                    uint32_t sx[kNH][16];
 #pragma unroll
-                    for (int hh = 0; hh < kHC; ++hh)
-                        tmem_ld_x16(lrow + kColS + kCH * hh + 16 * g, sx[hh]);
+                    for (int hh = 0; hh < kNH; ++hh)
+                        tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
                     tmem_wait_ld();
                     if (g == 1) {
                         tc_fence_before();
@@ -420,8 +424,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     }
                     // exponentials of all heads first (independent chains), one vote on
                     // whether any head of any row needs a redo against a new maximum
-                    uint32_t pk[kHC][8];
-                    float ls[kHC];
+                    uint32_t pk[kNH][8];
+                    float ls[kNH];
                     bool need = false;
                     const uint4 cw = g ? c1 : c0;
                     const uint32_t code0 = cw.x & 0xffu;
@@ -437,18 +441,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         if (!wuni) uni_skip = 16;
                     }
                     if (wuni) {
-                        score16_shifted(sx, lds_f4(tbl + code0 * 32u), m, scale_log2);
-                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
+                        float bb[kNH];
+                        load_bias<kNH>(tbl + code0 * 32u, bb);
+                        score16_shifted<kNH>(sx, bb, m, scale_log2);
+                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
 #pragma unroll
-                        for (int hh = 0; hh < kHC; ++hh) {
+                        for (int hh = 0; hh < kNH; ++hh) {
                             ls[hh] = exp_pack16_shifted(sx[hh], pk[hh]);
                             need |= !(ls[hh] <= kRedoSum);
                         }
                     } else {
-                        score16(sx, g ? c1 : c0, tbl, scale_log2);
-                        if (tail_block) mask16(sx, jc + 16 * g, j_end);
+                        score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
+                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
 #pragma unroll
-                        for (int hh = 0; hh < kHC; ++hh) {
+                        for (int hh = 0; hh < kNH; ++hh) {
                             ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
                             need |= !(ls[hh] <= kRedoSum);
                         }
@@ -456,7 +462,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (__any_sync(0xffffffffu, need)) {
                         wait_pv();
 #pragma unroll
-                        for (int hh = 0; hh < kHC; ++hh) {
+                        for (int hh = 0; hh < kNH; ++hh) {
                             if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
                             // a new maximum for this head: redo, and rescale l, the P already
                             // written for this chunk, and O (TMEM columns hold this CTA's heads)
@@ -472,29 +478,29 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             if (g == 1) {
                                 uint32_t pw[8];
                                 tmem_wait_st();   // the first half's P of this head is written
-                                tmem_ld_x8(lrow + kColP + 16 * hh, pw);
+                                tmem_ld_x8(lrow + kColP + 16 * (hl0 + hh), pw);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int k = 0; k < 8; ++k)
                                     pw[k] = pack_bf16x2(__uint_as_float(pw[k] << 16) * alpha,
                                                         __uint_as_float(pw[k] & 0xffff0000u) * alpha);
-                                tmem_st_x8(lrow + kColP + 16 * hh, pw);
+                                tmem_st_x8(lrow + kColP + 16 * (hl0 + hh), pw);
                             }
                             if (t > 0) {
                                 uint32_t ov[16];
-                                tmem_ld_x16(lrow + kColO + 16 * hh, ov);
+                                tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                                tmem_st_x16(lrow + kColO + 16 * hh, ov);
+                                tmem_st_x16(lrow + kColO + 16 * (hl0 + hh), ov);
                             }
                         }
                     }
                     wait_pv();
 #pragma unroll
-                    for (int hh = 0; hh < kHC; ++hh) {
+                    for (int hh = 0; hh < kNH; ++hh) {
                         l[hh] += ls[hh];
-                        tmem_st_x8(lrow + kColP + 16 * hh + 8 * g, pk[hh]);
+                        tmem_st_x8(lrow + kColP + 16 * (hl0 + hh) + 8 * g, pk[hh]);
                     }
                 }
                 tmem_wait_st();
@@ -516,10 +522,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                 const int row = i0 + r;
                 const bool live = row < n;
 #pragma unroll
-                for (int hh = 0; hh < kHC; ++hh) {
-                    const int h = kHC * hb + hh;
+                for (int hh = 0; hh < kNH; ++hh) {
+                    const int h = kHC * hb + hl0 + hh;
                     uint32_t ov[16];
-                    tmem_ld_x16(lrow + kColO + 16 * hh, ov);
+                    tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
                     tmem_wait_ld();
                     const float inv = 1.f / l[hh];
                     const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
