@@ -51,7 +51,7 @@ using namespace sm100;
 constexpr int kC = 64;          // width (8 heads x 8 channels)
 constexpr int kF = 64;          // FFN width
 constexpr int kTile = 128;      // node rows of a CTA
-constexpr int kThreads = kTile; // one thread per node row
+constexpr int kThreads = 2 * kTile;   // two threads per node row
 constexpr float kLnEps = 1e-5f;
 
 // GELU(a) = a Phi(a) and its derivative Phi(a) + a phi(a)
@@ -87,45 +87,12 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-// Weights go to shared memory with cp.async: every copy of a thread in flight at
-// once (one memory latency, not one per element), overlapped with the row loads.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// B operand (n, k) = W[n][k] of a row-major [N][K] fp32 matrix (v W^T): 16-byte copies.
-template <int N, int K>
-__device__ __forceinline__ void load_b_rows(uint8_t* dst, const float* __restrict__ W) {
-    const uint32_t d = smem_u32(dst);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < N * K / 4; i += kThreads) {
-        const int n = i / (K / 4), k = 4 * (i % (K / 4));
-        cp_async16(d + sw32(N, n, 4 * k), W + 4 * i);
-    }
-}
-
-// B operand (n, k) = W[k][n] of a row-major [K][N] fp32 matrix (v W): 4-byte
-// copies.  A warp takes a block of 4 n x 8 k: lane (n & 3, k & 7) writes word
-// (k & 7) of row n, so the 32 lanes hit 32 different banks (the 32-byte rows of
-// 4 consecutive n start 8 banks apart), and reads 8 runs of 16 bytes.
-template <int K, int N>
-__device__ __forceinline__ void load_b_cols(uint8_t* dst, const float* __restrict__ W) {
-    static_assert(N % 4 == 0 && K % 8 == 0, "4 x 8 blocks");
-    const uint32_t d = smem_u32(dst);
-    const int lane = threadIdx.x & 31;
-#pragma unroll 4
-    for (int b = threadIdx.x >> 5; b < (N / 4) * (K / 8); b += kThreads / 32) {
-        const int n = 4 * (b % (N / 4)) + (lane & 3), k = 8 * (b / (N / 4)) + (lane >> 2);
-        cp_async4(d + sw32(N, n, 4 * k), W + (size_t)k * N + n);
-    }
-}
-
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Column k = r (this thread's node row) of rows rho .. rho + NV - 1 of a bf16
@@ -153,43 +120,15 @@ __device__ __forceinline__ void put_ones_block(uint8_t* base, int rho) {
 
 // ------------------------------------------------------------ rows and TMEM
 //
-// A thread's node row is loaded into registers with all its global loads in
-// flight at once, and the rows a kernel needs are all requested before the first
-// of them is used.  Rows that must outlive a product wait in TMEM (the thread's
-// lane).  TMEM reads take 32 or 64 columns per wait; only the GELU loops, whose
-// per-element code is long, run in rolled 8-column chunks (the next chunk's read
-// in flight while the current one is computed): a tile kernel runs its code once
-// per CTA, so long unrolled loops spend their time fetching instructions.
+// Two threads share a node row: warps w and w + 4 reach the same 32 TMEM lanes,
+// so thread (row r, half h) takes features 32 h .. 32 h + 31 of row r, and the
+// row sums of the LayerNorms pass between the two through shared memory.  Rows
+// that must outlive a product wait in TMEM.  Only the GELU loops,
+// whose per-element code is long, run in rolled 8-column chunks (the next chunk's
+// read in flight while the current one is computed): a tile kernel runs its code
+// once per CTA, so long unrolled loops spend their time fetching instructions.
 
-__device__ __forceinline__ void ldg_row_f32(const float* __restrict__ src, int row, bool live, float (&v)[64]) {
-    if (live) {
-        const float4* s = reinterpret_cast<const float4*>(src + (size_t)row * kC);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float4 q = __ldg(s + i);
-            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.f;
-    }
-}
-
-// bf16 row as 32 words (element 2j in the low half of word j)
-__device__ __forceinline__ void ldg_row_bf16(const __nv_bfloat16* __restrict__ src, int row, bool live,
-                                             uint32_t (&w)[32]) {
-    if (live) {
-        const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)row * kC);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 q = __ldg(s + i);
-            w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = 0u;
-    }
-}
+constexpr int kHalf = kC / 2;   // features per thread
 
 template <int NV>
 __device__ __forceinline__ void tst(uint32_t t, const float (&v)[NV]) {
@@ -202,10 +141,10 @@ __device__ __forceinline__ void tst(uint32_t t, const float (&v)[NV]) {
     }
 }
 
-// a bf16 row (32 words) into 64 fp32 TMEM columns
-__device__ __forceinline__ void tst_bf16(uint32_t t, const uint32_t (&w)[32]) {
+// a bf16 half row (16 words) into 32 fp32 TMEM columns
+__device__ __forceinline__ void tst_bf16(uint32_t t, const uint32_t (&w)[kHalf / 2]) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
+    for (int h = 0; h < kHalf / 16; ++h) {
         uint32_t r[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -224,25 +163,14 @@ __device__ __forceinline__ void tld32(uint32_t t, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tld64(uint32_t t, float (&v)[64]) {
-    uint32_t r[64];
-    tmem_ld_x32(t, *reinterpret_cast<uint32_t(*)[32]>(r));
-    tmem_ld_x32(t + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+// two 32-column reads behind one wait
+__device__ __forceinline__ void tld32x2(uint32_t t0, float (&v0)[32], uint32_t t1, float (&v1)[32]) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_x32(t0, r0);
+    tmem_ld_x32(t1, r1);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// two 64-column reads behind one wait
-__device__ __forceinline__ void tld64x2(uint32_t t0, float (&v0)[64], uint32_t t1, float (&v1)[64]) {
-    uint32_t r0[64], r1[64];
-    tmem_ld_x32(t0, *reinterpret_cast<uint32_t(*)[32]>(r0));
-    tmem_ld_x32(t0 + 32, *reinterpret_cast<uint32_t(*)[32]>(r0 + 32));
-    tmem_ld_x32(t1, *reinterpret_cast<uint32_t(*)[32]>(r1));
-    tmem_ld_x32(t1 + 32, *reinterpret_cast<uint32_t(*)[32]>(r1 + 32));
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 64; ++i) { v0[i] = __uint_as_float(r0[i]); v1[i] = __uint_as_float(r1[i]); }
+    for (int i = 0; i < 32; ++i) { v0[i] = __uint_as_float(r0[i]); v1[i] = __uint_as_float(r1[i]); }
 }
 
 __device__ __forceinline__ void tst8(uint32_t t, const float (&v)[8]) {
@@ -252,45 +180,47 @@ __device__ __forceinline__ void tst8(uint32_t t, const float (&v)[8]) {
     tmem_st_x8(t, r);
 }
 
-template <int NV>
-__device__ __forceinline__ void stg_f32(float* dst, const float (&v)[NV]) {
-    float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int i = 0; i < NV / 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-
-template <int NV>
-__device__ __forceinline__ void stg_bf16(__nv_bfloat16* dst, const float (&v)[NV]) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < NV / 8; ++i)
-        d[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-}
-
-// Column k = r of rows rho .. rho + 63 of a bf16 operand from a bf16 row held as
-// 32 words (no rounding: the values are bf16 already).
-template <int R>
-__device__ __forceinline__ void put_col_bf16(uint32_t base, int rho, int r, const uint32_t (&w)[32]) {
+// Column k = r of rows rho .. rho + 2 NW - 1 of a bf16 operand from bf16 values
+// held as NW words (no rounding: the values are bf16 already).
+template <int R, int NW>
+__device__ __forceinline__ void put_col_bf16(uint32_t base, int rho, int r, const uint32_t (&w)[NW]) {
     const uint32_t a = base + (uint32_t)((r >> 4) * R * 32 + rho * 32 + (r & 7) * 2);
     const uint32_t c = (uint32_t)((r >> 3) & 1);
     const uint32_t a0 = a + (c << 4), a1 = a + ((c ^ 1u) << 4);
 #pragma unroll
-    for (int f = 0; f < 64; ++f)
+    for (int f = 0; f < 2 * NW; ++f)
         st_shared_u16((((f >> 2) & 1) ? a1 : a0) + 32u * f,
                       (uint16_t)((f & 1) ? (w[f >> 1] >> 16) : (w[f >> 1] & 0xffffu)));
 }
 
-// Mean and 1 / std of a row (LayerNorm statistics, two passes).
-__device__ __forceinline__ float2 ln_stats(const float (&v)[64]) {
+// Row sums over the two halves of a row: a thread adds its partner's partial
+// (same row, other half) through shared memory.  The two buffers alternate, so
+// one barrier per exchange suffices: a buffer is written again only after every
+// thread has passed the next exchange's barrier, by which time it has read it.
+// Callers keep exchanges in code that every thread of the CTA runs.
+struct RowXch {
+    float2* buf;   // [2][2][kTile]
+    int k;
+    __device__ __forceinline__ float2 sum(int hf, int r, float2 v) {
+        float2* b = buf + (k & 1) * 2 * kTile;
+        ++k;
+        b[hf * kTile + r] = v;
+        __syncthreads();
+        const float2 o = b[(hf ^ 1) * kTile + r];
+        return make_float2(v.x + o.x, v.y + o.y);
+    }
+};
+
+// Mean and 1 / std of a row from its two halves (LayerNorm statistics, two passes).
+__device__ __forceinline__ float2 ln_stats(RowXch& xc, int hf, int r, const float (&v)[kHalf]) {
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) s += v[i];
-    const float mu = s * (1.0f / kC);
+    for (int i = 0; i < kHalf; ++i) s += v[i];
+    const float mu = xc.sum(hf, r, make_float2(s, 0.f)).x * (1.0f / kC);
     float q = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) q = fmaf(v[i] - mu, v[i] - mu, q);
-    return make_float2(mu, rsqrtf(q * (1.0f / kC) + kLnEps));
+    for (int i = 0; i < kHalf; ++i) q = fmaf(v[i] - mu, v[i] - mu, q);
+    return make_float2(mu, rsqrtf(xc.sum(hf, r, make_float2(q, 0.f)).x * (1.0f / kC) + kLnEps));
 }
 
 // v[j] by selects (no local memory)
@@ -302,24 +232,155 @@ __device__ __forceinline__ float pick(const float (&v)[NV], int j) {
     return r;
 }
 
-// The GELU loops: for each 8-column chunk c of the 64 columns at `src`, f(c,
-// v) with v the chunk's values; the next chunk's TMEM read is issued before f
-// runs and waited for after it.
-template <typename F>
-__device__ __forceinline__ void chunks8_pipelined(uint32_t src, F&& f) {
-    uint32_t cur[8], nxt[8] = {};
-    tmem_ld_x8(src, cur);
-    tmem_wait_ld();
-#pragma unroll 1
-    for (int c = 0; c < 64; c += 8) {
-        if (c + 8 < 64) tmem_ld_x8(src + c + 8, nxt);
-        float v[8];
+// ------------------------------------------------------------ bulk tile copies
+//
+// A tile's node rows are contiguous in global memory, and so is each weight
+// matrix: each moves between global and shared memory as one 1D bulk copy on the
+// TMA engine (cp.async.bulk), issued by thread 0 (a thread-per-row global access
+// would touch 32 rows per warp instruction; a copy per row would queue hundreds
+// of small copies on the engine).  Loads complete on an mbarrier; stores are
+// drained by thread 0 before the CTA exits.  Staged rows keep the global layout,
+// so the 8 threads of a quarter warp, taking 16-byte chunk j of 8 consecutive
+// rows, would all hit one bank group: a thread reads and writes the chunks of its
+// row in an order rotated by its row number, and a select network puts them back
+// in place in registers.
+
+constexpr int kRow32 = kC * 4;   // an fp32 node row, bytes
+constexpr int kRow16 = kC * 2;   // a bf16 node row
+
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+
+// this thread's bulk stores: committed, then waited for (their shared-memory
+// sources may be reused or released afterwards)
+__device__ __forceinline__ void bulk_store_drain() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Staged rows written with ordinary stores become visible to the bulk stores
+// issued after this (every thread calls it).
+__device__ __forceinline__ void staged_ready() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+}
+
+// a 4-byte shared load ordered like ordinary memory accesses (staged data lands
+// by bulk copy: its reads must stay behind the barrier wait)
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts_u4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// out chunk j = in chunk (j + s) mod NC (NC chunks of 4 words, 0 <= s < NC), in
+// log2 NC stages of selects
+template <int NC>
+__device__ __forceinline__ void rotate_chunks(uint32_t (&v)[4 * NC], int s) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(cur[i]);
-        f(c, v);
-        tmem_wait_ld();
+    for (int b = 1; b < NC; b <<= 1) {
+        const bool on = (s & b) != 0;
+        uint32_t t[4 * NC];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+        for (int i = 0; i < 4 * NC; ++i) t[i] = v[(i + 4 * b) % (4 * NC)];
+#pragma unroll
+        for (int i = 0; i < 4 * NC; ++i) v[i] = on ? t[i] : v[i];
+    }
+}
+
+// NC 16-byte chunks starting at `addr` (row r's part of a staged tile), in order
+template <int NC>
+__device__ __forceinline__ void lds_chunks(uint32_t addr, int r, uint32_t (&v)[4 * NC]) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        const uint4 q = lds_u4(addr + 16 * ((j + r) & (NC - 1)));   // slot j = chunk (j + r)
+        v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+    }
+    rotate_chunks<NC>(v, (NC - (r & (NC - 1))) & (NC - 1));
+}
+
+template <int NC>
+__device__ __forceinline__ void sts_chunks(uint32_t addr, int r, uint32_t (&v)[4 * NC]) {
+    rotate_chunks<NC>(v, r & (NC - 1));                   // slot j = chunk (j + r)
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+        sts_u4(addr + 16 * ((j + r) & (NC - 1)), make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+}
+
+// the half row (32 fp32) of row r from a staged fp32 tile (zeros for a dead row)
+__device__ __forceinline__ void lds_half_f32(uint32_t stg, int r, int hf, bool live, float (&v)[kHalf]) {
+    uint32_t w[kHalf];
+    lds_chunks<8>(stg + r * kRow32 + hf * (kHalf * 4), r, w);
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) v[i] = live ? __uint_as_float(w[i]) : 0.f;
+}
+
+// the half row of row r from a staged bf16 tile, as 16 words (zeros for a dead row)
+__device__ __forceinline__ void lds_half_bf16(uint32_t stg, int r, int hf, bool live, uint32_t (&w)[kHalf / 2]) {
+    lds_chunks<4>(stg + r * kRow16 + hf * (kHalf * 2), r, w);
+#pragma unroll
+    for (int i = 0; i < kHalf / 2; ++i) w[i] = live ? w[i] : 0u;
+}
+
+// 32 fp32 values at byte offset `off` of row r of a staged tile with row pitch P
+__device__ __forceinline__ void sts_f32x32(uint32_t stg, int P, int r, int off, const float (&v)[32]) {
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    sts_chunks<8>(stg + r * P + off, r, w);
+}
+
+// 32 values as bf16 at byte offset `off` of row r of a staged bf16 tile
+__device__ __forceinline__ void sts_bf16x32(uint32_t stg, int r, int off, const float (&v)[32]) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    sts_chunks<4>(stg + r * kRow16 + off, r, w);
+}
+
+// B operand (n, k) = W[n][k] from a row-major [N][K] matrix staged as is: 16-byte
+// moves, a warp filling 16 whole rows of one sub-tile.
+template <int N, int K>
+__device__ __forceinline__ void relayout_rows(uint8_t* dst, uint32_t nat) {
+    static_assert(N % 16 == 0 && K % 8 == 0, "16 x 8 blocks");
+    const uint32_t d = smem_u32(dst);
+    const int lane = threadIdx.x & 31;
+#pragma unroll 4
+    for (int b = threadIdx.x >> 5; b < (N / 16) * (K / 8); b += kThreads / 32) {
+        const int n = 16 * (b / (K / 8)) + (lane >> 1), k = 8 * (b % (K / 8)) + 4 * (lane & 1);
+        sts_u4(d + sw32(N, n, 4 * k), lds_u4(nat + (n * K + k) * 4));
+    }
+}
+
+// B operand (n, k) = W[k][n] from a row-major [K][N] matrix staged as is.  A warp
+// step moves 32 consecutive n of 4 rows k: lane l takes n = n0 + l and k = k0 +
+// ((l >> 3) + t) % 4 at turn t, so its loads (one row each, 32 consecutive words)
+// and its stores (bank 8 (l % 4) + 4 (l / 4 % 2) + k % 4) both cover 32 banks.
+template <int K, int N>
+__device__ __forceinline__ void relayout_cols(uint8_t* dst, uint32_t nat) {
+    static_assert(N % 32 == 0 && K % 8 == 0, "32 x 4 blocks");
+    const int lane = threadIdx.x & 31;
+#pragma unroll 2
+    for (int b = threadIdx.x >> 5; b < (N / 32) * (K / 4); b += kThreads / 32) {
+        const int n = 32 * (b % (N / 32)) + lane, k0 = 4 * (b / (N / 32));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int k = k0 + (((lane >> 3) + t) & 3);
+            *reinterpret_cast<float*>(dst + sw32(N, n, 4 * k)) = __uint_as_float(lds_b32(nat + (k * N + n) * 4));
+        }
     }
 }
 
@@ -327,6 +388,7 @@ __device__ __forceinline__ void chunks8_pipelined(uint32_t src, F&& f) {
 
 struct Ctl {
     uint64_t bar;      // one arrival per committed group of MMAs
+    uint64_t ldbar;    // the bulk loads (thread 0 arrives with their bytes)
     uint32_t tbase;    // TMEM base address
     int abort;
 };
@@ -335,20 +397,31 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
+// Barriers and TMEM; ends with the CTA barrier that makes both visible.
 __device__ __forceinline__ void ctl_init(Ctl& c, uint32_t cols) {
     if (threadIdx.x == 0) {
         mbar_init(&c.bar, 1);
+        mbar_init(&c.ldbar, 1);
         c.abort = 0;
         fence_barrier_init();
     }
     if (threadIdx.x < 32) tmem_alloc(&c.tbase, cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 }
 
-// This thread's weight copies, TMEM stores and shared-memory operand stores are complete and
+// Waits for the bulk loads, in every thread; one decision for the CTA.
+__device__ __forceinline__ bool loads_wait(Ctl& c, int* status) {
+    const bool ok = mbar_wait_all(&c.ldbar, 0, &c.abort, tc::kWaitNs);
+    if (!ok && (threadIdx.x & 31) == 0) tc::fail(&c.abort, status);
+    return __syncthreads_and(ok) != 0;
+}
+
+// This thread's TMEM stores and shared-memory operand stores are complete and
 // visible to the tensor core, in every thread of the CTA; returns whether every
 // thread's `ok` held (one uniform decision per phase).
 __device__ __forceinline__ bool operands_ready(bool ok) {
-    cp_async_wait_all();
     tmem_wait_st();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -366,14 +439,23 @@ __device__ __forceinline__ bool mma_wait(Ctl& c, uint32_t& phase, int* status) {
     return ok;
 }
 
-// End of a tile kernel: if a wait gave up, give the last group a second bounded
-// wait so that no MMA is still writing TMEM, then free the columns.
+// mma_wait in every warp, then one decision for the whole CTA (the row
+// exchanges that follow need every thread at their barriers).
+__device__ __forceinline__ bool mma_wait_cta(Ctl& c, uint32_t& phase, int* status) {
+    const bool ok = mma_wait(c, phase, status);
+    return __syncthreads_and(ok) != 0;
+}
+
+// End of a tile kernel: if a wait gave up, give the bulk loads and the last MMA
+// group a second bounded wait so that nothing is still writing shared memory or
+// TMEM, then free the columns.  (A bulk store is drained by its own thread.)
 __device__ __forceinline__ void ctl_finish(Ctl& c, bool ok, uint32_t phase, uint32_t cols) {
     tc_fence_before();
     const bool all = __syncthreads_and(ok) != 0;
     if (threadIdx.x < 32) {
         if (!all) {
             int never = 0;
+            mbar_wait(&c.ldbar, 0, &never, tc::kWaitNs);
             mbar_wait(&c.bar, phase ^ 1u, &never, tc::kWaitNs);
         }
         tc_fence_after();
@@ -384,9 +466,12 @@ __device__ __forceinline__ void ctl_finish(Ctl& c, bool ok, uint32_t phase, uint
 // ------------------------------------------------------------------ forward
 
 struct SmemLnQkv {
-    uint8_t w[3 * kC * kC * 4];     // B (n, k) = W_qkv[k][n], n < 192
+    uint8_t w[3 * kC * kC * 4];                    // B (n, k) = W_qkv[k][n], n < 192
+    uint8_t stg[3 * kC * kC * 4 + kTile * kRow32];   // W_qkv and the x tile as copied; then the q, k, v tiles
     float g1[kC], b1[kC], bq[3 * kC];
+    float2 xch[4 * kTile];
 };
+static_assert(3 * kTile * kRow16 <= 3 * kC * kC * 4 + kTile * kRow32, "q, k, v staging");
 constexpr uint32_t kLnQkvCols = 256;   // u (A, 64 columns), then the q | k | v accumulator (192)
 
 __global__ void __launch_bounds__(kThreads)
@@ -396,53 +481,78 @@ layer_ln_qkv(int n, const float* __restrict__ x, const float* __restrict__ ln_g,
     extern __shared__ uint8_t smem_raw[];
     SmemLnQkv& S = *reinterpret_cast<SmemLnQkv*>(align1024(smem_raw));
     __shared__ Ctl ctl;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = blockIdx.x * kTile + tid;
+    const int tid = threadIdx.x, warp = tid >> 5, hf = warp >> 2;
+    const int r = ((warp & 3) << 5) | (tid & 31), c0 = kHalf * hf;
+    const int row = blockIdx.x * kTile + r;
     const bool live = row < n;
     ctl_init(ctl, kLnQkvCols);
-    load_b_cols<kC, 3 * kC>(S.w, w_qkv);
-    float u[64];
-    ldg_row_f32(x, row, live, u);
+    const int row0 = blockIdx.x * kTile, rows = n - row0 < kTile ? n - row0 : kTile;
+    const uint32_t stg = smem_u32(S.stg), xs = stg + 3 * kC * kC * 4;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&ctl.ldbar, 3 * kC * kC * 4 + rows * kRow32);
+        bulk_load(stg, w_qkv, 3 * kC * kC * 4, &ctl.ldbar);
+        bulk_load(xs, x + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
+    }
     for (int i = tid; i < kC; i += kThreads) { S.g1[i] = ln_g[i]; S.b1[i] = ln_b[i]; }
     for (int i = tid; i < 3 * kC; i += kThreads) S.bq[i] = b_qkv[i];
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * warp) << 16);
-    const float2 st = ln_stats(u);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) u[i] = fmaf((u[i] - st.x) * st.y, S.g1[i], S.b1[i]);
-    tst(tl, u);
-    bool ok = operands_ready(true);
+    bool ok = loads_wait(ctl, status);
     uint32_t phase = 0;
-    if (warp == 0) {
-        if (elect_one()) {
-            const SmemDesc dw = smem_desc_split(smem_u32(S.w), 16, 256, 6);
+    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    if (ok) {
+        relayout_cols<kC, 3 * kC>(S.w, stg);
+        float u[kHalf];
+        lds_half_f32(xs, r, hf, live, u);
+        RowXch xc{S.xch, 0};
+        const float2 st = ln_stats(xc, hf, r, u);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_tf32_ts(tb + 64, tb + 8 * kk, desc_at(dw, kk * 3 * kC * 32), idesc_tf32(128, 3 * kC), kk > 0);
-            mma_commit(&ctl.bar);
-        }
-        __syncwarp();
+        for (int i = 0; i < kHalf; ++i) u[i] = fmaf((u[i] - st.x) * st.y, S.g1[c0 + i], S.b1[c0 + i]);
+        tst(tl + c0, u);
     }
-    ok = mma_wait(ctl, phase, status);
+    ok = operands_ready(ok);
+    if (ok) {
+        if (warp == 0) {
+            if (elect_one()) {
+                const SmemDesc dw = smem_desc_split(smem_u32(S.w), 16, 256, 6);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_tf32_ts(tb + 64, tb + 8 * kk, desc_at(dw, kk * 3 * kC * 32), idesc_tf32(128, 3 * kC),
+                                kk > 0);
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
+        }
+        ok = mma_wait(ctl, phase, status);
+    }
     if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < 3 * kC; c += 32) {
+        for (int c = 3 * kHalf * hf; c < 3 * kHalf * (hf + 1); c += 32) {
             float t[32];
             tld32(tl + 64 + c, t);
 #pragma unroll
             for (int i = 0; i < 32; ++i) t[i] += S.bq[c + i];
-            __nv_bfloat16* dst = c < kC ? q : c < 2 * kC ? k : v;
-            if (live) stg_bf16(dst + (size_t)row * kC + (c & (kC - 1)), t);
+            sts_bf16x32(stg + (c >> 6) * kTile * kRow16, r, (c & (kC - 1)) * 2, t);
         }
+    }
+    ok = __syncthreads_and(ok) != 0;
+    staged_ready();
+    if (tid == 0) {
+        if (ok) {
+            __nv_bfloat16* dst[3] = {q, k, v};
+#pragma unroll
+            for (int s = 0; s < 3; ++s) bulk_store(dst[s] + (size_t)row0 * kC, stg + s * kTile * kRow16, rows * kRow16);
+        }
+        bulk_store_drain();
     }
     ctl_finish(ctl, ok, phase, kLnQkvCols);
 }
 
 struct SmemOutFfn {
     uint8_t wo[kC * kC * 4], w1[kC * kF * 4], w2[kF * kC * 4];   // B (n, k) = W[k][n]
+    uint8_t wn[3 * kC * kC * 4];                                 // W_o, W_1, W_2 as copied
+    uint8_t os[kTile * kRow16];                                  // the o tile
+    uint8_t xs[kTile * kRow32];                                  // the x tile, then the y tile
     float bo[kC], b1[kF], b2[kC], g2[kC], s2[kC];
+    float2 xch[4 * kTile];
 };
 // TMEM: slot 0 (o, then a, then GELU(a)), slot 1 at 64 (t, then z, then f), hh at 128
 constexpr uint32_t kOutFfnCols = 256;
@@ -455,27 +565,37 @@ layer_out_ffn(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
     extern __shared__ uint8_t smem_raw[];
     SmemOutFfn& S = *reinterpret_cast<SmemOutFfn*>(align1024(smem_raw));
     __shared__ Ctl ctl;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = blockIdx.x * kTile + tid;
+    const int tid = threadIdx.x, warp = tid >> 5, hf = warp >> 2;
+    const int r = ((warp & 3) << 5) | (tid & 31), c0 = kHalf * hf;
+    const int row = blockIdx.x * kTile + r;
     const bool live = row < n;
     ctl_init(ctl, kOutFfnCols);
-    load_b_cols<kC, kC>(S.wo, w_o);
-    load_b_cols<kC, kF>(S.w1, w_1);
-    load_b_cols<kF, kC>(S.w2, w_2);
-    uint32_t ow[32];
-    float hh[64];
-    ldg_row_bf16(o, row, live, ow);
-    ldg_row_f32(x, row, live, hh);
+    const int row0 = blockIdx.x * kTile, rows = n - row0 < kTile ? n - row0 : kTile;
+    const uint32_t wn = smem_u32(S.wn), os = smem_u32(S.os), xs = smem_u32(S.xs);
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&ctl.ldbar, 3 * kC * kC * 4 + rows * (kRow16 + kRow32));
+        const float* src[3] = {w_o, w_1, w_2};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) bulk_load(wn + m * kC * kC * 4, src[m], kC * kC * 4, &ctl.ldbar);
+        bulk_load(os, o + (size_t)row0 * kC, rows * kRow16, &ctl.ldbar);
+        bulk_load(xs, x + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
+    }
     for (int i = tid; i < kC; i += kThreads) {
         S.bo[i] = b_o[i]; S.b1[i] = b_1[i]; S.b2[i] = b_2[i]; S.g2[i] = ln_g[i]; S.s2[i] = ln_b[i];
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * warp) << 16);
-    tst_bf16(tl, ow);                                     // slot 0: o
-    bool ok = operands_ready(true);
+    bool ok = loads_wait(ctl, status);
     uint32_t phase = 0;
+    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    RowXch xc{S.xch, 0};
+    float hh[kHalf];
+    if (ok) {
+        relayout_cols<kC, kC>(S.wo, wn);
+        uint32_t ow[kHalf / 2];
+        lds_half_bf16(os, r, hf, live, ow);
+        lds_half_f32(xs, r, hf, live, hh);
+        tst_bf16(tl + c0, ow);                            // slot 0: o
+    }
+    ok = operands_ready(ok);
     const SmemDesc dwo = smem_desc_split(smem_u32(S.wo), 16, 256, 6);
     const SmemDesc dw1 = smem_desc_split(smem_u32(S.w1), 16, 256, 6);
     const SmemDesc dw2 = smem_desc_split(smem_u32(S.w2), 16, 256, 6);
@@ -491,38 +611,61 @@ layer_out_ffn(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
             __syncwarp();
         }
     };
-    issue(64, 0, dwo);
-    ok = mma_wait(ctl, phase, status);
     if (ok) {
-        float t[64];
-        tld64(tl + 64, t);
+        issue(64, 0, dwo);
+        relayout_cols<kC, kF>(S.w1, wn + kC * kC * 4);    // while the product runs
+        relayout_cols<kF, kC>(S.w2, wn + 2 * kC * kC * 4);
+        ok = mma_wait_cta(ctl, phase, status);
+    }
+    if (ok) {
+        float t[kHalf];
+        tld32(tl + 64 + c0, t);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) hh[i] += t[i] + S.bo[i];
-        tst(tl + 128, hh);                                // hh, for the last residual
-        const float2 st = ln_stats(hh);
+        for (int i = 0; i < kHalf; ++i) hh[i] += t[i] + S.bo[c0 + i];
+        tst(tl + 128 + c0, hh);                           // hh, for the last residual
+        const float2 st = ln_stats(xc, hf, r, hh);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) t[i] = fmaf((hh[i] - st.x) * st.y, S.g2[i], S.s2[i]);
-        tst(tl + 64, t);                                  // slot 1: z
+        for (int i = 0; i < kHalf; ++i) t[i] = fmaf((hh[i] - st.x) * st.y, S.g2[c0 + i], S.s2[c0 + i]);
+        tst(tl + 64 + c0, t);                             // slot 1: z
     }
     ok = operands_ready(ok);
-    if (ok) issue(0, 64, dw1);
-    ok = ok && mma_wait(ctl, phase, status);
     if (ok) {
-        chunks8_pipelined(tl, [&](int c, float (&a)[8]) {
+        issue(0, 64, dw1);
+        ok = mma_wait(ctl, phase, status);
+    }
+    if (ok) {
+        uint32_t cur[8], nxt[8] = {};
+        tmem_ld_x8(tl + c0, cur);
+        tmem_wait_ld();
+#pragma unroll 1
+        for (int c = c0; c < c0 + kHalf; c += 8) {
+            if (c + 8 < c0 + kHalf) tmem_ld_x8(tl + c + 8, nxt);
+            float a[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = gelu(a[i] + S.b1[c + i]);
+            for (int i = 0; i < 8; ++i) a[i] = gelu(__uint_as_float(cur[i]) + S.b1[c + i]);
             tst8(tl + c, a);                              // slot 0: GELU(a)
-        });
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+        }
     }
     ok = operands_ready(ok);
-    if (ok) issue(64, 0, dw2);
-    ok = ok && mma_wait(ctl, phase, status);
     if (ok) {
-        float f[64];
-        tld64x2(tl + 64, f, tl + 128, hh);
+        issue(64, 0, dw2);
+        ok = mma_wait(ctl, phase, status);
+    }
+    if (ok) {
+        float f[kHalf];
+        tld32x2(tl + 64 + c0, f, tl + 128 + c0, hh);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) f[i] += hh[i] + S.b2[i];
-        if (live) stg_f32(y + (size_t)row * kC, f);
+        for (int i = 0; i < kHalf; ++i) f[i] += hh[i] + S.b2[c0 + i];
+        sts_f32x32(xs, kRow32, r, hf * kHalf * 4, f);    // the y tile (x is consumed)
+    }
+    ok = __syncthreads_and(ok) != 0;
+    staged_ready();
+    if (tid == 0) {
+        if (ok) bulk_store(y + (size_t)row0 * kC, xs, rows * kRow32);
+        bulk_store_drain();
     }
     ctl_finish(ctl, ok, phase, kOutFfnCols);
 }
@@ -578,6 +721,10 @@ __global__ void __launch_bounds__(256) reduce_partials(const float* __restrict__
 constexpr int kTR = 256;
 constexpr int kTBytes = 8 * kTR * 32;
 
+// At the start ta | tb stage the inputs as copied: W_o, W_2, W_1 and the o, dy, x
+// tiles; at the end the image area stages dO and dh and ta the partial sums.
+static_assert(3 * kC * kC * 4 + kTile * (kRow16 + 2 * kRow32) <= 2 * kTBytes, "input staging");
+
 struct SmemFfnBwd {
     uint8_t wo_c[kC * kC * 4];   // (n = i, k = m) = W_o[m][i]:  t  = o W_o
     uint8_t w1_c[kC * kF * 4];   // (n = j, k = i) = W_1[i][j]:  a  = z W_1
@@ -588,7 +735,10 @@ struct SmemFfnBwd {
     uint8_t tb[kTBytes];         // rows: da | dy | dh | dz       (B of the gradient products)
     float bo[kC], b1[kF], g2[kC], s2[kC];
     float vec[4 * kC];           // column sums: db_1 | db_2 | db_o | dLN2 shift
+    float2 xch[4 * kTile];
 };
+static_assert(kTile * (kRow16 + kRow32) <= 5 * kC * kC * 4, "dO and dh staging");
+static_assert(kPartStride * 4 <= kTBytes, "partial staging");
 // TMEM columns: o then zh 0, dy 64 (A operands), t then z 128, dg 192, a then da
 // 256, dz 320, dh 384, dO 448; once those are consumed the gradient products take
 // 0..255 (zh | ones against da | dy | dh | dz) and 256..383 (GELU(a) | o against
@@ -604,36 +754,52 @@ layer_ffn_bwd(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
     extern __shared__ uint8_t smem_raw[];
     SmemFfnBwd& S = *reinterpret_cast<SmemFfnBwd*>(align1024(smem_raw));
     __shared__ Ctl ctl;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = blockIdx.x * kTile + tid;
+    const int tid = threadIdx.x, warp = tid >> 5, hf = warp >> 2;
+    const int r = ((warp & 3) << 5) | (tid & 31), c0 = kHalf * hf;
+    const int row = blockIdx.x * kTile + r;
     const bool live = row < n;
     ctl_init(ctl, kFfnBwdCols);
-    load_b_cols<kC, kC>(S.wo_c, w_o);
-    load_b_cols<kC, kF>(S.w1_c, w_1);
-    load_b_rows<kF, kC>(S.w2_r, w_2);
-    load_b_rows<kC, kF>(S.w1_r, w_1);
-    load_b_rows<kC, kC>(S.wo_r, w_o);
-    uint32_t ow[32];
-    float v[64], w[64];
-    ldg_row_bf16(o, row, live, ow);
-    ldg_row_f32(dy, row, live, v);
-    ldg_row_f32(x, row, live, w);
-    put_ones_block<kTR>(S.ta, 192);
+    const uint32_t ta = smem_u32(S.ta), tbb = smem_u32(S.tb);
+    const int row0 = blockIdx.x * kTile, rows = n - row0 < kTile ? n - row0 : kTile;
+    const uint32_t wn = ta, os = wn + 3 * kC * kC * 4, dys = os + kTile * kRow16, xs = dys + kTile * kRow32;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&ctl.ldbar, 3 * kC * kC * 4 + rows * (kRow16 + 2 * kRow32));
+        const float* src[3] = {w_o, w_2, w_1};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) bulk_load(wn + m * kC * kC * 4, src[m], kC * kC * 4, &ctl.ldbar);
+        bulk_load(os, o + (size_t)row0 * kC, rows * kRow16, &ctl.ldbar);
+        bulk_load(dys, dy + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
+        bulk_load(xs, x + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
+    }
     for (int i = tid; i < kC; i += kThreads) {
         S.bo[i] = b_o[i]; S.b1[i] = b_1[i]; S.g2[i] = ln_g[i]; S.s2[i] = ln_b[i];
     }
-    const uint32_t ta = smem_u32(S.ta), tbb = smem_u32(S.tb);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * warp) << 16);
-    // rows past the end are zeros, so their columns of the gradient operands are too
-    tst_bf16(tl + 0, ow);
-    tst(tl + 64, v);
-    put_col_bf16<kTR>(ta, 64, tid, ow);                   // o^T
-    put_col<kTR>(tbb, 64, tid, v, 1.f);                   // dy^T
-    bool ok = operands_ready(true);
+    bool ok = loads_wait(ctl, status);
     uint32_t phase = 0;
+    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    RowXch xc{S.xch, 0};
+    uint32_t ow[kHalf / 2];
+    float v[kHalf], w[kHalf];
+    if (ok) {
+        relayout_cols<kC, kC>(S.wo_c, wn);
+        relayout_rows<kC, kC>(S.wo_r, wn);
+        relayout_rows<kF, kC>(S.w2_r, wn + kC * kC * 4);
+        relayout_rows<kC, kF>(S.w1_r, wn + 2 * kC * kC * 4);
+        relayout_cols<kC, kF>(S.w1_c, wn + 2 * kC * kC * 4);
+        lds_half_bf16(os, r, hf, live, ow);
+        lds_half_f32(dys, r, hf, live, v);
+        lds_half_f32(xs, r, hf, live, w);
+    }
+    __syncthreads();                                      // the staged inputs are read: ta and tb are free
+    if (ok) {
+        put_ones_block<kTR>(S.ta, 192);
+        // rows past the end are zeros, so their columns of the gradient operands are too
+        tst_bf16(tl + 0 + c0, ow);
+        tst(tl + 64 + c0, v);
+        put_col_bf16<kTR>(ta, 64 + c0, r, ow);            // o^T
+        put_col<kTR>(tbb, 64 + c0, r, v, 1.f);            // dy^T
+    }
+    ok = operands_ready(ok);
     const bool issuer = warp == 0;
     auto mma64 = [&](uint32_t d, uint32_t a, const uint8_t* wm) {   // D (64 columns) = A (TMEM, K = 64) W
         const SmemDesc dw = smem_desc_split(smem_u32(wm), 16, 256, 6);
@@ -641,49 +807,53 @@ layer_ffn_bwd(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
         for (int kk = 0; kk < 8; ++kk)
             mma_tf32_ts(tb + d, tb + a + 8 * kk, desc_at(dw, kk * 64 * 32), idesc_tf32(128, 64), kk > 0);
     };
-    if (issuer) {
-        if (elect_one()) {
-            mma64(128, 0, S.wo_c);                        // t
-            mma64(192, 64, S.w2_r);                       // dg = dy W_2^T
-            mma_commit(&ctl.bar);
+    if (ok) {
+        if (issuer) {
+            if (elect_one()) {
+                mma64(128, 0, S.wo_c);                    // t
+                mma64(192, 64, S.w2_r);                   // dg = dy W_2^T
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
         }
-        __syncwarp();
+        ok = mma_wait_cta(ctl, phase, status);
     }
-    ok = mma_wait(ctl, phase, status);
     float r2 = 0.f;
     if (ok) {
-        tld64(tl + 128, v);
+        tld32(tl + 128 + c0, v);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) w[i] += v[i] + S.bo[i];   // hh
-        const float2 st = ln_stats(w);
+        for (int i = 0; i < kHalf; ++i) w[i] += v[i] + S.bo[c0 + i];   // hh
+        const float2 st = ln_stats(xc, hf, r, w);
         r2 = st.y;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < kHalf; ++i) {
             w[i] = (w[i] - st.x) * st.y;                  // zh
-            v[i] = fmaf(w[i], S.g2[i], S.s2[i]);          // z
+            v[i] = fmaf(w[i], S.g2[c0 + i], S.s2[c0 + i]);   // z
         }
-        tst(tl + 0, w);                                   // zh (o is consumed)
-        tst(tl + 128, v);
-        put_col<kTR>(ta, 128, tid, w, 1.f);               // zh^T
+        tst(tl + 0 + c0, w);                              // zh (o is consumed)
+        tst(tl + 128 + c0, v);
+        put_col<kTR>(ta, 128 + c0, r, w, 1.f);            // zh^T
     }
     ok = operands_ready(ok);
-    if (ok && issuer) {
-        if (elect_one()) {
-            mma64(256, 128, S.w1_c);                      // a = z W_1
-            mma_commit(&ctl.bar);
+    if (ok) {
+        if (issuer) {
+            if (elect_one()) {
+                mma64(256, 128, S.w1_c);                  // a = z W_1
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
         }
-        __syncwarp();
+        ok = mma_wait(ctl, phase, status);
     }
-    ok = ok && mma_wait(ctl, phase, status);
     if (ok) {
         const float lm = live ? 1.f : 0.f;
         uint32_t ca[8], cg[8], na[8] = {}, ng[8] = {};
-        tmem_ld_x8(tl + 256, ca);
-        tmem_ld_x8(tl + 192, cg);
+        tmem_ld_x8(tl + 256 + c0, ca);
+        tmem_ld_x8(tl + 192 + c0, cg);
         tmem_wait_ld();
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 8) {
-            if (c + 8 < 64) {
+        for (int c = c0; c < c0 + kHalf; c += 8) {
+            if (c + 8 < c0 + kHalf) {
                 tmem_ld_x8(tl + 256 + c + 8, na);
                 tmem_ld_x8(tl + 192 + c + 8, ng);
             }
@@ -695,110 +865,135 @@ layer_ffn_bwd(int n, const float* __restrict__ x, const __nv_bfloat16* __restric
                 g[i] = gelu(av);                                  // GELU(a)
             }
             tst8(tl + 256 + c, a);
-            put_col<kTR>(ta, c, tid, g, lm);              // GELU(a)^T (a dead row's GELU(b_1) is not zero)
-            put_col<kTR>(tbb, c, tid, a, 1.f);            // da^T
+            put_col<kTR>(ta, c, r, g, lm);                // GELU(a)^T (a dead row's GELU(b_1) is not zero)
+            put_col<kTR>(tbb, c, r, a, 1.f);              // da^T
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i) { ca[i] = na[i]; cg[i] = ng[i]; }
         }
     }
     ok = operands_ready(ok);
-    if (ok && issuer) {
-        if (elect_one()) {
-            mma64(320, 256, S.w1_r);                      // dz = da W_1^T
-            mma_commit(&ctl.bar);
-        }
-        __syncwarp();
-    }
-    ok = ok && mma_wait(ctl, phase, status);
     if (ok) {
-        tld64x2(tl + 320, v, tl + 0, w);                  // dz, zh
-        put_col<kTR>(tbb, 192, tid, v, 1.f);              // dz^T
+        if (issuer) {
+            if (elect_one()) {
+                mma64(320, 256, S.w1_r);                  // dz = da W_1^T
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
+        }
+        ok = mma_wait_cta(ctl, phase, status);
+    }
+    if (ok) {
+        tld32x2(tl + 320 + c0, v, tl + 0 + c0, w);        // dz, zh
+        put_col<kTR>(tbb, 192 + c0, r, v, 1.f);           // dz^T
         float m1 = 0.f, m2 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            v[i] *= S.g2[i];
+        for (int i = 0; i < kHalf; ++i) {
+            v[i] *= S.g2[c0 + i];
             m1 += v[i];
             m2 = fmaf(v[i], w[i], m2);
         }
-        m1 *= 1.0f / kC;
-        m2 *= 1.0f / kC;
+        const float2 m = xc.sum(hf, r, make_float2(m1, m2));
+        m1 = m.x * (1.0f / kC);
+        m2 = m.y * (1.0f / kC);
+        float d[kHalf];
+        tld32(tl + 64 + c0, d);                           // dy
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float d[32];
-            tld32(tl + 64 + 32 * h, d);                   // dy
-#pragma unroll
-            for (int i = 0; i < 32; ++i) d[i] += r2 * (v[32 * h + i] - m1 - w[32 * h + i] * m2);   // dh
-            if (live) stg_f32(dh + (size_t)row * kC + 32 * h, d);
-            tst(tl + 384 + 32 * h, d);
-            put_col<kTR>(tbb, 128 + 32 * h, tid, d, 1.f); // dh^T
-        }
+        for (int i = 0; i < kHalf; ++i) d[i] += r2 * (v[i] - m1 - w[i] * m2);   // dh
+        tst(tl + 384 + c0, d);
+        put_col<kTR>(tbb, 128 + c0, r, d, 1.f);           // dh^T
     }
     ok = operands_ready(ok);
-    if (ok && issuer) {
-        if (elect_one()) {
-            mma64(448, 384, S.wo_r);                      // dO = dh W_o^T
-            const SmemDesc da_ = smem_desc_split(ta, 16, 256, 6), db_ = smem_desc_split(tbb, 16, 256, 6);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)                // [GELU(a) | o]^T [dy | dh]
-                mma_ss(tb + 256, desc_at(da_, kk * kTR * 32), desc_at(db_, kk * kTR * 32 + 64 * 32),
-                       idesc_bf16(128, 128, false, false), kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)                // [zh | ones]^T [da | dy | dh | dz]
-                mma_ss(tb + 0, desc_at(da_, kk * kTR * 32 + 128 * 32), desc_at(db_, kk * kTR * 32),
-                       idesc_bf16(128, 256, false, false), kk > 0);
-            mma_commit(&ctl.bar);
-        }
-        __syncwarp();
-    }
-    ok = ok && mma_wait(ctl, phase, status);
     if (ok) {
-        tld64(tl + 448, v);
-        if (live) stg_bf16(dO + (size_t)row * kC, v);
-        if (warp == 2) {                                  // lane 64: the column sums
+        if (issuer) {
+            if (elect_one()) {
+                mma64(448, 384, S.wo_r);                  // dO = dh W_o^T
+                const SmemDesc da_ = smem_desc_split(ta, 16, 256, 6), db_ = smem_desc_split(tbb, 16, 256, 6);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)            // [GELU(a) | o]^T [dy | dh]
+                    mma_ss(tb + 256, desc_at(da_, kk * kTR * 32), desc_at(db_, kk * kTR * 32 + 64 * 32),
+                           idesc_bf16(128, 128, false, false), kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)            // [zh | ones]^T [da | dy | dh | dz]
+                    mma_ss(tb + 0, desc_at(da_, kk * kTR * 32 + 128 * 32), desc_at(db_, kk * kTR * 32),
+                           idesc_bf16(128, 256, false, false), kk > 0);
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
+        }
+        ok = mma_wait(ctl, phase, status);
+    }
+    // staging: dO and dh in the image area, the CTA's partial-sum row in ta (all
+    // consumed now), laid out as in global memory: dW_2, dW_1, dW_o rows, then
+    // db_2 | db_1 | db_o | dLN2 gain | shift
+    const uint32_t dos = smem_u32(S.wo_c), dhs = dos + kTile * kRow16, ps = ta, pvec = ps + 3 * kC * kRow32;
+    if (ok) {
+        tld32x2(tl + 448 + c0, v, tl + 384 + c0, w);      // dO, dh
+        sts_bf16x32(dos, r, hf * kHalf * 2, v);
+        sts_f32x32(dhs, kRow32, r, hf * kHalf * 4, w);
+        if ((warp & 3) == 2) {                            // lane 64: the column sums, 128 columns per half
 #pragma unroll 1
-            for (int c = 0; c < 4 * kC; c += 64) {
-                tld64(tl + c, v);
-                if (tid == 64) stg_f32(S.vec + c, v);
+            for (int c = 128 * hf; c < 128 * (hf + 1); c += 32) {
+                tld32(tl + c, v);
+                if (r == 64) sts_f32x32(smem_u32(S.vec), 0, r, 4 * c, v);
             }
         }
     }
     ok = __syncthreads_and(ok) != 0;
-    float* pp = part + (size_t)blockIdx.x * kPartStride;
     if (ok) {
-        // partial layout: dW_2, dW_1, dW_o (4096 each), then db_2, db_1, db_o, dLN2 gain, shift
-        if (tid < 64) {
-            tld64x2(tl + 256, v, tl + 0, w);
-            stg_f32(pp + tid * kC, v);                    // dW_2 row j
-            const float gi = S.g2[tid], si = S.s2[tid];
+        if (r < 64) {
+            tld32x2(tl + 256 + c0, v, tl + 0 + c0, w);
+            sts_f32x32(ps, kRow32, r, 4 * c0, v);         // dW_2 row j
+            const float gi = S.g2[r], si = S.s2[r];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) w[j] = fmaf(gi, w[j], si * S.vec[j]);
-            stg_f32(pp + kF * kC + tid * kC, w);          // dW_1 row i
-            tld64(tl + 192, v);
-            pp[3 * kC * kC + 3 * kC + tid] = pick(v, tid);   // dLN2 gain: the diagonal of zh^T dz
+            for (int j = 0; j < kHalf; ++j) w[j] = fmaf(gi, w[j], si * S.vec[c0 + j]);
+            sts_f32x32(ps, kRow32, kC + r, 4 * c0, w);    // dW_1 row i
+            tld32(tl + 192 + c0, v);
+            if ((r >> 5) == hf) st_shared_f32(pvec + 4 * (3 * kC + r), pick(v, r - c0));   // gain: diag of zh^T dz
         } else {
-            const int f = tid - 64;
-            tld64(tl + 256 + 64, v);
-            stg_f32(pp + 2 * kC * kC + f * kC, v);        // dW_o row m
-            pp[3 * kC * kC + f] = S.vec[64 + f];          // db_2
-            pp[3 * kC * kC + kC + f] = S.vec[f];          // db_1
-            pp[3 * kC * kC + 2 * kC + f] = S.vec[128 + f];   // db_o
-            pp[3 * kC * kC + 4 * kC + f] = S.vec[192 + f];   // dLN2 shift
+            const int f = r - 64;
+            tld32(tl + 256 + 64 + c0, v);
+            sts_f32x32(ps, kRow32, 2 * kC + f, 4 * c0, v);   // dW_o row m
+            if (hf == 0) {
+                st_shared_f32(pvec + 4 * f, S.vec[64 + f]);            // db_2
+                st_shared_f32(pvec + 4 * (kC + f), S.vec[f]);          // db_1
+            } else {
+                st_shared_f32(pvec + 4 * (2 * kC + f), S.vec[128 + f]);   // db_o
+                st_shared_f32(pvec + 4 * (4 * kC + f), S.vec[192 + f]);   // dLN2 shift
+            }
         }
+    }
+    ok = __syncthreads_and(ok) != 0;
+    staged_ready();
+    if (tid == 0) {
+        if (ok) {
+            bulk_store(dO + (size_t)row0 * kC, dos, rows * kRow16);
+            bulk_store(dh + (size_t)row0 * kC, dhs, rows * kRow32);
+            bulk_store(part + (size_t)blockIdx.x * kPartStride, ps, kPartStride * 4);
+        }
+        bulk_store_drain();
     }
     ctl_finish(ctl, ok, phase, kFfnBwdCols);
 }
+
+// At the start ta | tb | extra stage the inputs as copied: W_qkv and the dq, dk,
+// dv, x, dh tiles; later the image area stages dx and ta the partial sums.
+constexpr int kQkvIn = 3 * kC * kC * 4 + 3 * kTile * kRow16 + 2 * kTile * kRow32;
+constexpr int kQkvExtra = kQkvIn - 8 * 128 * 32 - kTBytes;
 
 struct SmemQkvBwd {
     uint8_t w[kC * 3 * kC * 4];  // (n = m, k = c) = W_qkv[m][c]: du = dqkv W_qkv^T (24 k-steps)
     uint8_t ta[8 * 128 * 32];    // rows: uh | ones (A of the gradient product)
     uint8_t tb[kTBytes];         // rows: dq | dk | dv | du
+    uint8_t extra[kQkvExtra];
     float g1[kC], b1[kC];
     float vec[4 * kC];           // column sums: db_qkv | dLN1 shift
+    float2 xch[4 * kTile];
 };
-// TMEM columns: dq | dk | dv 0..191 (A operand), du 192, uh 256; then the
-// gradient product 0..255.
-constexpr uint32_t kQkvBwdCols = 512;
+static_assert(kTile * kRow32 <= kC * 3 * kC * 4, "dx staging");
+static_assert(kPartStride * 4 <= 8 * 128 * 32 + kTBytes, "partial staging");
+// TMEM columns: dq | dk | dv 0..191 (A operand), du 192; then the gradient product 0..255.
+constexpr uint32_t kQkvBwdCols = 256;
 
 __global__ void __launch_bounds__(kThreads)
 layer_qkv_bwd(int n, const float* __restrict__ x, const float* __restrict__ ln_g, const float* __restrict__ ln_b,
@@ -808,109 +1003,143 @@ layer_qkv_bwd(int n, const float* __restrict__ x, const float* __restrict__ ln_g
     extern __shared__ uint8_t smem_raw[];
     SmemQkvBwd& S = *reinterpret_cast<SmemQkvBwd*>(align1024(smem_raw));
     __shared__ Ctl ctl;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = blockIdx.x * kTile + tid;
+    const int tid = threadIdx.x, warp = tid >> 5, hf = warp >> 2;
+    const int r = ((warp & 3) << 5) | (tid & 31), c0 = kHalf * hf;
+    const int row = blockIdx.x * kTile + r;
     const bool live = row < n;
     ctl_init(ctl, kQkvBwdCols);
-    load_b_rows<kC, 3 * kC>(S.w, w_qkv);
-    uint32_t gq[32], gk[32], gv[32];
-    float u[64];
-    ldg_row_bf16(dq, row, live, gq);
-    ldg_row_bf16(dk, row, live, gk);
-    ldg_row_bf16(dv, row, live, gv);
-    ldg_row_f32(x, row, live, u);
-    put_ones_block<128>(S.ta, 64);
-    for (int i = tid; i < kC; i += kThreads) { S.g1[i] = ln_g[i]; S.b1[i] = ln_b[i]; }
     const uint32_t ta = smem_u32(S.ta), tbb = smem_u32(S.tb);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * warp) << 16);
-    // rows past the end are zeros, so their columns of the gradient operands are too
-    tst_bf16(tl + 0, gq);
-    tst_bf16(tl + 64, gk);
-    tst_bf16(tl + 128, gv);
-    put_col_bf16<kTR>(tbb, 0, tid, gq);                   // dq^T
-    put_col_bf16<kTR>(tbb, 64, tid, gk);                  // dk^T
-    put_col_bf16<kTR>(tbb, 128, tid, gv);                 // dv^T
-    const float2 st = ln_stats(u);
+    const int row0 = blockIdx.x * kTile, rows = n - row0 < kTile ? n - row0 : kTile;
+    const uint32_t wn = ta, gs = wn + 3 * kC * kC * 4, xs = gs + 3 * kTile * kRow16, hs = xs + kTile * kRow32;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&ctl.ldbar, 3 * kC * kC * 4 + rows * (3 * kRow16 + 2 * kRow32));
+        bulk_load(wn, w_qkv, 3 * kC * kC * 4, &ctl.ldbar);
+        const __nv_bfloat16* src[3] = {dq, dk, dv};
 #pragma unroll
-    for (int i = 0; i < 64; ++i) u[i] = (u[i] - st.x) * st.y;
-    tst(tl + 256, u);                                     // uh
-    put_col<128>(ta, 0, tid, u, live ? 1.f : 0.f);        // uh^T
-    bool ok = operands_ready(true);
-    uint32_t phase = 0;
-    if (warp == 0) {
-        if (elect_one()) {
-            const SmemDesc dw = smem_desc_split(smem_u32(S.w), 16, 256, 6);
-#pragma unroll
-            for (int kk = 0; kk < 24; ++kk)
-                mma_tf32_ts(tb + 192, tb + 8 * kk, desc_at(dw, kk * 64 * 32), idesc_tf32(128, 64), kk > 0);
-            mma_commit(&ctl.bar);
-        }
-        __syncwarp();
+        for (int s = 0; s < 3; ++s) bulk_load(gs + s * kTile * kRow16, src[s] + (size_t)row0 * kC, rows * kRow16, &ctl.ldbar);
+        bulk_load(xs, x + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
+        bulk_load(hs, dh + (size_t)row0 * kC, rows * kRow32, &ctl.ldbar);
     }
-    float d[64];
-    ldg_row_f32(dh, row, live, d);                        // while the product runs
-    ok = mma_wait(ctl, phase, status);
+    for (int i = tid; i < kC; i += kThreads) { S.g1[i] = ln_g[i]; S.b1[i] = ln_b[i]; }
+    bool ok = loads_wait(ctl, status);
+    uint32_t phase = 0;
+    const uint32_t tb = ctl.tbase, tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    RowXch xc{S.xch, 0};
+    uint32_t gq[kHalf / 2], gk[kHalf / 2], gv[kHalf / 2];
+    float u[kHalf], d[kHalf];
     if (ok) {
-        float du[64];
-        tld64(tl + 192, du);
-        put_col<kTR>(tbb, 192, tid, du, 1.f);             // du^T
+        relayout_rows<kC, 3 * kC>(S.w, wn);
+        lds_half_bf16(gs, r, hf, live, gq);
+        lds_half_bf16(gs + kTile * kRow16, r, hf, live, gk);
+        lds_half_bf16(gs + 2 * kTile * kRow16, r, hf, live, gv);
+        lds_half_f32(xs, r, hf, live, u);
+        lds_half_f32(hs, r, hf, live, d);
+    }
+    __syncthreads();                                      // the staged inputs are read: ta and tb are free
+    float2 st = make_float2(0.f, 0.f);
+    if (ok) {
+        put_ones_block<128>(S.ta, 64);
+        // rows past the end are zeros, so their columns of the gradient operands are too
+        tst_bf16(tl + 0 + c0, gq);
+        tst_bf16(tl + 64 + c0, gk);
+        tst_bf16(tl + 128 + c0, gv);
+        put_col_bf16<kTR>(tbb, 0 + c0, r, gq);            // dq^T
+        put_col_bf16<kTR>(tbb, 64 + c0, r, gk);           // dk^T
+        put_col_bf16<kTR>(tbb, 128 + c0, r, gv);          // dv^T
+        st = ln_stats(xc, hf, r, u);
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) u[i] = (u[i] - st.x) * st.y;   // uh
+        put_col<128>(ta, c0, r, u, live ? 1.f : 0.f);     // uh^T
+    }
+    ok = operands_ready(ok);
+    if (ok) {
+        if (warp == 0) {
+            if (elect_one()) {
+                const SmemDesc dw = smem_desc_split(smem_u32(S.w), 16, 256, 6);
+#pragma unroll
+                for (int kk = 0; kk < 24; ++kk)
+                    mma_tf32_ts(tb + 192, tb + 8 * kk, desc_at(dw, kk * 64 * 32), idesc_tf32(128, 64), kk > 0);
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
+        }
+        ok = mma_wait_cta(ctl, phase, status);
+    }
+    const uint32_t dxs = smem_u32(S.w);                   // dx staging (W_qkv is consumed)
+    if (ok) {
+        float du[kHalf];
+        tld32(tl + 192 + c0, du);
+        put_col<kTR>(tbb, 192 + c0, r, du, 1.f);          // du^T
         float m1 = 0.f, m2 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            du[i] *= S.g1[i];
+        for (int i = 0; i < kHalf; ++i) {
+            du[i] *= S.g1[c0 + i];
             m1 += du[i];
             m2 = fmaf(du[i], u[i], m2);
         }
-        m1 *= 1.0f / kC;
-        m2 *= 1.0f / kC;
+        const float2 m = xc.sum(hf, r, make_float2(m1, m2));
+        m1 = m.x * (1.0f / kC);
+        m2 = m.y * (1.0f / kC);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) d[i] += st.y * (du[i] - m1 - u[i] * m2);
-        if (live) stg_f32(dx + (size_t)row * kC, d);
+        for (int i = 0; i < kHalf; ++i) d[i] += st.y * (du[i] - m1 - u[i] * m2);
+        sts_f32x32(dxs, kRow32, r, hf * kHalf * 4, d);
     }
-    ok = operands_ready(ok);
-    if (ok && warp == 0) {
-        if (elect_one()) {
-            const SmemDesc da_ = smem_desc_split(ta, 16, 256, 6), db_ = smem_desc_split(tbb, 16, 256, 6);
+    ok = operands_ready(ok);                              // also makes the dx tile visible to bulk stores
+    if (ok) {
+        if (warp == 0) {
+            if (elect_one()) {
+                const SmemDesc da_ = smem_desc_split(ta, 16, 256, 6), db_ = smem_desc_split(tbb, 16, 256, 6);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)                // [uh | ones]^T [dq | dk | dv | du]
-                mma_ss(tb + 0, desc_at(da_, kk * 128 * 32), desc_at(db_, kk * kTR * 32),
-                       idesc_bf16(128, 256, false, false), kk > 0);
-            mma_commit(&ctl.bar);
+                for (int kk = 0; kk < 8; ++kk)            // [uh | ones]^T [dq | dk | dv | du]
+                    mma_ss(tb + 0, desc_at(da_, kk * 128 * 32), desc_at(db_, kk * kTR * 32),
+                           idesc_bf16(128, 256, false, false), kk > 0);
+                mma_commit(&ctl.bar);
+            }
+            __syncwarp();
         }
-        __syncwarp();
+        if (tid == 0) bulk_store(dx + (size_t)row0 * kC, dxs, rows * kRow32);   // while it runs
+        ok = mma_wait(ctl, phase, status);
     }
-    ok = ok && mma_wait(ctl, phase, status);
-    if (ok && warp == 2) {                                // lane 64: the column sums
+    const uint32_t ps = ta, pvec = ps + 3 * kC * kC * 4;   // dW_qkv rows, then db_qkv | dLN1 gain | shift
+    if (ok && (warp & 3) == 2) {                          // lane 64: the column sums, 128 columns per half
 #pragma unroll 1
-        for (int c = 0; c < 4 * kC; c += 64) {
-            tld64(tl + c, d);
-            if (tid == 64) stg_f32(S.vec + c, d);
+        for (int c = 128 * hf; c < 128 * (hf + 1); c += 32) {
+            float t[32];
+            tld32(tl + c, t);
+            if (r == 64) sts_f32x32(smem_u32(S.vec), 0, r, 4 * c, t);
         }
     }
     ok = __syncthreads_and(ok) != 0;
-    float* pp = part + (size_t)blockIdx.x * kPartStride;
     if (ok) {
-        // partial layout: dW_qkv (64 x 192), db_qkv (192), dLN1 gain, shift
-        if (tid < 64) {
-            const float gm = S.g1[tid], bm = S.b1[tid];
+        if (r < 64) {
+            const float gm = S.g1[r], bm = S.b1[r];
 #pragma unroll 1
-            for (int c = 0; c < 3 * kC; c += 64) {
-                tld64(tl + c, d);
+            for (int c = 3 * kHalf * hf; c < 3 * kHalf * (hf + 1); c += 32) {
+                float t[32];
+                tld32(tl + c, t);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) d[j] = fmaf(gm, d[j], bm * S.vec[c + j]);
-                stg_f32(pp + tid * 3 * kC + c, d);
+                for (int j = 0; j < 32; ++j) t[j] = fmaf(gm, t[j], bm * S.vec[c + j]);
+                sts_f32x32(ps, 3 * kC * 4, r, 4 * c, t);
             }
-            tld64(tl + 192, d);
-            pp[3 * kC * kC + 3 * kC + tid] = pick(d, tid);   // dLN1 gain: the diagonal of uh^T du
+            float t[32];
+            tld32(tl + 192 + c0, t);
+            if ((r >> 5) == hf) st_shared_f32(pvec + 4 * (3 * kC + r), pick(t, r - c0));   // gain: diag of uh^T du
         } else {
-            const int f = tid - 64;
-#pragma unroll
-            for (int c = 0; c < 3; ++c) pp[3 * kC * kC + 64 * c + f] = S.vec[64 * c + f];   // db_qkv
-            pp[3 * kC * kC + 4 * kC + f] = S.vec[192 + f];                                 // dLN1 shift
+            const int f = r - 64;
+            if (hf == 0) {
+                st_shared_f32(pvec + 4 * f, S.vec[f]);                    // db_qkv 0..63
+                st_shared_f32(pvec + 4 * (kC + f), S.vec[kC + f]);        // db_qkv 64..127
+            } else {
+                st_shared_f32(pvec + 4 * (2 * kC + f), S.vec[2 * kC + f]);   // db_qkv 128..191
+                st_shared_f32(pvec + 4 * (4 * kC + f), S.vec[3 * kC + f]);   // dLN1 shift
+            }
         }
+    }
+    ok = __syncthreads_and(ok) != 0;
+    staged_ready();
+    if (tid == 0) {
+        if (ok) bulk_store(part + (size_t)blockIdx.x * kPartStride, ps, kPartStride * 4);
+        bulk_store_drain();                               // the dx tile too
     }
     ctl_finish(ctl, ok, phase, kQkvBwdCols);
 }
@@ -989,6 +1218,8 @@ int gt_layer_fwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     using namespace gt;
     if (h != 8 || d != 8 || f != kF) return GT_ERR_UNSUPPORTED;
     if (n < 1 || !x || !gt::weights_ok(w) || !q || !k || !v || !o || !lse || !y) return GT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(y))
+        return GT_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
@@ -1022,6 +1253,9 @@ int gt_layer_bwd(int32_t n, int32_t h, int32_t d, int32_t f, const float* x, con
     if (h != 8 || d != 8 || f != kF) return GT_ERR_UNSUPPORTED;
     if (n < 1 || !x || !gt::weights_ok(w) || !gt::grads_ok(g) || !q || !k || !v || !o || !lse || !dy || !dx ||
         !dT)
+        return GT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dy) ||
+        !aligned16(dx))
         return GT_ERR_INVALID_ARG;
     LayerBwdWs ws;
     const size_t need = layer_bwd_carve(n, workspace, ws_bytes, &ws);

@@ -274,11 +274,15 @@ int gt_bias_attn_bwd_noalloc(int32_t dtype, int32_t n, int32_t h, int32_t d,
  * features of a node, GELU(a) = a Phi(a) (Phi the normal CDF), the attention
  * scale 1/sqrt(8), and q, k, v split into heads as [n][8][8] (feature = head * 8
  * + channel).  Supported: h = 8, d = 8, f = 64 (else GT_ERR_UNSUPPORTED); the
- * attention runs in bf16 on the tensor cores.
+ * attention runs in bf16 on the tensor cores, and so do the layer's products:
+ * tf32 (fp32 storage) for the projections and the FFN, bf16 for the products
+ * over node rows that form the weight gradients, fp32 accumulation in both.
  *
  * All weights are device fp32, row-major: ln*_g / ln*_b [64]; w_qkv [64][192]
  * (columns q | k | v); b_qkv [192]; w_o [64][64]; b_o [64]; w_1 [64][64] (in x
- * out); b_1 [64]; w_2 [64][64]; b_2 [64]; the four matrices 16-byte aligned.
+ * out); b_1 [64]; w_2 [64][64]; b_2 [64]; the four matrices 16-byte aligned,
+ * and so every node-row array (x, y, dy, dx, q, k, v, o): the layer kernels move
+ * whole rows with bulk copies.
  * gt_layer_grads has the same shapes and receives dL/d(weight) (overwritten).
  */
 typedef struct {
