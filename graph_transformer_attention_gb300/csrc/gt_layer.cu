@@ -8,13 +8,16 @@
 // (LayerNorm before each sublayer, GELU(a) = a Phi(a): the Graphormer encoder
 // layer; the pages give the widths, not the order of the steps.)
 //
-// Four tile kernels, one CTA of 128 threads per 128 node rows, thread r = node
-// row r of the tile = TMEM lane r.  Every product with a layer matrix is a
-// tcgen05.mma (M = 128 node rows): the activation row goes into TMEM as the A
-// operand (tf32, fp32 storage), the matrix sits in shared memory as the B
-// operand, the fp32 accumulator comes back with tcgen05.ld, and the thread does
-// the LayerNorms, GELU, residuals and the LayerNorm backward on its own row in
-// registers:
+// Four tile kernels, one CTA of 256 threads per 128 node rows; row r of the tile
+// is TMEM lane r, and threads r and r + 128 (warps w and w + 4, which reach the
+// same lanes) each take half of its 64 features.  Every product with a layer
+// matrix is a tcgen05.mma (M = 128 node rows): the activation rows go into TMEM
+// as the A operand (tf32, fp32 storage), the matrix sits in shared memory as the
+// B operand, the fp32 accumulator comes back with tcgen05.ld, and the threads do
+// the LayerNorms (row sums passed between the two halves), GELU, residuals and
+// the LayerNorm backward in registers.  Tiles of node rows and the weight
+// matrices move between global and shared memory as whole-tile bulk copies on
+// the TMA engine:
 //   layer_ln_qkv    x -> LN1 -> u W_qkv + b -> q, k, v (bf16, the attention's inputs)
 //   layer_out_ffn   o, x -> hh -> LN2 -> FFN -> y
 //   layer_ffn_bwd   dy, and hh, z, a, GELU(a) recomputed from x and o -> dO for
