@@ -834,15 +834,15 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                     any |= nw[r];
                 }
                 if (nw[0] | nw[1] | nw[2] | nw[3]) {
+                    // the level's bits are new, so the slices take them with
+                    // reductions (no read, no wait on L2); the output pass reads
+                    // the slices at L2
                     for (int k = 0; k < nslices; ++k) {
                         if (!((level >> k) & 1)) continue;
                         uint32_t* dk = db + (size_t)k * nwp;
-                        uint32_t old[kUpdateWords];
-#pragma unroll
-                        for (int r = 0; r < kUpdateWords; ++r) old[r] = nw[r] ? dk[p0 + r * blockDim.x] : 0u;
 #pragma unroll
                         for (int r = 0; r < kUpdateWords; ++r)
-                            if (nw[r]) dk[p0 + r * blockDim.x] = old[r] | nw[r];
+                            if (nw[r]) atomicOr(dk + p0 + r * blockDim.x, nw[r]);
                     }
                 }
             }
@@ -921,7 +921,7 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int v = v0 + t;
-                    dw[t][k] = k < nslices ? (db[(size_t)k * nwp + SW::word(v)] >> SW::shift(v)) & SW::MASK : 0u;
+                    dw[t][k] = k < nslices ? (__ldcg(db + (size_t)k * nwp + SW::word(v)) >> SW::shift(v)) & SW::MASK : 0u;
                 }
             }
             for (int b0 = 0; b0 < nsrc; b0 += 4) {
