@@ -687,8 +687,10 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                         const uint32_t ww = (fr[SW::word(r)] >> SW::shift(r)) & SW::MASK;
                         if (ww) {
                             atomicOr(&acc[SW::word(u)], ww << SW::shift(u));
-                            umin = min(umin, u);
-                            umax = max(umax, u);
+                            if (!whole) {                 // the range can still grow
+                                umin = min(umin, u);
+                                umax = max(umax, u);
+                            }
                         }
                     }
                 }
@@ -919,9 +921,12 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
 #pragma unroll
             for (int k = 0; k < 7; ++k) {
 #pragma unroll
+                for (int t = 0; t < 4; ++t) dw[t][k] = 0u;
+                if (k >= nslices) continue;              // uniform: the slices past the count cost nothing
+#pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int v = v0 + t;
-                    dw[t][k] = k < nslices ? (__ldcg(db + (size_t)k * nwp + SW::word(v)) >> SW::shift(v)) & SW::MASK : 0u;
+                    dw[t][k] = (__ldcg(db + (size_t)k * nwp + SW::word(v)) >> SW::shift(v)) & SW::MASK;
                 }
             }
             for (int b0 = 0; b0 < nsrc; b0 += 4) {
@@ -930,8 +935,10 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
                 for (int t = 0; t < 4; ++t) {
                     uint32_t code4 = 0u;
 #pragma unroll
-                    for (int k = 0; k < 7; ++k)
-                        if (k < nslices) code4 |= spread4((dw[t][k] >> b0) & 0xfu) << k;
+                    for (int k = 0; k < 7; ++k) {
+                        if (k >= nslices) break;                 // uniform
+                        code4 |= spread4((dw[t][k] >> b0) & 0xfu) << k;
+                    }
                     const uint32_t m = spread4((vw[t] >> b0) & 0xfu) * 0xffu;
                     uint32_t fill4;
                     if (csrc >= 0) {
