@@ -29,7 +29,7 @@ def _rel(a, b):
 
 
 @pytest.mark.parametrize("n,graph,D", [(300, "ba", 6), (1000, "dba", 12), (2049, "er", 5), (1, "empty", 3),
-                                       (129, "path", 4)])
+                                       (129, "path", 4), (128, "path", 5), (256, "er", 4), (383, "ba", 5)])
 def test_layer_forward_and_backward_match_the_oracle(gt, n, graph, D):
     if graph == "empty":
         g = gi.csr_from_edges(n, np.zeros(0, np.int64), np.zeros(0, np.int64))
