@@ -64,6 +64,18 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.gt_layer_fwd(100, 8, 8, 64, fake, None, fake, 112, fake, 8, fake, fake, fake, fake, fake, fake,
                             fake, 1 << 20, None) == -1
     assert lib.gt_layer_workspace_size(100, 8, 16, 64) == 0 and lib.gt_layer_workspace_size(100, 8, 8, 64) > 0
+    # GT layer: node-row arrays must be 16-byte aligned (whole tiles move by bulk copies)
+    class Twelve(ctypes.Structure):
+        _fields_ = [(f"p{i}", P) for i in range(12)]
+    wts = Twelve(*([fake] * 12))
+    grads = Twelve(*([fake] * 12))
+    odd = P(0x1004)
+    assert lib.gt_layer_fwd(100, 8, 8, 64, odd, ctypes.byref(wts), fake, 112, fake, 8, fake, fake, fake, fake,
+                            fake, fake, fake, 1 << 20, None) == -1
+    assert lib.gt_layer_fwd(100, 8, 8, 64, fake, ctypes.byref(wts), fake, 112, fake, 8, fake, fake, fake, fake,
+                            fake, odd, fake, 1 << 20, None) == -1
+    assert lib.gt_layer_bwd(100, 8, 8, 64, fake, ctypes.byref(wts), fake, 112, fake, 8, fake, fake, fake, fake,
+                            fake, odd, fake, ctypes.byref(grads), fake, fake, 1 << 20, None) == -1
     # bounded-wait self-test: limits out of range
     assert lib.gt_selftest_wait_timeout(ctypes.c_int64(10), None) == -1
     assert lib.gt_selftest_wait_timeout(ctypes.c_int64(2_000_000_000), None) == -1
