@@ -599,12 +599,14 @@ def run_layer(args, w: gi.Workload, rank: int, world: int) -> dict | None:
         "metric": LAYER_METRIC, "value": round(whole_job_tflops(flops, args.steps, ms_total, world), 3),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 attention, fp32 around it",
+        "vs_baseline": None,
+        "dtype": "bf16 attention; tf32 projections and bf16 weight-gradient products around it, fp32 accumulation",
         "data": "synthetic (seeded random graph, weights, x and dy)",
         "config": {**workload_config(w), "model": "GT encoder layer, 8 heads, hidden 64, FFN 64"},
         "kernels_ms": {k: {"launches_per_step": round(v["launches_per_step"], 3),
                            "ms_per_launch": round(v["ms_per_launch"], 4)} for k, v in kernels.items()},
         "around_attention_ms_per_step": round(sum(per_step.get(k, 0.0) for k in around), 4),
+        "around_attention_ms_per_layer": round(sum(per_step.get(k, 0.0) for k in around) / w.layers, 4),
         "gpu_launches": int(launches), "clocks": clk.summary(),
     }
 
