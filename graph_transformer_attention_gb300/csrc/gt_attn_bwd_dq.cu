@@ -430,7 +430,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     for (int hh = 0; hh < 4; ++hh) {
                         const float2 ml = wuni ? make_float2(0.f, 0.f) : make_float2(-L2[hh], -L2[hh]);
                         const float2 md = make_float2(-Dh[hh], -Dh[hh]);
-                        float2 sum = make_float2(0.f, 0.f);
                         uint32_t pk[4];
 #pragma unroll
                         for (int k = 0; k < 8; k += 2) {
@@ -442,10 +441,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             const float2 ds = __fmul2_rn(p, dv);
                             rd[hh][k] = __float_as_uint(ds.x);
                             rd[hh][k + 1] = __float_as_uint(ds.y);
-                            sum = __fadd2_rn(sum, ds);
                             pk[k / 2] = pack_bf16x2(ds.x, ds.y);
                         }
-                        if (uniform) acc[hh] += sum.x + sum.y;
+                        if (uniform) {      // the row's sum for its register bin (mixed rows bin each element)
+                            float2 sum = make_float2(__uint_as_float(rd[hh][0]), __uint_as_float(rd[hh][1]));
+#pragma unroll
+                            for (int k = 2; k < 8; k += 2)
+                                sum = __fadd2_rn(sum, make_float2(__uint_as_float(rd[hh][k]), __uint_as_float(rd[hh][k + 1])));
+                            acc[hh] += sum.x + sum.y;
+                        }
                         tmem_st_x4(lrow + s_col(ss) + 16 * hh + 4 * g, pk);
                     }
                     if (!uniform) {
