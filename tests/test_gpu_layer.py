@@ -29,7 +29,8 @@ def _rel(a, b):
 
 
 @pytest.mark.parametrize("n,graph,D", [(300, "ba", 6), (1000, "dba", 12), (2049, "er", 5), (1, "empty", 3),
-                                       (129, "path", 4), (128, "path", 5), (256, "er", 4), (383, "ba", 5)])
+                                       (129, "path", 4), (128, "path", 5), (256, "er", 4), (383, "ba", 5),
+                                       (6800, "ba6800", 20)])
 def test_layer_forward_and_backward_match_the_oracle(gt, n, graph, D):
     if graph == "empty":
         g = gi.csr_from_edges(n, np.zeros(0, np.int64), np.zeros(0, np.int64))
@@ -37,6 +38,8 @@ def test_layer_forward_and_backward_match_the_oracle(gt, n, graph, D):
         g = gi.csr_from_edges(n, np.arange(n - 1), np.arange(1, n))
     elif graph == "ba":
         g = gi.barabasi_albert(n, 3, seed=21)
+    elif graph == "ba6800":
+        g = gi.config_graph(gi.CONFIGS[3])      # one layer of the 16-layer workload, full size
     elif graph == "dba":
         g = gi.disjoint_ba(4, n // 4, 2, seed=22)
     else:
