@@ -87,6 +87,8 @@ def load_library():
         lib.gt_bias_attn_workspace_size.restype = sz
         lib.gt_bias_attn_fwd_kv_block.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_fwd_kv_block.restype = i32
+        lib.gt_bias_attn_fwd_ctas.argtypes = [i32, i32, i32, i32, i32]
+        lib.gt_bias_attn_fwd_ctas.restype = i32
         lib.gt_bias_attn_bwd_split.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_bwd_split.restype = i32
         lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
@@ -162,8 +164,9 @@ def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0, nb:
     code = GT_F32 if dtype == "f32" else GT_BF16
     kvb = int(lib.gt_bias_attn_fwd_kv_block(code, n, h, d, kv_block))
     nsplit = -(-n // kvb) if kvb > 0 else 1
+    balanced = int(lib.gt_bias_attn_fwd_ctas(code, n, h, d, kv_block)) > 0
     split = int(lib.gt_bias_attn_bwd_split(code, n, h, d, nb))
-    return {"fwd": 1 + (1 if nsplit > 1 else 0), "bwd": 4 + (1 if split > 1 else 0)}
+    return {"fwd": 1 + (1 if nsplit > 1 or balanced else 0), "bwd": 4 + (1 if split > 1 else 0)}
 
 
 def gt_status_string(status: int) -> str:

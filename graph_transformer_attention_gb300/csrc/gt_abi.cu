@@ -20,6 +20,8 @@ int attn_fwd_simt(int dtype, int n, int h, int d, const void* q, const void* k, 
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale, int kv_block,
                   void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s);
 bool fwd_tc_supported(int h, int d);
+size_t fwd_tc_piece_floats(int n, int d);
+int fwd_tc_balanced_ctas(int n);
 int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
                 int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
                 float* o_part, float* lse_part, cudaStream_t s);
@@ -86,28 +88,21 @@ struct BwdWs {
     float* acc;     // split backward: fp32 dq, dk, dv accumulators, else null
 };
 
-// The KV block the forward uses.  An explicit kv_block is kept; with 0 the
-// tensor-core path splits the KV columns itself when the graph has too few
-// 128-row tiles to give every SM two CTAs (grid = tiles x 2 head halves x
-// splits), and merges the partials exactly: up to 4 splits, each a multiple of
-// 128 columns.
-int effective_kv_block(int dtype, int n, int h, int d, int kv_block) {
-    if (kv_block > 0 || dtype != GT_BF16 || !fwd_tc_supported(h, d)) return kv_block;
-    const int ctas = 2 * ((n + 127) / 128);
-    int nsplit = 2 * num_sms() / ctas;
-    if (nsplit > 4) nsplit = 4;
-    if (nsplit < 2) return 0;
-    const int per = ((n + nsplit - 1) / nsplit + 127) / 128 * 128;
-    return per >= n ? 0 : per;
-}
+// The KV block the forward uses: an explicit kv_block is kept (uniform splits
+// merged exactly); with 0 the tensor-core path balances its work over a whole
+// number of waves itself (balance_for) and needs no uniform split.
+int effective_kv_block(int dtype, int n, int h, int d, int kv_block) { return kv_block; }
 
-size_t fwd_ws(int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
+size_t fwd_ws(int dtype, int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
     Carve c(base, cap);
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
     FwdWs w{nullptr, nullptr};
     if (nsplit > 1) {
         w.o_part = c.take<float>((size_t)nsplit * n * h * d);
         w.lse_part = c.take<float>((size_t)nsplit * h * n);
+    } else if (dtype == GT_BF16 && fwd_tc_supported(h, d)) {
+        const size_t f = fwd_tc_piece_floats(n, d);
+        if (f) w.o_part = c.take<float>(f);
     }
     if (out) *out = w;
     return c.off;
@@ -199,7 +194,7 @@ int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64
 size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
-    size_t a = gt::fwd_ws(n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
+    size_t a = gt::fwd_ws(dtype, n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
     const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1;
     size_t b = gt::bwd_ws(n, h, d, acc, nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
@@ -216,6 +211,13 @@ int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d
     return gt::effective_kv_block(dtype, n, h, d, kv_block);
 }
 
+int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
+    if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return -1;
+    if (kv_block >= n) kv_block = 0;
+    if (kv_block > 0 || dtype != GT_BF16 || !gt::fwd_tc_supported(h, d)) return 0;
+    return gt::fwd_tc_balanced_ctas(n);
+}
+
 int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,
                      const void* v, const int8_t* spd, int64_t ld_spd, const float* T, int32_t nb,
                      float scale, int32_t kv_block, void* o, float* lse, void* workspace,
@@ -226,10 +228,10 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     if (kv_block < 0 || (kv_block > 0 && kv_block % 128 != 0)) return GT_ERR_INVALID_ARG;
     if (kv_block >= n) kv_block = 0;
     kv_block = gt::effective_kv_block(dtype, n, h, d, kv_block);
-    const size_t need = gt::fwd_ws(n, h, d, kv_block, nullptr, 0, nullptr);
+    const size_t need = gt::fwd_ws(dtype, n, h, d, kv_block, nullptr, 0, nullptr);
     if (need > 0 && (!workspace || ws_bytes < need)) return GT_ERR_WORKSPACE;
     gt::FwdWs w;
-    gt::fwd_ws(n, h, d, kv_block, workspace, ws_bytes, &w);
+    gt::fwd_ws(dtype, n, h, d, kv_block, workspace, ws_bytes, &w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::fwd_tc_supported(h, d))
         return gt::attn_fwd_tc(n, d, q, k, v, spd, ld_spd, T, nb, scale, kv_block, o, lse, w.o_part,

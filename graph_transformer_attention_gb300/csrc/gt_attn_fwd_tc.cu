@@ -55,7 +55,8 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int kHC = 4;                  // heads per CTA
-constexpr int kCtasPerSm = kH / kHC;
+constexpr int kCtasPerSm = 2;
+constexpr int kHalves = kH / kHC;       // head groups: tasks per query tile
 constexpr int kBQ = 128;
 constexpr int kBKV = 64;
 constexpr int kCH = 32;                 // KV columns per MMA chunk
@@ -79,8 +80,9 @@ struct Cfg {
     static constexpr uint32_t SPD_BYTES = kBQ * kBKV;
     static constexpr uint32_t SLOT_BYTES = kBKV * 32;
     static constexpr uint32_t STAGE_BYTES = SPD_BYTES + 2 * NSLOT * SLOT_BYTES;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_STAGE = Q_BYTES;
+    static constexpr uint32_t OFF_Q = 0;                  // Q of the first piece
+    static constexpr uint32_t OFF_Q2 = Q_BYTES;           // Q of the second piece (balanced grid)
+    static constexpr uint32_t OFF_STAGE = 2 * Q_BYTES;
     static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
     static constexpr uint32_t T_BYTES = 256 * kH * 4;
     static constexpr uint32_t OFF_BAR = OFF_T + T_BYTES;
@@ -105,6 +107,40 @@ __device__ __forceinline__ void fail(Bars* bars, int* status) {
 }
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// One stretch of a CTA's work: query tile i0, head half hb, KV columns
+// [j_begin, j_end) in nblocks blocks.  part < 0: the stretch is the task's whole
+// KV range and its rows go to o and lse; else they go to partial slot `part`.
+struct Seg {
+    int i0, hb, j_begin, j_end, nblocks, part;
+};
+
+// Stretch si of this CTA.  Plain grid (bl.ctas == 0): one stretch, tile
+// blockIdx.x, head half blockIdx.z, KV split blockIdx.y of kv_block columns.
+// Balanced grid: task = head half * tiles + tile, nblk blocks of kBKV columns.
+__device__ __forceinline__ bool seg_of(const Balance& bl, int si, int kv_begin, int kv_end, int kv_block,
+                                       int parts, Seg& sg) {
+    if (bl.ctas == 0) {
+        if (si > 0) return false;
+        sg.i0 = blockIdx.x * kBQ;
+        sg.hb = blockIdx.z;
+        sg.j_begin = kv_begin + (kv_block > 0 ? (int)blockIdx.y * kv_block : 0);
+        sg.j_end = kv_block > 0 ? min(kv_end, sg.j_begin + kv_block) : kv_end;
+        sg.nblocks = (sg.j_end - sg.j_begin + kBKV - 1) / kBKV;
+        sg.part = parts ? (int)blockIdx.y : -1;
+        return true;
+    }
+    Piece p;
+    if (!piece_of(bl, blockIdx.x, si, p)) return false;
+    const int tiles = bl.tasks / kHalves;
+    sg.i0 = (p.task % tiles) * kBQ;
+    sg.hb = p.task / tiles;
+    sg.j_begin = kv_begin + p.b0 * kBKV;
+    sg.j_end = min(kv_end, kv_begin + p.b1 * kBKV);
+    sg.nblocks = p.b1 - p.b0;
+    sg.part = (p.b0 == 0 && p.b1 == bl.nblk) ? -1 : 2 * (int)blockIdx.x + si;
+    return true;
+}
 
 // x = s * scale * log2(e) + T[h][code] * log2(e) for 4 heads and the 16 columns of
 // half g of a chunk, in place over the raw S bits; one 16-byte load per code
@@ -205,7 +241,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const float* __restrict__ T, int nb, int n, float scale_log2, int kv_begin, int kv_end,
               int kv_block, int parts, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
               float* __restrict__ o_part,
-              float* __restrict__ lse_part, int* status) {
+              float* __restrict__ lse_part, const Balance bal, int* status) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -213,13 +249,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i0 = blockIdx.x * kBQ;
-    const int split = blockIdx.y;
-    const int hb = blockIdx.z;                 // heads kHC hb .. kHC hb + kHC - 1
-    // KV columns [kv_begin, kv_end), cut into grid.y splits of kv_block columns
-    const int j_begin = kv_begin + (kv_block > 0 ? split * kv_block : 0);
-    const int j_end = kv_block > 0 ? min(kv_end, j_begin + kv_block) : kv_end;
-    const int nblocks = (j_end - j_begin + kBKV - 1) / kBKV;
+    // this CTA's one or two stretches (heads kHC hb .. kHC hb + kHC - 1 of each)
+    Seg sg0, sg1;
+    seg_of(bal, 0, kv_begin, kv_end, kv_block, parts, sg0);
+    const int nseg = seg_of(bal, 1, kv_begin, kv_end, kv_block, parts, sg1) ? 2 : 1;
+    const int nblocks0 = sg0.nblocks;
+    const int nblocks = nblocks0 + (nseg > 1 ? sg1.nblocks : 0);
+    const int nchunks0 = nblocks0 * kNCH;
     const int nchunks = nblocks * kNCH;
 
     if (tid == kTmaWarp * 32) {
@@ -245,11 +281,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         Ts[x] = code < nb ? T[h * nb + code] * kLog2e : 0.f;
     }
     // per-head Q operands of this CTA's heads: [128 rows][16] bf16, 32-byte swizzle, K-major
-    if (tid < kBQ) {
-        const int row = i0 + tid;
+    // (threads 0-127 the first stretch's tile, 128-255 the second's)
+    if (tid < kBQ || (nseg > 1 && tid < 2 * kBQ)) {
+        const Seg& sg = tid < kBQ ? sg0 : sg1;
+        const int rr = tid & (kBQ - 1);
+        const int row = sg.i0 + rr;
         const bool live = row < n;
-        write_head_operands<HD, kHC>(smem + C::OFF_Q, tid, q + (int64_t)(live ? row : 0) * kH * HD, live,
-                                     kHC * hb);
+        write_head_operands<HD, kHC>(smem + (tid < kBQ ? C::OFF_Q : C::OFF_Q2), rr,
+                                     q + (int64_t)(live ? row : 0) * kH * HD, live, kHC * sg.hb);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before();
@@ -269,8 +308,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     fail(bars, status);
                     break;
                 }
+                const bool second = b >= nblocks0;
+                const int i0 = second ? sg1.i0 : sg0.i0;
+                const int hb = second ? sg1.hb : sg0.hb;
                 uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                const int j0 = j_begin + b * kBKV;
+                const int j0 = second ? sg1.j_begin + (b - nblocks0) * kBKV : sg0.j_begin + b * kBKV;
                 mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
                 tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
 #pragma unroll
@@ -299,6 +341,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             const uint32_t idPV = idesc_bf16(128, 16, false, true);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
             const SmemDesc dQ = smem_desc_split(smem_u32(smem + C::OFF_Q), 16, 256, 6);
+            const SmemDesc dQ2 = smem_desc_split(smem_u32(smem + C::OFF_Q2), 16, 256, 6);
             const SmemDesc dKk = smem_desc_split(stage_base + C::SPD_BYTES, 16, 256, 6);     // K-major K
             const SmemDesc dVm = smem_desc_split(stage_base + C::SPD_BYTES, 256, 256, 6);    // MN-major V
             bool ok = true;
@@ -318,7 +361,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
                     for (int h = 0; h < kHC; ++h) {
                         const int slot = h * HD / 16;
-                        mma_ss(tbase + kColS + kCH * h, desc_at(dQ, h * 4096),
+                        mma_ss(tbase + kColS + kCH * h, desc_at(tt < nchunks0 ? dQ : dQ2, h * 4096),
                                desc_at(dKk, koff(tt) + slot * C::SLOT_BYTES), idQK, 0);
                     }
                     mma_commit(&bars->s_full);
@@ -341,7 +384,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         for (int st = 0; st < 2; ++st)
                             mma_ts(tbase + kColO + 16 * h, tbase + kColP + 16 * h + 8 * st,
                                    desc_at(dVm, voff + slot * C::SLOT_BYTES + 512 * st), idPV,
-                                   (tt > 0 || st > 0) ? 1u : 0u);
+                                   ((tt != 0 && tt != nchunks0) || st > 0) ? 1u : 0u);
                     }
                     mma_commit(&bars->pv_done);
                     if (c == kNCH - 1) mma_commit(&bars->kv_empty[ks]);
@@ -363,199 +406,205 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
         const int hl0 = kNH * (tid >> 7);        // this thread's first head among the CTA's
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 4u * (kHC * hb + hl0);   // 32-byte rows of 8 head biases
-        float m[kNH], l[kNH];
-#pragma unroll
-        for (int h = 0; h < kNH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
-        int t = 0;
+        int t = 0, bg = 0;   // chunks and KV blocks so far: the mbarrier phases
         bool ok = true;
-        int uni_skip = 0;   // half chunks left before the next uniformity vote (warp-uniform)
-        for (int b = 0; ok && b < nblocks; ++b) {
-            const int ks = b & 1;
-            if (!mbar_wait(&bars->kv_full[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * kBKV;
-            const int j0 = j_begin + b * kBKV;
-            const bool tail_block = j0 + kBKV > j_end;
-            for (int c = 0; c < kNCH; ++c, ++t) {
-                if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-                // codes of the 32 columns: two 16-byte chunks of the row (64-byte swizzle)
-                const uint32_t swz = (uint32_t)((r >> 1) & 3);
-                const uint4 c0 = lds_u4(sp + (((uint32_t)(2 * c) ^ swz) << 4));
-                const uint4 c1 = lds_u4(sp + (((uint32_t)(2 * c + 1) ^ swz) << 4));
-                const int jc = j0 + c * kCH;
-                if (t == 0) {
-                    // the first chunk sets the running maximum exactly (both halves)
+        for (int si = 0; ok && si < nseg; ++si) {
+            const Seg sg = si ? sg1 : sg0;
+            const uint32_t tbl = smem_u32(Ts) + 4u * (kHC * sg.hb + hl0);   // 32-byte rows of 8 head biases
+            float m[kNH], l[kNH];
 #pragma unroll
+            for (int h = 0; h < kNH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+            const int t0 = t;    // the stretch's first chunk
+            int uni_skip = 0;    // half chunks left before the next uniformity vote (warp-uniform)
+            for (int b = 0; ok && b < sg.nblocks; ++b, ++bg) {
+                const int ks = bg & 1;
+                if (!mbar_wait(&bars->kv_full[ks], (bg >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * kBKV;
+                const int j0 = sg.j_begin + b * kBKV;
+                const bool tail_block = j0 + kBKV > sg.j_end;
+                for (int c = 0; c < kNCH; ++c, ++t) {
+                    if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    // codes of the 32 columns: two 16-byte chunks of the row (64-byte swizzle)
+                    const uint32_t swz = (uint32_t)((r >> 1) & 3);
+                    const uint4 c0 = lds_u4(sp + (((uint32_t)(2 * c) ^ swz) << 4));
+                    const uint4 c1 = lds_u4(sp + (((uint32_t)(2 * c + 1) ^ swz) << 4));
+                    const int jc = j0 + c * kCH;
+                    if (t == t0) {
+                        // the first chunk sets the running maximum exactly (both halves)
+    #pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            uint32_t sx[kNH][16];
+    #pragma unroll
+                            for (int hh = 0; hh < kNH; ++hh)
+                                tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
+                            tmem_wait_ld();
+                            score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+    #pragma unroll
+                            for (int hh = 0; hh < kNH; ++hh)
+    #pragma unroll
+                                for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
+                        }
+                    }
+                    // P and O must not be touched before the previous chunk's PV is done with
+                    // them; the wait is put off until the first write, so that the S loads and
+                    // the first half's exponentials overlap that PV
+                    bool pv_waited = t == t0;
+                    auto wait_pv = [&]() {
+                        if (pv_waited) return;
+                        if (!mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+                        tc_fence_after();
+                        pv_waited = true;
+                    };
+    #pragma unroll
                     for (int g = 0; g < 2; ++g) {
                         uint32_t sx[kNH][16];
-#pragma unroll
+    #pragma unroll
                         for (int hh = 0; hh < kNH; ++hh)
                             tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
                         tmem_wait_ld();
-                        score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
-                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
-#pragma unroll
-                        for (int hh = 0; hh < kNH; ++hh)
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) m[hh] = fmaxf(m[hh], __uint_as_float(sx[hh][k]));
-                    }
-                }
-                // P and O must not be touched before the previous chunk's PV is done with
-                // them; the wait is put off until the first write, so that the S loads and
-                // the first half's exponentials overlap that PV
-                bool pv_waited = t == 0;
-                auto wait_pv = [&]() {
-                    if (pv_waited) return;
-                    if (!mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
-                    tc_fence_after();
-                    pv_waited = true;
-                };
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t sx[kNH][16];
-#pragma unroll
-                    for (int hh = 0; hh < kNH; ++hh)
-                        tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
-                    tmem_wait_ld();
-                    if (g == 1) {
-                        tc_fence_before();
-                        mbar_arrive(&bars->s_free);      // S is consumed: the next QK^T may start
-                    }
-                    // exponentials of all heads first (independent chains), one vote on
-                    // whether any head of any row needs a redo against a new maximum
-                    uint32_t pk[kNH][8];
-                    float ls[kNH];
-                    bool need = false;
-                    const uint4 cw = g ? c1 : c0;
-                    const uint32_t code0 = cw.x & 0xffu;
-                    bool wuni = false;
-                    if (uni_skip > 0) {
-                        --uni_skip;
-                    } else if (t > 0) {
-                        const bool uni = cw.x == code0 * 0x01010101u && cw.y == cw.x && cw.z == cw.x && cw.w == cw.x;
-                        wuni = __all_sync(0xffffffffu, uni);
-                        // after a failed vote the warp votes again 16 half chunks (256
-                        // columns) later: where codes are mixed the vote seldom succeeds, and
-                        // the mixed columns of a graph of small components come in runs
-                        if (!wuni) uni_skip = 16;
-                    }
-                    if (wuni) {
-                        float bb[kNH];
-                        load_bias<kNH>(tbl + code0 * 32u, bb);
-                        score16_shifted<kNH>(sx, bb, m, scale_log2);
-                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
-#pragma unroll
-                        for (int hh = 0; hh < kNH; ++hh) {
-                            ls[hh] = exp_pack16_shifted(sx[hh], pk[hh]);
-                            need |= !(ls[hh] <= kRedoSum);
+                        if (g == 1) {
+                            tc_fence_before();
+                            mbar_arrive(&bars->s_free);      // S is consumed: the next QK^T may start
                         }
-                    } else {
-                        score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
-                        if (tail_block) mask16<kNH>(sx, jc + 16 * g, j_end);
-#pragma unroll
-                        for (int hh = 0; hh < kNH; ++hh) {
-                            ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
-                            need |= !(ls[hh] <= kRedoSum);
+                        // exponentials of all heads first (independent chains), one vote on
+                        // whether any head of any row needs a redo against a new maximum
+                        uint32_t pk[kNH][8];
+                        float ls[kNH];
+                        bool need = false;
+                        const uint4 cw = g ? c1 : c0;
+                        const uint32_t code0 = cw.x & 0xffu;
+                        bool wuni = false;
+                        if (uni_skip > 0) {
+                            --uni_skip;
+                        } else if (t > t0) {
+                            const bool uni = cw.x == code0 * 0x01010101u && cw.y == cw.x && cw.z == cw.x && cw.w == cw.x;
+                            wuni = __all_sync(0xffffffffu, uni);
+                            // after a failed vote the warp votes again 16 half chunks (256
+                            // columns) later: where codes are mixed the vote seldom succeeds, and
+                            // the mixed columns of a graph of small components come in runs
+                            if (!wuni) uni_skip = 16;
                         }
-                    }
-                    if (__any_sync(0xffffffffu, need)) {
+                        if (wuni) {
+                            float bb[kNH];
+                            load_bias<kNH>(tbl + code0 * 32u, bb);
+                            score16_shifted<kNH>(sx, bb, m, scale_log2);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+    #pragma unroll
+                            for (int hh = 0; hh < kNH; ++hh) {
+                                ls[hh] = exp_pack16_shifted(sx[hh], pk[hh]);
+                                need |= !(ls[hh] <= kRedoSum);
+                            }
+                        } else {
+                            score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+    #pragma unroll
+                            for (int hh = 0; hh < kNH; ++hh) {
+                                ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
+                                need |= !(ls[hh] <= kRedoSum);
+                            }
+                        }
+                        if (__any_sync(0xffffffffu, need)) {
+                            wait_pv();
+    #pragma unroll
+                            for (int hh = 0; hh < kNH; ++hh) {
+                                if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
+                                // a new maximum for this head: redo, and rescale l, the P already
+                                // written for this chunk, and O (TMEM columns hold this CTA's heads)
+                                // (x of a uniform step is already shifted by m: its new maximum is
+                                // m + the largest shifted x above 0)
+                                float mx = wuni ? 0.f : m[hh];
+    #pragma unroll
+                                for (int k = 0; k < 16; ++k) mx = fmaxf(mx, __uint_as_float(sx[hh][k]));
+                                const float alpha = wuni ? ex2(-mx) : ex2(m[hh] - mx);
+                                m[hh] = wuni ? m[hh] + mx : mx;
+                                l[hh] *= alpha;
+                                ls[hh] = exp_pack16(sx[hh], mx, pk[hh]);
+                                if (g == 1) {
+                                    uint32_t pw[8];
+                                    tmem_wait_st();   // the first half's P of this head is written
+                                    tmem_ld_x8(lrow + kColP + 16 * (hl0 + hh), pw);
+                                    tmem_wait_ld();
+    #pragma unroll
+                                    for (int k = 0; k < 8; ++k)
+                                        pw[k] = pack_bf16x2(__uint_as_float(pw[k] << 16) * alpha,
+                                                            __uint_as_float(pw[k] & 0xffff0000u) * alpha);
+                                    tmem_st_x8(lrow + kColP + 16 * (hl0 + hh), pw);
+                                }
+                                if (t > t0) {
+                                    uint32_t ov[16];
+                                    tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
+                                    tmem_wait_ld();
+    #pragma unroll
+                                    for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                                    tmem_st_x16(lrow + kColO + 16 * (hl0 + hh), ov);
+                                }
+                            }
+                        }
                         wait_pv();
-#pragma unroll
+    #pragma unroll
                         for (int hh = 0; hh < kNH; ++hh) {
-                            if (!__any_sync(0xffffffffu, !(ls[hh] <= kRedoSum))) continue;
-                            // a new maximum for this head: redo, and rescale l, the P already
-                            // written for this chunk, and O (TMEM columns hold this CTA's heads)
-                            // (x of a uniform step is already shifted by m: its new maximum is
-                            // m + the largest shifted x above 0)
-                            float mx = wuni ? 0.f : m[hh];
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) mx = fmaxf(mx, __uint_as_float(sx[hh][k]));
-                            const float alpha = wuni ? ex2(-mx) : ex2(m[hh] - mx);
-                            m[hh] = wuni ? m[hh] + mx : mx;
-                            l[hh] *= alpha;
-                            ls[hh] = exp_pack16(sx[hh], mx, pk[hh]);
-                            if (g == 1) {
-                                uint32_t pw[8];
-                                tmem_wait_st();   // the first half's P of this head is written
-                                tmem_ld_x8(lrow + kColP + 16 * (hl0 + hh), pw);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int k = 0; k < 8; ++k)
-                                    pw[k] = pack_bf16x2(__uint_as_float(pw[k] << 16) * alpha,
-                                                        __uint_as_float(pw[k] & 0xffff0000u) * alpha);
-                                tmem_st_x8(lrow + kColP + 16 * (hl0 + hh), pw);
-                            }
-                            if (t > 0) {
-                                uint32_t ov[16];
-                                tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                                tmem_st_x16(lrow + kColO + 16 * (hl0 + hh), ov);
-                            }
+                            l[hh] += ls[hh];
+                            tmem_st_x8(lrow + kColP + 16 * (hl0 + hh) + 8 * g, pk[hh]);
                         }
                     }
-                    wait_pv();
-#pragma unroll
-                    for (int hh = 0; hh < kNH; ++hh) {
-                        l[hh] += ls[hh];
-                        tmem_st_x8(lrow + kColP + 16 * (hl0 + hh) + 8 * g, pk[hh]);
-                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars->p_ready);
+                    if (!ok) break;
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars->p_ready);
                 if (!ok) break;
+                mbar_arrive(&bars->kv_empty[ks]);
             }
             if (!ok) break;
-            mbar_arrive(&bars->kv_empty[ks]);
-        }
-        if (!ok) {
-            fail(bars, status);
-        } else {
-            // ---------------------------------------------------- epilogue
-            if (!mbar_wait(&bars->pv_done, (nchunks - 1) & 1, abort_flag, kWaitNs)) {
-                fail(bars, status);
-            } else {
-                tc_fence_after();
-                const int row = i0 + r;
-                const bool live = row < n;
+            // ------------------------------------------ epilogue of the stretch
+            // (the next stretch's first PV overwrites O only after every thread's
+            // p_ready of that chunk, which follows these reads)
+            if (!mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const int row = sg.i0 + r;
+            const bool live = row < n;
 #pragma unroll
-                for (int hh = 0; hh < kNH; ++hh) {
-                    const int h = kHC * hb + hl0 + hh;
-                    uint32_t ov[16];
-                    tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
-                    tmem_wait_ld();
-                    const float inv = 1.f / l[hh];
-                    const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
-                    if (live) {
-                        if (!parts) {
-                            uint32_t w[HD / 2];
+            for (int hh = 0; hh < kNH; ++hh) {
+                const int h = kHC * sg.hb + hl0 + hh;
+                uint32_t ov[16];
+                tmem_ld_x16(lrow + kColO + 16 * (hl0 + hh), ov);
+                tmem_wait_ld();
+                const float inv = 1.f / l[hh];
+                const int c0 = (HD == 8) ? (h & 1) * 8 : 0;
+                const float lse_v = (m[hh] + log2f(l[hh])) * kLn2;
+                if (!live) continue;
+                if (sg.part < 0) {
+                    uint32_t w[HD / 2];
 #pragma unroll
-                            for (int k = 0; k < HD / 2; ++k)
-                                w[k] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * k]) * inv,
-                                                   __uint_as_float(ov[c0 + 2 * k + 1]) * inv);
-                            uint4* dst = reinterpret_cast<uint4*>(o + ((int64_t)row * kH + h) * HD);
+                    for (int k = 0; k < HD / 2; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * k]) * inv,
+                                           __uint_as_float(ov[c0 + 2 * k + 1]) * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(o + ((int64_t)row * kH + h) * HD);
 #pragma unroll
-                            for (int k = 0; k < HD / 8; ++k)
-                                dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                            lse[(int64_t)h * n + row] = (m[hh] + log2f(l[hh])) * kLn2;
-                        } else {
-                            float4* dst = reinterpret_cast<float4*>(
-                                o_part + (((int64_t)split * n + row) * kH + h) * HD);
+                    for (int k = 0; k < HD / 8; ++k)
+                        dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    lse[(int64_t)h * n + row] = lse_v;
+                } else {
+                    // KV-split partials: [split][n][8][HD] and [split][8][n]; balanced
+                    // pieces: slot [128 rows][4 heads][HD] and [4 heads][128 rows]
+                    const int64_t oo = bal.ctas == 0 ? (((int64_t)sg.part * n + row) * kH + h) * HD
+                                                     : (((int64_t)sg.part * kBQ + r) * kHC + hl0 + hh) * HD;
+                    const int64_t lo = bal.ctas == 0 ? ((int64_t)sg.part * kH + h) * n + row
+                                                     : ((int64_t)sg.part * kHC + hl0 + hh) * kBQ + r;
+                    float4* dst = reinterpret_cast<float4*>(o_part + oo);
 #pragma unroll
-                            for (int k = 0; k < HD / 4; ++k)
-                                dst[k] = make_float4(__uint_as_float(ov[c0 + 4 * k]) * inv,
-                                                     __uint_as_float(ov[c0 + 4 * k + 1]) * inv,
-                                                     __uint_as_float(ov[c0 + 4 * k + 2]) * inv,
-                                                     __uint_as_float(ov[c0 + 4 * k + 3]) * inv);
-                            lse_part[((int64_t)split * kH + h) * n + row] = (m[hh] + log2f(l[hh])) * kLn2;
-                        }
-                    }
+                    for (int k = 0; k < HD / 4; ++k)
+                        dst[k] = make_float4(__uint_as_float(ov[c0 + 4 * k]) * inv,
+                                             __uint_as_float(ov[c0 + 4 * k + 1]) * inv,
+                                             __uint_as_float(ov[c0 + 4 * k + 2]) * inv,
+                                             __uint_as_float(ov[c0 + 4 * k + 3]) * inv);
+                    lse_part[lo] = lse_v;
                 }
             }
         }
+        if (!ok) fail(bars, status);
     }
     tc_fence_before();
     __syncthreads();
@@ -571,10 +620,76 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 namespace gt {
 namespace {
 
+constexpr int kMinBlocks = 8;   // shortest balanced share: 8 KV blocks (512 columns)
+
+// CTAs of the balanced grid: a whole number of waves of kCtasPerSm CTAs per SM,
+// at least as many CTAs as tasks (so a share meets at most two tasks) and at
+// most one per kMinBlocks KV blocks; an even count, so that CTAs c and
+// c + ctas / 2 take the same KV blocks of the two head halves of a tile.
+// 0 when one CTA per task already fills the waves exactly.
+Balance balance_for(int n) {
+    const int tiles = (n + kBQ - 1) / kBQ;
+    const int tasks = kHalves * tiles;
+    const int nblk = (n + kBKV - 1) / kBKV;
+    const int64_t slots = (int64_t)kCtasPerSm * num_sms();
+    int64_t g = slots * ((tasks + slots - 1) / slots);
+    const int64_t cap = (int64_t)tasks * nblk / kMinBlocks;
+    if (g > cap) g = cap;
+    g &= ~int64_t(1);
+    if (g <= tasks) return Balance{0, tasks, nblk};
+    return Balance{(int)g, tasks, nblk};
+}
+
+// Rows of the tasks that more than one CTA took: the pieces' normalised outputs
+// and log-sum-exps combined exactly, o = sum_k e^(lse_k - M) o_k / sum_k e^(lse_k - M),
+// lse = M + log sum_k e^(lse_k - M).  One thread per (row, head).
+template <int HD>
+__global__ void __launch_bounds__(256)
+merge_pieces(const Balance bl, int n, const float* __restrict__ o_part, const float* __restrict__ lse_part,
+             __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)n * kH) return;
+    const int row = (int)(idx / kH), h = (int)(idx % kH);
+    const int tiles = bl.tasks / kHalves;
+    const int r = row % kBQ, hl = h % kHC;
+    const int64_t p0 = (int64_t)((h / kHC) * tiles + row / kBQ) * bl.nblk;
+    const int c0 = bl.cta_of(p0), c1 = bl.cta_of(p0 + bl.nblk - 1);
+    if (c0 == c1) return;   // one CTA took the whole task and wrote the row itself
+    auto slot = [&](int c) { return 2 * c + ((c == c0 && bl.lo(c) < p0) ? 1 : 0); };
+    float mx = -INFINITY;
+    for (int c = c0; c <= c1; ++c) mx = fmaxf(mx, lse_part[((int64_t)slot(c) * kHC + hl) * kBQ + r]);
+    float acc[HD];
+#pragma unroll
+    for (int k = 0; k < HD; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+        const int sl = slot(c);
+        const float w = __expf(lse_part[((int64_t)sl * kHC + hl) * kBQ + r] - mx);
+        wsum += w;
+        const float4* src = reinterpret_cast<const float4*>(o_part + (((int64_t)sl * kBQ + r) * kHC + hl) * HD);
+#pragma unroll
+        for (int k = 0; k < HD / 4; ++k) {
+            const float4 v = src[k];
+            acc[4 * k] += w * v.x;
+            acc[4 * k + 1] += w * v.y;
+            acc[4 * k + 2] += w * v.z;
+            acc[4 * k + 3] += w * v.w;
+        }
+    }
+    const float inv = 1.f / wsum;
+    uint32_t pk[HD / 2];
+#pragma unroll
+    for (int k = 0; k < HD / 2; ++k) pk[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    uint4* dst = reinterpret_cast<uint4*>(o + ((int64_t)row * kH + h) * HD);
+#pragma unroll
+    for (int k = 0; k < HD / 8; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+    lse[(int64_t)h * n + row] = mx + __logf(wsum);
+}
+
 template <int HD>
 int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8_t* spd, int64_t ld,
                   const float* T, int nb, float scale, int kv_begin, int kv_end, int kv_block, int parts,
-                  void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s) {
+                  const Balance& bal, void* o, float* lse, float* o_part, float* lse_part, cudaStream_t s) {
     using C = Cfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -591,13 +706,21 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int nsplit = kv_block > 0 ? (kv_end - kv_begin + kv_block - 1) / kv_block : 1;
-    dim3 grid((n + kBQ - 1) / kBQ, nsplit, kH / kHC);
+    const dim3 grid = bal.ctas > 0 ? dim3(bal.ctas) : dim3((n + kBQ - 1) / kBQ, nsplit, kHalves);
     {
         LaunchScope ls("fwd_tc", s);
         fwd_tc_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
             mk, mv, ms, static_cast<const __nv_bfloat16*>(q), T, nb, n, scale * kLog2e, kv_begin, kv_end,
-            nsplit > 1 ? kv_block : 0, parts, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part,
+            nsplit > 1 ? kv_block : 0, parts, static_cast<__nv_bfloat16*>(o), lse, o_part, lse_part, bal,
             status);
+    }
+    int rc = check_launch();
+    if (rc != GT_OK || bal.ctas == 0) return rc;
+    {
+        LaunchScope ls("fwd_merge", s);
+        const int64_t threads = (int64_t)n * kH;
+        merge_pieces<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+            bal, n, o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse);
     }
     return check_launch();
 }
@@ -606,17 +729,34 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
 
 bool fwd_tc_supported(int h, int d) { return h == kH && (d == 8 || d == 16); }
 
+int fwd_tc_balanced_ctas(int n) { return balance_for(n).ctas; }
+
+// Floats of the balanced forward's partial slots (0: the plain grid needs none):
+// two slots per CTA of [128 rows][4 heads][d] outputs and [4][128] log-sum-exps.
+size_t fwd_tc_piece_floats(int n, int d) {
+    const Balance bl = balance_for(n);
+    return bl.ctas == 0 ? 0 : (size_t)2 * bl.ctas * kBQ * kHC * (d + 1);
+}
+
 int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_part,
                    const float* lse_part, void* o, float* lse, cudaStream_t s);
 
+// kv_block > 0: grid.y splits of kv_block columns merged by merge_partials;
+// 0: the balanced grid, whose partial slots start at o_part (lse_part after
+// the outputs: fwd_tc_piece_floats in all).
 int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
                 int64_t ld, const float* T, int nb, float scale, int kv_block, void* o, float* lse,
                 float* o_part, float* lse_part, cudaStream_t s) {
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
     const int parts = nsplit > 1;
-    int rc = d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, o, lse,
+    Balance bal = parts ? Balance{0, 0, 0} : balance_for(n);
+    if (bal.ctas > 0) {
+        if (!o_part) return GT_ERR_WORKSPACE;
+        lse_part = o_part + (size_t)2 * bal.ctas * kBQ * kHC * d;
+    }
+    int rc = d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, bal, o, lse,
                                        o_part, lse_part, s)
-                    : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, o, lse,
+                    : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, 0, n, kv_block, parts, bal, o, lse,
                                         o_part, lse_part, s);
     if (rc != GT_OK || nsplit == 1) return rc;
     return merge_partials(GT_BF16, n, kH, d, nsplit, o_part, lse_part, o, lse, s);
@@ -627,9 +767,10 @@ int attn_fwd_tc(int n, int d, const void* q, const void* k, const void* v, const
 int attn_fwd_tc_range(int n, int d, const void* q, const void* k, const void* v, const int8_t* spd,
                       int64_t ld, const float* T, int nb, float scale, int kv_begin, int kv_end,
                       float* o_part, float* lse_part, cudaStream_t s) {
-    return d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, nullptr,
+    const Balance none{0, 0, 0};
+    return d == 8 ? launch_fwd_tc<8>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, none, nullptr,
                                      nullptr, o_part, lse_part, s)
-                  : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, nullptr,
+                  : launch_fwd_tc<16>(n, q, k, v, spd, ld, T, nb, scale, kv_begin, kv_end, 0, 1, none, nullptr,
                                       nullptr, o_part, lse_part, s);
 }
 

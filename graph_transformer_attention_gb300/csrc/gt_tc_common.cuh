@@ -21,6 +21,45 @@ __device__ __forceinline__ void fail(int* abort_flag, int* status) {
     atomicOr(status, kStatusTimeout);
 }
 
+// Balanced split of a streamed loop over a fixed number of CTAs.  The work is
+// `tasks` tasks of `nblk` steps each; CTA c takes the steps
+// [c W / ctas, (c + 1) W / ctas) of their concatenation (W = tasks nblk).  With
+// ctas >= tasks a share is at most nblk steps long, so it meets at most two
+// tasks: the end of one and the start of the next.
+struct Balance {
+    int ctas;   // 0: no balancing (one CTA per task, from the grid)
+    int tasks;
+    int nblk;
+    __host__ __device__ int64_t total() const { return (int64_t)tasks * nblk; }
+    __host__ __device__ int64_t lo(int c) const { return (int64_t)c * total() / ctas; }
+    // the CTA whose share holds step p: the largest c with lo(c) <= p
+    __host__ __device__ int cta_of(int64_t p) const {
+        return (int)(((p + 1) * ctas + total() - 1) / total()) - 1;
+    }
+};
+
+// Steps [b0, b1) of task `task`: piece `which` (0 or 1) of CTA c's share;
+// returns false when the share has no such piece.
+struct Piece {
+    int task, b0, b1;
+};
+__host__ __device__ inline bool piece_of(const Balance& bl, int c, int which, Piece& p) {
+    const int64_t lo = bl.lo(c), hi = bl.lo(c + 1);
+    const int t0 = (int)(lo / bl.nblk);
+    const int64_t e0 = (int64_t)(t0 + 1) * bl.nblk;
+    if (which == 0) {
+        p.task = t0;
+        p.b0 = (int)(lo - (int64_t)t0 * bl.nblk);
+        p.b1 = (int)((hi < e0 ? hi : e0) - (int64_t)t0 * bl.nblk);
+        return true;
+    }
+    if (hi <= e0) return false;
+    p.task = t0 + 1;
+    p.b0 = 0;
+    p.b1 = (int)(hi - e0);
+    return true;
+}
+
 // Row r of NH per-head K-major [128][16] bf16 MMA operands (32-byte swizzle,
 // 4096 bytes per head) for heads h_first .. h_first + NH - 1 of one node's
 // [8][HD] row of x.  Head dim 8 is zero-padded to 16 per head so that products

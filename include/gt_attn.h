@@ -127,14 +127,26 @@ int gt_spd_build_algo(int32_t algo, const int64_t* indptr, const int32_t* indice
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * The KV block gt_bias_attn_fwd uses for these arguments on the current device
- * (0 = one pass over all columns; -1 for invalid arguments).  An explicit
- * kv_block (< n) is used as given.  With kv_block = 0 the bf16 tensor-core path
- * splits the columns itself when the graph has too few 128-row tiles to give
- * every SM two CTAs (up to 4 splits of a multiple of 128 columns, merged
- * exactly, as with an explicit kv_block).
+ * The uniform KV block gt_bias_attn_fwd uses for these arguments (0 = none;
+ * -1 for invalid arguments): an explicit kv_block (< n) is used as given.  With
+ * kv_block = 0 no uniform split is made; the bf16 tensor-core path instead
+ * deals its (query tile, head half, KV block) work out in equal contiguous
+ * shares to a whole number of waves of two CTAs per SM, whenever one CTA per
+ * tile and head half would leave part of the last wave idle.  A share covers
+ * the end of one tile's KV range and the start of the next; rows whose range
+ * more than one CTA covered are merged exactly through their lse (the same
+ * merge as for KV blocks, Fig. 4), the others are written directly.
  */
 int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block);
+
+/*
+ * CTAs of that balanced tensor-core forward for these arguments on the current
+ * device (-1 for invalid arguments): 0 when the forward runs one CTA per 128-row
+ * tile and head half (an explicit kv_block, another dtype or shape, or a grid
+ * whose waves are full already).  A balanced forward launches one merge kernel
+ * after the attention kernel.
+ */
+int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block);
 
 /*
  * How many CTAs share each 128-row tile's streamed dimension in the bf16
@@ -160,7 +172,8 @@ size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t 
  *            16-byte aligned).
  *   T        device fp32 [h][nb], nb <= 128.
  *   scale    multiplies q.k before the bias is added (1/sqrt(d) is usual).
- *   kv_block 0: every Q tile streams all n KV columns in one pass.
+ *   kv_block 0: every Q tile streams all n KV columns (in at most a few
+ *            balanced pieces: see gt_bias_attn_fwd_kv_block).
  *            > 0 (a multiple of 128): the columns are cut into blocks of
  *            kv_block (the KV blocks of Fig. 4); each block yields a partial
  *            (o, lse) and the partials are merged exactly through their lse.

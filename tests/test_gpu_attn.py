@@ -263,6 +263,33 @@ def test_kv_block_matches_single_pass(gt):
         assert np.linalg.norm(a[nm] - b[nm]) <= 1e-2 * np.linalg.norm(a[nm])
 
 
+@pytest.mark.parametrize("n,d,kind", [(1000, 16, "random"), (2048, 8, "graph"), (4096, 16, "random")])
+def test_balanced_forward_pieces(gt, n, d, kind):
+    """The forward's balanced grid: each CTA takes an equal contiguous share of
+    the (tile, head half, KV block) work, so one tile's KV range is covered by up
+    to six CTAs here (n = 4096), whose pieces are merged through their lse while
+    whole ranges are written directly.  Every row against the oracle."""
+    tiles = (n + 127) // 128
+    assert gt.load_library().gt_bias_attn_fwd_ctas(1, n, 8, d, 0) > 2 * tiles
+    nb = 26
+    x = gi.make_layer_tensors(n, 8, d, nb, "bf16", seed=60 + d)
+    if kind == "graph":
+        g = gi.disjoint_ba(n // 64, 64, 2, seed=61)
+        spd = O.spd(n, g.indptr, g.indices, nb - 2)
+    else:
+        spd = np.random.default_rng(62).integers(0, nb, size=(n, n)).astype(np.int8)
+    q, k, v = (to_dev(x[a], "bf16") for a in ("q", "k", "v"))
+    T = torch.from_numpy(x["T"]).cuda()
+    o, lse = gt.gt_bias_attn_fwd(q, k, v, _spd_dev(spd), T)
+    gt.gt_check_device_status()
+    ro, rl = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"])
+    assert_close("o", host(o), ro, "bf16")
+    assert_close("lse", host(lse), rl, "bf16")
+    # no row is left unwritten or written twice over: every row's error is small
+    err = np.abs(host(lse) - rl).max(axis=0)
+    assert np.all(err < 0.05), np.argsort(err)[-5:]
+
+
 def _config_spd(w):
     g = gi.config_graph(w)
     return O.spd(g.n, g.indptr, g.indices, w.D)

@@ -53,9 +53,12 @@ def test_counts_and_times_of_one_layer(gt, timing):
 
 
 def test_small_graphs_split_their_streams(gt):
-    """On a GB300 a graph of 4096 nodes has 32 tiles of 128 rows: the forward
-    splits its KV columns and the backward its streams; 16384 nodes do not."""
+    """On a GB300 a graph of 4096 nodes has 32 tiles of 128 rows: the backward
+    splits its streams; 16384 nodes do not.  The forward makes no uniform KV
+    split of its own (it balances its work instead), and an explicit kv_block
+    is kept."""
     assert gt.load_library().gt_bias_attn_bwd_split(1, 4096, 8, 8, 18) >= 2
-    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 0) > 0
+    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 0) == 0
+    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 1024) == 1024
     assert gt.load_library().gt_bias_attn_bwd_split(1, 16384, 8, 16, 26) == 1
     assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 16384, 8, 16, 0) == 0
