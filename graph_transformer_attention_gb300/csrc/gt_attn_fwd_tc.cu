@@ -131,14 +131,15 @@ __device__ __forceinline__ bool seg_of(const Balance& bl, int si, int kv_begin, 
         return true;
     }
     Piece p;
-    if (!piece_of(bl, blockIdx.x, si, p)) return false;
+    const int bl_share = bl.share_of(blockIdx.x);
+    if (!piece_of(bl, bl_share, si, p)) return false;
     const int tiles = bl.tasks / kHalves;
     sg.i0 = (p.task % tiles) * kBQ;
     sg.hb = p.task / tiles;
     sg.j_begin = kv_begin + p.b0 * kBKV;
     sg.j_end = min(kv_end, kv_begin + p.b1 * kBKV);
     sg.nblocks = p.b1 - p.b0;
-    sg.part = (p.b0 == 0 && p.b1 == bl.nblk) ? -1 : 2 * (int)blockIdx.x + si;
+    sg.part = (p.b0 == 0 && p.b1 == bl.nblk) ? -1 : 2 * bl_share + si;
     return true;
 }
 
@@ -250,11 +251,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // this CTA's one or two stretches (heads kHC hb .. kHC hb + kHC - 1 of each)
-    Seg sg0, sg1;
-    seg_of(bal, 0, kv_begin, kv_end, kv_block, parts, sg0);
-    const int nseg = seg_of(bal, 1, kv_begin, kv_end, kv_block, parts, sg1) ? 2 : 1;
-    const int nblocks0 = sg0.nblocks;
-    const int nblocks = nblocks0 + (nseg > 1 ? sg1.nblocks : 0);
+    // (recomputed from the parameters where needed: kept in registers they would
+    // be live across the whole softmax loop)
+    auto seg = [&](int si) {
+        Seg sg{0, 0, 0, 0, 0, -1};
+        seg_of(bal, si, kv_begin, kv_end, kv_block, parts, sg);
+        return sg;
+    };
+    const int nblocks0 = seg(0).nblocks;
+    const int nblocks1 = seg(1).nblocks;
+    const int nseg = nblocks1 > 0 ? 2 : 1;
+    const int nblocks = nblocks0 + nblocks1;
     const int nchunks0 = nblocks0 * kNCH;
     const int nchunks = nblocks * kNCH;
 
@@ -283,7 +290,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     // per-head Q operands of this CTA's heads: [128 rows][16] bf16, 32-byte swizzle, K-major
     // (threads 0-127 the first stretch's tile, 128-255 the second's)
     if (tid < kBQ || (nseg > 1 && tid < 2 * kBQ)) {
-        const Seg& sg = tid < kBQ ? sg0 : sg1;
+        const Seg sg = seg(tid < kBQ ? 0 : 1);
         const int rr = tid & (kBQ - 1);
         const int row = sg.i0 + rr;
         const bool live = row < n;
@@ -309,10 +316,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     break;
                 }
                 const bool second = b >= nblocks0;
-                const int i0 = second ? sg1.i0 : sg0.i0;
-                const int hb = second ? sg1.hb : sg0.hb;
+                const Seg sg = seg(second ? 1 : 0);
+                const int i0 = sg.i0;
+                const int hb = sg.hb;
                 uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                const int j0 = second ? sg1.j_begin + (b - nblocks0) * kBKV : sg0.j_begin + b * kBKV;
+                const int j0 = sg.j_begin + (b - (second ? nblocks0 : 0)) * kBKV;
                 mbar_arrive_expect_tx(&bars->kv_full[ks], C::STAGE_BYTES);
                 tma_load_2d(st, &mapS, j0, i0, &bars->kv_full[ks]);
 #pragma unroll
@@ -406,22 +414,30 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         const int r = tid & (kBQ - 1);           // row within the tile = TMEM lane
         const int hl0 = kNH * (tid >> 7);        // this thread's first head among the CTA's
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        int t = 0, bg = 0;   // chunks and KV blocks so far: the mbarrier phases
+        int t = 0;   // chunks so far (kNCH per KV block): the mbarrier phases
         bool ok = true;
         for (int si = 0; ok && si < nseg; ++si) {
-            const Seg sg = si ? sg1 : sg0;
-            const uint32_t tbl = smem_u32(Ts) + 4u * (kHC * sg.hb + hl0);   // 32-byte rows of 8 head biases
+            uint32_t tbl;    // 32-byte rows of 8 head biases
+            int jb, je, nbs;  // the stretch's KV columns [jb, je) in nbs blocks
+            {
+                const Seg sg = seg(si);
+                tbl = smem_u32(Ts) + 4u * (kHC * sg.hb + hl0);
+                jb = sg.j_begin;
+                je = sg.j_end;
+                nbs = sg.nblocks;
+            }
             float m[kNH], l[kNH];
 #pragma unroll
             for (int h = 0; h < kNH; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
             const int t0 = t;    // the stretch's first chunk
             int uni_skip = 0;    // half chunks left before the next uniformity vote (warp-uniform)
-            for (int b = 0; ok && b < sg.nblocks; ++b, ++bg) {
+            for (int b = 0; ok && b < nbs; ++b) {
+                const int bg = t / kNCH;   // KV blocks so far
                 const int ks = bg & 1;
                 if (!mbar_wait(&bars->kv_full[ks], (bg >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
                 const uint32_t sp = smem_u32(smem + C::OFF_STAGE + ks * C::STAGE_BYTES) + r * kBKV;
-                const int j0 = sg.j_begin + b * kBKV;
-                const bool tail_block = j0 + kBKV > sg.j_end;
+                const int j0 = jb + b * kBKV;
+                const bool tail_block = j0 + kBKV > je;
                 for (int c = 0; c < kNCH; ++c, ++t) {
                     if (!mbar_wait(&bars->s_full, t & 1, abort_flag, kWaitNs)) { ok = false; break; }
                     tc_fence_after();
@@ -440,7 +456,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                                 tmem_ld_x16(lrow + kColS + kCH * (hl0 + hh) + 16 * g, sx[hh]);
                             tmem_wait_ld();
                             score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
-                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, je);
     #pragma unroll
                             for (int hh = 0; hh < kNH; ++hh)
     #pragma unroll
@@ -490,7 +506,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             float bb[kNH];
                             load_bias<kNH>(tbl + code0 * 32u, bb);
                             score16_shifted<kNH>(sx, bb, m, scale_log2);
-                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, je);
     #pragma unroll
                             for (int hh = 0; hh < kNH; ++hh) {
                                 ls[hh] = exp_pack16_shifted(sx[hh], pk[hh]);
@@ -498,7 +514,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             }
                         } else {
                             score16<kNH>(sx, g ? c1 : c0, tbl, scale_log2);
-                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, sg.j_end);
+                            if (tail_block) mask16<kNH>(sx, jc + 16 * g, je);
     #pragma unroll
                             for (int hh = 0; hh < kNH; ++hh) {
                                 ls[hh] = exp_pack16(sx[hh], m[hh], pk[hh]);
@@ -563,6 +579,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             // p_ready of that chunk, which follows these reads)
             if (!mbar_wait(&bars->pv_done, (t - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             tc_fence_after();
+            const Seg sg = seg(si);
             const int row = sg.i0 + r;
             const bool live = row < n;
 #pragma unroll
@@ -622,22 +639,8 @@ namespace {
 
 constexpr int kMinBlocks = 8;   // shortest balanced share: 8 KV blocks (512 columns)
 
-// CTAs of the balanced grid: a whole number of waves of kCtasPerSm CTAs per SM,
-// at least as many CTAs as tasks (so a share meets at most two tasks) and at
-// most one per kMinBlocks KV blocks; an even count, so that CTAs c and
-// c + ctas / 2 take the same KV blocks of the two head halves of a tile.
-// 0 when one CTA per task already fills the waves exactly.
 Balance balance_for(int n) {
-    const int tiles = (n + kBQ - 1) / kBQ;
-    const int tasks = kHalves * tiles;
-    const int nblk = (n + kBKV - 1) / kBKV;
-    const int64_t slots = (int64_t)kCtasPerSm * num_sms();
-    int64_t g = slots * ((tasks + slots - 1) / slots);
-    const int64_t cap = (int64_t)tasks * nblk / kMinBlocks;
-    if (g > cap) g = cap;
-    g &= ~int64_t(1);
-    if (g <= tasks) return Balance{0, tasks, nblk};
-    return Balance{(int)g, tasks, nblk};
+    return balance_grid((n + kBQ - 1) / kBQ, kHalves, (n + kBKV - 1) / kBKV, kCtasPerSm, kMinBlocks);
 }
 
 // Rows of the tasks that more than one CTA took: the pieces' normalised outputs

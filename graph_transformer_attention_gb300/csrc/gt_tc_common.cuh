@@ -32,13 +32,34 @@ struct Balance {
     int nblk;
     __host__ __device__ int64_t total() const { return (int64_t)tasks * nblk; }
     __host__ __device__ int64_t lo(int c) const { return (int64_t)c * total() / ctas; }
-    // the CTA whose share holds step p: the largest c with lo(c) <= p
+    // the share whose steps hold step p: the largest c with lo(c) <= p
     __host__ __device__ int cta_of(int64_t p) const {
         return (int)(((p + 1) * ctas + total() - 1) / total()) - 1;
     }
+    // The share CTA b takes (ctas even): CTAs 2k and 2k + 1 take shares k and
+    // k + ctas / 2, the same steps of the two halves.  The block scheduler hands
+    // consecutive CTAs to different SMs, so the two CTAs that share an SM do not
+    // run the same steps in lockstep.
+    __host__ __device__ int share_of(int b) const { return (b & 1) * (ctas / 2) + (b >> 1); }
 };
 
-// Steps [b0, b1) of task `task`: piece `which` (0 or 1) of CTA c's share;
+// The balanced grid for tasks = halves x tiles tasks of nblk steps each: a whole
+// number of waves of per_sm CTAs per SM, at least one CTA per task (so a share
+// meets at most two tasks) and at most one per min_steps steps, and an even
+// count, so that the two halves split at a share boundary and shares c and
+// c + ctas / 2 take the same steps of the two halves (with halves = 2).
+// ctas = 0 when one CTA per task already fills its waves exactly.
+inline Balance balance_grid(int tiles, int halves, int nblk, int per_sm, int min_steps) {
+    const int tasks = halves * tiles;
+    const int64_t slots = (int64_t)per_sm * num_sms();
+    int64_t g = slots * ((tasks + slots - 1) / slots);
+    const int64_t cap = (int64_t)tasks * nblk / min_steps;
+    if (g > cap) g = cap;
+    g &= ~int64_t(1);
+    return Balance{g > tasks ? (int)g : 0, tasks, nblk};
+}
+
+// Steps [b0, b1) of task `task`: piece `which` (0 or 1) of share c;
 // returns false when the share has no such piece.
 struct Piece {
     int task, b0, b1;

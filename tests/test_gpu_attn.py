@@ -290,6 +290,36 @@ def test_balanced_forward_pieces(gt, n, d, kind):
     assert np.all(err < 0.05), np.argsort(err)[-5:]
 
 
+def test_backward_after_balanced_forward_ragged(gt):
+    """The unsplit backward at a ragged size just past the split threshold
+    (n = 9857: 78 tiles, the last one 1 row), fed by the balanced forward (156
+    tasks over two waves' worth of CTAs, up to three CTAs per tile).  Rows: the
+    first and last of every tile plus random ones, against the oracle; dT by its
+    zero-sum property."""
+    n, h, d, nb = 9857, 8, 16, 26
+    lib = gt.load_library()
+    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) == 1
+    assert lib.gt_bias_attn_fwd_ctas(1, n, h, d, 0) > 0
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=70)
+    spd = np.random.default_rng(71).integers(0, nb, size=(n, n)).astype(np.int8)
+    got = _run_gpu(gt, x, spd, "bf16")
+    rng = np.random.default_rng(72)
+    ends = np.concatenate([np.arange(0, n, 128), np.minimum(np.arange(127, n + 127, 128), n - 1)])
+    rows = np.unique(np.concatenate([ends, rng.choice(n, 64, replace=False)]))
+    o_r, lse_r = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], rows=rows)
+    assert_close("o[rows]", got["o"][rows], o_r, "bf16")
+    assert_close("lse[rows]", got["lse"][:, rows], lse_r, "bf16")
+    Dv_rows = (o_r * x["dO"][rows].astype(np.float64)).sum(-1).T
+    lse_full = np.zeros((h, n)); Dv_full = np.zeros((h, n))
+    lse_full[:, rows] = lse_r; Dv_full[:, rows] = Dv_rows
+    g = O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_full, Dv_full,
+                   rows=rows, want_dT=False, want_dkdv=False)
+    assert_close("dq[rows]", got["dq"][rows], g["dq"], "bf16")
+    dT = got["dT"]
+    bound = 2.0 ** -8 * np.abs(x["dO"].astype(np.float64) * got["o"]).sum(axis=(0, 2)) + 1e-4
+    assert np.all(np.abs(dT.sum(1)) <= bound), (dT.sum(1), bound)
+
+
 def _config_spd(w):
     g = gi.config_graph(w)
     return O.spd(g.n, g.indptr, g.indices, w.D)
