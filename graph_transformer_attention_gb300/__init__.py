@@ -89,6 +89,8 @@ def load_library():
         lib.gt_bias_attn_fwd_kv_block.restype = i32
         lib.gt_bias_attn_fwd_ctas.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_fwd_ctas.restype = i32
+        lib.gt_bias_attn_launches.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.gt_bias_attn_launches.restype = ctypes.c_int
         lib.gt_bias_attn_bwd_split.argtypes = [i32, i32, i32, i32, i32]
         lib.gt_bias_attn_bwd_split.restype = i32
         lib.gt_bias_attn_fwd.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i32, f32, i32,
@@ -160,13 +162,11 @@ def spd_ld(n: int) -> int:
 def launches_per_call(dtype: str, h: int, d: int, n: int, kv_block: int = 0, nb: int = 18) -> dict:
     """Number of libgt kernels gt_bias_attn_fwd and gt_bias_attn_bwd launch for
     these sizes on the current device (memsets not counted)."""
-    lib = load_library()
     code = GT_F32 if dtype == "f32" else GT_BF16
-    kvb = int(lib.gt_bias_attn_fwd_kv_block(code, n, h, d, kv_block))
-    nsplit = -(-n // kvb) if kvb > 0 else 1
-    balanced = int(lib.gt_bias_attn_fwd_ctas(code, n, h, d, kv_block)) > 0
-    split = int(lib.gt_bias_attn_bwd_split(code, n, h, d, nb))
-    return {"fwd": 1 + (1 if nsplit > 1 or balanced else 0), "bwd": 4 + (1 if split > 1 else 0)}
+    fwd, bwd = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("gt_bias_attn_launches",
+           load_library().gt_bias_attn_launches(code, n, h, d, nb, kv_block, ctypes.byref(fwd), ctypes.byref(bwd)))
+    return {"fwd": int(fwd.value), "bwd": int(bwd.value)}
 
 
 def gt_status_string(status: int) -> str:

@@ -41,8 +41,10 @@ bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, int tail, float* acc, cudaStream_t s);
+                float* Dv, double* dT64, float* aux, int nsplit, int tail, int dq_tail, float* acc,
+                cudaStream_t s);
 int bwd_dkdv_tail_split(int n);
+int bwd_dq_tail_split(int n);
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -127,6 +129,13 @@ int bwd_tail(int dtype, int n, int h, int d, int nb) {
     return bwd_dkdv_tail_split(n);
 }
 
+// KV split of the dq tasks past the last full wave (1 = none); its sums take
+// the dq part of `acc`.
+int bwd_dq_tail(int dtype, int n, int h, int d, int nb) {
+    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb) || bwd_split(dtype, n, h, d, nb) > 1) return 1;
+    return bwd_dq_tail_split(n);
+}
+
 size_t bwd_ws(int n, int h, int d, bool with_acc, void* base, size_t cap, BwdWs* out) {
     Carve c(base, cap);
     BwdWs w;
@@ -195,7 +204,8 @@ size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t 
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
     size_t a = gt::fwd_ws(dtype, n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
-    const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1;
+    const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1 ||
+                     gt::bwd_dq_tail(dtype, n, h, d, 128) > 1;
     size_t b = gt::bwd_ws(n, h, d, acc, nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
 }
@@ -216,6 +226,28 @@ int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, in
     if (kv_block >= n) kv_block = 0;
     if (kv_block > 0 || dtype != GT_BF16 || !gt::fwd_tc_supported(h, d)) return 0;
     return gt::fwd_tc_balanced_ctas(n);
+}
+
+int gt_bias_attn_launches(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb, int32_t kv_block,
+                          int32_t* fwd, int32_t* bwd) {
+    if (!fwd || !bwd || !gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || nb < 1 || kv_block < 0)
+        return GT_ERR_INVALID_ARG;
+    if (kv_block >= n) kv_block = 0;
+    const bool tc_fwd = dtype == GT_BF16 && gt::fwd_tc_supported(h, d);
+    const bool kv_split = kv_block > 0 && (n + kv_block - 1) / kv_block > 1;
+    *fwd = 1 + ((kv_split || (tc_fwd && kv_block == 0 && gt::fwd_tc_balanced_ctas(n) > 0)) ? 1 : 0);
+    if (!(dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))) {
+        *bwd = 4;   // D, rows, columns, dT
+        return GT_OK;
+    }
+    // prep, dq, dk/dv, dT; the small-graph split adds one conversion; a tail
+    // split adds its second launch (when full waves come first) and a conversion
+    int count = 4;
+    if (gt::bwd_split(dtype, n, h, d, nb) > 1) count += 1;
+    if (gt::bwd_tail(dtype, n, h, d, nb) > 1) count += 2;
+    if (gt::bwd_dq_tail(dtype, n, h, d, nb) > 1) count += (2 * ((n + 127) / 128) >= 2 * gt::num_sms()) ? 2 : 1;
+    *bwd = count;
+    return GT_OK;
 }
 
 int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void* q, const void* k,
@@ -280,10 +312,11 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     // (a caller's fixed scratch) runs unsplit
     int nsplit = gt::bwd_split(dtype, n, h, d, nb);
     int tail = gt::bwd_tail(dtype, n, h, d, nb);
-    bool with_acc = nsplit > 1 || tail > 1;
+    int dq_tail = gt::bwd_dq_tail(dtype, n, h, d, nb);
+    bool with_acc = nsplit > 1 || tail > 1 || dq_tail > 1;
     if (with_acc && ws_bytes < gt::bwd_ws(n, h, d, true, nullptr, 0, nullptr)) {
         with_acc = false;
-        nsplit = tail = 1;
+        nsplit = tail = dq_tail = 1;
     }
     const size_t need = gt::bwd_ws(n, h, d, with_acc, nullptr, 0, nullptr);
     if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
@@ -292,7 +325,7 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, tail, w.acc, s);
+                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, tail, dq_tail, w.acc, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

@@ -5,9 +5,11 @@
 // the matching bias slice of the int8 bucket matrix (MegaGraph, Fig. 4), and
 //   dS = P (dO V^T - D),  dq = scale dS K,  dT[h][c] = sum over spd = c of dS.
 //
-// One CTA = one tile of 128 query rows and one half of the heads (4 of 8:
-// grid.y); two CTAs share an SM, so one's softmax runs while the other waits on
-// its tensor-core products.  192 threads:
+// One CTA = one task: a tile of 128 query rows and one half of the heads (4 of
+// 8); two CTAs share an SM, so one's softmax runs while the other waits on its
+// tensor-core products.  Tasks past the last full wave of two CTAs per SM are
+// split over several CTAs along the KV blocks (grid.z), which sum dq in fp32;
+// so are all tasks of a graph too small to give every SM two.  192 threads:
 //   warps 0-3  thread r owns query row r (TMEM lane r), so lse and D are
 //              registers.  Per chunk of
 //              16 KV columns: S_h and dP_h from TMEM, one 16-byte shared load of
@@ -120,7 +122,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LD, int ldl,
               const float* __restrict__ vmax,
               const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
-              int split_blocks, __nv_bfloat16* __restrict__ dq, float* __restrict__ dq_acc,
+              int task_first, int split_blocks, __nv_bfloat16* __restrict__ dq, float* __restrict__ dq_acc,
               double* __restrict__ dT64, int* status) {
     using C = DqCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -130,8 +132,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     int* bins = reinterpret_cast<int*>(smem + C::OFF_BIN);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int i0 = blockIdx.x * kBQ;
-    const int hb = blockIdx.y;                 // heads 4 hb .. 4 hb + 3
+    // task task_first + blockIdx.x: query tile task / 2, head half task % 2 (heads
+    // 4 hb .. 4 hb + 3), so that the two halves of a tile, which read the same
+    // bucket rows, run side by side
+    const int task = task_first + (int)blockIdx.x;
+    const int i0 = (task >> 1) * kBQ;
+    const int hb = task & 1;
     // KV blocks kb0 .. kb0 + nblocks - 1 (all of them unless the columns are split
     // over grid.z, in which case dq is summed into dq_acc in fp32)
     const int total_blocks = (n + C::BKV - 1) / C::BKV;
@@ -504,7 +510,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (live && dq_acc) {
                         float* dst = dq_acc + ((int64_t)row * kH + h) * HD;
 #pragma unroll
-                        for (int k = 0; k < HD; ++k) atomicAdd(dst + k, __uint_as_float(ov[c0h + k]) * qscale);
+                        for (int k = 0; k < HD; k += 4)
+                            asm volatile("red.global.v4.f32.add [%0], {%1, %2, %3, %4};" ::"l"(dst + k),
+                                         "f"(__uint_as_float(ov[c0h + k]) * qscale),
+                                         "f"(__uint_as_float(ov[c0h + k + 1]) * qscale),
+                                         "f"(__uint_as_float(ov[c0h + k + 2]) * qscale),
+                                         "f"(__uint_as_float(ov[c0h + k + 3]) * qscale)
+                                         : "memory");
                     } else if (live) {
                         uint32_t wq[HD / 2];
 #pragma unroll
@@ -538,10 +550,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
 }
 
+// The tail tasks' fp32 dq sums to bf16: rows row0 .. n - 1, every head.
+template <int HD>
+__global__ void dq_tail_to_bf16(int n, int row0, const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq) {
+    const int64_t begin = (int64_t)row0 * kH * HD / 4, end = (int64_t)n * kH * HD / 4;
+    for (int64_t x = begin + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < end;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4*>(acc)[x];
+        reinterpret_cast<uint2*>(dq)[x] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+}
+
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
            int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, const float* vmax,
-           int nsplit, void* dq, float* dq_acc, double* dT64, cudaStream_t s) {
+           int nsplit, int tail, void* dq, float* dq_acc, double* dT64, cudaStream_t s) {
     using C = DqCfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -562,27 +585,67 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GT_ERR_CUDA;
     const int total_blocks = (n + C::BKV - 1) / C::BKV;
-    const int per = nsplit > 1 ? (total_blocks + nsplit - 1) / nsplit : 0;
-    const int nz = per > 0 ? (total_blocks + per - 1) / per : 1;
-    dim3 grid((n + kBQ - 1) / kBQ, kH / kHC, nz);
-    {
+    const int tasks = 2 * ((n + kBQ - 1) / kBQ);
+    // tasks [first, first + count), each split over `split` CTAs (1: whole, into dq)
+    auto run = [&](int first, int count, int split) -> int {
+        const int per = split > 1 ? (total_blocks + split - 1) / split : 0;
+        const int nz = per > 0 ? (total_blocks + per - 1) / per : 1;
         LaunchScope ls("bwd_dq", s);
-        kern<<<grid, kThreads, smem, s>>>(
+        kern<<<dim3(count, 1, nz), kThreads, smem, s>>>(
             mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-            ldl, vmax, T, nb, n, scale, scale * kLog2e, per, static_cast<__nv_bfloat16*>(dq),
+            ldl, vmax, T, nb, n, scale, scale * kLog2e, first, per, static_cast<__nv_bfloat16*>(dq),
             per > 0 ? dq_acc : nullptr, dT64, status);
+        return check_launch();
+    };
+    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit);   // every tile split (small graphs)
+    const int slots = 2 * num_sms();
+    if (tail > 1 && dq_acc && tasks % slots != 0) {
+        // full waves of whole tasks, then the rest split `tail` ways along the KV
+        // blocks so that the last waves fill the SMs; their fp32 sums become bf16
+        const int g1 = tasks / slots * slots;
+        if (g1 > 0) {
+            const int rc = run(0, g1, 1);
+            if (rc != GT_OK) return rc;
+        }
+        const int row0 = (g1 >> 1) * kBQ;
+        if (cudaMemsetAsync(dq_acc + (size_t)row0 * kH * HD, 0, sizeof(float) * (size_t)(n - row0) * kH * HD, s) !=
+            cudaSuccess)
+            return GT_ERR_CUDA;
+        const int rc = run(g1, tasks - g1, tail);
+        if (rc != GT_OK) return rc;
+        LaunchScope ls("bwd_dq_tail_to_bf16", s);
+        dq_tail_to_bf16<HD><<<num_sms(), 256, 0, s>>>(n, row0, dq_acc, static_cast<__nv_bfloat16*>(dq));
+        return check_launch();
     }
-    return check_launch();
+    return run(0, tasks, 1);
 }
 
 }  // namespace
 
+// KV split of the dq tasks (tile, head half) past the last full wave of two CTAs
+// per SM (1 = none): the k in [2, 8] that makes the last, partial wave plus the
+// split tail shortest, in units of one task's time; 1 when no k beats one more
+// wave of whole tasks.
+int bwd_dq_tail_split(int n) {
+    const int slots = 2 * num_sms();
+    const int tasks = 2 * ((n + kBQ - 1) / kBQ);
+    if (tasks % slots == 0) return 1;
+    const int rem = tasks % slots;
+    int best = 1;
+    double best_t = 1.0;
+    for (int k = 2; k <= 8; ++k) {
+        const double t = (double)((rem * k + slots - 1) / slots) / k;
+        if (t < best_t - 1e-9) { best_t = t; best = k; }
+    }
+    return best;
+}
+
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, int nsplit, void* dq, float* dq_acc,
+                  const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, dq, dq_acc, dT64, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, dq, dq_acc, dT64, s);
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, tail, dq, dq_acc, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, tail, dq, dq_acc, dT64, s);
 }
 
 }  // namespace gt

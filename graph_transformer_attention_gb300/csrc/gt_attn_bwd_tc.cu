@@ -112,7 +112,7 @@ bool bwd_tc_supported(int h, int d, int nb) { return h == kH && (d == 8 || d == 
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, int nsplit, void* dq, float* dq_acc,
+                  const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
@@ -123,11 +123,13 @@ int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, c
 // [n][8][16], Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j|
 // of head h), and the fp32 sums acc [3][n][8][d] when either split applies
 // (nsplit > 1: every tile's streamed dimension split; tail > 1: the dk/dv groups
-// of the last, partial wave split), else null.
+// of the last, partial wave split; dq_tail > 1: the same for the dq tasks), else
+// null.
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, int tail, float* acc, cudaStream_t s) {
+                float* Dv, double* dT64, float* aux, int nsplit, int tail, int dq_tail, float* acc,
+                cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
     if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
     if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;
@@ -149,8 +151,8 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
         // split streams: fp32 sums, then bf16
         if (cudaMemsetAsync(acc, 0, sizeof(float) * 3 * elems, s) != cudaSuccess) return GT_ERR_CUDA;
     }
-    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1, dq,
-                           split ? acc : nullptr, dT64, s);
+    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1,
+                           acc ? dq_tail : 1, dq, acc, dT64, s);
     if (rc != GT_OK) return rc;
     rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, split ? nsplit : 1, acc ? tail : 1, dk, dv,
                          acc ? acc + elems : nullptr, acc ? acc + 2 * elems : nullptr, s);

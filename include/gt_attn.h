@@ -155,8 +155,24 @@ int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, in
  * kernel splits its KV blocks and the dk/dv kernel its query tiles over up to 4
  * CTAs each, which sum in fp32 (workspace included in
  * gt_bias_attn_workspace_size; a workspace too small for the sums runs unsplit).
+ * Larger graphs split only the work past each kernel's last full wave: the dq
+ * tasks (tile, head half) that would leave the SMs' second slots partly idle
+ * over up to 8 CTAs along the KV blocks, the dk/dv groups the same way along
+ * the query tiles, with the same fp32 sums.
  */
 int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb);
+
+/*
+ * Kernel launches of one gt_bias_attn_fwd call (*fwd, with this kv_block) and of
+ * one gt_bias_attn_bwd call (*bwd, with these nb buckets) on the current device,
+ * given a workspace of gt_bias_attn_workspace_size bytes; memsets are not
+ * counted.  The backward's splits (see gt_bias_attn_bwd_split) each add an fp32
+ * to bf16 conversion, and a split of the tasks past the last full wave its own
+ * second launch when whole tasks fill waves before it.  Returns GT_OK, or
+ * GT_ERR_INVALID_ARG for invalid arguments or NULL outputs.
+ */
+int gt_bias_attn_launches(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb, int32_t kv_block,
+                          int32_t* fwd, int32_t* bwd);
 
 /*
  * Bytes of device workspace needed by gt_bias_attn_fwd (with this kv_block)

@@ -62,3 +62,29 @@ def test_small_graphs_split_their_streams(gt):
     assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 1024) == 1024
     assert gt.load_library().gt_bias_attn_bwd_split(1, 16384, 8, 16, 26) == 1
     assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 16384, 8, 16, 0) == 0
+
+
+def test_counts_of_a_graph_past_one_wave(gt):
+    """n = 16384 (128 tiles): the balanced forward merges its split tiles, and the
+    backward splits the dq tasks and dk/dv groups past their last full wave,
+    each with an fp32-to-bf16 conversion; the library's own launch count
+    matches what ran."""
+    n, h, d, nb = 16384, 8, 16, 26
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=6)
+    q, k, v, dO = (to_dev(x[a], "bf16") for a in ("q", "k", "v", "dO"))
+    T = torch.from_numpy(x["T"]).cuda()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    spd = torch.randint(0, nb, (n, gt.spd_ld(n)), dtype=torch.int8, device="cuda", generator=g)
+    torch.cuda.synchronize()
+    gt.gt_kernel_stats_reset(False)
+    o, lse = gt.gt_bias_attn_fwd(q, k, v, spd, T)
+    gt.gt_bias_attn_bwd(q, k, v, o, dO, lse, spd, T)
+    gt.gt_check_device_status()
+    stats = gt.gt_kernel_stats()
+    gt.gt_kernel_stats_reset(False)
+    per = gt.launches_per_call("bf16", h, d, n, nb=nb)
+    assert sum(c for c, _ in stats.values()) == per["fwd"] + per["bwd"], (stats, per)
+    assert ("fwd_merge" in stats) == (per["fwd"] == 2)
+    if gt.load_library().gt_bias_attn_fwd_ctas(1, n, h, d, 0) > 0:
+        assert stats["fwd_merge"][0] == 1
