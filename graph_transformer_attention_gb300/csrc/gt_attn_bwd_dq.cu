@@ -344,7 +344,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
         auto fx = [&](float v) -> uint32_t { return (uint32_t)__float2int_rn(v); };
         const float qscale = scale / bscale;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // a uniform row's dS sums per head, kept as column pairs until the bin is flushed
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         int acc_code = -1;
         int t = 0;
         bool ok = true;
@@ -372,10 +373,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     if (acc_code >= 0 && acc_code < nb) {
 #pragma unroll
                         for (int hh = 0; hh < 4; ++hh)
-                            red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh]));
+                            red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh].x + acc[hh].y));
                     }
 #pragma unroll
-                    for (int hh = 0; hh < 4; ++hh) acc[hh] = 0.f;
+                    for (int hh = 0; hh < 4; ++hh) acc[hh] = make_float2(0.f, 0.f);
                     acc_code = (int)c0;
                 }
                 const int jc = j0 + c * kCH;
@@ -392,12 +393,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         tc_fence_before();
                         mbar_arrive(&bars->dp_free);
                     }
-                    // x = s scale log2e + bias (scalar FMA), then packed: x - lse, exp, dS;
+                    // x - lse = s scale log2e + bias (scalar FMA) - lse (packed), then exp, dS;
                     // when each of the warp's 32 rows has 16 equal codes (a warp vote, so
                     // the warp never splits), a row takes its 4 head biases once
                     if (wuni) {
                         // x - lse log2 e = s scale log2 e + (b - lse log2 e): one packed FMA
-                        // per two columns (the subtraction below then takes 0)
+                        // per two columns
                         const float4 bv = lds_f4(tbl + c0 * 32u);
                         const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -413,6 +414,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             }
                         }
                     } else {
+                        // then (head dim 16) x - lse log2 e, packed, per column pair as it is
+                        // formed; head dim 8 takes it in the exponential loop below, which
+                        // measured faster there (on uniform chunks it adds 0)
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int kk = 8 * g + k;
@@ -422,6 +426,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
                             rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
                             rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
+                            if (HD == 16 && (k & 1)) {
+#pragma unroll
+                                for (int hh = 0; hh < 4; ++hh) {
+                                    const float2 xv = __fadd2_rn(
+                                        make_float2(__uint_as_float(rs[hh][k - 1]), __uint_as_float(rs[hh][k])),
+                                        make_float2(-L2[hh], -L2[hh]));
+                                    rs[hh][k - 1] = __float_as_uint(xv.x);
+                                    rs[hh][k] = __float_as_uint(xv.y);
+                                }
+                            }
                         }
                     }
                     if (tail_block) {
@@ -434,13 +448,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     }
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        const float2 ml = wuni ? make_float2(0.f, 0.f) : make_float2(-L2[hh], -L2[hh]);
                         const float2 md = make_float2(-Dh[hh], -Dh[hh]);
+                        const float2 ml = wuni ? make_float2(0.f, 0.f) : make_float2(-L2[hh], -L2[hh]);
                         uint32_t pk[4];
 #pragma unroll
                         for (int k = 0; k < 8; k += 2) {
-                            const float2 xv = __fadd2_rn(make_float2(__uint_as_float(rs[hh][k]),
-                                                                     __uint_as_float(rs[hh][k + 1])), ml);
+                            float2 xv = make_float2(__uint_as_float(rs[hh][k]), __uint_as_float(rs[hh][k + 1]));
+                            if (HD == 8) xv = __fadd2_rn(xv, ml);
                             const float2 p = make_float2(ex2(xv.x), ex2(xv.y));
                             const float2 dv = __fadd2_rn(make_float2(__uint_as_float(rd[hh][k]),
                                                                      __uint_as_float(rd[hh][k + 1])), md);
@@ -450,11 +464,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             pk[k / 2] = pack_bf16x2(ds.x, ds.y);
                         }
                         if (uniform) {      // the row's sum for its register bin (mixed rows bin each element)
-                            float2 sum = make_float2(__uint_as_float(rd[hh][0]), __uint_as_float(rd[hh][1]));
 #pragma unroll
-                            for (int k = 2; k < 8; k += 2)
-                                sum = __fadd2_rn(sum, make_float2(__uint_as_float(rd[hh][k]), __uint_as_float(rd[hh][k + 1])));
-                            acc[hh] += sum.x + sum.y;
+                            for (int k = 0; k < 8; k += 2)
+                                acc[hh] = __fadd2_rn(acc[hh], make_float2(__uint_as_float(rd[hh][k]),
+                                                                         __uint_as_float(rd[hh][k + 1])));
                         }
                         tmem_st_x4(lrow + s_col(ss) + 16 * hh + 4 * g, pk);
                     }
@@ -490,7 +503,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         if (acc_code >= 0 && acc_code < nb) {
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh)
-                red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh]));
+                red_shared_add_u32(binb + acc_code * kCodeStride + hh * kHeadStride, fx(acc[hh].x + acc[hh].y));
         }
         if (!ok) {
             fail(abort_flag, status);
