@@ -126,6 +126,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();   // the split tail may take SMs as this launch frees them
     const int g = g0 + (int)blockIdx.x;        // group: KV tile g / 2, head half g % 2
     const int j0 = (g >> 1) * kBKV;
     const int hb = g & 1;                      // heads 4 hb .. 4 hb + 3
@@ -496,6 +497,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
     }
+    if (tid == 0) pdl_wait();   // complete after the kernel before, which this one may overlap
 }
 
 // the tail groups' fp32 sums to bf16: one thread per (row, head) of rows row0 ..
@@ -531,6 +533,15 @@ __global__ void dkdv_tail_to_bf16(int n, int row0, int g1, const float* __restri
     }
 }
 
+// First KV row of the groups the tail split takes (groups past the last full
+// wave of one CTA per SM, summed in fp32), or -1 when there is no such split.
+int dkdv_tail_row0(int n, int tail, bool have_acc) {
+    const int sms = num_sms();
+    const int groups = 2 * ((n + kBKV - 1) / kBKV);
+    if (tail <= 1 || !have_acc || groups <= sms || groups % sms == 0) return -1;
+    return (groups / sms * sms / 2) * kBKV;
+}
+
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
            int64_t ld, const float* T, int nb, float scale, float fold_scale, const uint16_t* LB, int nsplit,
@@ -554,14 +565,18 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     if (!status) return GT_ERR_CUDA;
     const int total_tiles = (n + C::BQ - 1) / C::BQ;
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
+    // every launch may overlap the kernel before it (the dq kernel, or the full
+    // waves): it reads only the inputs and the prep tables
     auto run = [&](int g_first, int g_count, int per, bool sums) -> int {
         const int nz = per > 0 ? (total_tiles + per - 1) / per : 1;
         dim3 grid(g_count, 1, nz);
         LaunchScope ls("bwd_dkdv", s);
-        bwd_dkdv_kernel<HD><<<grid, kThreads, C::SMEM, s>>>(
-            mq, mg, ms, ml, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T, nb,
-            n, scale, fold_scale * kLog2e, g_first, per, static_cast<__nv_bfloat16*>(dk),
-            static_cast<__nv_bfloat16*>(dv), sums ? dk_acc : nullptr, sums ? dv_acc : nullptr, status);
+        if (launch_overlapped(bwd_dkdv_kernel<HD>, grid, dim3(kThreads), C::SMEM, s, mq, mg, ms, ml,
+                              static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T, nb, n,
+                              scale, fold_scale * kLog2e, g_first, per, static_cast<__nv_bfloat16*>(dk),
+                              static_cast<__nv_bfloat16*>(dv), sums ? dk_acc : nullptr, sums ? dv_acc : nullptr,
+                              status) != cudaSuccess)
+            return GT_ERR_CUDA;
         return check_launch();
     };
     if (nsplit > 1 && dk_acc) {
@@ -569,17 +584,14 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         return run(0, groups, (total_tiles + nsplit - 1) / nsplit, true);
     }
     const int sms = num_sms();
-    if (tail > 1 && dk_acc && groups > sms && groups % sms != 0) {
+    const int row0 = dkdv_tail_row0(n, tail, dk_acc != nullptr);
+    if (row0 >= 0) {
         // full waves of whole groups, then the remaining groups split tail ways so
-        // that the last wave fills the SMs; their fp32 sums become bf16 at the end
-        const int g1 = groups / sms * sms;
+        // that the last wave fills the SMs; the caller cleared their rows of the
+        // sums before, and they become bf16 at the end
+        const int g1 = (row0 / kBKV) * 2;
         int rc = run(0, g1, 0, false);
         if (rc != GT_OK) return rc;
-        const int row0 = (g1 >> 1) * kBKV;
-        const size_t bytes = sizeof(float) * (size_t)(n - row0) * kH * HD;
-        if (cudaMemsetAsync(dk_acc + (size_t)row0 * kH * HD, 0, bytes, s) != cudaSuccess ||
-            cudaMemsetAsync(dv_acc + (size_t)row0 * kH * HD, 0, bytes, s) != cudaSuccess)
-            return GT_ERR_CUDA;
         rc = run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
         if (rc != GT_OK) return rc;
         LaunchScope ls("bwd_dkdv_tail_to_bf16", s);
@@ -591,6 +603,8 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
 }
 
 }  // namespace
+
+int bwd_dkdv_tail_row0(int n, int tail, bool have_acc) { return dkdv_tail_row0(n, tail, have_acc); }
 
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,

@@ -132,6 +132,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     int* bins = reinterpret_cast<int*>(smem + C::OFF_BIN);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();   // the next kernel (dk/dv, or this one's split tail) may take SMs as this one's free
     // task task_first + blockIdx.x: query tile task / 2, head half task % 2 (heads
     // 4 hb .. 4 hb + 3), so that the two halves of a tile, which read the same
     // bucket rows, run side by side
@@ -561,6 +562,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
     }
+    if (tid == 0) pdl_wait();   // complete after the kernel before, if this one overlapped it
 }
 
 // The tail tasks' fp32 dq sums to bf16: rows row0 .. n - 1, every head.
@@ -572,6 +574,15 @@ __global__ void dq_tail_to_bf16(int n, int row0, const float* __restrict__ acc, 
         const float4 v = reinterpret_cast<const float4*>(acc)[x];
         reinterpret_cast<uint2*>(dq)[x] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     }
+}
+
+// First row of the tasks the tail split takes (tasks past the last full wave of
+// two CTAs per SM, whose dq goes through dq_acc), or -1 when there is no such split.
+int dq_tail_row0(int n, int tail, bool have_acc) {
+    const int slots = 2 * num_sms();
+    const int tasks = 2 * ((n + kBQ - 1) / kBQ);
+    if (tail <= 1 || !have_acc || tasks % slots == 0) return -1;
+    return (tasks / slots * slots / 2) * kBQ;
 }
 
 template <int HD>
@@ -599,38 +610,42 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         return GT_ERR_CUDA;
     const int total_blocks = (n + C::BKV - 1) / C::BKV;
     const int tasks = 2 * ((n + kBQ - 1) / kBQ);
-    // tasks [first, first + count), each split over `split` CTAs (1: whole, into dq)
-    auto run = [&](int first, int count, int split) -> int {
+    // tasks [first, first + count), each split over `split` CTAs (1: whole, into dq);
+    // `overlap`: may start while the launch before it finishes
+    auto run = [&](int first, int count, int split, bool overlap) -> int {
         const int per = split > 1 ? (total_blocks + split - 1) / split : 0;
         const int nz = per > 0 ? (total_blocks + per - 1) / per : 1;
+        const dim3 grid(count, 1, nz);
         LaunchScope ls("bwd_dq", s);
-        kern<<<dim3(count, 1, nz), kThreads, smem, s>>>(
-            mk, mv, ms, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), LD,
-            ldl, vmax, T, nb, n, scale, scale * kLog2e, first, per, static_cast<__nv_bfloat16*>(dq),
-            per > 0 ? dq_acc : nullptr, dT64, status);
+        auto* qp = static_cast<const __nv_bfloat16*>(q);
+        auto* gp = static_cast<const __nv_bfloat16*>(dO);
+        auto* dqp = static_cast<__nv_bfloat16*>(dq);
+        float* accp = per > 0 ? dq_acc : nullptr;
+        if (overlap) {
+            if (launch_overlapped(kern, grid, dim3(kThreads), smem, s, mk, mv, ms, qp, gp, LD, ldl, vmax, T, nb, n,
+                                  scale, scale * kLog2e, first, per, dqp, accp, dT64, status) != cudaSuccess)
+                return GT_ERR_CUDA;
+        } else {
+            kern<<<grid, kThreads, smem, s>>>(mk, mv, ms, qp, gp, LD, ldl, vmax, T, nb, n, scale, scale * kLog2e,
+                                              first, per, dqp, accp, dT64, status);
+        }
         return check_launch();
     };
-    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit);   // every tile split (small graphs)
-    const int slots = 2 * num_sms();
-    if (tail > 1 && dq_acc && tasks % slots != 0) {
+    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit, false);   // every tile split (small graphs)
+    const int row0 = dq_tail_row0(n, tail, dq_acc != nullptr);
+    if (row0 >= 0) {
         // full waves of whole tasks, then the rest split `tail` ways along the KV
-        // blocks so that the last waves fill the SMs; their fp32 sums become bf16
-        const int g1 = tasks / slots * slots;
+        // blocks so that the last waves fill the SMs, overlapping the whole
+        // tasks' last wave; the caller cleared their rows of dq_acc before and
+        // converts them after (bwd_dq_tail_finish)
+        const int g1 = (row0 / kBQ) * 2;
         if (g1 > 0) {
-            const int rc = run(0, g1, 1);
+            const int rc = run(0, g1, 1, false);
             if (rc != GT_OK) return rc;
         }
-        const int row0 = (g1 >> 1) * kBQ;
-        if (cudaMemsetAsync(dq_acc + (size_t)row0 * kH * HD, 0, sizeof(float) * (size_t)(n - row0) * kH * HD, s) !=
-            cudaSuccess)
-            return GT_ERR_CUDA;
-        const int rc = run(g1, tasks - g1, tail);
-        if (rc != GT_OK) return rc;
-        LaunchScope ls("bwd_dq_tail_to_bf16", s);
-        dq_tail_to_bf16<HD><<<num_sms(), 256, 0, s>>>(n, row0, dq_acc, static_cast<__nv_bfloat16*>(dq));
-        return check_launch();
+        return run(g1, tasks - g1, tail, g1 > 0);
     }
-    return run(0, tasks, 1);
+    return run(0, tasks, 1, false);
 }
 
 }  // namespace
@@ -651,6 +666,16 @@ int bwd_dq_tail_split(int n) {
         if (t < best_t - 1e-9) { best_t = t; best = k; }
     }
     return best;
+}
+
+int bwd_dq_tail_row0(int n, int tail, bool have_acc) { return dq_tail_row0(n, tail, have_acc); }
+
+// The tail tasks' fp32 dq sums (rows row0 .. n - 1 of dq_acc) to bf16.
+int bwd_dq_tail_finish(int n, int d, int row0, const float* dq_acc, void* dq, cudaStream_t s) {
+    LaunchScope ls("bwd_dq_tail_to_bf16", s);
+    auto conv = d == 8 ? dq_tail_to_bf16<8> : dq_tail_to_bf16<16>;
+    conv<<<num_sms(), 256, 0, s>>>(n, row0, dq_acc, static_cast<__nv_bfloat16*>(dq));
+    return check_launch();
 }
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,

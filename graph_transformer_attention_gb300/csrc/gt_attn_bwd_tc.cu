@@ -114,6 +114,9 @@ int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, con
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
                   const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s);
+int bwd_dq_tail_row0(int n, int tail, bool have_acc);
+int bwd_dq_tail_finish(int n, int d, int row0, const float* dq_acc, void* dq, cudaStream_t s);
+int bwd_dkdv_tail_row0(int n, int tail, bool have_acc);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
                     const uint16_t* LB, int nsplit, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
@@ -138,18 +141,31 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     // the dk/dv kernel takes -lse / scale; a zero scale (scores = bias alone) uses a
     // scale far below any product's resolution instead, with the same results
     const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
+    const size_t elems = (size_t)n * kH * d;
+    const bool split = nsplit > 1 && acc;
+    // the fp32 sums are cleared before the kernels, so that nothing stands between
+    // the dq and dk/dv launches in the stream (the dk/dv kernel may start on the
+    // SMs the dq kernel's last wave leaves free; it reads only the inputs and the
+    // prep tables)
+    const int dq_row0 = split ? -1 : bwd_dq_tail_row0(n, dq_tail, acc != nullptr);
+    const int kv_row0 = split ? -1 : bwd_dkdv_tail_row0(n, tail, acc != nullptr);
+    if (split) {
+        if (cudaMemsetAsync(acc, 0, sizeof(float) * 3 * elems, s) != cudaSuccess) return GT_ERR_CUDA;
+    } else {
+        const size_t row = (size_t)kH * d;
+        if (dq_row0 >= 0 && cudaMemsetAsync(acc + dq_row0 * row, 0, sizeof(float) * (n - dq_row0) * row, s) != cudaSuccess)
+            return GT_ERR_CUDA;
+        if (kv_row0 >= 0 &&
+            (cudaMemsetAsync(acc + elems + kv_row0 * row, 0, sizeof(float) * (n - kv_row0) * row, s) != cudaSuccess ||
+             cudaMemsetAsync(acc + 2 * elems + kv_row0 * row, 0, sizeof(float) * (n - kv_row0) * row, s) != cudaSuccess))
+            return GT_ERR_CUDA;
+    }
     {
         LaunchScope ls("bwd_prep", s);
         auto prep = d == 8 ? bwd_prep<8> : bwd_prep<16>;
         prep<<<pblocks, 256, 0, s>>>(n, ldl, 1.f / fold_scale, static_cast<const __nv_bfloat16*>(o),
                                      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(v),
                                      lse, LD, LB, Dv, aux);
-    }
-    const size_t elems = (size_t)n * kH * d;
-    const bool split = nsplit > 1 && acc;
-    if (split) {
-        // split streams: fp32 sums, then bf16
-        if (cudaMemsetAsync(acc, 0, sizeof(float) * 3 * elems, s) != cudaSuccess) return GT_ERR_CUDA;
     }
     int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1,
                            acc ? dq_tail : 1, dq, acc, dT64, s);
@@ -161,6 +177,9 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
         LaunchScope ls("bwd_acc_to_bf16", s);
         acc_to_bf16<<<2 * num_sms(), 256, 0, s>>>(elems, acc, static_cast<__nv_bfloat16*>(dq),
                                                  static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
+    } else if (dq_row0 >= 0) {
+        rc = bwd_dq_tail_finish(n, d, dq_row0, acc, dq, s);
+        if (rc != GT_OK) return rc;
     }
     {
         LaunchScope ls("bwd_dT_to_f32", s);

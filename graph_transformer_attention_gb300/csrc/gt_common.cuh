@@ -1,6 +1,8 @@
 // gt_common.cuh -- shared host/device helpers of libgt (status codes, launch checks).
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -31,6 +33,28 @@ inline int num_sms() {
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
     return sms > 0 ? sms : 1;
+}
+
+// Launches `kern` so that it may overlap the kernel before it in the stream
+// (programmatic dependent launch): its CTAs can be scheduled once every CTA of
+// that kernel has executed griddepcontrol.launch_dependents or exited, while
+// that kernel still runs.  A kernel launched this way reads nothing the one
+// before it writes, and ends with griddepcontrol.wait, so that it completes
+// after it and the stream's later work sees both.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Element access for the two storage types.

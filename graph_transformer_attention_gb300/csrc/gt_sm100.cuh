@@ -91,6 +91,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // cycles and one with both operands in shared memory 39 (the 4 KB A operand at
 // 128 B per clock); from a lane-0 branch of a diverged warp, or behind a plain
 // lane test, every MMA costs 45-55 cycles whatever its operands.
+// Programmatic dependent launch.  pdl_trigger: this CTA lets the next kernel of
+// the stream, when that one is launched with programmatic stream serialization,
+// be scheduled once every CTA of this grid has triggered or exited.  pdl_wait:
+// waits until the grid before this one in the stream has completed and its
+// memory is visible (returns at once when nothing precedes it that way).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
     asm volatile(
