@@ -240,12 +240,11 @@ int gt_bias_attn_launches(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_
         *bwd = 4;   // D, rows, columns, dT
         return GT_OK;
     }
-    // prep, dq, dk/dv, dT; the small-graph split adds one conversion; a tail
-    // split adds its second launch (when full waves come first) and a conversion
+    // prep, dq, dk/dv, and the finish (fp32 sums and dT converted); a tail split
+    // adds its second launch when whole tasks fill waves before it
     int count = 4;
-    if (gt::bwd_split(dtype, n, h, d, nb) > 1) count += 1;
-    if (gt::bwd_tail(dtype, n, h, d, nb) > 1) count += 2;
-    if (gt::bwd_dq_tail(dtype, n, h, d, nb) > 1) count += (2 * ((n + 127) / 128) >= 2 * gt::num_sms()) ? 2 : 1;
+    if (gt::bwd_tail(dtype, n, h, d, nb) > 1) count += 1;
+    if (gt::bwd_dq_tail(dtype, n, h, d, nb) > 1 && 2 * ((n + 127) / 128) >= 2 * gt::num_sms()) count += 1;
     *bwd = count;
     return GT_OK;
 }

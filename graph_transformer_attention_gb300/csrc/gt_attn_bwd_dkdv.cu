@@ -500,38 +500,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (tid == 0) pdl_wait();   // complete after the kernel before, which this one may overlap
 }
 
-// the tail groups' fp32 sums to bf16: one thread per (row, head) of rows row0 ..
-// n - 1, converting the head's HD values when its group (KV tile row / 128, head
-// half) is one of the split groups >= g1
-template <int HD>
-__global__ void dkdv_tail_to_bf16(int n, int row0, int g1, const float* __restrict__ dk_acc,
-                                  const float* __restrict__ dv_acc, __nv_bfloat16* __restrict__ dk,
-                                  __nv_bfloat16* __restrict__ dv) {
-    const int total = (n - row0) * kH;
-    for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < total; x += gridDim.x * blockDim.x) {
-        const int row = row0 + x / kH, h = x % kH;
-        if ((row / kBKV) * 2 + h / kHC < g1) continue;
-        const int64_t e = ((int64_t)row * kH + h) * HD;
-        const float4* sk = reinterpret_cast<const float4*>(dk_acc + e);
-        const float4* sv = reinterpret_cast<const float4*>(dv_acc + e);
-        uint32_t wk[HD / 2], wv[HD / 2];
-#pragma unroll
-        for (int q = 0; q < HD / 4; ++q) {
-            const float4 a = sk[q], b = sv[q];
-            wk[2 * q] = pack_bf16x2(a.x, a.y);
-            wk[2 * q + 1] = pack_bf16x2(a.z, a.w);
-            wv[2 * q] = pack_bf16x2(b.x, b.y);
-            wv[2 * q + 1] = pack_bf16x2(b.z, b.w);
-        }
-        uint4* dk4 = reinterpret_cast<uint4*>(dk + e);
-        uint4* dv4 = reinterpret_cast<uint4*>(dv + e);
-#pragma unroll
-        for (int q = 0; q < HD / 8; ++q) {
-            dk4[q] = make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-            dv4[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-        }
-    }
-}
 
 // First KV row of the groups the tail split takes (groups past the last full
 // wave of one CTA per SM, summed in fp32), or -1 when there is no such split.
@@ -583,21 +551,15 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         // every group split over nsplit CTAs (graphs with fewer groups than SMs)
         return run(0, groups, (total_tiles + nsplit - 1) / nsplit, true);
     }
-    const int sms = num_sms();
     const int row0 = dkdv_tail_row0(n, tail, dk_acc != nullptr);
     if (row0 >= 0) {
         // full waves of whole groups, then the remaining groups split tail ways so
         // that the last wave fills the SMs; the caller cleared their rows of the
-        // sums before, and they become bf16 at the end
+        // sums before and turns them into bf16 after
         const int g1 = (row0 / kBKV) * 2;
-        int rc = run(0, g1, 0, false);
+        const int rc = run(0, g1, 0, false);
         if (rc != GT_OK) return rc;
-        rc = run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
-        if (rc != GT_OK) return rc;
-        LaunchScope ls("bwd_dkdv_tail_to_bf16", s);
-        dkdv_tail_to_bf16<HD><<<sms, 256, 0, s>>>(n, row0, g1, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
-                                                  static_cast<__nv_bfloat16*>(dv));
-        return check_launch();
+        return run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
     }
     return run(0, groups, 0, false);
 }

@@ -565,17 +565,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     if (tid == 0) pdl_wait();   // complete after the kernel before, if this one overlapped it
 }
 
-// The tail tasks' fp32 dq sums to bf16: rows row0 .. n - 1, every head.
-template <int HD>
-__global__ void dq_tail_to_bf16(int n, int row0, const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq) {
-    const int64_t begin = (int64_t)row0 * kH * HD / 4, end = (int64_t)n * kH * HD / 4;
-    for (int64_t x = begin + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < end;
-         x += (int64_t)gridDim.x * blockDim.x) {
-        const float4 v = reinterpret_cast<const float4*>(acc)[x];
-        reinterpret_cast<uint2*>(dq)[x] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    }
-}
-
 // First row of the tasks the tail split takes (tasks past the last full wave of
 // two CTAs per SM, whose dq goes through dq_acc), or -1 when there is no such split.
 int dq_tail_row0(int n, int tail, bool have_acc) {
@@ -637,7 +626,7 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         // full waves of whole tasks, then the rest split `tail` ways along the KV
         // blocks so that the last waves fill the SMs, overlapping the whole
         // tasks' last wave; the caller cleared their rows of dq_acc before and
-        // converts them after (bwd_dq_tail_finish)
+        // converts them after
         const int g1 = (row0 / kBQ) * 2;
         if (g1 > 0) {
             const int rc = run(0, g1, 1, false);
@@ -669,14 +658,6 @@ int bwd_dq_tail_split(int n) {
 }
 
 int bwd_dq_tail_row0(int n, int tail, bool have_acc) { return dq_tail_row0(n, tail, have_acc); }
-
-// The tail tasks' fp32 dq sums (rows row0 .. n - 1 of dq_acc) to bf16.
-int bwd_dq_tail_finish(int n, int d, int row0, const float* dq_acc, void* dq, cudaStream_t s) {
-    LaunchScope ls("bwd_dq_tail_to_bf16", s);
-    auto conv = d == 8 ? dq_tail_to_bf16<8> : dq_tail_to_bf16<16>;
-    conv<<<num_sms(), 256, 0, s>>>(n, row0, dq_acc, static_cast<__nv_bfloat16*>(dq));
-    return check_launch();
-}
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,

@@ -16,7 +16,8 @@
 //               largest row norm of v (bounds the dT sums, see bwd_dq).
 //   bwd_dq      (gt_attn_bwd_dq.cu) Q-stationary: dq and dT.
 //   bwd_dkdv    (gt_attn_bwd_dkdv.cu) KV-stationary: dk and dv.
-//   dT_to_f32   the fp64 bucket sums to the fp32 output.
+//   bwd_finish  the fp32 sums of split work to bf16 and the fp64 bucket sums
+//               to the fp32 output, in one launch.
 // Everything runs on the caller's stream, in this order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -91,19 +92,38 @@ __global__ void bwd_prep(int n, int ldl, float inv_scale, const __nv_bfloat16* _
     }
 }
 
-// the split backward's fp32 sums [3][elems] (dq, dk, dv) to the bf16 outputs
-__global__ void acc_to_bf16(size_t elems, const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                            __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv) {
-    for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < elems; x += (size_t)gridDim.x * blockDim.x) {
-        dq[x] = __float2bfloat16_rn(acc[x]);
-        dk[x] = __float2bfloat16_rn(acc[elems + x]);
-        dv[x] = __float2bfloat16_rn(acc[2 * elems + x]);
-    }
+__device__ __forceinline__ uint2 bf16x4(float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
 }
 
-__global__ void dT_to_f32(int count, const double* __restrict__ dT64, float* __restrict__ dT) {
-    for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < count; x += gridDim.x * blockDim.x)
-        dT[x] = (float)dT64[x];
+// The backward's last step, one launch: the fp32 sums of split work to bf16 --
+// dq rows dq_row0 .. n - 1 (dq_row0 < 0: none), dk and dv rows kv_row0 .. n - 1
+// of the (KV tile, head half) groups >= kv_g1 (kv_row0 < 0: none); acc holds
+// [3][n][8][HD] (dq, dk, dv) -- and the fp64 bucket sums dT64 to fp32.  Grid-
+// stride over 4-value pieces.
+template <int HD>
+__global__ void bwd_finish(int n, const float* __restrict__ acc, int dq_row0, int kv_row0, int kv_g1,
+                           __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
+                           __nv_bfloat16* __restrict__ dv, int dT_count, const double* __restrict__ dT64,
+                           float* __restrict__ dT) {
+    constexpr int kRow4 = kH * HD / 4;   // 4-value pieces per node
+    const int64_t elems4 = (int64_t)n * kRow4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const float4* a4 = reinterpret_cast<const float4*>(acc);
+    if (dq_row0 >= 0)
+        for (int64_t x = (int64_t)dq_row0 * kRow4 + t0; x < elems4; x += stride)
+            reinterpret_cast<uint2*>(dq)[x] = bf16x4(a4[x]);
+    if (kv_row0 >= 0)
+        for (int64_t x = (int64_t)kv_row0 * kRow4 + t0; x < elems4; x += stride) {
+            const int64_t row = x / kRow4;
+            const int h = (int)((x % kRow4) / (HD / 4));
+            if ((int)(row / 128) * 2 + h / 4 < kv_g1) continue;   // a whole group, written by its CTA
+            reinterpret_cast<uint2*>(dk)[x] = bf16x4(a4[elems4 + x]);
+            reinterpret_cast<uint2*>(dv)[x] = bf16x4(a4[2 * elems4 + x]);
+        }
+    for (int64_t x = t0; x < dT_count; x += stride) dT[x] = (float)dT64[x];
 }
 
 }  // namespace
@@ -115,7 +135,6 @@ int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, con
                   const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s);
 int bwd_dq_tail_row0(int n, int tail, bool have_acc);
-int bwd_dq_tail_finish(int n, int d, int row0, const float* dq_acc, void* dq, cudaStream_t s);
 int bwd_dkdv_tail_row0(int n, int tail, bool have_acc);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
@@ -173,17 +192,14 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, split ? nsplit : 1, acc ? tail : 1, dk, dv,
                          acc ? acc + elems : nullptr, acc ? acc + 2 * elems : nullptr, s);
     if (rc != GT_OK) return rc;
-    if (split) {
-        LaunchScope ls("bwd_acc_to_bf16", s);
-        acc_to_bf16<<<2 * num_sms(), 256, 0, s>>>(elems, acc, static_cast<__nv_bfloat16*>(dq),
-                                                 static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
-    } else if (dq_row0 >= 0) {
-        rc = bwd_dq_tail_finish(n, d, dq_row0, acc, dq, s);
-        if (rc != GT_OK) return rc;
-    }
     {
-        LaunchScope ls("bwd_dT_to_f32", s);
-        dT_to_f32<<<1, 256, 0, s>>>(kH * nb, dT64, dT);
+        // the small-graph split sums every row of dq, dk and dv
+        LaunchScope ls("bwd_finish", s);
+        auto fin = d == 8 ? bwd_finish<8> : bwd_finish<16>;
+        fin<<<2 * num_sms(), 512, 0, s>>>(n, acc, split ? 0 : dq_row0, split ? 0 : kv_row0,
+                                          split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
+                                          static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+                                          static_cast<__nv_bfloat16*>(dv), kH * nb, dT64, dT);
     }
     return check_launch();
 }

@@ -166,9 +166,10 @@ int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, i
  * Kernel launches of one gt_bias_attn_fwd call (*fwd, with this kv_block) and of
  * one gt_bias_attn_bwd call (*bwd, with these nb buckets) on the current device,
  * given a workspace of gt_bias_attn_workspace_size bytes; memsets are not
- * counted.  The backward's splits (see gt_bias_attn_bwd_split) each add an fp32
- * to bf16 conversion, and a split of the tasks past the last full wave its own
- * second launch when whole tasks fill waves before it.  Returns GT_OK, or
+ * counted.  A split of the tasks past the last full wave (see
+ * gt_bias_attn_bwd_split) adds the split tasks' own launch when whole tasks
+ * fill waves before them; the backward's last launch converts every split's
+ * fp32 sums and the bucket sums at once.  Returns GT_OK, or
  * GT_ERR_INVALID_ARG for invalid arguments or NULL outputs.
  */
 int gt_bias_attn_launches(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb, int32_t kv_block,
