@@ -123,7 +123,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const float* __restrict__ vmax,
               const float* __restrict__ T, int nb, int n, float scale, float scale_log2,
               int task_first, int split_blocks, __nv_bfloat16* __restrict__ dq, float* __restrict__ dq_acc,
-              double* __restrict__ dT64, int* status) {
+              double* __restrict__ dT64, int after_prep, int* status) {
     using C = DqCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -132,7 +132,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     int* bins = reinterpret_cast<int*>(smem + C::OFF_BIN);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_trigger();   // the next kernel (dk/dv, or this one's split tail) may take SMs as this one's free
+    // after_prep: launched to overlap the prep kernel, whose tables (LD, vmax) it
+    // may read only after griddepcontrol.wait (below, once the prologue has run on
+    // the inputs alone); its dependents, which read those tables too, are let in
+    // only then.  Otherwise the kernel before it wrote nothing it reads.
+    if (!after_prep) pdl_trigger();   // the next kernel may take SMs as this one's free
     // task task_first + blockIdx.x: query tile task / 2, head half task % 2 (heads
     // 4 hb .. 4 hb + 3), so that the two halves of a tile, which read the same
     // bucket rows, run side by side
@@ -175,6 +179,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         write_head_operands<HD, kHC>(smem + C::OFF_Q, tid, q + off, live, kHC * hb);
         write_head_operands<HD, kHC>(smem + C::OFF_G, tid, dO + off, live, kHC * hb);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (after_prep) {
+        pdl_wait();
+        pdl_trigger();
     }
     tc_fence_before();
     __syncthreads();
@@ -600,8 +608,10 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
     const int total_blocks = (n + C::BKV - 1) / C::BKV;
     const int tasks = 2 * ((n + kBQ - 1) / kBQ);
     // tasks [first, first + count), each split over `split` CTAs (1: whole, into dq);
-    // `overlap`: may start while the launch before it finishes
-    auto run = [&](int first, int count, int split, bool overlap) -> int {
+    // every launch may start while the one before it finishes: the first one
+    // overlaps the prep kernel (and waits for it before reading its tables), the
+    // split tail the whole tasks' last wave
+    auto run = [&](int first, int count, int split, bool after_prep) -> int {
         const int per = split > 1 ? (total_blocks + split - 1) / split : 0;
         const int nz = per > 0 ? (total_blocks + per - 1) / per : 1;
         const dim3 grid(count, 1, nz);
@@ -610,17 +620,13 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         auto* gp = static_cast<const __nv_bfloat16*>(dO);
         auto* dqp = static_cast<__nv_bfloat16*>(dq);
         float* accp = per > 0 ? dq_acc : nullptr;
-        if (overlap) {
-            if (launch_overlapped(kern, grid, dim3(kThreads), smem, s, mk, mv, ms, qp, gp, LD, ldl, vmax, T, nb, n,
-                                  scale, scale * kLog2e, first, per, dqp, accp, dT64, status) != cudaSuccess)
-                return GT_ERR_CUDA;
-        } else {
-            kern<<<grid, kThreads, smem, s>>>(mk, mv, ms, qp, gp, LD, ldl, vmax, T, nb, n, scale, scale * kLog2e,
-                                              first, per, dqp, accp, dT64, status);
-        }
+        if (launch_overlapped(kern, grid, dim3(kThreads), smem, s, mk, mv, ms, qp, gp, LD, ldl, vmax, T, nb, n,
+                              scale, scale * kLog2e, first, per, dqp, accp, dT64, after_prep ? 1 : 0,
+                              status) != cudaSuccess)
+            return GT_ERR_CUDA;
         return check_launch();
     };
-    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit, false);   // every tile split (small graphs)
+    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit, true);   // every tile split (small graphs)
     const int row0 = dq_tail_row0(n, tail, dq_acc != nullptr);
     if (row0 >= 0) {
         // full waves of whole tasks, then the rest split `tail` ways along the KV
@@ -629,12 +635,12 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         // converts them after
         const int g1 = (row0 / kBQ) * 2;
         if (g1 > 0) {
-            const int rc = run(0, g1, 1, false);
+            const int rc = run(0, g1, 1, true);
             if (rc != GT_OK) return rc;
         }
-        return run(g1, tasks - g1, tail, g1 > 0);
+        return run(g1, tasks - g1, tail, g1 == 0);
     }
-    return run(0, tasks, 1, false);
+    return run(0, tasks, 1, true);
 }
 
 }  // namespace

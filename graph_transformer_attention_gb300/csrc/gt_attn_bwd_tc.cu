@@ -26,6 +26,7 @@
 
 #include "gt_common.cuh"
 #include "gt_stats.cuh"
+#include "gt_sm100.cuh"
 #include "gt_tc_common.cuh"
 
 namespace gt {
@@ -34,6 +35,8 @@ namespace {
 using tc::kH;
 using tc::kLog2e;
 using tc::split3_bf16;
+using sm100::pdl_trigger;
+using sm100::pdl_wait;
 
 constexpr int kMaxNb = 128;
 
@@ -44,6 +47,7 @@ __global__ void bwd_prep(int n, int ldl, float inv_scale, const __nv_bfloat16* _
                          const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ v,
                          const float* __restrict__ lse, float* __restrict__ LD, uint16_t* __restrict__ LB,
                          float* __restrict__ Dv, float* __restrict__ vmax) {
+    pdl_trigger();   // the dq kernel's prologue may run meanwhile; it waits for this grid before reading
     const int64_t total = (int64_t)n * kH;
     // the loop bound is the same for the whole block, so every lane reaches the shuffles
     for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
@@ -107,6 +111,7 @@ __global__ void bwd_finish(int n, const float* __restrict__ acc, int dq_row0, in
                            __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
                            __nv_bfloat16* __restrict__ dv, int dT_count, const double* __restrict__ dT64,
                            float* __restrict__ dT) {
+    pdl_wait();   // launched to overlap the dk/dv kernel's end: its sums are complete after this
     constexpr int kRow4 = kH * HD / 4;   // 4-value pieces per node
     const int64_t elems4 = (int64_t)n * kRow4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -196,10 +201,11 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
         // the small-graph split sums every row of dq, dk and dv
         LaunchScope ls("bwd_finish", s);
         auto fin = d == 8 ? bwd_finish<8> : bwd_finish<16>;
-        fin<<<2 * num_sms(), 512, 0, s>>>(n, acc, split ? 0 : dq_row0, split ? 0 : kv_row0,
-                                          split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
-                                          static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                          static_cast<__nv_bfloat16*>(dv), kH * nb, dT64, dT);
+        if (launch_overlapped(fin, dim3(2 * num_sms()), dim3(512), 0, s, n, (const float*)acc, split ? 0 : dq_row0,
+                              split ? 0 : kv_row0, split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
+                              static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+                              static_cast<__nv_bfloat16*>(dv), (int)(kH * nb), (const double*)dT64, dT) != cudaSuccess)
+            return GT_ERR_CUDA;
     }
     return check_launch();
 }

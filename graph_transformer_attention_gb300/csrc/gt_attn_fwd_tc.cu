@@ -250,6 +250,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();   // the merge may launch meanwhile; it waits for this grid before reading
     // this CTA's one or two stretches (heads kHC hb .. kHC hb + kHC - 1 of each)
     // (recomputed from the parameters where needed: kept in registers they would
     // be live across the whole softmax loop)
@@ -650,6 +651,7 @@ template <int HD>
 __global__ void __launch_bounds__(256)
 merge_pieces(const Balance bl, int n, const float* __restrict__ o_part, const float* __restrict__ lse_part,
              __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    pdl_wait();   // launched to overlap the attention kernel's end: its partials are complete after this
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)n * kH) return;
     const int row = (int)(idx / kH), h = (int)(idx % kH);
@@ -722,8 +724,10 @@ int launch_fwd_tc(int n, const void* q, const void* k, const void* v, const int8
     {
         LaunchScope ls("fwd_merge", s);
         const int64_t threads = (int64_t)n * kH;
-        merge_pieces<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-            bal, n, o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse);
+        if (launch_overlapped(merge_pieces<HD>, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, bal, n,
+                              (const float*)o_part, (const float*)lse_part, static_cast<__nv_bfloat16*>(o),
+                              lse) != cudaSuccess)
+            return GT_ERR_CUDA;
     }
     return check_launch();
 }
