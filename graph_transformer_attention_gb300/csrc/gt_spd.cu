@@ -82,6 +82,31 @@ __global__ void uf_hook(const int64_t* __restrict__ indptr, const int32_t* __res
     }
 }
 
+// The same union over the packed edge list (`target | source << 16` per CSR
+// entry, csr_pairs): one thread per entry, so a vertex's few edges do not leave
+// the rest of a warp idle behind its dependent loads.
+__global__ void uf_hook_pairs(const uint32_t* __restrict__ pairs, int64_t nnz, int* parent, int n, int* status) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < nnz; e += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t pr = pairs[e];
+        const int w = (int)(pr & 0xffffu), u = (int)(pr >> 16);
+        if (w <= u || w >= n) continue;
+        // link root b under the smaller root a with an atomic min; if b had
+        // already been linked (to c), the min keeps the smaller of a and c, and
+        // the larger of the two still has to be joined to it: continue with that
+        // pair (parents only move to smaller ids, so this ends)
+        int a = uf_find(parent, u), b = uf_find(parent, w);
+        int tries = 0;
+        while (a != b) {
+            if (a > b) { int t = a; a = b; b = t; }
+            const int c = atomicMin(parent + b, a);
+            if (c == b) break;                     // b was a root: linked
+            b = uf_find(parent, c);                // c or a is now b's parent: join the other
+            a = uf_find(parent, a);
+            if (++tries > kUfRetryCap) { atomicOr(status, kStatusTimeout); break; }
+        }
+    }
+}
+
 __global__ void uf_compress(int* parent, int n) {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n; v += gridDim.x * blockDim.x)
         parent[v] = uf_find(parent, v);
@@ -563,11 +588,12 @@ __host__ __device__ inline int scan_nwp(int n, int W) {
 // 0xffff, which is >= n and so never pushed).  One warp per vertex; entries
 // outside [0, nnz) are never written.
 __global__ void csr_pairs(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices, int n,
-                          int64_t nnz, uint32_t* __restrict__ pairs) {
+                          int64_t nnz, uint32_t* __restrict__ pairs, int* __restrict__ parent) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int v = warp; v < n; v += nwarps) {
+        if (lane == 0) parent[v] = v;   // union-find roots, for uf_hook_pairs
         const int64_t e0 = max(indptr[v], (int64_t)0), e1 = min(indptr[v + 1], nnz);
         for (int64_t e = e0 + lane; e < e1; e += 32) {
             const int u = indices[e];
@@ -1120,11 +1146,27 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int sms = num_sms();
-    {
-        LaunchScope ls("spd_uf_init", stream);
-        uf_init<<<sms * 4, 256, 0, stream>>>(comp, n);
-    }
-    {
+    // every search keeps its global state zero between batches; start from zero
+    if (per * (size_t)nctas > 0 && cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess)
+        return GT_ERR_CUDA;
+    // components: union-find over the edges (the scan searches first pack the edge
+    // list, with the roots set alongside, and hook over it one thread per entry)
+    if (is_scan(a)) {
+        {
+            LaunchScope ls("spd_pairs", stream);
+            csr_pairs<<<sms * 8, 256, 0, stream>>>(indptr, indices, n, nnz, pairs, comp);
+        }
+        if (nnz > 0) {
+            LaunchScope ls("spd_uf_hook", stream);
+            const int64_t blocks = (nnz + 255) / 256;
+            uf_hook_pairs<<<(unsigned)(blocks < sms * 16 ? blocks : sms * 16), 256, 0, stream>>>(pairs, nnz, comp, n,
+                                                                                               status);
+        }
+    } else {
+        {
+            LaunchScope ls("spd_uf_init", stream);
+            uf_init<<<sms * 4, 256, 0, stream>>>(comp, n);
+        }
         LaunchScope ls("spd_uf_hook", stream);
         uf_hook<<<sms * 8, 256, 0, stream>>>(indptr, indices, comp, n, status);
     }
@@ -1132,14 +1174,7 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         LaunchScope ls("spd_uf_compress", stream);
         uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
     }
-    // every search keeps its global state zero between batches; start from zero
-    if (per * (size_t)nctas > 0 && cudaMemsetAsync(bfs_ws, 0, per * (size_t)nctas, stream) != cudaSuccess)
-        return GT_ERR_CUDA;
     if (is_scan(a)) {
-        if (nnz > 0) {
-            LaunchScope ls("spd_pairs", stream);
-            csr_pairs<<<sms * 8, 256, 0, stream>>>(indptr, indices, n, nnz, pairs);
-        }
         const int W = a == GT_SPD_SCAN32 ? 32 : 16;
         const int smem = scan_smem_bytes(n, W);
         auto kern = W == 32 ? bfs_scan<32> : bfs_scan<16>;
