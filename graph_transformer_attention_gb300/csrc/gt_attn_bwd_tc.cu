@@ -46,9 +46,28 @@ template <int HD>
 __global__ void bwd_prep(int n, int ldl, float inv_scale, const __nv_bfloat16* __restrict__ o,
                          const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ v,
                          const float* __restrict__ lse, float* __restrict__ LD, uint16_t* __restrict__ LB,
-                         float* __restrict__ Dv, float* __restrict__ vmax) {
+                         float* __restrict__ Dv, float* __restrict__ vmax, float* __restrict__ acc, int dq_row0,
+                         int kv_row0, double* __restrict__ dT64, int dT_count) {
     pdl_trigger();   // the dq kernel's prologue may run meanwhile; it waits for this grid before reading
     const int64_t total = (int64_t)n * kH;
+    // clear what the backward sums into: the fp32 sums of split work (acc [3][n][8][HD]:
+    // dq rows >= dq_row0, dk and dv rows >= kv_row0; negative = none) and the fp64
+    // bucket sums; the dq kernel reads them only after this grid has completed
+    {
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const int64_t row4 = kH * HD / 4, elems4 = (int64_t)n * row4;
+        float4* a4 = reinterpret_cast<float4*>(acc);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dq_row0 >= 0)
+            for (int64_t x = dq_row0 * row4 + t0; x < elems4; x += stride) a4[x] = z;
+        if (kv_row0 >= 0)
+            for (int64_t x = kv_row0 * row4 + t0; x < elems4; x += stride) {
+                a4[elems4 + x] = z;
+                a4[2 * elems4 + x] = z;
+            }
+        for (int64_t x = t0; x < dT_count; x += stride) dT64[x] = 0.0;
+    }
     // the loop bound is the same for the whole block, so every lane reaches the shuffles
     for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
         const int64_t x = base + threadIdx.x;
@@ -158,8 +177,7 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
                 float* Dv, double* dT64, float* aux, int nsplit, int tail, int dq_tail, float* acc,
                 cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
-    if (cudaMemsetAsync(dT64, 0, sizeof(double) * (size_t)kH * nb, s) != cudaSuccess) return GT_ERR_CUDA;
-    if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;
+    if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;   // prep's maxima
     const int64_t total = (int64_t)n * kH;
     const int pblocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     // the dk/dv kernel takes -lse / scale; a zero scale (scores = bias alone) uses a
@@ -167,29 +185,19 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
     const size_t elems = (size_t)n * kH * d;
     const bool split = nsplit > 1 && acc;
-    // the fp32 sums are cleared before the kernels, so that nothing stands between
-    // the dq and dk/dv launches in the stream (the dk/dv kernel may start on the
-    // SMs the dq kernel's last wave leaves free; it reads only the inputs and the
-    // prep tables)
-    const int dq_row0 = split ? -1 : bwd_dq_tail_row0(n, dq_tail, acc != nullptr);
-    const int kv_row0 = split ? -1 : bwd_dkdv_tail_row0(n, tail, acc != nullptr);
-    if (split) {
-        if (cudaMemsetAsync(acc, 0, sizeof(float) * 3 * elems, s) != cudaSuccess) return GT_ERR_CUDA;
-    } else {
-        const size_t row = (size_t)kH * d;
-        if (dq_row0 >= 0 && cudaMemsetAsync(acc + dq_row0 * row, 0, sizeof(float) * (n - dq_row0) * row, s) != cudaSuccess)
-            return GT_ERR_CUDA;
-        if (kv_row0 >= 0 &&
-            (cudaMemsetAsync(acc + elems + kv_row0 * row, 0, sizeof(float) * (n - kv_row0) * row, s) != cudaSuccess ||
-             cudaMemsetAsync(acc + 2 * elems + kv_row0 * row, 0, sizeof(float) * (n - kv_row0) * row, s) != cudaSuccess))
-            return GT_ERR_CUDA;
-    }
+    // the fp32 sums (all of them for the small-graph split, else the tail splits'
+    // rows) and the bucket sums are cleared by the prep kernel, so that nothing
+    // stands between the launches (dq's prologue overlaps prep; the dk/dv kernel
+    // may start on the SMs the dq kernel's last wave leaves free)
+    const int dq_row0 = split ? 0 : bwd_dq_tail_row0(n, dq_tail, acc != nullptr);
+    const int kv_row0 = split ? 0 : bwd_dkdv_tail_row0(n, tail, acc != nullptr);
     {
         LaunchScope ls("bwd_prep", s);
         auto prep = d == 8 ? bwd_prep<8> : bwd_prep<16>;
         prep<<<pblocks, 256, 0, s>>>(n, ldl, 1.f / fold_scale, static_cast<const __nv_bfloat16*>(o),
                                      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(v),
-                                     lse, LD, LB, Dv, aux);
+                                     lse, LD, LB, Dv, aux, acc, acc ? dq_row0 : -1, acc ? kv_row0 : -1, dT64,
+                                     (int)(kH * nb));
     }
     int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1,
                            acc ? dq_tail : 1, dq, acc, dT64, s);
@@ -201,8 +209,8 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
         // the small-graph split sums every row of dq, dk and dv
         LaunchScope ls("bwd_finish", s);
         auto fin = d == 8 ? bwd_finish<8> : bwd_finish<16>;
-        if (launch_overlapped(fin, dim3(2 * num_sms()), dim3(512), 0, s, n, (const float*)acc, split ? 0 : dq_row0,
-                              split ? 0 : kv_row0, split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
+        if (launch_overlapped(fin, dim3(2 * num_sms()), dim3(512), 0, s, n, (const float*)acc, acc ? dq_row0 : -1,
+                              acc ? kv_row0 : -1, split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
                               static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                               static_cast<__nv_bfloat16*>(dv), (int)(kH * nb), (const double*)dT64, dT) != cudaSuccess)
             return GT_ERR_CUDA;

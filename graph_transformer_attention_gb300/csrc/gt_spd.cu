@@ -31,6 +31,7 @@
 
 #include "gt_common.cuh"
 #include "gt_stats.cuh"
+#include "gt_sm100.cuh"
 
 namespace gt {
 namespace {
@@ -86,6 +87,8 @@ __global__ void uf_hook(const int64_t* __restrict__ indptr, const int32_t* __res
 // entry, csr_pairs): one thread per entry, so a vertex's few edges do not leave
 // the rest of a warp idle behind its dependent loads.
 __global__ void uf_hook_pairs(const uint32_t* __restrict__ pairs, int64_t nnz, int* parent, int n, int* status) {
+    sm100::pdl_wait();      // launched to overlap csr_pairs, which writes the pairs and the roots
+    sm100::pdl_trigger();
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < nnz; e += (int64_t)gridDim.x * blockDim.x) {
         const uint32_t pr = pairs[e];
         const int w = (int)(pr & 0xffffu), u = (int)(pr >> 16);
@@ -108,6 +111,8 @@ __global__ void uf_hook_pairs(const uint32_t* __restrict__ pairs, int64_t nnz, i
 }
 
 __global__ void uf_compress(int* parent, int n) {
+    sm100::pdl_wait();      // may be launched to overlap the hook kernel
+    sm100::pdl_trigger();
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n; v += gridDim.x * blockDim.x)
         parent[v] = uf_find(parent, v);
 }
@@ -592,6 +597,7 @@ __global__ void csr_pairs(const int64_t* __restrict__ indptr, const int32_t* __r
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    sm100::pdl_trigger();   // the hook kernel may launch meanwhile; it waits for this grid
     for (int v = warp; v < n; v += nwarps) {
         if (lane == 0) parent[v] = v;   // union-find roots, for uf_hook_pairs
         const int64_t e0 = max(indptr[v], (int64_t)0), e1 = min(indptr[v + 1], nnz);
@@ -626,6 +632,9 @@ bfs_scan(const int64_t* __restrict__ indptr, const int32_t* __restrict__ indices
     const unsigned full = 0xffffffffu;
     const bool comp16 = (reinterpret_cast<uintptr_t>(comp) & 15u) == 0;
     for (int p = tid; p < 3 * nwp; p += blockDim.x) sw[p] = 0u;
+    // launched to overlap the components kernel: the shared state above is this
+    // CTA's own; the components, pairs and global state are read only after it
+    sm100::pdl_wait();
     __syncthreads();
 
     for (int batch = blockIdx.x; batch < nbatches; batch += gridDim.x) {
@@ -1159,8 +1168,9 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         if (nnz > 0) {
             LaunchScope ls("spd_uf_hook", stream);
             const int64_t blocks = (nnz + 255) / 256;
-            uf_hook_pairs<<<(unsigned)(blocks < sms * 16 ? blocks : sms * 16), 256, 0, stream>>>(pairs, nnz, comp, n,
-                                                                                               status);
+            if (launch_overlapped(uf_hook_pairs, dim3((unsigned)(blocks < sms * 16 ? blocks : sms * 16)), dim3(256), 0,
+                                  stream, (const uint32_t*)pairs, nnz, comp, n, status) != cudaSuccess)
+                return GT_ERR_CUDA;
         }
     } else {
         {
@@ -1172,7 +1182,8 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
     }
     {
         LaunchScope ls("spd_uf_compress", stream);
-        uf_compress<<<sms * 4, 256, 0, stream>>>(comp, n);
+        if (launch_overlapped(uf_compress, dim3(sms * 4), dim3(256), 0, stream, comp, n) != cudaSuccess)
+            return GT_ERR_CUDA;
     }
     if (is_scan(a)) {
         const int W = a == GT_SPD_SCAN32 ? 32 : 16;
@@ -1181,8 +1192,10 @@ int spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64_t 
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return GT_ERR_CUDA;
         LaunchScope ls("spd_bfs", stream);
-        kern<<<nctas, kScanThreads / scan_per_sm(n, W), smem, stream>>>(indptr, indices, pairs, comp, n, D, nslices, spd, ld,
-                                                   reinterpret_cast<uint32_t*>(bfs_ws));
+        if (launch_overlapped(kern, dim3(nctas), dim3(kScanThreads / scan_per_sm(n, W)), (size_t)smem, stream, indptr,
+                              indices, (const uint32_t*)pairs, (const int*)comp, n, D, nslices, spd, ld,
+                              reinterpret_cast<uint32_t*>(bfs_ws)) != cudaSuccess)
+            return GT_ERR_CUDA;
     } else if (a == GT_SPD_QUEUE32) {
         const size_t smem = (size_t)n * 4;
         if (cudaFuncSetAttribute(bfs32_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
