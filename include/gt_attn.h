@@ -36,7 +36,11 @@
  *   - All calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream).  They check their arguments on the host before any
  *     launch and return a negative gt_status without launching if a check
- *     fails.  GT_OK means the work was enqueued.
+ *     fails.  GT_OK means the work was enqueued.  Within a call, a kernel may
+ *     be scheduled while the one before it finishes (programmatic dependent
+ *     launch); each such kernel waits for its predecessor before reading that
+ *     one's output and before it completes, so what the caller's later work
+ *     on the stream sees is the same as with plain stream order.
  *   - Bucket codes are read as unsigned bytes; codes >= nb select a zero bias
  *     in the forward and are dropped from dT (they never occur in the output of
  *     gt_spd_build).
