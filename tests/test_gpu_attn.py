@@ -320,6 +320,42 @@ def test_backward_after_balanced_forward_ragged(gt):
     assert np.all(np.abs(dT.sum(1)) <= bound), (dT.sum(1), bound)
 
 
+def test_back_to_back_calls_on_one_stream(gt):
+    """Calls of three sizes with different splits (n = 3000 and 700: every tile's
+    stream split; n = 10000: only the tasks past the last full wave split; all
+    three with the balanced forward), enqueued back to back on one non-default
+    stream with no host
+    synchronisation between them, give what each gives alone (the launches of
+    a call overlap one another; completion order must still hold across calls).
+    The split sums add in fp32 in any order, so equality is to 1e-5 relative."""
+    cases = []
+    for n, d, seed in ((3000, 16, 80), (10000, 8, 81), (700, 16, 82)):
+        x = gi.make_layer_tensors(n, 8, d, 26, "bf16", seed=seed)
+        spd = torch.randint(0, 26, (n, gt.spd_ld(n)), dtype=torch.int8, device="cuda",
+                            generator=torch.Generator(device="cuda").manual_seed(seed))
+        args = [to_dev(x[a], "bf16") for a in ("q", "k", "v")] + [spd, torch.from_numpy(x["T"]).cuda()]
+        cases.append((args, to_dev(x["dO"], "bf16")))
+    alone = []
+    for args, dO in cases:
+        o, lse = gt.gt_bias_attn_fwd(*args)
+        g = gt.gt_bias_attn_bwd(*args[:3], o, dO, lse, *args[3:])
+        torch.cuda.synchronize()
+        alone.append([t.clone() for t in (o, lse, *g)])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        outs = []
+        for args, dO in cases:
+            o, lse = gt.gt_bias_attn_fwd(*args)
+            g = gt.gt_bias_attn_bwd(*args[:3], o, dO, lse, *args[3:])
+            outs.append([o, lse, *g])
+    s.synchronize()
+    gt.gt_check_device_status()
+    for ref, got in zip(alone, outs):
+        for a, b in zip(ref, got):
+            a64, b64 = a.double(), b.double()
+            assert torch.allclose(a64, b64, rtol=1e-5, atol=1e-6 * a64.abs().max().item())
+
+
 def _config_spd(w):
     g = gi.config_graph(w)
     return O.spd(g.n, g.indptr, g.indices, w.D)
