@@ -90,11 +90,6 @@ struct BwdWs {
     float* acc;     // split backward: fp32 dq, dk, dv accumulators, else null
 };
 
-// The KV block the forward uses: an explicit kv_block is kept (uniform splits
-// merged exactly); with 0 the tensor-core path balances its work over a whole
-// number of waves itself (balance_for) and needs no uniform split.
-int effective_kv_block(int dtype, int n, int h, int d, int kv_block) { return kv_block; }
-
 size_t fwd_ws(int dtype, int n, int h, int d, int kv_block, void* base, size_t cap, FwdWs* out) {
     Carve c(base, cap);
     const int nsplit = kv_block > 0 ? (n + kv_block - 1) / kv_block : 1;
@@ -203,7 +198,7 @@ int gt_spd_build(const int64_t* indptr, const int32_t* indices, int32_t n, int64
 size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
-    size_t a = gt::fwd_ws(dtype, n, h, d, gt::effective_kv_block(dtype, n, h, d, kv_block), nullptr, 0, nullptr);
+    size_t a = gt::fwd_ws(dtype, n, h, d, kv_block, nullptr, 0, nullptr);
     const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1 ||
                      gt::bwd_dq_tail(dtype, n, h, d, 128) > 1;
     size_t b = gt::bwd_ws(n, h, d, acc, nullptr, 0, nullptr);
@@ -218,7 +213,7 @@ int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, i
 int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return -1;
     if (kv_block >= n) kv_block = 0;
-    return gt::effective_kv_block(dtype, n, h, d, kv_block);
+    return kv_block;   // used as given; 0 (no uniform split) lets the tensor-core path balance its work
 }
 
 int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
@@ -258,7 +253,6 @@ int gt_bias_attn_fwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     if (!o || !lse || !gt::aligned16(o)) return GT_ERR_INVALID_ARG;
     if (kv_block < 0 || (kv_block > 0 && kv_block % 128 != 0)) return GT_ERR_INVALID_ARG;
     if (kv_block >= n) kv_block = 0;
-    kv_block = gt::effective_kv_block(dtype, n, h, d, kv_block);
     const size_t need = gt::fwd_ws(dtype, n, h, d, kv_block, nullptr, 0, nullptr);
     if (need > 0 && (!workspace || ws_bytes < need)) return GT_ERR_WORKSPACE;
     gt::FwdWs w;
