@@ -320,6 +320,41 @@ def test_backward_after_balanced_forward_ragged(gt):
     assert np.all(np.abs(dT.sum(1)) <= bound), (dT.sum(1), bound)
 
 
+def test_two_wave_balanced_forward_and_split_dq(gt):
+    """n = 20000: 157 tiles, 314 tasks for 304 resident slots, so the forward's
+    balanced grid is two waves (608 CTAs) and the dq kernel runs a full wave of
+    whole tasks and then the 10 tasks past it split along the KV blocks, that
+    launch overlapping the first.  Rows: the first and last of every 16th tile,
+    the last tile's, and random ones, against the oracle (o, lse, dq); dT and dv
+    by their sum properties."""
+    n, h, d, nb = 20000, 8, 16, 26
+    lib = gt.load_library()
+    tiles = (n + 127) // 128
+    assert lib.gt_bias_attn_fwd_ctas(1, n, h, d, 0) >= 2 * tiles
+    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) == 1
+    x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=90)
+    spd = np.random.default_rng(91).integers(0, nb, size=(n, n), dtype=np.int8)
+    got = _run_gpu(gt, x, spd, "bf16")
+    rng = np.random.default_rng(92)
+    starts = np.arange(0, n, 128 * 16)
+    split_rows = [152 * 128, 152 * 128 + 77, 155 * 128 + 5]   # tiles of the split tasks (past 304 tasks)
+    rows = np.unique(np.concatenate([starts, np.minimum(starts + 127, n - 1), [n - 1, n - 2, (tiles - 1) * 128],
+                                     split_rows, rng.choice(n, 48, replace=False)]))
+    o_r, lse_r = O.attn_fwd(x["q"], x["k"], x["v"], spd, x["T"], rows=rows)
+    assert_close("o[rows]", got["o"][rows], o_r, "bf16")
+    assert_close("lse[rows]", got["lse"][:, rows], lse_r, "bf16")
+    Dv_rows = (o_r * x["dO"][rows].astype(np.float64)).sum(-1).T
+    lse_full = np.zeros((h, n)); Dv_full = np.zeros((h, n))
+    lse_full[:, rows] = lse_r; Dv_full[:, rows] = Dv_rows
+    g = O.attn_bwd(x["q"], x["k"], x["v"], x["dO"], spd, x["T"], lse_full, Dv_full,
+                   rows=rows, want_dT=False, want_dkdv=False)
+    assert_close("dq[rows]", got["dq"][rows], g["dq"], "bf16")
+    bound = 2.0 ** -8 * np.abs(x["dO"].astype(np.float64) * got["o"]).sum(axis=(0, 2)) + 1e-4
+    assert np.all(np.abs(got["dT"].sum(1)) <= bound)
+    dsum = got["dv"].sum(0)
+    assert np.linalg.norm(dsum - x["dO"].astype(np.float64).sum(0)) <= 2e-2 * np.linalg.norm(dsum) + 1e-3
+
+
 def test_back_to_back_calls_on_one_stream(gt):
     """Calls of three sizes with different splits (n = 3000 and 700: every tile's
     stream split; n = 10000: only the tasks past the last full wave split; all
