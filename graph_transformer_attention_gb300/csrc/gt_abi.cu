@@ -41,7 +41,7 @@ bool bwd_tc_supported(int h, int d, int nb);
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, int tail, int dq_tail, float* acc,
+                float* Dv, double* dT64, float* aux, int tail, int dq_tail, float* acc,
                 cudaStream_t s);
 int bwd_dkdv_tail_split(int n);
 int bwd_dq_tail_split(int n);
@@ -105,29 +105,20 @@ size_t fwd_ws(int dtype, int n, int h, int d, int kv_block, void* base, size_t c
     return c.off;
 }
 
-// Splits of the streamed dimension of the tensor-core backward kernels: with too
-// few 128-row tiles to give every SM two CTAs, each kernel's tiles also split
-// their KV blocks (dq) or query tiles (dk, dv) over up to 4 CTAs, which sum into
-// fp32 accumulators (workspace `acc`, 3 [n][h][d] arrays) turned into bf16 at
-// the end.  1 = no split.
-int bwd_split(int dtype, int n, int h, int d, int nb) {
-    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb)) return 1;
-    const int ctas = 2 * ((n + 127) / 128);
-    int s = 2 * num_sms() / ctas;
-    return s > 4 ? 4 : (s < 2 ? 1 : s);
-}
-
-// Query-range split of the last, partial wave of the tensor-core dk/dv groups
-// (1 = none); its sums share `acc` with the small-graph split.
+// Splits of the tensor-core backward kernels' work past their last full wave:
+// the dq tasks (tile, head half; two CTAs per SM) along their KV blocks, the
+// dk/dv groups (KV tile, head half; one CTA per SM) along their query tiles, k
+// ways each (1 = none), chosen so that the last waves fill the SMs; on a graph
+// too small to fill one wave every task or group is split.  The split CTAs sum
+// into fp32 accumulators (workspace `acc`, 3 [n][h][d] arrays) turned into bf16
+// at the end.
 int bwd_tail(int dtype, int n, int h, int d, int nb) {
-    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb) || bwd_split(dtype, n, h, d, nb) > 1) return 1;
+    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb)) return 1;
     return bwd_dkdv_tail_split(n);
 }
 
-// KV split of the dq tasks past the last full wave (1 = none); its sums take
-// the dq part of `acc`.
 int bwd_dq_tail(int dtype, int n, int h, int d, int nb) {
-    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb) || bwd_split(dtype, n, h, d, nb) > 1) return 1;
+    if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb)) return 1;
     return bwd_dq_tail_split(n);
 }
 
@@ -199,15 +190,14 @@ size_t gt_bias_attn_workspace_size(int32_t dtype, int32_t n, int32_t h, int32_t 
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || kv_block < 0) return 0;
     if (kv_block >= n) kv_block = 0;
     size_t a = gt::fwd_ws(dtype, n, h, d, kv_block, nullptr, 0, nullptr);
-    const bool acc = gt::bwd_split(dtype, n, h, d, 128) > 1 || gt::bwd_tail(dtype, n, h, d, 128) > 1 ||
-                     gt::bwd_dq_tail(dtype, n, h, d, 128) > 1;
+    const bool acc = gt::bwd_tail(dtype, n, h, d, 128) > 1 || gt::bwd_dq_tail(dtype, n, h, d, 128) > 1;
     size_t b = gt::bwd_ws(n, h, d, acc, nullptr, 0, nullptr);
     return (a > b ? a : b) + 256;
 }
 
 int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb) {
     if (!gt::valid_dtype(dtype) || n < 1 || h < 1 || d < 1 || nb < 1) return -1;
-    return gt::bwd_split(dtype, n, h, d, nb);
+    return gt::bwd_dq_tail(dtype, n, h, d, nb);
 }
 
 int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block) {
@@ -238,7 +228,7 @@ int gt_bias_attn_launches(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_
     // prep, dq, dk/dv, and the finish (fp32 sums and dT converted); a tail split
     // adds its second launch when whole tasks fill waves before it
     int count = 4;
-    if (gt::bwd_tail(dtype, n, h, d, nb) > 1) count += 1;
+    if (gt::bwd_tail(dtype, n, h, d, nb) > 1 && 2 * ((n + 127) / 128) >= gt::num_sms()) count += 1;
     if (gt::bwd_dq_tail(dtype, n, h, d, nb) > 1 && 2 * ((n + 127) / 128) >= 2 * gt::num_sms()) count += 1;
     *bwd = count;
     return GT_OK;
@@ -301,15 +291,14 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     if (!gt::aligned16(o) || !gt::aligned16(dO) || !gt::aligned16(dq) || !gt::aligned16(dk) ||
         !gt::aligned16(dv))
         return GT_ERR_INVALID_ARG;
-    // the split needs its accumulators; a workspace sized for the unsplit pass
+    // the splits need their accumulators; a workspace sized for the unsplit pass
     // (a caller's fixed scratch) runs unsplit
-    int nsplit = gt::bwd_split(dtype, n, h, d, nb);
     int tail = gt::bwd_tail(dtype, n, h, d, nb);
     int dq_tail = gt::bwd_dq_tail(dtype, n, h, d, nb);
-    bool with_acc = nsplit > 1 || tail > 1 || dq_tail > 1;
+    bool with_acc = tail > 1 || dq_tail > 1;
     if (with_acc && ws_bytes < gt::bwd_ws(n, h, d, true, nullptr, 0, nullptr)) {
         with_acc = false;
-        nsplit = tail = dq_tail = 1;
+        tail = dq_tail = 1;
     }
     const size_t need = gt::bwd_ws(n, h, d, with_acc, nullptr, 0, nullptr);
     if (!workspace || ws_bytes < need) return GT_ERR_WORKSPACE;
@@ -318,7 +307,7 @@ int gt_bias_attn_bwd(int32_t dtype, int32_t n, int32_t h, int32_t d, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GT_BF16 && gt::bwd_tc_supported(h, d, nb))
         return gt::attn_bwd_tc(n, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk, dv, dT,
-                               w.LD, w.LB, w.Dv, w.dT64, w.aux, nsplit, tail, dq_tail, w.acc, s);
+                               w.LD, w.LB, w.Dv, w.dT64, w.aux, tail, dq_tail, w.acc, s);
     return gt::attn_bwd_simt(dtype, n, h, d, q, k, v, o, dO, lse, spd, ld_spd, T, nb, scale, dq, dk,
                              dv, dT, w.Dv, w.dT64, s);
 }

@@ -506,13 +506,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 int dkdv_tail_row0(int n, int tail, bool have_acc) {
     const int sms = num_sms();
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
-    if (tail <= 1 || !have_acc || groups <= sms || groups % sms == 0) return -1;
+    if (tail <= 1 || !have_acc || groups % sms == 0) return -1;
     return (groups / sms * sms / 2) * kBKV;
 }
 
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
-           int64_t ld, const float* T, int nb, float scale, float fold_scale, const uint16_t* LB, int nsplit,
+           int64_t ld, const float* T, int nb, float scale, float fold_scale, const uint16_t* LB,
            int tail, void* dk, void* dv, float* dk_acc, float* dv_acc, cudaStream_t s) {
     using C = KvCfg<HD>;
     CUtensorMap mq, mg, ms, ml;
@@ -547,18 +547,17 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
             return GT_ERR_CUDA;
         return check_launch();
     };
-    if (nsplit > 1 && dk_acc) {
-        // every group split over nsplit CTAs (graphs with fewer groups than SMs)
-        return run(0, groups, (total_tiles + nsplit - 1) / nsplit, true);
-    }
     const int row0 = dkdv_tail_row0(n, tail, dk_acc != nullptr);
     if (row0 >= 0) {
-        // full waves of whole groups, then the remaining groups split tail ways so
-        // that the last wave fills the SMs; the caller cleared their rows of the
-        // sums before and turns them into bf16 after
+        // full waves of whole groups (none on a graph too small to fill one), then
+        // the remaining groups split tail ways so that the last waves fill the SMs;
+        // the caller cleared their rows of the sums before and turns them into
+        // bf16 after
         const int g1 = (row0 / kBKV) * 2;
-        const int rc = run(0, g1, 0, false);
-        if (rc != GT_OK) return rc;
+        if (g1 > 0) {
+            const int rc = run(0, g1, 0, false);
+            if (rc != GT_OK) return rc;
+        }
         return run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
     }
     return run(0, groups, 0, false);
@@ -570,24 +569,25 @@ int bwd_dkdv_tail_row0(int n, int tail, bool have_acc) { return dkdv_tail_row0(n
 
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const uint16_t* LB, int nsplit, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    const uint16_t* LB, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
                     cudaStream_t s) {
     // LB holds -lse / fold_scale with fold_scale = scale, or a tiny stand-in for a
     // zero scale; dk takes the true scale
     const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, tail, dk, dv, dk_acc,
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, tail, dk, dv, dk_acc,
                               dv_acc, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, nsplit, tail, dk, dv, dk_acc,
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, fold_scale, LB, tail, dk, dv, dk_acc,
                                dv_acc, s);
 }
 
-// Query-range split of the tail groups (see launch): the k in [2, 8] that makes
-// the last wave of whole-group CTAs plus the split tail the shortest, in units of
-// one group's time, or 1 when the groups fill whole waves (or do not fill one).
+// Query-range split of the groups past the last full wave of one CTA per SM (all
+// of them on a graph too small to fill one; see launch): the k in [2, 8] that
+// makes the last waves the shortest, in units of one group's time, or 1 when the
+// groups fill whole waves or no k beats one more wave of whole groups.
 int bwd_dkdv_tail_split(int n) {
     const int sms = num_sms();
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
-    if (groups <= sms || groups % sms == 0) return 1;
+    if (groups % sms == 0) return 1;
     const int rem = groups % sms;
     int best = 1;
     double best_t = 1.0;                        // the tail unsplit: one more wave of whole groups

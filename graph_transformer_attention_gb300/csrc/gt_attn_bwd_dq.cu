@@ -585,7 +585,7 @@ int dq_tail_row0(int n, int tail, bool have_acc) {
 template <int HD>
 int launch(int n, const void* q, const void* k, const void* v, const void* dO, const int8_t* spd,
            int64_t ld, const float* T, int nb, float scale, const float* LD, int ldl, const float* vmax,
-           int nsplit, int tail, void* dq, float* dq_acc, double* dT64, cudaStream_t s) {
+           int tail, void* dq, float* dq_acc, double* dT64, cudaStream_t s) {
     using C = DqCfg<HD>;
     CUtensorMap mk, mv, ms;
     const uint64_t cols = (uint64_t)kH * HD;
@@ -626,10 +626,10 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
             return GT_ERR_CUDA;
         return check_launch();
     };
-    if (nsplit > 1 && dq_acc) return run(0, tasks, nsplit, true);   // every tile split (small graphs)
     const int row0 = dq_tail_row0(n, tail, dq_acc != nullptr);
     if (row0 >= 0) {
-        // full waves of whole tasks, then the rest split `tail` ways along the KV
+        // full waves of whole tasks (none on a graph too small to fill one), then
+        // the rest split `tail` ways along the KV
         // blocks so that the last waves fill the SMs, overlapping the whole
         // tasks' last wave; the caller cleared their rows of dq_acc before and
         // converts them after
@@ -667,10 +667,10 @@ int bwd_dq_tail_row0(int n, int tail, bool have_acc) { return dq_tail_row0(n, ta
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
+                  const float* LD, int ldl, const float* vmax, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s) {
-    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, tail, dq, dq_acc, dT64, s)
-                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, nsplit, tail, dq, dq_acc, dT64, s);
+    return d == 8 ? launch<8>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, tail, dq, dq_acc, dT64, s)
+                  : launch<16>(n, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, vmax, tail, dq, dq_acc, dT64, s);
 }
 
 }  // namespace gt

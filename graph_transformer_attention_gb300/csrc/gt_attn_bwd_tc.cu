@@ -156,25 +156,25 @@ bool bwd_tc_supported(int h, int d, int nb) { return h == kH && (d == 8 || d == 
 
 int launch_bwd_dq(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                   const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                  const float* LD, int ldl, const float* vmax, int nsplit, int tail, void* dq, float* dq_acc,
+                  const float* LD, int ldl, const float* vmax, int tail, void* dq, float* dq_acc,
                   double* dT64, cudaStream_t s);
 int bwd_dq_tail_row0(int n, int tail, bool have_acc);
 int bwd_dkdv_tail_row0(int n, int tail, bool have_acc);
 int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, const void* dO,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
-                    const uint16_t* LB, int nsplit, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
+                    const uint16_t* LB, int tail, void* dk, void* dv, float* dk_acc, float* dv_acc,
                     cudaStream_t s);
 
 // Backward on the tensor cores.  Workspace: LD [16][bwd_ld_ld(n)] fp32, LB bf16
 // [n][8][16], Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j|
 // of head h), and the fp32 sums acc [3][n][8][d] when either split applies
-// (nsplit > 1: every tile's streamed dimension split; tail > 1: the dk/dv groups
-// of the last, partial wave split; dq_tail > 1: the same for the dq tasks), else
-// null.
+// (tail > 1: the dk/dv groups past the last full wave split along their query
+// tiles; dq_tail > 1: the dq tasks past the last full wave split along their KV
+// blocks; on a graph too small to fill a wave, all of them), else null.
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,
-                float* Dv, double* dT64, float* aux, int nsplit, int tail, int dq_tail, float* acc,
+                float* Dv, double* dT64, float* aux, int tail, int dq_tail, float* acc,
                 cudaStream_t s) {
     const int ldl = bwd_ld_ld(n);
     if (cudaMemsetAsync(aux, 0, sizeof(float) * 16, s) != cudaSuccess) return GT_ERR_CUDA;   // prep's maxima
@@ -184,13 +184,12 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
     // scale far below any product's resolution instead, with the same results
     const float fold_scale = (scale == 0.f || !isfinite(scale)) ? 1e-30f : scale;
     const size_t elems = (size_t)n * kH * d;
-    const bool split = nsplit > 1 && acc;
-    // the fp32 sums (all of them for the small-graph split, else the tail splits'
-    // rows) and the bucket sums are cleared by the prep kernel, so that nothing
+    // the fp32 sums (the split tasks' rows) and the bucket sums are cleared by the
+    // prep kernel, so that nothing
     // stands between the launches (dq's prologue overlaps prep; the dk/dv kernel
     // may start on the SMs the dq kernel's last wave leaves free)
-    const int dq_row0 = split ? 0 : bwd_dq_tail_row0(n, dq_tail, acc != nullptr);
-    const int kv_row0 = split ? 0 : bwd_dkdv_tail_row0(n, tail, acc != nullptr);
+    const int dq_row0 = bwd_dq_tail_row0(n, dq_tail, acc != nullptr);
+    const int kv_row0 = bwd_dkdv_tail_row0(n, tail, acc != nullptr);
     {
         LaunchScope ls("bwd_prep", s);
         auto prep = d == 8 ? bwd_prep<8> : bwd_prep<16>;
@@ -199,18 +198,17 @@ int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const
                                      lse, LD, LB, Dv, aux, acc, acc ? dq_row0 : -1, acc ? kv_row0 : -1, dT64,
                                      (int)(kH * nb));
     }
-    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, split ? nsplit : 1,
-                           acc ? dq_tail : 1, dq, acc, dT64, s);
+    int rc = launch_bwd_dq(n, d, q, k, v, dO, spd, ld, T, nb, scale, LD, ldl, aux, acc ? dq_tail : 1, dq, acc,
+                           dT64, s);
     if (rc != GT_OK) return rc;
-    rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, split ? nsplit : 1, acc ? tail : 1, dk, dv,
+    rc = launch_bwd_dkdv(n, d, q, k, v, dO, spd, ld, T, nb, scale, LB, acc ? tail : 1, dk, dv,
                          acc ? acc + elems : nullptr, acc ? acc + 2 * elems : nullptr, s);
     if (rc != GT_OK) return rc;
     {
-        // the small-graph split sums every row of dq, dk and dv
         LaunchScope ls("bwd_finish", s);
         auto fin = d == 8 ? bwd_finish<8> : bwd_finish<16>;
         if (launch_overlapped(fin, dim3(2 * num_sms()), dim3(512), 0, s, n, (const float*)acc, acc ? dq_row0 : -1,
-                              acc ? kv_row0 : -1, split ? 0 : (kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0),
+                              acc ? kv_row0 : -1, kv_row0 >= 0 ? kv_row0 / 128 * 2 : 0,
                               static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                               static_cast<__nv_bfloat16*>(dv), (int)(kH * nb), (const double*)dT64, dT) != cudaSuccess)
             return GT_ERR_CUDA;

@@ -153,16 +153,15 @@ int32_t gt_bias_attn_fwd_kv_block(int32_t dtype, int32_t n, int32_t h, int32_t d
 int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t kv_block);
 
 /*
- * How many CTAs share each 128-row tile's streamed dimension in the bf16
- * tensor-core backward for these sizes on the current device (1 = none; -1 for
- * invalid arguments).  With too few tiles to give every SM two CTAs, the dq
- * kernel splits its KV blocks and the dk/dv kernel its query tiles over up to 4
- * CTAs each, which sum in fp32 (workspace included in
- * gt_bias_attn_workspace_size; a workspace too small for the sums runs unsplit).
- * Larger graphs split only the work past each kernel's last full wave: the dq
- * tasks (tile, head half) that would leave the SMs' second slots partly idle
- * over up to 8 CTAs along the KV blocks, the dk/dv groups the same way along
- * the query tiles, with the same fp32 sums.
+ * How many CTAs share each dq task (a 128-row query tile and a head half) of
+ * the bf16 tensor-core backward for these sizes on the current device (1 = none;
+ * -1 for invalid arguments).  The dq tasks that do not fill a whole wave of two
+ * CTAs per SM (all of them on a graph too small to fill one) are split along
+ * their KV blocks, and the dk/dv groups (a 128-row KV tile and a head half) that
+ * do not fill a wave of one CTA per SM along their query tiles, k ways each with
+ * k in 2..8 chosen so that the last waves fill the SMs; the split CTAs sum in
+ * fp32 (workspace included in gt_bias_attn_workspace_size; a workspace too small
+ * for the sums runs unsplit).
  */
 int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb);
 

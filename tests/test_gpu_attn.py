@@ -291,14 +291,16 @@ def test_balanced_forward_pieces(gt, n, d, kind):
 
 
 def test_backward_after_balanced_forward_ragged(gt):
-    """The unsplit backward at a ragged size just past the split threshold
-    (n = 9857: 78 tiles, the last one 1 row), fed by the balanced forward (156
+    """The backward at a ragged size (n = 9857: 78 tiles, the last one 1 row):
+    its 156 dq tasks fill no wave of two CTAs per SM and are all split along
+    their KV blocks, its 156 dk/dv groups fill one wave of one CTA per SM and the
+    4 past it are split along their query tiles; fed by the balanced forward (156
     tasks over two waves' worth of CTAs, up to three CTAs per tile).  Rows: the
     first and last of every tile plus random ones, against the oracle; dT by its
     zero-sum property."""
     n, h, d, nb = 9857, 8, 16, 26
     lib = gt.load_library()
-    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) == 1
+    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) >= 2
     assert lib.gt_bias_attn_fwd_ctas(1, n, h, d, 0) > 0
     x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=70)
     spd = np.random.default_rng(71).integers(0, nb, size=(n, n)).astype(np.int8)
@@ -331,7 +333,7 @@ def test_two_wave_balanced_forward_and_split_dq(gt):
     lib = gt.load_library()
     tiles = (n + 127) // 128
     assert lib.gt_bias_attn_fwd_ctas(1, n, h, d, 0) >= 2 * tiles
-    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) == 1
+    assert lib.gt_bias_attn_bwd_split(1, n, h, d, nb) >= 2
     x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=90)
     spd = np.random.default_rng(91).integers(0, nb, size=(n, n), dtype=np.int8)
     got = _run_gpu(gt, x, spd, "bf16")

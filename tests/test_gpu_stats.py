@@ -51,16 +51,22 @@ def test_counts_and_times_of_one_layer(gt, timing):
             assert ms == -1.0
 
 
-def test_small_graphs_split_their_streams(gt):
-    """On a GB300 a graph of 4096 nodes has 32 tiles of 128 rows: the backward
-    splits its streams; 16384 nodes do not.  The forward makes no uniform KV
-    split of its own (it balances its work instead), and an explicit kv_block
-    is kept."""
-    assert gt.load_library().gt_bias_attn_bwd_split(1, 4096, 8, 8, 18) >= 2
-    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 0) == 0
-    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 1024) == 1024
-    assert gt.load_library().gt_bias_attn_bwd_split(1, 16384, 8, 16, 26) == 1
-    assert gt.load_library().gt_bias_attn_fwd_kv_block(1, 16384, 8, 16, 0) == 0
+def test_splits_fill_the_last_waves(gt):
+    """The dq split on a GB300 (152 SMs, two dq CTAs each): 4096 nodes give 64
+    tasks, split 4 ways (256 CTAs, one wave); 16384 nodes give 256 tasks, split
+    7 ways (1792 CTAs in six waves); 19456 nodes give 304 tasks, exactly one
+    wave, unsplit.  The forward makes no uniform KV split of its own (it
+    balances its work instead), and an explicit kv_block is kept."""
+    lib = gt.load_library()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert lib.gt_bias_attn_bwd_split(1, 4096, 8, 8, 18) == 4
+        assert lib.gt_bias_attn_bwd_split(1, 16384, 8, 16, 26) == 7
+        assert lib.gt_bias_attn_bwd_split(1, 19456, 8, 16, 26) == 1
+    assert lib.gt_bias_attn_bwd_split(1, 4096, 8, 8, 18) >= 2
+    assert lib.gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 0) == 0
+    assert lib.gt_bias_attn_fwd_kv_block(1, 4096, 8, 8, 1024) == 1024
+    assert lib.gt_bias_attn_fwd_kv_block(1, 16384, 8, 16, 0) == 0
 
 
 def test_counts_of_a_graph_past_one_wave(gt):
