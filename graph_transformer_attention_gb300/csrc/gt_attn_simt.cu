@@ -45,10 +45,12 @@ __device__ __forceinline__ void stage_tile(float (*dst)[DP], const TE* __restric
 }
 
 // Forward over the KV columns [kv_begin, kv_end), cut into nsplit splits of
-// kv_block columns.  grid = (ceil(n/128), h, nsplit); block = 128.
+// kv_block columns.  grid = (ceil(n / (128 / SPL)), h, nsplit); block = 128: SPL
+// adjacent threads per query row, thread phase ph taking the columns j = ph mod
+// SPL of each tile, their running (max, sum, output) merged exactly at the end.
 // parts == 0: writes o (TE) and lse.  Otherwise writes fp32 partials
 // o_part[z][n][h][d] and lse_part[z][h][n] for the KV columns of split z.
-template <typename TE, int DP>
+template <typename TE, int DP, int SPL>
 __global__ void __launch_bounds__(kRows)
 fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
          const TE* __restrict__ v, const uint8_t* __restrict__ spd, int64_t ld,
@@ -59,7 +61,8 @@ fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k
     __shared__ float sV[kTile][DP];
     __shared__ float sT[kCodes];
     const int head = blockIdx.y;
-    const int i = blockIdx.x * kRows + threadIdx.x;
+    const int ph = (int)threadIdx.x % SPL;
+    const int i = blockIdx.x * (kRows / SPL) + (int)threadIdx.x / SPL;
     const int split = blockIdx.z;
     const int j_begin = kv_begin + (kv_block > 0 ? split * kv_block : 0);
     const int j_end = kv_block > 0 ? min(kv_end, j_begin + kv_block) : kv_end;
@@ -80,7 +83,7 @@ fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k
         __syncthreads();
         const int jn = min(kTile, j_end - j0);
 #pragma unroll 1
-        for (int jj = 0; jj < jn; ++jj) {
+        for (int jj = ph; jj < jn; jj += SPL) {
             float dot = 0.f;
 #pragma unroll
             for (int c = 0; c < DP; ++c) dot = fmaf(qi[c], sK[jj][c], dot);
@@ -98,7 +101,24 @@ fwd_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k
             for (int c = 0; c < DP; ++c) acc[c] = fmaf(p, sV[jj][c], acc[c]);
         }
     }
-    if (!live) return;
+    // the row's SPL phases: (m, l, acc) combined through their maxima (a phase
+    // that saw no column has m = -inf and l = 0)
+#pragma unroll
+    for (int off = SPL / 2; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+        const float mn = fmaxf(m, m2);
+        const float a = mn == -INFINITY ? 0.f : expf(m - mn);
+        const float b = mn == -INFINITY ? 0.f : expf(m2 - mn);
+        l = l * a + l2 * b;
+#pragma unroll
+        for (int c = 0; c < DP; ++c) {
+            const float o2 = __shfl_xor_sync(0xffffffffu, acc[c], off);
+            acc[c] = acc[c] * a + o2 * b;
+        }
+        m = mn;
+    }
+    if (!live || ph != 0) return;
     const float inv = 1.f / l;
     if (!parts) {
         TE* oi = o + ((int64_t)i * h + head) * d;
@@ -131,8 +151,10 @@ __global__ void bwd_delta(int n, int h, int d, const TE* __restrict__ o, const T
     }
 }
 
-// Row pass: dq_i and dS summed per bucket.  grid = (ceil(n/128), h); block = 128.
-template <typename TE, int DP>
+// Row pass: dq_i and dS summed per bucket.  grid = (ceil(n / (128 / SPL)), h);
+// block = 128, SPL adjacent threads per query row taking every SPL-th column,
+// their dq partials added at the end.
+template <typename TE, int DP, int SPL>
 __global__ void __launch_bounds__(kRows)
 bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
               const TE* __restrict__ v, const TE* __restrict__ dO, const float* __restrict__ lse,
@@ -146,7 +168,8 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
     // rows of a warp that share a code do not all contend for one address
     __shared__ float sH[kCodes][kHCopies];
     const int head = blockIdx.y;
-    const int i = blockIdx.x * kRows + threadIdx.x;
+    const int ph = (int)threadIdx.x % SPL;
+    const int i = blockIdx.x * (kRows / SPL) + (int)threadIdx.x / SPL;
     for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
     for (int c = threadIdx.x; c < kCodes * kHCopies; c += blockDim.x) (&sH[0][0])[c] = 0.f;
     const bool live = i < n;
@@ -168,7 +191,7 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
         if (!live) continue;
         const int jn = min(kTile, n - j0);
 #pragma unroll 1
-        for (int jj = 0; jj < jn; ++jj) {
+        for (int jj = ph; jj < jn; jj += SPL) {
             float dot = 0.f, dp = 0.f;
 #pragma unroll
             for (int c = 0; c < DP; ++c) {
@@ -183,7 +206,11 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
             atomicAdd(&sH[code][threadIdx.x % kHCopies], ds);
         }
     }
-    if (live) {
+#pragma unroll
+    for (int off = SPL / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int c = 0; c < DP; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
+    if (live && ph == 0) {
         TE* out = dq + ((int64_t)i * h + head) * d;
 #pragma unroll
         for (int c = 0; c < DP; ++c)
@@ -198,8 +225,10 @@ bwd_rows_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
     }
 }
 
-// Column pass: dk_j, dv_j.  grid = (ceil(n/128), h); block = 128.
-template <typename TE, int DP>
+// Column pass: dk_j, dv_j.  grid = (ceil(n / (128 / SPL)), h); block = 128, SPL
+// adjacent threads per key column taking every SPL-th query row, their dk and
+// dv partials added at the end.
+template <typename TE, int DP, int SPL>
 __global__ void __launch_bounds__(kRows)
 bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restrict__ k,
               const TE* __restrict__ v, const TE* __restrict__ dO, const float* __restrict__ lse,
@@ -211,9 +240,12 @@ bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
     __shared__ float sL[kTile], sD[kTile];
     __shared__ uint8_t sS[kTile][kRows];
     __shared__ float sT[kCodes];
+    constexpr int kCols = kRows / SPL;   // key columns per block
     const int head = blockIdx.y;
-    const int j = blockIdx.x * kRows + threadIdx.x;
-    const int jbase = blockIdx.x * kRows;
+    const int ph = (int)threadIdx.x % SPL;
+    const int jc = (int)threadIdx.x / SPL;
+    const int j = blockIdx.x * kCols + jc;
+    const int jbase = blockIdx.x * kCols;
     for (int c = threadIdx.x; c < kCodes; c += blockDim.x) sT[c] = c < nb ? T[head * nb + c] : 0.f;
     const bool live = j < n;
     const int jj_ = live ? j : 0;
@@ -232,8 +264,8 @@ bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
             sL[x] = row < n ? lse[(int64_t)head * n + row] : 0.f;
             sD[x] = row < n ? Dv[(int64_t)head * n + row] : 0.f;
         }
-        for (int x = threadIdx.x; x < kTile * kRows; x += blockDim.x) {
-            const int r = x / kRows, c = x % kRows;
+        for (int x = threadIdx.x; x < kTile * kCols; x += blockDim.x) {
+            const int r = x / kCols, c = x % kCols;
             const int row = i0 + r, col = jbase + c;
             sS[r][c] = (row < n && col < n) ? spd[(int64_t)row * ld + col] : 0;
         }
@@ -241,14 +273,14 @@ bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
         if (!live) continue;
         const int in_ = min(kTile, n - i0);
 #pragma unroll 1
-        for (int r = 0; r < in_; ++r) {
+        for (int r = ph; r < in_; r += SPL) {
             float dot = 0.f, dp = 0.f;
 #pragma unroll
             for (int c = 0; c < DP; ++c) {
                 dot = fmaf(sQ[r][c], kj[c], dot);
                 dp = fmaf(sG[r][c], vj[c], dp);
             }
-            const float p = expf(dot + sT[sS[r][threadIdx.x]] - sL[r]);
+            const float p = expf(dot + sT[sS[r][jc]] - sL[r]);
             const float ds = p * (dp - sD[r]);
 #pragma unroll
             for (int c = 0; c < DP; ++c) {
@@ -257,7 +289,14 @@ bwd_cols_simt(int n, int h, int d, const TE* __restrict__ q, const TE* __restric
             }
         }
     }
-    if (!live) return;
+#pragma unroll
+    for (int off = SPL / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int c = 0; c < DP; ++c) {
+            ak[c] += __shfl_xor_sync(0xffffffffu, ak[c], off);
+            av[c] += __shfl_xor_sync(0xffffffffu, av[c], off);
+        }
+    if (!live || ph != 0) return;
     TE* ok = dk + ((int64_t)j * h + head) * d;
     TE* ov = dv + ((int64_t)j * h + head) * d;
 #pragma unroll
@@ -305,18 +344,26 @@ int grid_for(int64_t total) {
     return (int)(b < 4096 ? (b > 0 ? b : 1) : 4096);
 }
 
+// Threads per row (or column) of the fp32 kernels: 8 when one per row would not
+// give every SM two blocks of 128, else 1.
+int simt_spl(int n, int h, int nsplit) {
+    return (int64_t)((n + kRows - 1) / kRows) * h * nsplit < 2 * num_sms() ? 8 : 1;
+}
+
 template <typename TE, int DP>
 int fwd_simt_launch(int n, int h, int d, const void* q, const void* k, const void* v,
                     const int8_t* spd, int64_t ld, const float* T, int nb, float scale,
                     int kv_begin, int kv_end, int kv_block, int parts, void* o, float* lse,
                     float* o_part, float* lse_part, cudaStream_t s) {
     const int nsplit = kv_block > 0 ? (kv_end - kv_begin + kv_block - 1) / kv_block : 1;
-    dim3 grid((n + kRows - 1) / kRows, h, nsplit);
+    const int spl = simt_spl(n, h, nsplit);
+    dim3 grid((n + kRows / spl - 1) / (kRows / spl), h, nsplit);
     {
         LaunchScope ls("fwd_simt", s);
-        fwd_simt<TE, DP><<<grid, kRows, 0, s>>>(
-            n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld, T, nb, scale,
-            kv_begin, kv_end, nsplit > 1 ? kv_block : 0, parts, (TE*)o, lse, o_part, lse_part);
+        auto kern = spl == 8 ? fwd_simt<TE, DP, 8> : fwd_simt<TE, DP, 1>;
+        kern<<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const uint8_t*)spd, ld,
+                                    T, nb, scale, kv_begin, kv_end, nsplit > 1 ? kv_block : 0, parts, (TE*)o,
+                                    lse, o_part, lse_part);
     }
     return check_launch();
 }
@@ -331,18 +378,19 @@ int bwd_simt_launch(int n, int h, int d, const void* q, const void* k, const voi
         LaunchScope ls("bwd_delta", s);
         bwd_delta<TE><<<grid_for((int64_t)n * h), 256, 0, s>>>(n, h, d, (const TE*)o, (const TE*)dO, Dv);
     }
-    dim3 grid((n + kRows - 1) / kRows, h);
+    const int spl = simt_spl(n, h, 1);
+    dim3 grid((n + kRows / spl - 1) / (kRows / spl), h);
     {
         LaunchScope ls("bwd_rows_simt", s);
-        bwd_rows_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
-                                                     (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
-                                                     nb, scale, (TE*)dq, dT64);
+        auto kern = spl == 8 ? bwd_rows_simt<TE, DP, 8> : bwd_rows_simt<TE, DP, 1>;
+        kern<<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const TE*)dO, lse, Dv,
+                                    (const uint8_t*)spd, ld, T, nb, scale, (TE*)dq, dT64);
     }
     {
         LaunchScope ls("bwd_cols_simt", s);
-        bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v,
-                                                     (const TE*)dO, lse, Dv, (const uint8_t*)spd, ld, T,
-                                                     nb, scale, (TE*)dk, (TE*)dv);
+        auto kern = spl == 8 ? bwd_cols_simt<TE, DP, 8> : bwd_cols_simt<TE, DP, 1>;
+        kern<<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k, (const TE*)v, (const TE*)dO, lse, Dv,
+                                    (const uint8_t*)spd, ld, T, nb, scale, (TE*)dk, (TE*)dv);
     }
     {
         LaunchScope ls("bwd_dT_finalize", s);
@@ -420,38 +468,6 @@ int merge_partials(int dtype, int n, int h, int d, int nsplit, const float* o_pa
             merge_splits<__nv_bfloat16><<<grid_for((int64_t)n * h), 256, 0, s>>>(
                 n, h, d, nsplit, o_part, lse_part, (__nv_bfloat16*)o, lse);
         }
-    return check_launch();
-}
-
-// The column pass alone (dk, dv), given D [h][n].
-int attn_bwd_cols_simt(int dtype, int n, int h, int d, const void* q, const void* k, const void* v,
-                       const void* dO, const float* lse, const float* Dv, const int8_t* spd,
-                       int64_t ld, const float* T, int nb, float scale, void* dk, void* dv,
-                       cudaStream_t s) {
-    dim3 grid((n + kRows - 1) / kRows, h);
-    auto go = [&](auto tag, auto dp) {
-        using TE = decltype(tag);
-        constexpr int DP = decltype(dp)::value;
-        {
-            LaunchScope ls("bwd_cols_simt", s);
-            bwd_cols_simt<TE, DP><<<grid, kRows, 0, s>>>(n, h, d, (const TE*)q, (const TE*)k,
-                                                         (const TE*)v, (const TE*)dO, lse, Dv,
-                                                         (const uint8_t*)spd, ld, T, nb, scale,
-                                                         (TE*)dk, (TE*)dv);
-        }
-    };
-    using I8 = std::integral_constant<int, 8>;
-    using I16 = std::integral_constant<int, 16>;
-    using I32 = std::integral_constant<int, 32>;
-    using I64 = std::integral_constant<int, 64>;
-    if (dtype == GT_F32) {
-        if (d <= 8) go(float(), I8()); else if (d <= 16) go(float(), I16());
-        else if (d <= 32) go(float(), I32()); else go(float(), I64());
-    } else {
-        const __nv_bfloat16 z{};
-        if (d <= 8) go(z, I8()); else if (d <= 16) go(z, I16());
-        else if (d <= 32) go(z, I32()); else go(z, I64());
-    }
     return check_launch();
 }
 
