@@ -156,7 +156,7 @@ EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd
 # the capture summaries live under profiles/.  A kernel changed since its capture
 # has no entry (its traffic is reported as null).
 DRAM_BYTES = {("fwd_tc", "ba64x256"): 295.499e6, ("bwd_dq", "ba64x256"): 319.841e6,
-              ("spd_bfs", "ba64x256"): 214.984e6}
+              ("spd_bfs", "ba64x256"): 214.420e6}
 
 
 def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float,
