@@ -37,6 +37,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "gt_common.cuh"
 #include "gt_stats.cuh"
 #include "gt_sm100.cuh"
@@ -389,8 +391,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     acc_code = (int)c0;
                 }
                 const int jc = j0 + c * kCH;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
+                // One half chunk (8 columns).  FAST: every row of the warp holds one code
+                // over the chunk (the vote above), so a row takes its 4 head biases once,
+                // forms x - lse log2 e with one packed FMA per two columns and keeps its
+                // dS sums in registers; no row needs the per-element bins.  Otherwise each
+                // column takes its own code's biases, and rows with mixed codes add every
+                // dS to the shared bins.  The two are separate code, so the uniform chunks
+                // that dominate a graph of components run without the mixed path's branches.
+                auto half = [&](int g, auto fast_tag) {
+                    constexpr bool FAST = decltype(fast_tag)::value;
                     uint32_t rs[4][8], rd[4][8];
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
@@ -402,12 +411,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         tc_fence_before();
                         mbar_arrive(&bars->dp_free);
                     }
-                    // x - lse = s scale log2e + bias (scalar FMA) - lse (packed), then exp, dS;
-                    // when each of the warp's 32 rows has 16 equal codes (a warp vote, so
-                    // the warp never splits), a row takes its 4 head biases once
-                    if (wuni) {
-                        // x - lse log2 e = s scale log2 e + (b - lse log2 e): one packed FMA
-                        // per two columns
+                    if constexpr (FAST) {
+                        // x - lse log2 e = s scale log2 e + (b - lse log2 e)
                         const float4 bv = lds_f4(tbl + c0 * 32u);
                         const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -423,9 +428,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             }
                         }
                     } else {
-                        // then (head dim 16) x - lse log2 e, packed, per column pair as it is
-                        // formed; head dim 8 takes it in the exponential loop below, which
-                        // measured faster there (on uniform chunks it adds 0)
+                        // x = s scale log2 e + bias (scalar FMA), then (head dim 16) x - lse
+                        // log2 e, packed, per column pair as it is formed; head dim 8 takes it
+                        // in the exponential loop below, which measured faster there
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int kk = 8 * g + k;
@@ -458,12 +463,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
                         const float2 md = make_float2(-Dh[hh], -Dh[hh]);
-                        const float2 ml = wuni ? make_float2(0.f, 0.f) : make_float2(-L2[hh], -L2[hh]);
                         uint32_t pk[4];
 #pragma unroll
                         for (int k = 0; k < 8; k += 2) {
                             float2 xv = make_float2(__uint_as_float(rs[hh][k]), __uint_as_float(rs[hh][k + 1]));
-                            if (HD == 8) xv = __fadd2_rn(xv, ml);
+                            if constexpr (!FAST && HD == 8) xv = __fadd2_rn(xv, make_float2(-L2[hh], -L2[hh]));
                             const float2 p = make_float2(ex2(xv.x), ex2(xv.y));
                             const float2 dv = __fadd2_rn(make_float2(__uint_as_float(rd[hh][k]),
                                                                      __uint_as_float(rd[hh][k + 1])), md);
@@ -472,7 +476,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             rd[hh][k + 1] = __float_as_uint(ds.y);
                             pk[k / 2] = pack_bf16x2(ds.x, ds.y);
                         }
-                        if (uniform) {      // the row's sum for its register bin (mixed rows bin each element)
+                        if (FAST || uniform) {   // the row's sum for its register bin
 #pragma unroll
                             for (int k = 0; k < 8; k += 2)
                                 acc[hh] = __fadd2_rn(acc[hh], make_float2(__uint_as_float(rd[hh][k]),
@@ -480,27 +484,37 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         }
                         tmem_st_x4(lrow + s_col(ss) + 16 * hh + 4 * g, pk);
                     }
-                    if (!uniform) {
-                        // dS in fixed point (|dS| < 2^29 by the choice of the scale)
+                    if constexpr (!FAST) {
+                        if (!uniform) {
+                            // dS in fixed point (|dS| < 2^29 by the choice of the scale)
 #pragma unroll
-                        for (int hh = 0; hh < 4; ++hh)
+                            for (int hh = 0; hh < 4; ++hh)
 #pragma unroll
-                            for (int k = 0; k < 8; k += 2) {
-                                const uint2 fv = round_fixed2(__uint_as_float(rd[hh][k]), __uint_as_float(rd[hh][k + 1]));
-                                rd[hh][k] = fv.x;
-                                rd[hh][k + 1] = fv.y;
-                            }
+                                for (int k = 0; k < 8; k += 2) {
+                                    const uint2 fv =
+                                        round_fixed2(__uint_as_float(rd[hh][k]), __uint_as_float(rd[hh][k + 1]));
+                                    rd[hh][k] = fv.x;
+                                    rd[hh][k + 1] = fv.y;
+                                }
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int kk = 8 * g + k;
-                            const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
-                            if (code < (uint32_t)nb) {
+                            for (int k = 0; k < 8; ++k) {
+                                const int kk = 8 * g + k;
+                                const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
+                                if (code < (uint32_t)nb) {
 #pragma unroll
-                                for (int hh = 0; hh < 4; ++hh)
-                                    red_shared_add_u32(binb + code * kCodeStride + hh * kHeadStride, rd[hh][k]);
+                                    for (int hh = 0; hh < 4; ++hh)
+                                        red_shared_add_u32(binb + code * kCodeStride + hh * kHeadStride, rd[hh][k]);
+                                }
                             }
                         }
                     }
+                };
+                if (wuni) {
+                    half(0, std::true_type());
+                    half(1, std::true_type());
+                } else {
+                    half(0, std::false_type());
+                    half(1, std::false_type());
                 }
                 tmem_wait_st();
                 tc_fence_before();
