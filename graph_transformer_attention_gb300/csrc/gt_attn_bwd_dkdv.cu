@@ -42,6 +42,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "gt_common.cuh"
 #include "gt_stats.cuh"
 #include "gt_sm100.cuh"
@@ -375,65 +377,77 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 // bucket codes of the 16 (i, j) pairs: column r of the tile, unless the
                 // warp's whole 32 x 32 block holds one code
                 const int ucode = meta[4 * c];
-                uint32_t code[16];
-                float4 bu = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (ucode >= 0) {
-                    bu = lds_f4(tbl + (uint32_t)ucode * 32u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) code[kk] = stp[(ir + kk) * kBKV + r];
-                }
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    if (!mbar_wait(&bars->sd_full[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t x = lrow + pair_buf(p) + 32 * e + 16 * half;
-                    uint32_t rs[16], rd[16];
-                    tmem_ld_x16(x, rs);
-                    tmem_ld_x16(x + 64, rd);
-                    tmem_wait_ld();
-                    // x = s' scale log2e + b(code); P = 2^x
-                    float pf[16];
-                    if (ucode >= 0) {
-                        const float bh = p ? (e ? bu.w : bu.z) : (e ? bu.y : bu.x);
-                        const float2 cc = make_float2(scale_log2, scale_log2);
-#pragma unroll
-                        for (int kk = 0; kk < 16; kk += 2) {
-                            const float2 xa = __ffma2_rn(
-                                make_float2(__uint_as_float(rs[kk]), __uint_as_float(rs[kk + 1])), cc,
-                                make_float2(bh, bh));
-                            pf[kk] = xa.x;
-                            pf[kk + 1] = xa.y;
-                        }
+                // One chunk, both head pairs.  FAST (the warp's 32 x 32 block holds one
+                // code): one bias per head, x with one packed FMA per two rows; otherwise
+                // each row's code and bias.  Separate instantiations, so the uniform
+                // blocks run without the per-code path.  Returns false on a timeout.
+                auto chunk = [&](auto fast_tag) -> bool {
+                    constexpr bool FAST = decltype(fast_tag)::value;
+                    uint32_t code[16];
+                    float4 bu = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if constexpr (FAST) {
+                        bu = lds_f4(tbl + (uint32_t)ucode * 32u);
                     } else {
-                        const uint32_t hofs = 4u * (uint32_t)(2 * p + e);
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const float bv = __uint_as_float(lds_u32(tbl + code[kk] * 32u + hofs));
-                            pf[kk] = fmaf(__uint_as_float(rs[kk]), scale_log2, bv);
+                        for (int kk = 0; kk < 16; ++kk) code[kk] = stp[(ir + kk) * kBKV + r];
+                    }
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        if (!mbar_wait(&bars->sd_full[p], t & 1, abort_flag, kWaitNs)) return false;
+                        tc_fence_after();
+                        const uint32_t x = lrow + pair_buf(p) + 32 * e + 16 * half;
+                        uint32_t rs[16], rd[16];
+                        tmem_ld_x16(x, rs);
+                        tmem_ld_x16(x + 64, rd);
+                        tmem_wait_ld();
+                        // x = s' scale log2e + b(code); P = 2^x
+                        float pf[16];
+                        if constexpr (FAST) {
+                            const float bh = p ? (e ? bu.w : bu.z) : (e ? bu.y : bu.x);
+                            const float2 cc = make_float2(scale_log2, scale_log2);
+#pragma unroll
+                            for (int kk = 0; kk < 16; kk += 2) {
+                                const float2 xa = __ffma2_rn(
+                                    make_float2(__uint_as_float(rs[kk]), __uint_as_float(rs[kk + 1])), cc,
+                                    make_float2(bh, bh));
+                                pf[kk] = xa.x;
+                                pf[kk + 1] = xa.y;
+                            }
+                        } else {
+                            const uint32_t hofs = 4u * (uint32_t)(2 * p + e);
+#pragma unroll
+                            for (int kk = 0; kk < 16; ++kk) {
+                                const float bv = __uint_as_float(lds_u32(tbl + code[kk] * 32u + hofs));
+                                pf[kk] = fmaf(__uint_as_float(rs[kk]), scale_log2, bv);
+                            }
                         }
-                    }
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) pf[kk] = ex2(pf[kk]);
-                    if (tail_tile) {
+                        for (int kk = 0; kk < 16; ++kk) pf[kk] = ex2(pf[kk]);
+                        if (tail_tile) {
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk)
-                            if (i0 + ir + kk >= n) pf[kk] = 0.f;
-                    }
-                    uint32_t pp[8], pd[8];
+                            for (int kk = 0; kk < 16; ++kk)
+                                if (i0 + ir + kk >= n) pf[kk] = 0.f;
+                        }
+                        uint32_t pp[8], pd[8];
 #pragma unroll
-                    for (int k2 = 0; k2 < 8; ++k2) {
-                        pp[k2] = pack_bf16x2(pf[2 * k2], pf[2 * k2 + 1]);
-                        const float2 ds = __fmul2_rn(
-                            make_float2(pf[2 * k2], pf[2 * k2 + 1]),
-                            make_float2(__uint_as_float(rd[2 * k2]), __uint_as_float(rd[2 * k2 + 1])));
-                        pd[k2] = pack_bf16x2(ds.x, ds.y);
+                        for (int k2 = 0; k2 < 8; ++k2) {
+                            pp[k2] = pack_bf16x2(pf[2 * k2], pf[2 * k2 + 1]);
+                            const float2 ds = __fmul2_rn(
+                                make_float2(pf[2 * k2], pf[2 * k2 + 1]),
+                                make_float2(__uint_as_float(rd[2 * k2]), __uint_as_float(rd[2 * k2 + 1])));
+                            pd[k2] = pack_bf16x2(ds.x, ds.y);
+                        }
+                        tmem_st_x8(x, pp);
+                        tmem_st_x8(x + 8, pd);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(&bars->ds_ready[p]);
                     }
-                    tmem_st_x8(x, pp);
-                    tmem_st_x8(x + 8, pd);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&bars->ds_ready[p]);
+                    return true;
+                };
+                if (!(ucode >= 0 ? chunk(std::true_type()) : chunk(std::false_type()))) {
+                    ok = false;
+                    break;
                 }
             }
             if (!ok) break;
