@@ -151,12 +151,14 @@ def measured_peaks() -> dict:
 # Exp-bound kernels: one exp per (query, key, head) per launch.
 EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd_cols_simt")
 
-# DRAM bytes (read + write) per launch of a kernel at a workload, from one ncu
-# capture of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
-# the capture summaries live under profiles/.  A kernel changed since its capture
-# has no entry (its traffic is reported as null).
+# DRAM bytes (read + write) per launch of a kernel at a workload, from ncu
+# captures of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
+# the capture summaries live under profiles/.  For a kernel launched more than once
+# per layer (bwd_dkdv: the full wave, 180.558 MB, and the split tail, 135.425 MB)
+# the entry is the mean over the layer's launches, like the work per launch.  A
+# kernel changed since its capture has no entry (its traffic is reported as null).
 DRAM_BYTES = {("fwd_tc", "ba64x256"): 295.499e6, ("bwd_dq", "ba64x256"): 316.789e6,
-              ("spd_bfs", "ba64x256"): 214.420e6}
+              ("bwd_dkdv", "ba64x256"): 157.992e6, ("spd_bfs", "ba64x256"): 214.420e6}
 
 
 def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float,
@@ -168,7 +170,7 @@ def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_p
     tail) the work per launch is the layer's N^2 H over its launches, and `ms` the
     mean launch time, so work / time is the layer's exps over the kernel's time."""
     t = ms * 1e-3
-    traffic = DRAM_BYTES.get((name, w.name)) if launches_per_layer == 1.0 else None
+    traffic = DRAM_BYTES.get((name, w.name))
     if name in EXP_KERNELS:
         work = float(w.n) * w.n * w.heads / launches_per_layer     # exps per launch
         return {"kernel": name, "bound": "exp", "achieved": round(work / t / 1e12, 4),
