@@ -103,16 +103,18 @@ struct Bars {
 // instead of the conversion unit (which shares its throughput with ex2 and
 // runs at half its rate).  v = a + b with a the nearest multiple of 128 (the
 // sum v + 1.5 * 2^30 has a unit in the last place of 128, so its low mantissa
-// bits hold a / 128) and b = v - a, |b| <= 64, exact; b + 1.5 * 2^23 holds
-// round(b) in its low mantissa bits.  a + round(b) = round(v) exactly.
+// bits hold a / 128) and b = v - a, |b| <= 64; v + (1.5 * 2^23 - a), with
+// 1.5 * 2^23 - a formed exactly from the first sum (it is a multiple of 128
+// below 2^30), rounds once, to 1.5 * 2^23 + round(b), whose low mantissa bits
+// hold round(b).  a + round(b) = round(v) exactly: three packed adds per pair.
 __device__ __forceinline__ uint2 round_fixed2(float x, float y) {
-    constexpr float kC1 = 1610612736.f;   // 1.5 * 2^30
-    constexpr float kC2 = 12582912.f;     // 1.5 * 2^23
+    constexpr float kC1 = 1610612736.f;    // 1.5 * 2^30
+    constexpr float kC12 = 1623195648.f;   // 1.5 * 2^30 + 1.5 * 2^23, exact
     const float2 v = make_float2(x, y);
-    const float2 h = __fadd2_rn(v, make_float2(kC1, kC1));
-    const float2 na = __fadd2_rn(make_float2(kC1, kC1), make_float2(-h.x, -h.y));   // -a, exact
-    const float2 b = __fadd2_rn(__fadd2_rn(v, na), make_float2(kC2, kC2));
-    constexpr uint32_t kBias = (0x4EC00000u << 7) + 0x4B400000u;   // bits(kC1) * 128 + bits(kC2)
+    const float2 h = __fadd2_rn(v, make_float2(kC1, kC1));                          // 1.5 * 2^30 + a
+    const float2 u = __fadd2_rn(make_float2(kC12, kC12), make_float2(-h.x, -h.y));  // 1.5 * 2^23 - a, exact
+    const float2 b = __fadd2_rn(v, u);                                              // 1.5 * 2^23 + round(b)
+    constexpr uint32_t kBias = (0x4EC00000u << 7) + 0x4B400000u;   // bits(1.5 * 2^30) * 128 + bits(1.5 * 2^23)
     return make_uint2((__float_as_uint(h.x) << 7) + __float_as_uint(b.x) - kBias,
                       (__float_as_uint(h.y) << 7) + __float_as_uint(b.y) - kBias);
 }
