@@ -101,22 +101,23 @@ struct Bars {
 
 // round(v) for a pair of floats with |v| < 2^29, on the FP32 and integer pipes
 // instead of the conversion unit (which shares its throughput with ex2 and
-// runs at half its rate).  v = a + b with a the nearest multiple of 128 (the
-// sum v + 1.5 * 2^30 has a unit in the last place of 128, so its low mantissa
-// bits hold a / 128) and b = v - a, |b| <= 64; v + (1.5 * 2^23 - a), with
-// 1.5 * 2^23 - a formed exactly from the first sum (it is a multiple of 128
-// below 2^30), rounds once, to 1.5 * 2^23 + round(b), whose low mantissa bits
-// hold round(b).  a + round(b) = round(v) exactly: three packed adds per pair.
+// runs at half its rate).  v = a + b with a the nearest multiple of 512: the sum
+// h = v + C1, C1 = 1.70703... * 2^32 (bits 0x4FDA7FFF), has a unit in the last
+// place of 512, so h = C1 + a and its low mantissa bits hold a / 512; |b| <= 256.
+// u = (C1 + C2) - h = C2 - a is exact (C2 = 2^23 + 512; C2 - a is a multiple of
+// 512 below 2^30), and v + u rounds once, to C2 + round(b), whose low mantissa
+// bits hold round(b).  So round(v) = a + round(b) = 512 (bits(h) - bits(C1)) +
+// bits(v + u) - bits(C2), and C1, C2 are chosen so that 512 bits(C1) + bits(C2)
+// = 0 mod 2^32: three packed adds and one shift-add per value.
 __device__ __forceinline__ uint2 round_fixed2(float x, float y) {
-    constexpr float kC1 = 1610612736.f;    // 1.5 * 2^30
-    constexpr float kC12 = 1623195648.f;   // 1.5 * 2^30 + 1.5 * 2^23, exact
+    constexpr float kC1 = 7331642880.f;    // bits 0x4FDA7FFF
+    constexpr float kC12 = 7340032000.f;   // kC1 + 2^23 + 512, exact
     const float2 v = make_float2(x, y);
-    const float2 h = __fadd2_rn(v, make_float2(kC1, kC1));                          // 1.5 * 2^30 + a
-    const float2 u = __fadd2_rn(make_float2(kC12, kC12), make_float2(-h.x, -h.y));  // 1.5 * 2^23 - a, exact
-    const float2 b = __fadd2_rn(v, u);                                              // 1.5 * 2^23 + round(b)
-    constexpr uint32_t kBias = (0x4EC00000u << 7) + 0x4B400000u;   // bits(1.5 * 2^30) * 128 + bits(1.5 * 2^23)
-    return make_uint2((__float_as_uint(h.x) << 7) + __float_as_uint(b.x) - kBias,
-                      (__float_as_uint(h.y) << 7) + __float_as_uint(b.y) - kBias);
+    const float2 h = __fadd2_rn(v, make_float2(kC1, kC1));                          // C1 + a
+    const float2 u = __fadd2_rn(make_float2(kC12, kC12), make_float2(-h.x, -h.y));  // C2 - a, exact
+    const float2 b = __fadd2_rn(v, u);                                              // C2 + round(b)
+    return make_uint2((__float_as_uint(h.x) << 9) + __float_as_uint(b.x),
+                      (__float_as_uint(h.y) << 9) + __float_as_uint(b.y));
 }
 
 template <int HD, int NCP>
