@@ -77,8 +77,15 @@ struct DqCfg {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_G = OP_BYTES;
     static constexpr uint32_t OFF_STAGE = 2 * OP_BYTES;
-    static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_T + 256 * kH * 4;
+    static constexpr uint32_t OFF_T = OFF_STAGE + kKVST * STAGE_BYTES;   // bias table of the CTA's 4 heads
+    // the fold operands: A_S and A_D [128 rows][16] (per head h, columns 4h .. 4h + 2
+    // hold -(lse log2 e - e) / (scale log2 e), resp. -D, as three bf16 parts whose
+    // sum is the fp32 value) and the B selector [64][16] that adds, to the 16 S (dP)
+    // columns of head h, A's columns 4h .. 4h + 2
+    static constexpr uint32_t OFF_FA = OFF_T + 256 * kHC * 4;
+    static constexpr uint32_t OFF_FD = OFF_FA + kBQ * 32;
+    static constexpr uint32_t OFF_FB = OFF_FD + kBQ * 32;
+    static constexpr uint32_t OFF_BAR = OFF_FB + 64 * 32;
     static constexpr uint32_t OFF_BIN = OFF_BAR + 256;
     // bins: [nb][4 heads][ncp] int32 fixed point, sized at launch
     static constexpr uint32_t smem_bytes(int nb, int ncp) { return OFF_BIN + (uint32_t)nb * kHC * ncp * 4 + 1024; }
@@ -175,20 +182,65 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         tma_prefetch_desc(&mapS);
     }
     if (warp == kMmaWarp) tmem_alloc(&bars->tmem_base, kTmemCols);
-    fill_bias_table(Ts, T, nb, tid, kThreads);
+    fill_bias_table_heads<kHC>(Ts, T, nb, kHC * hb, tid, kThreads);
     for (int x = tid; x < nb * kHC * NCP; x += kThreads) bins[x] = 0;
+    // the fold's B selector: row m (column m of the 64 S or dP columns, head m / 16)
+    // holds ones at columns 4 (m / 16) .. 4 (m / 16) + 2; 32-byte swizzle
+    for (int m = tid; m < 64; m += kThreads) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2)
+            w[k2] = k2 == 2 * (m >> 4) ? 0x3F803F80u : k2 == 2 * (m >> 4) + 1 ? 0x00003F80u : 0u;   // bf16 1.0
+        uint8_t* dst = smem + C::OFF_FB + m * 32;
+        const uint32_t sw = (uint32_t)((m >> 2) & 1);
+        *reinterpret_cast<uint4*>(dst + ((0u ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + ((1u ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
     if (tid < kBQ) {
         const int row = i0 + tid;
         const bool live = row < n;
         const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
         write_head_operands<HD, kHC>(smem + C::OFF_Q, tid, q + off, live, kHC * hb);
         write_head_operands<HD, kHC>(smem + C::OFF_G, tid, dO + off, live, kHC * hb);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (after_prep) {
-        pdl_wait();
-        pdl_trigger();
+    if (after_prep) pdl_wait();
+    // this row's lse log2 e and D per head go into the fold operands, so that the
+    // tensor core forms s - lse log2 e / (scale log2 e) and dP - D
+    float L2[4] = {0.f, 0.f, 0.f, 0.f}, Dh[4] = {0.f, 0.f, 0.f, 0.f};
+    if (tid < kBQ) {
+        const int row = i0 + tid;
+        const bool live = row < n;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            L2[hh] = live ? LD[(int64_t)(kHC * hb + hh) * ldl + row] : 0.f;
+            Dh[hh] = live ? LD[(int64_t)(kH + kHC * hb + hh) * ldl + row] : 0.f;
+        }
+        // each value as three bf16 parts (the value, then what each part leaves:
+        // 8 + 8 + 8 bits, so the parts sum to the fp32 value)
+        const float inv_c = 1.f / scale_log2;
+        uint32_t wa[8], wd[8];
+        auto parts = [](float v, uint32_t& w01, uint32_t& w2) {
+            const float p1 = __bfloat162float(__float2bfloat16_rn(v));
+            const float r1 = v - p1;
+            const float p2 = __bfloat162float(__float2bfloat16_rn(r1));
+            w01 = pack_bf16x2(p1, p2);
+            w2 = pack_bf16x2(r1 - p2, 0.f);
+        };
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            parts(-L2[hh] * inv_c, wa[2 * hh], wa[2 * hh + 1]);
+            parts(-Dh[hh], wd[2 * hh], wd[2 * hh + 1]);
+        }
+        const uint32_t sw = (uint32_t)((tid >> 2) & 1);
+        uint8_t* da = smem + C::OFF_FA + tid * 32;
+        uint8_t* dd = smem + C::OFF_FD + tid * 32;
+        *reinterpret_cast<uint4*>(da + ((0u ^ sw) << 4)) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(da + ((1u ^ sw) << 4)) = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+        *reinterpret_cast<uint4*>(dd + ((0u ^ sw) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        *reinterpret_cast<uint4*>(dd + ((1u ^ sw) << 4)) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
     }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (after_prep) pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -233,6 +285,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         {
             const uint32_t idKK = idesc_bf16(128, 16, false, false);
             const uint32_t idKM = idesc_bf16(128, 16, false, true);
+            const uint32_t idFold = idesc_bf16(128, 64, false, false);   // the 4 heads' 64 columns at once
+            const uint64_t dFA = desc_at(smem_desc_split(smem_u32(smem + C::OFF_FA), 16, 256, 6), 0);
+            const uint64_t dFD = desc_at(smem_desc_split(smem_u32(smem + C::OFF_FD), 16, 256, 6), 0);
+            const uint64_t dFB = desc_at(smem_desc_split(smem_u32(smem + C::OFF_FB), 16, 256, 6), 0);
             const uint32_t stage_base = smem_u32(smem + C::OFF_STAGE);
             const SmemDesc dQ = smem_desc_split(smem_u32(smem + C::OFF_Q), 16, 256, 6);
             const SmemDesc dG = smem_desc_split(smem_u32(smem + C::OFF_G), 16, 256, 6);
@@ -255,6 +311,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
                     for (int h = 0; h < kHC; ++h)
                         mma_ss(tbase + s_col(ss) + 16 * h, desc_at(dQ, h * 4096), desc_at(dKk, koff(tt, h)), idKK, 0);
+                    mma_ss(tbase + s_col(ss), dFA, dFB, idFold, 1);       // - (lse log2 e - e) / (scale log2 e)
                     mma_commit(&bars->s_full[ss]);
                 }
                 __syncwarp();
@@ -266,6 +323,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     for (int h = 0; h < kHC; ++h)
                         mma_ss(tbase + kColDp + 16 * h, desc_at(dG, h * 4096), desc_at(dKk, koff(tt, h) + kVoff),
                                idKK, 0);
+                    mma_ss(tbase + kColDp, dFD, dFB, idFold, 1);          // - D
                     mma_commit(&bars->dp_full);
                 }
                 __syncwarp();
@@ -306,18 +364,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         const int row = i0 + r;
         const bool live = row < n;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * hb;
+        const uint32_t tbl = smem_u32(Ts);     // 16-byte rows: the CTA's 4 head biases of a code
         // bin address: binb + code * kCodeStride + hh * kHeadStride
         constexpr uint32_t kHeadStride = 4u * NCP, kCodeStride = kHC * kHeadStride;
         const uint32_t binb = smem_u32(bins) + 4u * (uint32_t)(lane & (NCP - 1));
-        float L2[4], Dh[4];
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-            L2[hh] = live ? LD[(int64_t)(kHC * hb + hh) * ldl + row] : 0.f;
-            Dh[hh] = live ? LD[(int64_t)(kH + kHC * hb + hh) * ldl + row] : 0.f;
-        }
         // fixed-point scale of the dT bins: 2^e with (rows per copy) * max_i B_i * 2^e
-        // <= 2^30, B_i = |dO_i| max_j |v_j| + |D_i| bounding sum_j |dS_ij| (per head)
+        // <= 2^30, B_i = |dO_i| max_j |v_j| + |D_i| bounding sum_j |dS_ij| (per head).
+        // The scale rides in the exponent (P 2^e = 2^(x - lse log2 e + e)): e is
+        // added to every entry of the bias table, so dS comes out in fixed-point
+        // units (and dq carries 2^e, taken out in the epilogue)
         float bscale;
         {
             float bmax = 0.f;
@@ -350,11 +405,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             if (!(bound < INFINITY) || e < 0) e = 0;
             if (e > 60) e = 60;
             bscale = exp2f((float)e);
-            // the scale rides in the exponent: P 2^e = 2^(x - (lse log2 e - e)), so
-            // dS comes out already in fixed-point units (and dq carries 2^e, taken
-            // out in the epilogue)
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) L2[hh] -= (float)e;
+            for (int x = tid; x < 256 * kHC; x += kSoft) Ts[x] += (float)e;
+            asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory");
         }
         auto fx = [&](float v) -> uint32_t { return (uint32_t)__float2int_rn(v); };
         const float qscale = scale / bscale;
@@ -394,10 +446,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     acc_code = (int)c0;
                 }
                 const int jc = j0 + c * kCH;
-                // One half chunk (8 columns).  FAST: every row of the warp holds one code
-                // over the chunk (the vote above), so a row takes its 4 head biases once,
-                // forms x - lse log2 e with one packed FMA per two columns and keeps its
-                // dS sums in registers; no row needs the per-element bins.  Otherwise each
+                // One half chunk (8 columns).  The tensor core has already taken lse
+                // log2 e (less the bins' e) out of S, in units of scale log2 e, and D out
+                // of dP (the fold operand), so x - lse log2 e = s scale log2 e + b and dS =
+                // P dP.  FAST: every row of the warp holds one code over the chunk (the
+                // vote above), so a row takes its 4 head biases once, forms x with one
+                // packed FMA per two columns and keeps its dS sums in registers; no row
+                // needs the per-element bins.  Otherwise each
                 // column takes its own code's biases, and rows with mixed codes add every
                 // dS to the shared bins.  The two are separate code, so the uniform chunks
                 // that dominate a graph of components run without the mixed path's branches.
@@ -415,12 +470,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                         mbar_arrive(&bars->dp_free);
                     }
                     if constexpr (FAST) {
-                        // x - lse log2 e = s scale log2 e + (b - lse log2 e)
-                        const float4 bv = lds_f4(tbl + c0 * 32u);
+                        const float4 bv = lds_f4(tbl + c0 * 16u);
                         const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                         for (int hh = 0; hh < 4; ++hh) {
-                            const float2 bl = make_float2(bb[hh] - L2[hh], bb[hh] - L2[hh]);
+                            const float2 bl = make_float2(bb[hh], bb[hh]);
 #pragma unroll
                             for (int k = 0; k < 8; k += 2) {
                                 const float2 x = __ffma2_rn(
@@ -431,28 +485,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             }
                         }
                     } else {
-                        // x = s scale log2 e + bias (scalar FMA), then (head dim 16) x - lse
-                        // log2 e, packed, per column pair as it is formed; head dim 8 takes it
-                        // in the exponential loop below, which measured faster there
+                        // x = s scale log2 e + bias (scalar FMA), each column its own code
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int kk = 8 * g + k;
                             const uint32_t code = __byte_perm(w[kk >> 2], 0u, 0x4440u + (kk & 3));
-                            const float4 bv = lds_f4(tbl + code * 32u);
+                            const float4 bv = lds_f4(tbl + code * 16u);
                             rs[0][k] = __float_as_uint(fmaf(__uint_as_float(rs[0][k]), scale_log2, bv.x));
                             rs[1][k] = __float_as_uint(fmaf(__uint_as_float(rs[1][k]), scale_log2, bv.y));
                             rs[2][k] = __float_as_uint(fmaf(__uint_as_float(rs[2][k]), scale_log2, bv.z));
                             rs[3][k] = __float_as_uint(fmaf(__uint_as_float(rs[3][k]), scale_log2, bv.w));
-                            if (HD == 16 && (k & 1)) {
-#pragma unroll
-                                for (int hh = 0; hh < 4; ++hh) {
-                                    const float2 xv = __fadd2_rn(
-                                        make_float2(__uint_as_float(rs[hh][k - 1]), __uint_as_float(rs[hh][k])),
-                                        make_float2(-L2[hh], -L2[hh]));
-                                    rs[hh][k - 1] = __float_as_uint(xv.x);
-                                    rs[hh][k] = __float_as_uint(xv.y);
-                                }
-                            }
                         }
                     }
                     if (tail_block) {
@@ -465,16 +507,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     }
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        const float2 md = make_float2(-Dh[hh], -Dh[hh]);
                         uint32_t pk[4];
 #pragma unroll
                         for (int k = 0; k < 8; k += 2) {
-                            float2 xv = make_float2(__uint_as_float(rs[hh][k]), __uint_as_float(rs[hh][k + 1]));
-                            if constexpr (!FAST && HD == 8) xv = __fadd2_rn(xv, make_float2(-L2[hh], -L2[hh]));
-                            const float2 p = make_float2(ex2(xv.x), ex2(xv.y));
-                            const float2 dv = __fadd2_rn(make_float2(__uint_as_float(rd[hh][k]),
-                                                                     __uint_as_float(rd[hh][k + 1])), md);
-                            const float2 ds = __fmul2_rn(p, dv);
+                            const float2 p = make_float2(ex2(__uint_as_float(rs[hh][k])), ex2(__uint_as_float(rs[hh][k + 1])));
+                            const float2 ds = __fmul2_rn(p, make_float2(__uint_as_float(rd[hh][k]),
+                                                                        __uint_as_float(rd[hh][k + 1])));
                             rd[hh][k] = __float_as_uint(ds.x);
                             rd[hh][k + 1] = __float_as_uint(ds.y);
                             pk[k / 2] = pack_bf16x2(ds.x, ds.y);
