@@ -10,11 +10,11 @@
 // tensor-core products.  Tasks past the last full wave of two CTAs per SM are
 // split over several CTAs along the KV blocks (grid.z), which sum dq in fp32;
 // so are all tasks of a graph too small to give every SM two.  192 threads:
-//   warps 0-3  thread r owns query row r (TMEM lane r), so lse and D are
-//              registers.  Per chunk of
-//              16 KV columns: S_h and dP_h from TMEM, one 16-byte shared load of
-//              the 4 head biases per bucket byte, P = 2^(x - lse log2 e),
-//              dS = P (dP - D), dS (bf16) back to TMEM over S, and dS summed per
+//   warps 0-3  thread r owns query row r (TMEM lane r).  Per chunk of 16 KV
+//              columns: S'_h and dP'_h from TMEM (lse and D already taken out by
+//              the tensor core, below), one 16-byte shared load of the 4 head
+//              biases per bucket byte, P = 2^(s' scale log2 e + b), dS = P dP',
+//              dS (bf16) back to TMEM over S, and dS summed per
 //              bucket: in registers while the row's 16 codes are equal, else with
 //              shared-memory reductions into bins [code][head][NCP copies]; lane l
 //              adds into copy l mod NCP, so with NCP = 32 the 32 rows of a warp never
@@ -24,10 +24,14 @@
 //              sum_j |dS_ij| <= |dO_i| max_j |v_j| + |D_i| (the P_ij of a row sum to
 //              1), so one power-of-two scale 2^e per CTA keeps every copy's sum below
 //              2^30; the copies are summed exactly in 64 bits at the end.  The
-//              scale is folded into the exponent (P 2^e = 2^(x - lse log2 e + e)),
-//              so dS is formed in fixed-point units; dq drops the 2^e at the end.
+//              scale is folded into the exponent (P 2^e = 2^(x - lse log2 e + e):
+//              e is added to the bias table), so dS is formed in fixed-point units;
+//              dq drops the 2^e at the end.
 //   warp 4     MMA issuer: S_h = Q_h K_h^T and dP_h = dO_h V_h^T (M=128, N=16,
-//              K=16), then dq_h += dS_h K_h (A = dS from TMEM).
+//              K=16), each followed by one product over all 4 heads (N = 64) that
+//              adds -lse log2 e / (scale log2 e), resp. -D, per row and head: A
+//              holds them as three bf16 parts per value (written by the prologue),
+//              B selects each head's parts; then dq_h += dS_h K_h (A = dS from TMEM).
 //   warp 5     TMA producer: bucket tile and K / V column slots per KV block.
 // TMEM (256 columns): dq at 0..63 (16 per head), two S/dS stages at 64 and
 // 128, dP at 192.  All waits are bounded (timeout -> device status word, orderly
