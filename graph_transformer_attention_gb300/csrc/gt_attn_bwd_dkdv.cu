@@ -73,10 +73,6 @@ constexpr uint32_t kColOnesL = 192;        // A = [1 1 1 0 ...]: picks -lse / sc
 constexpr uint32_t kColOnesD = 200;        // A = [0 0 0 1 1 1 0 ...]: picks -D
 constexpr uint32_t kSmemOneCta = 120 * 1024;   // more than half an SM's shared memory: one CTA per SM
 
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
-    return __fadd2_rn(a, make_float2(-b.x, -b.y));
-}
-
 // TMEM buffer of head pair p
 __device__ __forceinline__ uint32_t pair_buf(int p) { return 256u + 128u * (uint32_t)p; }
 

@@ -163,9 +163,5 @@ __device__ __forceinline__ void red_shared_add_u32(uint32_t addr, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void red_shared_add(uint32_t addr, float v) {
-    asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 }  // namespace tc
 }  // namespace gt
