@@ -102,20 +102,21 @@ struct Bars {
     uint64_t q_empty[kQST];
     uint64_t sd_full[2];         // S^T and dP^T of a step are in its head pair's buffer
     uint64_t ds_ready[2];        // P^T and dS^T of a step are in (dP^T read)
-    uint64_t done;
+    uint64_t done;               // a group's last dk/dv products are complete (phase = its segment)
+    uint64_t seg_ready;          // the next group's K and V are in TMEM, the last one's dk/dv read
     uint64_t fin;
     uint32_t tmem_base;
     int abort;
 };
 
-template <int HD>
+template <int HD, bool kBal>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapG,
                 const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapB,
                 const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                 const float* __restrict__ T, int nb, int n, float scale, float scale_log2, int g0, int split_tiles,
-                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dk_acc,
-                float* __restrict__ dv_acc, int* status) {
+                int bal_ctas, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                float* __restrict__ dk_acc, float* __restrict__ dv_acc, int* status) {
     using C = KvCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned by pointer arithmetic on the shared array, so that the
@@ -125,15 +126,32 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     float* Ts = reinterpret_cast<float*>(smem + C::OFF_T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();   // the split tail may take SMs as this launch frees them
-    const int g = g0 + (int)blockIdx.x;        // group: KV tile g / 2, head half g % 2
-    const int j0 = (g >> 1) * kBKV;
-    const int hb = g & 1;                      // heads 4 hb .. 4 hb + 3
-    // Q tiles qt0 .. qt0 + ntiles - 1 (all of them unless the rows are split over
-    // grid.z, in which case dk and dv are summed into dk_acc / dv_acc in fp32)
+    // The CTA's work is a run of (group, Q tile) steps in group-major order: step
+    // s = g T + qt, group g = KV tile g / 2 and head half g % 2 (heads 4 hb .. 4 hb
+    // + 3), T Q tiles per group.  Balanced (kBal, bal_ctas CTAs): CTA x takes steps
+    // [x S / bal_ctas, (x + 1) S / bal_ctas) of all S = groups T, so that every CTA
+    // has the same work; the groups it shares with a neighbour (and, for
+    // simplicity, all others) are summed into dk_acc / dv_acc in fp32.  Otherwise
+    // one group g0 + blockIdx.x, its Q tiles split over grid.z when split_tiles > 0
+    // (then summed in fp32 too).  The b-th tile of the CTA is step sb + b; a change
+    // of group starts a new segment (K and V rewritten, dk and dv restarted).
     const int total_tiles = (n + C::BQ - 1) / C::BQ;
-    const int qt0 = split_tiles > 0 ? blockIdx.z * split_tiles : 0;
-    const int ntiles = split_tiles > 0 ? min(split_tiles, total_tiles - qt0) : total_tiles;
+    int64_t sb, se;
+    if (kBal) {
+        const int64_t steps = (int64_t)(2 * ((n + kBKV - 1) / kBKV)) * total_tiles;
+        sb = steps * blockIdx.x / bal_ctas;
+        se = steps * (blockIdx.x + 1) / bal_ctas;
+    } else {
+        const int qt0 = split_tiles > 0 ? blockIdx.z * split_tiles : 0;
+        sb = (int64_t)(g0 + (int)blockIdx.x) * total_tiles + qt0;
+        se = sb + (split_tiles > 0 ? min(split_tiles, total_tiles - qt0) : total_tiles);
+    }
+    const int ntiles = (int)(se - sb);
     const int nchunks = ntiles * C::NCH;
+    // the first tile's group and Q tile; the loops below walk the groups without
+    // dividing: the k-th segment ends before tile T - q_first + k T
+    const int g_first = (int)(sb / total_tiles);
+    const int q_first = (int)(sb - (int64_t)g_first * total_tiles);
 
     if (tid == kTmaWarp * 32) {
         for (int s = 0; s < kQST; ++s) {
@@ -146,6 +164,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mbar_init(&bars->ds_ready[p], kSoft);
         }
         mbar_init(&bars->done, 1);
+        mbar_init(&bars->seg_ready, kSoft);
         mbar_init(&bars->fin, 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -161,21 +180,26 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     tc_fence_after();
     const uint32_t tbase = bars->tmem_base;
     int* abort_flag = &bars->abort;
-    // K and V rows of this CTA's heads into TMEM (A operands), one row per lane
-    if (tid < kBKV) {
-        const int row = j0 + tid;
+    // K and V rows of group g's heads into TMEM (A operands), one row per lane of
+    // threads 0 .. 127 (again at each change of group)
+    auto write_kv = [&](int g) {
+        const int row = (g >> 1) * kBKV + tid;
         const bool live = row < n;
         const int64_t off = (int64_t)(live ? row : 0) * kH * HD;
         const uint32_t lr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll
         for (int hh = 0; hh < kHC; ++hh) {
             uint32_t a[8];
-            head_a_row<HD>(k + off, kHC * hb + hh, live, a);
+            head_a_row<HD>(k + off, kHC * (g & 1) + hh, live, a);
             tmem_st_x8(lr + kColKA + 8 * hh, a);
-            head_a_row<HD>(v + off, kHC * hb + hh, live, a);
+            head_a_row<HD>(v + off, kHC * (g & 1) + hh, live, a);
             tmem_st_x8(lr + kColVA + 8 * hh, a);
         }
+    };
+    if (tid < kBKV) {
+        write_kv(g_first);
         // ones operands (bf16 1.0 = 0x3f80; element 2c in the low half of column c)
+        const uint32_t lr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t onesL[8] = {0x3f803f80u, 0x00003f80u, 0u, 0u, 0u, 0u, 0u, 0u};
         const uint32_t onesD[8] = {0u, 0x3f800000u, 0x3f803f80u, 0u, 0u, 0u, 0u, 0u};
         tmem_st_x8(lr + kColOnesL, onesL);
@@ -194,6 +218,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
         int issued = 0;
         bool ok = true;
+        int ig = g_first, iq = q_first;   // group and Q tile of the next tile to issue (tiles in order)
         auto issue = [&](int b) -> bool {
             const int ks = b & 1;
             if (lane == 0) {
@@ -201,7 +226,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     fail(abort_flag, status);
                 } else {
                     uint8_t* st = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
-                    const int i0 = (qt0 + b) * C::BQ;
+                    const int i0 = iq * C::BQ, j0 = (ig >> 1) * kBKV, hb = ig & 1;
                     mbar_arrive_expect_tx(&bars->q_full[ks], C::STAGE_BYTES);
                     tma_load_2d(st, &mapS, j0, i0, &bars->q_full[ks]);
 #pragma unroll
@@ -220,6 +245,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             __syncwarp();
             if (*(volatile int*)abort_flag) return false;
             issued = b + 1;
+            if (++iq == total_tiles) {
+                iq = 0;
+                ++ig;
+            }
             return true;
         };
         auto summarise = [&](int b) -> bool {
@@ -311,30 +340,55 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 __syncwarp();
                 return true;
             };
-            bool ok = issue_sd(0);
-            if (ok && nsteps > 1) ok = issue_sd(1);
-            for (int st = 0; ok && st < nsteps; ++st) {
-                const int t = st >> 1, p = st & 1, b = t / C::NCH, c = t % C::NCH, ks = b & 1;
-                if (!mbar_wait_all(&bars->ds_ready[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t x = tbase + pair_buf(p);
-                if (elect_one()) {
+            // a group's steps end with its dk / dv products and a commit of `done`;
+            // the next group's S and dP wait for `seg_ready` (its K and V written,
+            // the last group's dk and dv read), and its first products restart dk, dv
+            // (the segment change sits outside the step loop, which stays as small
+            // as with one group)
+            int seg = 0;        // segments finished (the phase of done and seg_ready)
+            int t_seg = 0;      // first chunk of the current segment
+            int b_end = total_tiles - q_first;   // first tile past the current segment
+            bool ok = true;
+            int st = 0;
+#pragma unroll 1
+            for (int k0 = 0; ok && k0 < 2 && k0 < nsteps; ++k0) ok = issue_sd(k0);
+            while (ok && st < nsteps) {
+                const int st_end = kBal ? min(nsteps, 2 * C::NCH * b_end) : nsteps;   // the segment's steps
+                for (; st < st_end; ++st) {
+                    const int t = st >> 1, p = st & 1, b = t / C::NCH, c = t % C::NCH, ks = b & 1;
+                    if (!mbar_wait_all(&bars->ds_ready[p], t & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t x = tbase + pair_buf(p);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int h = 2 * p + e;
+                        for (int e = 0; e < 2; ++e) {
+                            const int h = 2 * p + e;
 #pragma unroll
-                        for (int k2 = 0; k2 < 2; ++k2) {
-                            const uint32_t acc = (t > 0 || k2 > 0) ? 1u : 0u;
-                            mma_ts(tbase + kColDv + 16 * h, x + 32 * e + 16 * k2,
-                                   desc_at(dQm, qoff(t, h) + kG + 512 * k2), idKM, acc);
-                            mma_ts(tbase + kColDk + 16 * h, x + 32 * e + 16 * k2 + 8,
-                                   desc_at(dQm, qoff(t, h) + 512 * k2), idKM, acc);
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                const uint32_t acc = (t > t_seg || k2 > 0) ? 1u : 0u;
+                                mma_ts(tbase + kColDv + 16 * h, x + 32 * e + 16 * k2,
+                                       desc_at(dQm, qoff(t, h) + kG + 512 * k2), idKM, acc);
+                                mma_ts(tbase + kColDk + 16 * h, x + 32 * e + 16 * k2 + 8,
+                                       desc_at(dQm, qoff(t, h) + 512 * k2), idKM, acc);
+                            }
                         }
+                        if (c == C::NCH - 1 && p == 1) mma_commit(&bars->q_empty[ks]);
                     }
-                    if (c == C::NCH - 1 && p == 1) mma_commit(&bars->q_empty[ks]);
+                    __syncwarp();
+                    if (st + 2 < st_end && !issue_sd(st + 2)) { ok = false; break; }
                 }
+                if (!kBal || !ok || st >= nsteps) break;
+                // the segment's products are all issued: signal them, then wait for
+                // the next group's K and V before its first S and dP
+                if (elect_one()) mma_commit(&bars->done);
                 __syncwarp();
-                if (st + 2 < nsteps && !issue_sd(st + 2)) { ok = false; break; }
+                if (!mbar_wait_all(&bars->seg_ready, seg & 1, abort_flag, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+                ++seg;
+                t_seg = st >> 1;
+                b_end += total_tiles;
+#pragma unroll 1
+                for (int k0 = 0; ok && k0 < 2 && st + k0 < nsteps; ++k0) ok = issue_sd(st + k0);
             }
             if (ok) {
                 if (elect_one()) mma_commit(&bars->done);
@@ -355,18 +409,71 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int r = tid & (kBKV - 1);
         const int e = (tid >> 7) & 1;
         const int half = tid >> 8;
-        const int row = j0 + r;
         const uint32_t lrow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t tbl = smem_u32(Ts) + 16u * hb;
+        // a group's dk and dv rows, after its last products (head 2 half + e of the
+        // CTA's four, KV row r): into bf16, or added into the fp32 sums
+        auto epilogue = [&](int g) {
+            const int row = (g >> 1) * kBKV + r;
+            const bool live = row < n;
+            const int hh = 2 * half + e;
+            const int h = kHC * (g & 1) + hh;
+            uint32_t ok16[16], ov16[16];
+            tmem_ld_x16(lrow + kColDk + 16 * hh, ok16);
+            tmem_ld_x16(lrow + kColDv + 16 * hh, ov16);
+            tmem_wait_ld();
+            // head dim 8: the head's channels are columns 8 (h & 1) .. of the 16;
+            // shift them down with constant register indices
+            if (HD == 8 && (h & 1)) {
+#pragma unroll
+                for (int q2 = 0; q2 < 8; ++q2) {
+                    ok16[q2] = ok16[q2 + 8];
+                    ov16[q2] = ov16[q2 + 8];
+                }
+            }
+            if (live && dk_acc) {
+                float* gk = dk_acc + ((int64_t)row * kH + h) * HD;
+                float* gv = dv_acc + ((int64_t)row * kH + h) * HD;
+#pragma unroll
+                for (int q4 = 0; q4 < HD / 4; ++q4) {
+                    red_add_v4(gk + 4 * q4, __uint_as_float(ok16[4 * q4]) * scale, __uint_as_float(ok16[4 * q4 + 1]) * scale,
+                               __uint_as_float(ok16[4 * q4 + 2]) * scale, __uint_as_float(ok16[4 * q4 + 3]) * scale);
+                    red_add_v4(gv + 4 * q4, __uint_as_float(ov16[4 * q4]), __uint_as_float(ov16[4 * q4 + 1]),
+                               __uint_as_float(ov16[4 * q4 + 2]), __uint_as_float(ov16[4 * q4 + 3]));
+                }
+            } else if (live) {
+                uint32_t wk[HD / 2], wv[HD / 2];
+#pragma unroll
+                for (int q2 = 0; q2 < HD / 2; ++q2) {
+                    wk[q2] = pack_bf16x2(__uint_as_float(ok16[2 * q2]) * scale,
+                                         __uint_as_float(ok16[2 * q2 + 1]) * scale);
+                    wv[q2] = pack_bf16x2(__uint_as_float(ov16[2 * q2]), __uint_as_float(ov16[2 * q2 + 1]));
+                }
+                uint4* dstk = reinterpret_cast<uint4*>(dk + ((int64_t)row * kH + h) * HD);
+                uint4* dstv = reinterpret_cast<uint4*>(dv + ((int64_t)row * kH + h) * HD);
+#pragma unroll
+                for (int q2 = 0; q2 < HD / 8; ++q2) {
+                    dstk[q2] = make_uint4(wk[4 * q2], wk[4 * q2 + 1], wk[4 * q2 + 2], wk[4 * q2 + 3]);
+                    dstv[q2] = make_uint4(wv[4 * q2], wv[4 * q2 + 1], wv[4 * q2 + 2], wv[4 * q2 + 3]);
+                }
+            }
+        };
         int t = 0;
+        int seg = 0;    // segments finished
+        int gb = g_first, qb = q_first;   // the tile's group and Q tile
         bool ok = true;
-        for (int b = 0; ok && b < ntiles; ++b) {
+        int b = 0;
+        while (ok) {
+          // the segment's tiles; its end (dk and dv out, the next group's K and V in)
+          // sits outside the tile loop, which stays as small as with one group
+          const int b_stop = kBal ? min(ntiles, b + (total_tiles - qb)) : ntiles;
+          for (; ok && b < b_stop; ++b, ++qb) {
             const int ks = b & 1;
+            const uint32_t tbl = smem_u32(Ts) + 16u * (uint32_t)(gb & 1);
             // (the summary is written after the tile's copies have landed)
             if (!mbar_wait(&bars->meta_ready[ks], (b >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             const uint8_t* stp = smem + C::OFF_STAGE + ks * C::STAGE_BYTES;
             const int* meta = reinterpret_cast<const int*>(smem + C::OFF_META) + ks * C::NMETA + (warp & 3);
-            const int i0 = (qt0 + b) * C::BQ;
+            const int i0 = qb * C::BQ;
             const bool tail_tile = i0 + C::BQ > n;
             for (int c = 0; ok && c < C::NCH; ++c, ++t) {
                 const int ir = c * kCH + 16 * half;       // this thread's first query row in the tile
@@ -448,58 +555,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
             if (!ok) break;
             mbar_arrive(&bars->q_empty[ks]);
+          }
+          if (!ok) break;
+          // the segment's last products are complete: its dk and dv
+          if (!mbar_wait(&bars->done, seg & 1, abort_flag, kWaitNs)) { ok = false; break; }
+          tc_fence_after();
+          epilogue(gb);
+          if (!kBal || b >= ntiles) break;
+          // the next group's K and V, then let the MMA warp on
+          qb = 0;
+          ++gb;
+          if (tid < kBKV) {
+              write_kv(gb);
+              tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->seg_ready);
+          ++seg;
         }
-        if (!ok) {
-            fail(abort_flag, status);
-        } else if (!mbar_wait(&bars->done, 0, abort_flag, kWaitNs)) {
-            fail(abort_flag, status);
-        } else {
-            tc_fence_after();
-            const bool live = row < n;
-            {
-                const int hh = 2 * half + e;
-                const int h = kHC * hb + hh;
-                uint32_t ok16[16], ov16[16];
-                tmem_ld_x16(lrow + kColDk + 16 * hh, ok16);
-                tmem_ld_x16(lrow + kColDv + 16 * hh, ov16);
-                tmem_wait_ld();
-                // head dim 8: the head's channels are columns 8 (h & 1) .. of the 16;
-                // shift them down with constant register indices
-                if (HD == 8 && (h & 1)) {
-#pragma unroll
-                    for (int q2 = 0; q2 < 8; ++q2) {
-                        ok16[q2] = ok16[q2 + 8];
-                        ov16[q2] = ov16[q2 + 8];
-                    }
-                }
-                constexpr int c0h = 0;
-                if (live && dk_acc) {
-                    float* gk = dk_acc + ((int64_t)row * kH + h) * HD;
-                    float* gv = dv_acc + ((int64_t)row * kH + h) * HD;
-#pragma unroll
-                    for (int q2 = 0; q2 < HD; ++q2) {
-                        atomicAdd(gk + q2, __uint_as_float(ok16[c0h + q2]) * scale);
-                        atomicAdd(gv + q2, __uint_as_float(ov16[c0h + q2]));
-                    }
-                } else if (live) {
-                    uint32_t wk[HD / 2], wv[HD / 2];
-#pragma unroll
-                    for (int q2 = 0; q2 < HD / 2; ++q2) {
-                        wk[q2] = pack_bf16x2(__uint_as_float(ok16[c0h + 2 * q2]) * scale,
-                                             __uint_as_float(ok16[c0h + 2 * q2 + 1]) * scale);
-                        wv[q2] = pack_bf16x2(__uint_as_float(ov16[c0h + 2 * q2]),
-                                             __uint_as_float(ov16[c0h + 2 * q2 + 1]));
-                    }
-                    uint4* dstk = reinterpret_cast<uint4*>(dk + ((int64_t)row * kH + h) * HD);
-                    uint4* dstv = reinterpret_cast<uint4*>(dv + ((int64_t)row * kH + h) * HD);
-#pragma unroll
-                    for (int q2 = 0; q2 < HD / 8; ++q2) {
-                        dstk[q2] = make_uint4(wk[4 * q2], wk[4 * q2 + 1], wk[4 * q2 + 2], wk[4 * q2 + 3]);
-                        dstv[q2] = make_uint4(wv[4 * q2], wv[4 * q2 + 1], wv[4 * q2 + 2], wv[4 * q2 + 3]);
-                    }
-                }
-            }
-        }
+        if (!ok) fail(abort_flag, status);
     }
     tc_fence_before();
     __syncthreads();
@@ -511,13 +585,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 }
 
 
-// First KV row of the groups the tail split takes (groups past the last full
-// wave of one CTA per SM, summed in fp32), or -1 when there is no such split.
+// First KV row whose dk and dv are summed in fp32 (then turned into bf16 by the
+// caller), or -1 when there are none.  Groups that do not fill one wave of one
+// CTA per SM all go through the sums (the balanced grid); past one wave, the
+// groups after the last full wave do (the split tail).
 int dkdv_tail_row0(int n, int tail, bool have_acc) {
     const int sms = num_sms();
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
     if (tail <= 1 || !have_acc || groups % sms == 0) return -1;
-    return (groups / sms * sms / 2) * kBKV;
+    return groups < sms ? 0 : (groups / sms * sms / 2) * kBKV;
 }
 
 template <int HD>
@@ -536,41 +612,50 @@ int launch(int n, const void* q, const void* k, const void* v, const void* dO, c
         !make_map_2d(&ml, const_cast<uint16_t*>(LB), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, (uint64_t)kH * 16,
                      (uint64_t)kH * 16 * 2, C::BQ, 16, CU_TENSOR_MAP_SWIZZLE_32B))
         return GT_ERR_CUDA;
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dkdv_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
         return GT_ERR_CUDA;
     int* status = device_status_ptr();
     if (!status) return GT_ERR_CUDA;
     const int total_tiles = (n + C::BQ - 1) / C::BQ;
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
-    // every launch may overlap the kernel before it (the dq kernel, or the full
-    // waves): it reads only the inputs and the prep tables
-    auto run = [&](int g_first, int g_count, int per, bool sums) -> int {
-        const int nz = per > 0 ? (total_tiles + per - 1) / per : 1;
-        dim3 grid(g_count, 1, nz);
+    // the launch may overlap the kernel before it (the dq kernel): it reads only
+    // the inputs and the prep tables
+    auto run = [&](dim3 grid, int g_first, int per, int bal, bool sums) -> int {
         LaunchScope ls("bwd_dkdv", s);
-        if (launch_overlapped(bwd_dkdv_kernel<HD>, grid, dim3(kThreads), C::SMEM, s, mq, mg, ms, ml,
+        auto kern = bal > 0 ? bwd_dkdv_kernel<HD, true> : bwd_dkdv_kernel<HD, false>;
+        if (launch_overlapped(kern, grid, dim3(kThreads), C::SMEM, s, mq, mg, ms, ml,
                               static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), T, nb, n,
-                              scale, fold_scale * kLog2e, g_first, per, static_cast<__nv_bfloat16*>(dk),
+                              scale, fold_scale * kLog2e, g_first, per, bal, static_cast<__nv_bfloat16*>(dk),
                               static_cast<__nv_bfloat16*>(dv), sums ? dk_acc : nullptr, sums ? dv_acc : nullptr,
                               status) != cudaSuccess)
             return GT_ERR_CUDA;
         return check_launch();
     };
     const int row0 = dkdv_tail_row0(n, tail, dk_acc != nullptr);
-    if (row0 >= 0) {
-        // full waves of whole groups (none on a graph too small to fill one), then
-        // the remaining groups split tail ways so that the last waves fill the SMs;
-        // the caller cleared their rows of the sums before and turns them into
-        // bf16 after
-        const int g1 = (row0 / kBKV) * 2;
-        if (g1 > 0) {
-            const int rc = run(0, g1, 0, false);
-            if (rc != GT_OK) return rc;
-        }
-        return run(g1, groups - g1, (total_tiles + tail - 1) / tail, true);
+    if (row0 == 0 && groups < num_sms()) {
+        // fewer groups than SMs: the balanced grid, one CTA per SM, each an equal
+        // share of the (group, Q tile) steps (the bucket matrix of such a graph
+        // stays in L2 for the second head half's reads); the caller cleared the
+        // sums before and turns them into bf16 after
+        const int64_t steps = (int64_t)groups * total_tiles;
+        const int ctas = (int)(steps < num_sms() ? steps : num_sms());
+        return run(dim3(ctas), 0, 0, ctas, true);
     }
-    return run(0, groups, 0, false);
+    if (row0 >= 0) {
+        // full waves of whole groups, then the remaining groups split tail ways
+        // over the SMs: the split CTAs are scheduled as SMs free up, which also
+        // absorbs the uneven end of the dq kernel this launch overlaps (equal
+        // static shares measured slower here)
+        const int g1 = (row0 / kBKV) * 2;
+        const int rc = run(dim3(g1), 0, 0, 0, false);
+        if (rc != GT_OK) return rc;
+        const int per = (total_tiles + tail - 1) / tail;
+        return run(dim3(groups - g1, 1, (total_tiles + per - 1) / per), g1, per, 0, true);
+    }
+    return run(dim3(groups), 0, 0, 0, false);
 }
 
 }  // namespace
@@ -590,14 +675,16 @@ int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, c
                                dv_acc, s);
 }
 
-// Query-range split of the groups past the last full wave of one CTA per SM (all
-// of them on a graph too small to fill one; see launch): the k in [2, 8] that
-// makes the last waves the shortest, in units of one group's time, or 1 when the
-// groups fill whole waves or no k beats one more wave of whole groups.
+// How the dk/dv kernel fills the SMs: 1 when whole groups fill whole waves of
+// one CTA per SM; 2 when the groups do not fill one wave (the balanced grid);
+// otherwise the query-range split of the groups past the last full wave: the k
+// in [2, 8] that makes the last waves the shortest, in units of one group's
+// time, or 1 when no k beats one more wave of whole groups.
 int bwd_dkdv_tail_split(int n) {
     const int sms = num_sms();
     const int groups = 2 * ((n + kBKV - 1) / kBKV);
     if (groups % sms == 0) return 1;
+    if (groups < sms) return 2;
     const int rem = groups % sms;
     int best = 1;
     double best_t = 1.0;                        // the tail unsplit: one more wave of whole groups

@@ -72,7 +72,7 @@ def test_splits_fill_the_last_waves(gt):
 def test_counts_of_a_graph_past_one_wave(gt):
     """n = 16384 (128 tiles): the balanced forward merges its split tiles, and the
     backward splits the dq tasks and dk/dv groups past their last full wave,
-    each with an fp32-to-bf16 conversion; the library's own launch count
+    with one fp32-to-bf16 conversion at the end; the library's own launch count
     matches what ran."""
     n, h, d, nb = 16384, 8, 16, 26
     x = gi.make_layer_tensors(n, h, d, nb, "bf16", seed=6)
