@@ -6,15 +6,19 @@
 //   dv_j = sum_i P_ij dO_i,   dk_j = scale sum_i dS_ij Q_i.
 //
 // One CTA per SM = one group: a tile of 128 KV rows and one half of the heads
-// (4 of 8), streaming every Q tile (or, for split groups, a range of them).  The CTA owns all 512 TMEM columns, so K and
+// (4 of 8), streaming every Q tile (or, for split groups, a range of them; or,
+// in the balanced grid of a graph whose groups do not fill one wave, an equal
+// share of all (group, Q tile) steps, the CTA switching groups as its share
+// crosses them: dk and dv out, the next K and V in).  The CTA owns all 512 TMEM columns, so K and
 // V sit in TMEM as the A operands of S^T = K Q^T and dP^T = V dO^T: every
 // product reads only its small B operand from shared memory (an MMA with A in
 // shared memory reads 4 KB of it, which both costs ~4x the tensor time and
 // delays the softmax warps' own shared loads).  The work is cut into steps of
 // one head pair and 32 query rows; the tensor core runs two steps ahead of the
-// softmax warps.  320 threads:
-//   warps 0-7  warp w owns KV rows 32 (w mod 4) .. + 31 (TMEM lanes) and query
-//              rows 16 (w / 4) .. + 15 of each step, for both heads of the pair: it
+// softmax warps.  576 threads:
+//   warps 0-15 warp w owns KV rows 32 (w mod 4) .. + 31 (TMEM lanes), head
+//              (w / 4) mod 2 of the pair and query rows 16 (w / 8) .. + 15 of each
+//              step: it
 //              reads S'^T and dP'^T from TMEM, the bucket codes from column r of the
 //              int8 tile, forms P^T = 2^(s' scale log2 e + b) and dS^T = P^T dP'^T
 //              and writes both (bf16) back over S'^T.  The tensor core has already
@@ -22,12 +26,12 @@
 //              dP'^T = V dO^T + 1 (-D_i), the second product of each with a constant
 //              A operand of ones in TMEM and B = the per-row values as three bf16
 //              parts (exact to fp32 rounding), so the softmax warps load neither.
-//   warp 8     MMA issuer (the whole warp waits, the elected lane issues): per
+//   warp 16    MMA issuer (the whole warp waits, the elected lane issues): per
 //              step, once its P^T and dS^T are in, dv_h += P^T_h dO_h and
 //              dk_h += dS^T_h Q_h (A from TMEM), then S^T and dP^T of the step two
 //              ahead into the same buffer (the tensor pipe runs one thread's MMAs
 //              in order, so they land after the products that read the buffer).
-//   warp 9     TMA producer: per Q tile the bucket tile and the Q, dO and LB
+//   warp 17    TMA producer: per Q tile the bucket tile and the Q, dO and LB
 //              column slots (LB: -lse_i / scale and -D_i per head in three bf16
 //              parts each); it also summarises each tile's codes.
 // TMEM (512 columns): dk at 0, dv at 64, K at 128 and V at 160 (8 columns of
