@@ -154,11 +154,11 @@ EXP_KERNELS = ("fwd_tc", "bwd_dq", "bwd_dkdv", "fwd_simt", "bwd_rows_simt", "bwd
 # DRAM bytes (read + write) per launch of a kernel at a workload, from ncu
 # captures of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
 # the capture summaries live under profiles/.  For a kernel launched more than once
-# per layer (bwd_dkdv: the full wave, 180.558 MB, and the split tail, 135.425 MB)
+# per layer (bwd_dkdv: the full wave, 179.953 MB, and the split tail, 132.676 MB)
 # the entry is the mean over the layer's launches, like the work per launch.  A
 # kernel changed since its capture has no entry (its traffic is reported as null).
 DRAM_BYTES = {("fwd_tc", "ba64x256"): 295.499e6, ("bwd_dq", "ba64x256"): 318.958e6,
-              ("bwd_dkdv", "ba64x256"): 157.992e6, ("spd_bfs", "ba64x256"): 214.420e6}
+              ("bwd_dkdv", "ba64x256"): 156.315e6, ("spd_bfs", "ba64x256"): 214.420e6}
 
 
 def kernel_roofline(name: str, w: gi.Workload, ms: float, exp_peak: float, hbm_peak: float,

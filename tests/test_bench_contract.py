@@ -37,11 +37,11 @@ def test_exp_kernel_roofline_is_work_over_time_over_peak():
     # a workload without a capture reports no traffic rather than another's
     assert bench.kernel_roofline("fwd_tc", gi.CONFIGS[2], 1.0, peak, 6693.5e9)["traffic"] is None
     # a kernel with several launches per layer: the layer's exps over its launches,
-    # and the mean DRAM bytes of its launches (the dk/dv full wave, 180.558 MB, and
-    # split tail, 135.425 MB, captured separately)
+    # and the mean DRAM bytes of its launches (the dk/dv full wave, 179.953 MB, and
+    # split tail, 132.676 MB, captured separately)
     r2 = bench.kernel_roofline("bwd_dkdv", w, 0.5, peak, 6693.5e9, launches_per_layer=2.0)
     assert r2["work_per_launch"] == work / 2
-    assert r2["traffic"] == pytest.approx((180.558e6 + 135.425e6) / 2, rel=1e-5)
+    assert r2["traffic"] == pytest.approx((179.953e6 + 132.676e6) / 2, rel=1e-5)
     assert r2["frac"] == pytest.approx(work / 2 / 0.5e-3 / peak, abs=1e-4)
 
 
