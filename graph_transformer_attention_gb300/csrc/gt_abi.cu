@@ -109,9 +109,10 @@ size_t fwd_ws(int dtype, int n, int h, int d, int kv_block, void* base, size_t c
 // the dq tasks (tile, head half; two CTAs per SM) along their KV blocks, the
 // dk/dv groups (KV tile, head half; one CTA per SM) along their query tiles, k
 // ways each (1 = none), chosen so that the last waves fill the SMs; on a graph
-// too small to fill one wave every task or group is split.  The split CTAs sum
-// into fp32 accumulators (workspace `acc`, 3 [n][h][d] arrays) turned into bf16
-// at the end.
+// too small to fill one wave every dq task is split, and dk/dv runs equal shares
+// of all its (group, query tile) steps instead (bwd_tail 2).  Split or shared
+// work sums into fp32 accumulators (workspace `acc`, 3 [n][h][d] arrays) turned
+// into bf16 at the end.
 int bwd_tail(int dtype, int n, int h, int d, int nb) {
     if (dtype != GT_BF16 || !bwd_tc_supported(h, d, nb)) return 1;
     return bwd_dkdv_tail_split(n);

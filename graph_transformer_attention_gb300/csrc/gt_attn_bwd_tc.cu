@@ -169,8 +169,9 @@ int launch_bwd_dkdv(int n, int d, const void* q, const void* k, const void* v, c
 // [n][8][16], Dv [8][n] fp32, dT64 [8][nb] fp64, aux [16] fp32 (aux[h]: largest |v_j|
 // of head h), and the fp32 sums acc [3][n][8][d] when either split applies
 // (tail > 1: the dk/dv groups past the last full wave split along their query
-// tiles; dq_tail > 1: the dq tasks past the last full wave split along their KV
-// blocks; on a graph too small to fill a wave, all of them), else null.
+// tiles, or, on a graph whose groups do not fill one wave, dk/dv's equal shares of
+// all its steps; dq_tail > 1: the dq tasks past the last full wave split along
+// their KV blocks, all of them on a graph too small to fill a wave), else null.
 int attn_bwd_tc(int n, int d, const void* q, const void* k, const void* v, const void* o,
                 const void* dO, const float* lse, const int8_t* spd, int64_t ld, const float* T,
                 int nb, float scale, void* dq, void* dk, void* dv, float* dT, float* LD, uint16_t* LB,

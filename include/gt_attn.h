@@ -157,11 +157,13 @@ int32_t gt_bias_attn_fwd_ctas(int32_t dtype, int32_t n, int32_t h, int32_t d, in
  * the bf16 tensor-core backward for these sizes on the current device (1 = none;
  * -1 for invalid arguments).  The dq tasks that do not fill a whole wave of two
  * CTAs per SM (all of them on a graph too small to fill one) are split along
- * their KV blocks, and the dk/dv groups (a 128-row KV tile and a head half) that
- * do not fill a wave of one CTA per SM along their query tiles, k ways each with
- * k in 2..8 chosen so that the last waves fill the SMs; the split CTAs sum in
- * fp32 (workspace included in gt_bias_attn_workspace_size; a workspace too small
- * for the sums runs unsplit).
+ * their KV blocks, k ways with k in 2..8 chosen so that the last waves fill the
+ * SMs.  The dk/dv groups (a 128-row KV tile and a head half) past the last full
+ * wave of one CTA per SM are split along their query tiles the same way; fewer
+ * groups than SMs run instead as equal shares of all (group, query tile) steps,
+ * one CTA per SM.  Split or shared work sums in fp32 (workspace included in
+ * gt_bias_attn_workspace_size; a workspace too small for the sums runs
+ * unsplit).
  */
 int32_t gt_bias_attn_bwd_split(int32_t dtype, int32_t n, int32_t h, int32_t d, int32_t nb);
 
